@@ -1,0 +1,305 @@
+/*
+ * CPU oracle for the batch-invariant exact GEMM — TEST INFRASTRUCTURE ONLY.
+ *
+ * Plain, slow, obviously correct definitions of what the CUDA path computes.
+ * Only the tests, the smoke check and the bench's CPU-baseline leg may load this
+ * library; the product path never does. It shares no code, header or table with
+ * the CUDA library: it is written from the definitions on the source pages.
+ *
+ * Build flags: -O2 -ffp-contract=off -fno-fast-math (no FMA contraction, IEEE
+ * semantics, subnormals kept). OpenMP over output rows only.
+ *
+ * Sources (page title, section):
+ *  [P4] "Deterministic LLM Inference Across GPU Kernels: Power-of-Two INT8
+ *       Quantization Scales and the Limits of Tolerance-Based Conformance",
+ *       §II "Pipeline and alibi" (Y = (A W^T) * s_a s_w, int32 accumulation,
+ *       one rounding to bf16; pow2 commutation), §II.E "Measurement design"
+ *       (int64 reference accumulator), §V / §V.C (nearest and ceiling pow2 arms,
+ *       weights requantized under the pow2 scale).
+ *  [P3] "GPU Mechanism", §3 "Method", Interventions (a) ExactGEMM (frexp-scaled
+ *       7-bit integer slices, exact integer slice products, fixed-order fp64
+ *       recombination, one rounding); §2 "Exact GEMM by error-free
+ *       transformation" (Ozaki scheme).
+ *  [P1] "Taming Bitwise Behavior in GPU Kernels with Tensor Core", §3.2.2
+ *       (split-K cuts the contracted axis into contiguous parts).
+ *
+ * Readings where the pages are silent (each listed in the design notes):
+ *  - bf16 rounding is IEEE round-to-nearest-even with subnormals and overflow
+ *    to infinity; acc = 0 gives +0; a negative value that underflows gives -0.
+ *  - "nearest" power of two is nearest in the log domain; "ceiling" never
+ *    shrinks the scale. Quantized values are round-half-even, clamped to +-127.
+ *  - slice digits are truncated toward zero, 7 bits each, signed, with the
+ *    exponent e of the row/column max from frexp (max|x| < 2^e).
+ *  - the slice pairs kept are s + t <= max_diag with slices numbered from 1;
+ *    diagonals are combined from the smallest weight (g = max_diag) up to g = 2.
+ *
+ * Status codes: 0 ok, 3 precondition (|acc| >= 2^31), 8 non-finite input.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_OK 0
+#define ORACLE_ERR_PRECONDITION 3
+#define ORACLE_ERR_NONFINITE 8
+
+/* ------------------------------------------------------------------------------------ */
+/* Round a double to the nearest bfloat16, ties to even (IEEE 754 RNE).                  */
+/* bf16: 8 significant bits, exponent range of fp32, subnormal spacing 2^-133.           */
+/* ------------------------------------------------------------------------------------ */
+uint16_t oracle_rne_bf16(double v) {
+    if (isnan(v)) return 0x7FC0;
+    uint16_t sign = signbit(v) ? 0x8000 : 0;
+    double a = fabs(v);
+    if (isinf(a)) return sign | 0x7F80;
+    if (a == 0.0) return sign;
+    int k;
+    frexp(a, &k);                        /* a in [2^(k-1), 2^k) */
+    int p = k - 1;                       /* a in [2^p, 2^(p+1)) */
+    int q = (p < -126) ? -133 : p - 7;   /* log2 of the bf16 spacing at a */
+    double n = ldexp(a, -q);             /* exact: power-of-two scaling */
+    double fl = floor(n);
+    double fr = n - fl;                  /* exact */
+    if (fr > 0.5 || (fr == 0.5 && fmod(fl, 2.0) != 0.0)) fl += 1.0;
+    double r = ldexp(fl, q);             /* exact: fl <= 256 */
+    if (r >= 0x1p128) return sign | 0x7F80;
+    float f = (float)r;                  /* exact: r is on the bf16 grid */
+    uint32_t bits;
+    memcpy(&bits, &f, 4);
+    return sign | (uint16_t)((bits >> 16) & 0x7FFF);
+}
+
+static int clamp_exp(int64_t e) {
+    /* beyond +-1200 every |acc| * 2^e is 0 or inf in bf16/fp32 after the fp64 step */
+    if (e > 1200) return 1200;
+    if (e < -1200) return -1200;
+    return (int)e;
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* W8A8 [P4 §II]: acc_ij = sum_k A_ik * W_jk (int64, must fit int32),                    */
+/*                C_ij   = rne_bf16(acc_ij * 2^(ea_i + ew_j)).                           */
+/* A [M x K] row-major (lda), W [N x K] row-major (ldw) = B^T, C [rows x N] (ldc).        */
+/* rows == NULL: all M rows; else output row r is A-row rows[r].                         */
+/* ------------------------------------------------------------------------------------ */
+int oracle_w8a8(const int8_t* A, int64_t lda, const int8_t* W, int64_t ldw, const int32_t* ea,
+                const int32_t* ew, uint16_t* C, int64_t ldc, int M, int N, int K,
+                const int32_t* rows, int nrows) {
+    int n_out = rows ? nrows : M;
+    int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+    for (int r = 0; r < n_out; ++r) {
+        int i = rows ? rows[r] : r;
+        for (int j = 0; j < N; ++j) {
+            int64_t acc = 0;
+            for (int k = 0; k < K; ++k) acc += (int64_t)A[(int64_t)i * lda + k] * (int64_t)W[(int64_t)j * ldw + k];
+            if (acc >= 2147483648LL || acc < -2147483648LL) bad = 1;
+            double v = ldexp((double)acc, clamp_exp((int64_t)ea[i] + (int64_t)ew[j]));
+            C[(int64_t)r * ldc + j] = oracle_rne_bf16(v);
+        }
+    }
+    return bad ? ORACLE_ERR_PRECONDITION : ORACLE_OK;
+}
+
+/* The exact int32 accumulator alone: C_ij = sum_k A_ik * W_jk. */
+int oracle_gemm_s8_i32(const int8_t* A, int64_t lda, const int8_t* W, int64_t ldw, int32_t* C,
+                       int64_t ldc, int M, int N, int K, const int32_t* rows, int nrows) {
+    int n_out = rows ? nrows : M;
+    int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+    for (int r = 0; r < n_out; ++r) {
+        int i = rows ? rows[r] : r;
+        for (int j = 0; j < N; ++j) {
+            int64_t acc = 0;
+            for (int k = 0; k < K; ++k) acc += (int64_t)A[(int64_t)i * lda + k] * (int64_t)W[(int64_t)j * ldw + k];
+            if (acc >= 2147483648LL || acc < -2147483648LL) bad = 1;
+            C[(int64_t)r * ldc + j] = (int32_t)acc;
+        }
+    }
+    return bad ? ORACLE_ERR_PRECONDITION : ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* Pow2 quantization [P4 §V, §V.C]: per row a = max|x|; s = a / 127;                     */
+/*   ceiling arm: e = smallest integer with 2^e >= s   (never shrinks the scale)         */
+/*   nearest arm: e = the integer nearest to log2(s)   (may clip the row's outliers)     */
+/*   q = clamp(rne(x / 2^e), -127, 127).   a == 0: e = 0, q = 0.                          */
+/* x_dtype 0 = bf16 bits, 1 = fp32. mode 0 = nearest, 1 = ceiling.                       */
+/* ------------------------------------------------------------------------------------ */
+static double load_x(const void* X, int x_dtype, int64_t idx) {
+    if (x_dtype == 0) {
+        uint32_t bits = (uint32_t)((const uint16_t*)X)[idx] << 16;
+        float f;
+        memcpy(&f, &bits, 4);
+        return (double)f;
+    }
+    return (double)((const float*)X)[idx];
+}
+
+int oracle_quantize_pow2(const void* X, int x_dtype, int64_t ldx, int rows, int cols, int mode,
+                         int8_t* Q, int64_t ldq, int32_t* e_out) {
+    int bad = 0;
+#pragma omp parallel for schedule(dynamic, 16) reduction(| : bad)
+    for (int i = 0; i < rows; ++i) {
+        double a = 0.0;
+        for (int j = 0; j < cols; ++j) {
+            double x = load_x(X, x_dtype, (int64_t)i * ldx + j);
+            if (!isfinite(x)) bad = 1;
+            if (fabs(x) > a) a = fabs(x);
+        }
+        if (!isfinite(a)) { e_out[i] = 0; continue; }
+        int e = 0;
+        if (a > 0.0) {
+            /* smallest e with 127 * 2^e >= a, found by exact comparisons */
+            e = ilogb(a) - 7;
+            while (ldexp(127.0, e) < a) ++e;
+            while (ldexp(127.0, e - 1) >= a) --e;
+            if (mode == 0) {
+                /* log2(s) >= e - 1/2  <=>  s^2 >= 2^(2e-1)  <=>  a^2 >= 127^2 * 2^(2e-1)
+                 * (a has <= 24 significant bits, so a*a is exact in fp64; no tie exists) */
+                if (!(a * a >= ldexp(16129.0, 2 * e - 1))) e -= 1;
+            }
+        }
+        e_out[i] = e;
+        for (int j = 0; j < cols; ++j) {
+            double x = load_x(X, x_dtype, (int64_t)i * ldx + j);
+            double q = nearbyint(ldexp(x, -e)); /* default rounding mode: ties to even */
+            if (q > 127.0) q = 127.0;
+            if (q < -127.0) q = -127.0;
+            Q[(int64_t)i * ldq + j] = (int8_t)q;
+        }
+    }
+    return bad ? ORACLE_ERR_NONFINITE : ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* Ozaki slicing [P3 §3 (a)]: one shared exponent per row (axis 0) or column (axis 1):   */
+/*   e = frexp exponent of the max |x|   (max|x| < 2^e; e = 0 for an all-zero line)      */
+/*   r = x * 2^-e  in (-1, 1)                                                            */
+/*   for t = 1..nslices:  d_t = trunc(r * 2^7);  r = r * 2^7 - d_t                       */
+/* All steps are exact in fp64. Output planes S[t-1]:                                    */
+/*   axis 0: [rows x cols] row-major;  axis 1: [cols x rows] (each column contiguous).   */
+/* ------------------------------------------------------------------------------------ */
+static void slice_line(const float* X, int64_t stride, int len, int nslices, int8_t* S,
+                       int64_t plane, int64_t sstride, int32_t* e_out, int* bad) {
+    double a = 0.0;
+    for (int k = 0; k < len; ++k) {
+        double x = X[(int64_t)k * stride];
+        if (!isfinite(x)) *bad = 1;
+        if (fabs(x) > a) a = fabs(x);
+    }
+    int e = 0;
+    if (a > 0.0 && isfinite(a)) frexp(a, &e);
+    *e_out = e;
+    for (int k = 0; k < len; ++k) {
+        double r = ldexp((double)X[(int64_t)k * stride], -e);
+        if (!isfinite(r)) r = 0.0;
+        for (int t = 0; t < nslices; ++t) {
+            double v = r * 128.0;
+            double d = trunc(v);
+            r = v - d;
+            S[(int64_t)t * plane + (int64_t)k * sstride] = (int8_t)d;
+        }
+    }
+}
+
+int oracle_slice_f32(const float* X, int64_t ldx, int rows, int cols, int axis, int nslices,
+                     int8_t* S, int32_t* e_out) {
+    int bad = 0;
+    int64_t plane = (int64_t)rows * cols;
+    if (axis == 0) {
+#pragma omp parallel for schedule(dynamic, 16) reduction(| : bad)
+        for (int i = 0; i < rows; ++i) {
+            int b = 0;
+            slice_line(X + (int64_t)i * ldx, 1, cols, nslices, S + (int64_t)i * cols, plane, 1,
+                       e_out + i, &b);
+            bad |= b;
+        }
+    } else {
+#pragma omp parallel for schedule(dynamic, 16) reduction(| : bad)
+        for (int j = 0; j < cols; ++j) {
+            int b = 0;
+            slice_line(X + j, ldx, rows, nslices, S + (int64_t)j * rows, plane, 1, e_out + j, &b);
+            bad |= b;
+        }
+    }
+    return bad ? ORACLE_ERR_NONFINITE : ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* Ozaki fp32 GEMM [P3 §3 (a)]: C = A B with A [M x K], B [K x N] fp32 row-major.         */
+/*   slice A per row (e_i, DA_s) and B per column (f_j, DB_t);                           */
+/*   T_g = sum_{s+t=g, 1<=s,t<=nslices} sum_k DA_s[i,k] * DB_t[k,j]   (exact, int64)     */
+/*   acc = 0.0;  for g = max_diag down to 2:  acc = acc + T_g * 2^(-7g)   (fp64)         */
+/*   C_ij = (float) (acc * 2^(e_i + f_j))          (one rounding to fp32, RNE)           */
+/* rows == NULL: all rows; else output row r is A-row rows[r].                           */
+/* ------------------------------------------------------------------------------------ */
+int oracle_ozaki_f32(const float* A, int64_t lda, const float* B, int64_t ldb, float* C,
+                     int64_t ldc, int M, int N, int K, int nslices, int max_diag,
+                     const int32_t* rows, int nrows) {
+    int n_out = rows ? nrows : M;
+    int8_t* DB = (int8_t*)malloc((size_t)nslices * N * K);
+    int32_t* f = (int32_t*)malloc(sizeof(int32_t) * N);
+    int8_t* DA = (int8_t*)malloc((size_t)nslices * n_out * K);
+    int32_t* e = (int32_t*)malloc(sizeof(int32_t) * n_out);
+    if (!DB || !f || !DA || !e) { free(DB); free(f); free(DA); free(e); return 1; }
+    int bad = oracle_slice_f32(B, ldb, K, N, 1, nslices, DB, f) != 0;
+    /* slice the requested rows of A */
+    int bad_rows = 0;
+    for (int r = 0; r < n_out; ++r) {
+        int i = rows ? rows[r] : r;
+        int b = 0;
+        slice_line(A + (int64_t)i * lda, 1, K, nslices, DA + (int64_t)r * K, (int64_t)n_out * K, 1,
+                   e + r, &b);
+        bad_rows |= b;
+    }
+    int64_t planeA = (int64_t)n_out * K, planeB = (int64_t)N * K;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int r = 0; r < n_out; ++r) {
+        int64_t* T = (int64_t*)malloc(sizeof(int64_t) * (size_t)(max_diag + 1));
+        for (int j = 0; j < N; ++j) {
+            for (int g = 0; g <= max_diag; ++g) T[g] = 0;
+            for (int g = 2; g <= max_diag; ++g) {
+                for (int s = 1; s <= nslices; ++s) {
+                    int t = g - s;
+                    if (t < 1 || t > nslices) continue;
+                    const int8_t* da = DA + (int64_t)(s - 1) * planeA + (int64_t)r * K;
+                    const int8_t* db = DB + (int64_t)(t - 1) * planeB + (int64_t)j * K;
+                    int64_t acc = 0;
+                    for (int k = 0; k < K; ++k) acc += (int64_t)da[k] * (int64_t)db[k];
+                    T[g] += acc;
+                }
+            }
+            double acc = 0.0;
+            for (int g = max_diag; g >= 2; --g) acc = acc + ldexp((double)T[g], -7 * g);
+            C[(int64_t)r * ldc + j] = (float)ldexp(acc, clamp_exp((int64_t)e[r] + (int64_t)f[j]));
+        }
+        free(T);
+    }
+    free(DB); free(f); free(DA); free(e);
+    return (bad || bad_rows) ? ORACLE_ERR_NONFINITE : ORACLE_OK;
+}
+
+/* Per-diagonal exact sums T_g (int64) for one output element set, for tests of the     */
+/* slice GEMMs: T[(r * N + j) * (max_diag + 1) + g].                                     */
+int oracle_ozaki_diagonals(const int8_t* DA, const int8_t* DB, int M, int N, int K, int nslices,
+                           int max_diag, int64_t* T) {
+    int64_t planeA = (int64_t)M * K, planeB = (int64_t)N * K;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int i = 0; i < M; ++i) {
+        for (int j = 0; j < N; ++j) {
+            int64_t* Tij = T + ((int64_t)i * N + j) * (max_diag + 1);
+            for (int g = 0; g <= max_diag; ++g) Tij[g] = 0;
+            for (int g = 2; g <= max_diag; ++g)
+                for (int s = 1; s <= nslices; ++s) {
+                    int t = g - s;
+                    if (t < 1 || t > nslices) continue;
+                    for (int k = 0; k < K; ++k)
+                        Tij[g] += (int64_t)DA[(int64_t)(s - 1) * planeA + (int64_t)i * K + k] *
+                                  (int64_t)DB[(int64_t)(t - 1) * planeB + (int64_t)j * K + k];
+                }
+        }
+    }
+    return ORACLE_OK;
+}
