@@ -1,0 +1,386 @@
+#!/usr/bin/env python
+"""Benchmark of the batch-invariant exact GEMM on GB300.
+
+Headline step: the 8B-class FFN W8A8 workload at M = 8192 tokens — the gate/up GEMM
+(K = 4096, N = 12288) then the down GEMM (K = 12288, N = 4096), int8 operands
+~ rne(N(0, 30)) clipped to +-127, pow2 exponents in [-14, -6], bf16 out. The metric is
+INT8 TOPS (2 M N K per GEMM / time) with the dominant kernel's roofline fraction.
+
+The same JSON line carries extra measurements of the other hot-path rows: the skinny
+decode-shaped GEMM (M=16, N=4096, K=65536, split-K 8/16/32) in GB/s against the HBM
+roofline, the Ozaki fp32 GEMM (4096^3) in effective fp32 TFLOP/s, and the sweep
+linear (M=2048, K=2048, N=6144).
+
+Timing: W warm-up steps, then K timed steps; L2 is flushed (a 256 MiB write) before
+every timed step, outside the timed events; each step is timed with CUDA events on
+the launching stream; barrier + synchronize bracket the timed loop; max over ranks.
+With --impl reference the CPU oracle is timed instead on a bounded sample of rows.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "INT8 TOPS & fraction of dense INT8 / HBM roofline, bit-exact, 1×GB300"
+WORKLOAD = ("8B-class FFN W8A8 at M=8192: gate/up GEMM K=4096 N=12288, then down GEMM "
+            "K=12288 N=4096; int8 ~ rne(N(0,30)) clipped to +-127; pow2 exponents in [-14,-6]; bf16 out")
+M_FFN, N1, K1, N2, K2 = 8192, 12288, 4096, 4096, 12288
+OPS_STEP = 2.0 * M_FFN * (N1 * K1 + N2 * K2)
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-extras", action="store_true", help="skip the extra rows")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ------------------------------------------------------------------------------------------
+# clocks during the timed region
+# ------------------------------------------------------------------------------------------
+class Clocks:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------------------
+# helpers
+# ------------------------------------------------------------------------------------------
+def ffn_inputs():
+    import synthetic
+    return synthetic.ffn_gate_up(M_FFN), synthetic.ffn_down(M_FFN)
+
+
+def cpu_baseline_ffn(gate, down, budget_s=12.0):
+    """Time the CPU oracle (as it stands) on a bounded row sample of both FFN GEMMs."""
+    import oracle
+    oracle.build()
+    A1, W1, ea1, ew1 = gate
+    A2, W2, ea2, ew2 = down
+    t0 = time.perf_counter()
+    oracle.w8a8(A1, W1, ea1, ew1, rows=[0])
+    oracle.w8a8(A2, W2, ea2, ew2, rows=[0])
+    per_row = max(time.perf_counter() - t0, 1e-3)
+    nrows = int(max(1, min(M_FFN, budget_s / per_row)))
+    rows = np.linspace(0, M_FFN - 1, nrows).astype(np.int32)
+    t0 = time.perf_counter()
+    oracle.w8a8(A1, W1, ea1, ew1, rows=rows)
+    oracle.w8a8(A2, W2, ea2, ew2, rows=rows)
+    dt = time.perf_counter() - t0
+    ops = 2.0 * nrows * (N1 * K1 + N2 * K2)
+    return {"value": ops / dt / 1e12, "unit": "TOPS", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{nrows} of {M_FFN} rows of both FFN GEMMs ({dt:.1f} s, int64 triple loop, OpenMP)"}
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+
+    import torch
+    import torch.distributed as dist
+    import deterministic_detgemm_w8a8_gb300 as dg
+
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dg.load()
+    pk = peaks()
+
+    gate, down = ffn_inputs()
+    tdev = lambda x: torch.from_numpy(x).to(dev)
+    G = [tdev(x) for x in gate]
+    D = [tdev(x) for x in down]
+    C1 = torch.empty((M_FFN, N1), dtype=torch.bfloat16, device=dev)
+    C2 = torch.empty((M_FFN, N2), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(evs=None):
+        if evs:
+            evs[0].record(stream)
+        dg.w8a8(*G, out=C1)
+        if evs:
+            evs[1].record(stream)
+        dg.w8a8(*D, out=C2)
+        if evs:
+            evs[2].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = Clocks(local)
+    clocks.start()
+    time.sleep(0.3)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        step(evs[i])
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    g_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    d_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    step_ms = [a + b for a, b in zip(g_ms, d_ms)]
+    ms = statistics.mean(step_ms)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * OPS_STEP / (ms * 1e-3) / 1e12
+
+    # roofline of the dominant kernel (both GEMMs run the same kernel): algorithmic ops of
+    # its launches over their event-timed durations
+    ops_g, ops_d = 2.0 * M_FFN * N1 * K1, 2.0 * M_FFN * N2 * K2
+    achieved = (ops_g + ops_d) * args.steps / ((sum(g_ms) + sum(d_ms)) * 1e-3) / 1e12
+    peak = pk["bf16_tflops_sustained"]
+    roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(achieved / peak, 4), "traffic": None, "kernel": "igemm_tile_kernel",
+                "peak_source": f"{pk['source']} bf16 dense (sustained) — the GB300 tensor pipe's measured peak"}
+
+    out = {"metric": METRIC, "value": round(value, 2), "unit": "TOPS", "n_gpus": world, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "int8", "data": "synthetic (seeded; see synthetic/)",
+           "config": {"workload": WORKLOAD, "M": M_FFN, "gemms": [[N1, K1], [N2, K2]], "split_k": 1,
+                      "l2": "flushed before every timed step (256 MiB write, outside the events)",
+                      "parallelism": f"replicas x{world} (independent problems per rank)"},
+           "roofline": roofline, "gpu_launches": 2 * args.steps, "clocks": clk,
+           "wall_s_timed_loop": round(t_wall, 3)}
+
+    if rank == 0:
+        # sampled bit-exact check of this run's outputs against the oracle
+        import oracle
+        rows = [0, 127, 4096, M_FFN - 1]
+        c1 = C1.view(torch.int16).cpu().numpy().view(np.uint16)[rows]
+        c2 = C2.view(torch.int16).cpu().numpy().view(np.uint16)[rows]
+        ok = (c1 == oracle.w8a8(*gate, rows=rows)).all() and (c2 == oracle.w8a8(*down, rows=rows)).all()
+        out["bitexact_sample"] = bool(ok)
+        out["e2e"] = e2e_ffn(dg, torch, dev, gate, down, args)
+        if not args.no_extras:
+            out["extras"] = extras(dg, torch, dev, pk, flush)
+        if world == 1 and not args.no_cpu_baseline:
+            out["cpu_baseline"] = cpu_baseline_ffn(gate, down)
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def e2e_ffn(dg, torch, dev, gate, down, args):
+    """Same metric through the C-ABI with host buffers: H2D of every input, both GEMMs,
+    D2H of both outputs, all inside the timed region."""
+    pin = lambda x: torch.from_numpy(x).pin_memory()
+    Gh = [pin(x) for x in gate]
+    Dh = [pin(x) for x in down]
+    Gd = [torch.empty_like(x, device=dev) for x in Gh]
+    Dd = [torch.empty_like(x, device=dev) for x in Dh]
+    C1 = torch.empty((M_FFN, N1), dtype=torch.bfloat16, device=dev)
+    C2 = torch.empty((M_FFN, N2), dtype=torch.bfloat16, device=dev)
+    C1h = torch.empty((M_FFN, N1), dtype=torch.bfloat16).pin_memory()
+    C2h = torch.empty((M_FFN, N2), dtype=torch.bfloat16).pin_memory()
+    s = torch.cuda.current_stream()
+
+    def once():
+        for d, h in zip(Gd + Dd, Gh + Dh):
+            d.copy_(h, non_blocking=True)
+        dg.w8a8(*Gd, out=C1)
+        dg.w8a8(*Dd, out=C2)
+        C1h.copy_(C1, non_blocking=True)
+        C2h.copy_(C2, non_blocking=True)
+
+    for _ in range(2):
+        once()
+    torch.cuda.synchronize()
+    n = max(3, min(args.steps, 10))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for _ in range(n):
+        once()
+    e1.record(s)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / n
+    h2d = sum(x.numel() * x.element_size() for x in Gh + Dh)
+    d2h = C1h.numel() * 2 + C2h.numel() * 2
+    return {"value": round(OPS_STEP / (ms * 1e-3) / 1e12, 2), "unit": "TOPS", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 3)}
+
+
+def _time(torch, fn, flush, reps=5, warm=2):
+    for _ in range(warm):
+        fn()
+    s = torch.cuda.current_stream()
+    ts = []
+    for i in range(reps):
+        flush.fill_(i)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(s)
+        fn()
+        b.record(s)
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    return statistics.median(ts)
+
+
+def extras(dg, torch, dev, pk, flush):
+    import synthetic
+    res = {}
+    tdev = lambda x: torch.from_numpy(x).to(dev)
+    # skinny decode-shaped GEMM, HBM-bound
+    A, W, ea, ew = (tdev(x) for x in synthetic.skinny())
+    C = torch.empty((16, 4096), dtype=torch.bfloat16, device=dev)
+    algo_bytes = 16 * 65536 + 4096 * 65536 + 16 * 4096 * 2 + 4 * (16 + 4096)
+    sk = {}
+    outs = []
+    for split in (8, 16, 32):
+        ws = torch.empty(max(dg.w8a8_workspace_size(16, 4096, 65536, split), 1), dtype=torch.uint8, device=dev)
+        ms = _time(torch, lambda: dg.w8a8(A, W, ea, ew, split_k=split, out=C, ws=ws), flush)
+        gbs = algo_bytes / (ms * 1e-3) / 1e9
+        sk[str(split)] = {"us": round(ms * 1e3, 1), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / pk["hbm_gbs"], 4),
+                          "TOPS": round(2.0 * 16 * 4096 * 65536 / (ms * 1e-3) / 1e12, 2)}
+        outs.append(C.clone())
+    sk["identical_across_split"] = bool(all(torch.equal(outs[0].view(torch.int16), o.view(torch.int16))
+                                            for o in outs))
+    res["skinny_M16_N4096_K65536"] = sk
+    del A, W
+    # Ozaki fp32 GEMM 4096^3
+    Af, Bf = (tdev(x) for x in synthetic.ozaki(4096))
+    Cf = torch.empty((4096, 4096), dtype=torch.float32, device=dev)
+    ws = torch.empty(dg.ozaki_workspace_size(4096, 4096, 4096), dtype=torch.uint8, device=dev)
+    ms = _time(torch, lambda: dg.ozaki_f32(Af, Bf, out=Cf, ws=ws), flush, reps=3, warm=1)
+    res["ozaki_f32_4096"] = {"ms": round(ms, 3), "effective_fp32_TFLOPs": round(2 * 4096 ** 3 / (ms * 1e-3) / 1e12, 2),
+                             "slice_TOPS": round(28 * 2 * 4096 ** 3 / (ms * 1e-3) / 1e12, 1)}
+    del Af, Bf, Cf, ws
+    # sweep linear at M = 2048
+    A, W, ea, ew = (tdev(x) for x in synthetic.sweep(2048))
+    C = torch.empty((2048, 6144), dtype=torch.bfloat16, device=dev)
+    ms = _time(torch, lambda: dg.w8a8(A, W, ea, ew, out=C), flush)
+    res["sweep_M2048_N6144_K2048"] = {"us": round(ms * 1e3, 1),
+                                      "TOPS": round(2.0 * 2048 * 6144 * 2048 / (ms * 1e-3) / 1e12, 1)}
+    return res
+
+
+def run_reference(args, world, rank):
+    """The CPU oracle on a bounded row sample of the FFN workload (rank 0 only)."""
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    gate, down = ffn_inputs()
+    A1, W1, ea1, ew1 = gate
+    A2, W2, ea2, ew2 = down
+    # size the per-step sample so that the whole run stays within a few minutes
+    t0 = time.perf_counter()
+    oracle.w8a8(A1, W1, ea1, ew1, rows=[0])
+    oracle.w8a8(A2, W2, ea2, ew2, rows=[0])
+    per_row = max(time.perf_counter() - t0, 1e-3)
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    nrows = int(max(1, min(M_FFN, budget / per_row)))
+    rows = np.linspace(0, M_FFN - 1, nrows).astype(np.int32)
+
+    def one():
+        oracle.w8a8(A1, W1, ea1, ew1, rows=rows)
+        oracle.w8a8(A2, W2, ea2, ew2, rows=rows)
+
+    for _ in range(args.warmup):
+        one()
+    ts = []
+    for _ in range(args.steps):
+        t = time.perf_counter()
+        one()
+        ts.append(time.perf_counter() - t)
+    ms = statistics.mean(ts) * 1e3
+    ops = 2.0 * nrows * (N1 * K1 + N2 * K2)
+    value = ops / (ms * 1e-3) / 1e12
+    sample = f"{nrows} of {M_FFN} rows of both FFN GEMMs per step"
+    out = {"metric": METRIC, "value": round(value, 5), "unit": "TOPS", "n_gpus": world, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": round(ms, 2), "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "int8", "data": "synthetic (seeded; see synthetic/)",
+           "config": {"workload": WORKLOAD, "M": M_FFN, "gemms": [[N1, K1], [N2, K2]]}, "impl": "reference",
+           "cpu_baseline": {"value": round(value, 5), "unit": "TOPS", "cores": os.cpu_count(), "kind": "oracle",
+                            "sample": sample},
+           "e2e": {"value": round(value, 5), "unit": "TOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main() or 0)

@@ -1,0 +1,237 @@
+"""Batch-invariant exact GEMM for NVIDIA GB300 — Python binding of libdetgemm.
+
+A thin ctypes layer over the C ABI declared in ``include/detgemm.h``: it checks
+tensor dtypes/devices, allocates outputs and scratch with PyTorch, and passes raw
+device pointers and the current CUDA stream. Every step of the computation runs in
+the library's CUDA kernels; there is no CPU path. If ``libdetgemm.so`` has not been
+built, importing works but every call raises ``DetGemmError``.
+
+Functions mirror the C entry points:
+
+* :func:`w8a8`           C = rne_bf16((A W^T) * 2^(ea_i + ew_j))      (bf16 out)
+* :func:`gemm_s8_i32`    C = A W^T, exact int32
+* :func:`quantize_pow2`  per-row power-of-two scale and int8 values
+* :func:`slice_f32`      Ozaki digit planes with shared exponents
+* :func:`ozaki_f32`      Ozaki-scheme fp32 GEMM C = A B
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libdetgemm.so")
+
+OK, ERR_INVALID_ARG, ERR_ALIGNMENT, ERR_PRECONDITION, ERR_WORKSPACE = 0, 1, 2, 3, 4
+ERR_UNSUPPORTED_DEVICE, ERR_CUDA, ERR_TIMEOUT, ERR_NONFINITE = 5, 6, 7, 8
+DTYPE_BF16, DTYPE_F32 = 0, 1
+POW2_NEAREST, POW2_CEIL = 0, 1
+AXIS_ROWS, AXIS_COLS = 0, 1
+MAX_K = 131071
+
+# every symbol include/detgemm.h declares, with its ctypes signature
+_P, _I64, _I32, _SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+SIGNATURES = {
+    "detgemm_status_string": ([_I32], ctypes.c_char_p),
+    "detgemm_version": ([], _I32),
+    "detgemm_w8a8": ([_P, _I64, _P, _I64, _P, _P, _P, _I64, _I32, _I32, _I32, _I32, _P, _SZ, _P], _I32),
+    "detgemm_w8a8_workspace_size": ([_I32, _I32, _I32, _I32], _SZ),
+    "detgemm_gemm_s8_i32": ([_P, _I64, _P, _I64, _P, _I64, _I32, _I32, _I32, _I32, _P, _SZ, _P], _I32),
+    "detgemm_quantize_pow2": ([_P, _I32, _I64, _I32, _I32, _I32, _P, _I64, _P, _P], _I32),
+    "detgemm_slice_f32": ([_P, _I64, _I32, _I32, _I32, _I32, _P, _P, _P], _I32),
+    "detgemm_ozaki_f32": ([_P, _I64, _P, _I64, _P, _I64, _I32, _I32, _I32, _I32, _I32, _I32, _P, _SZ, _P], _I32),
+    "detgemm_ozaki_workspace_size": ([_I32, _I32, _I32, _I32, _I32, _I32], _SZ),
+    "detgemm_get_device_status": ([_P], _I32),
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class DetGemmError(RuntimeError):
+    def __init__(self, status: int, where: str = ""):
+        self.status = status
+        name = status_string(status) if _lib is not None else str(status)
+        super().__init__(f"{where}: {name}" if where else name)
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libdetgemm.so (raises DetGemmError-compatible RuntimeError if absent)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    f"libdetgemm.so not found at {path}; build it with "
+                    "`python -c 'import __graft_entry__ as g; g.build()'`")
+            lib = ctypes.CDLL(path)
+            for name, (args, res) in SIGNATURES.items():
+                fn = getattr(lib, name)
+                fn.argtypes = args
+                fn.restype = res
+            _lib = lib
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return load().detgemm_status_string(status).decode()
+
+
+def _check(status: int, where: str):
+    if status != OK:
+        raise DetGemmError(status, where)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def _req(t: torch.Tensor, dtype, name):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dim() == 2 and t.stride(1) != 1:
+        raise ValueError(f"{name} must have unit stride along its last dimension")
+    if t.dim() == 1 and not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _ld(t: torch.Tensor) -> int:
+    """Row stride in elements; a single row may use any stride, so report an aligned one."""
+    if t.shape[0] > 1:
+        return t.stride(0)
+    per = 16 // t.element_size()
+    return max(per, (t.shape[1] + per - 1) // per * per)
+
+
+def empty2d(rows: int, cols: int, dtype, device) -> torch.Tensor:
+    """[rows, cols] tensor whose row stride is a multiple of 16 bytes (the library's rule)."""
+    esize = torch.empty((), dtype=dtype).element_size()
+    per = 16 // esize
+    ld = max(per, (cols + per - 1) // per * per)
+    return torch.empty((rows, ld), dtype=dtype, device=device)[:, :cols]
+
+
+def _workspace(nbytes: int, device, ws):
+    if nbytes == 0:
+        return None, 0
+    if ws is not None:
+        if ws.numel() * ws.element_size() < nbytes:
+            raise ValueError(f"workspace too small: need {nbytes} bytes")
+        return ws, ws.numel() * ws.element_size()
+    return torch.empty(nbytes, dtype=torch.uint8, device=device), nbytes
+
+
+def w8a8_workspace_size(M: int, N: int, K: int, split_k: int = 1) -> int:
+    return int(load().detgemm_w8a8_workspace_size(M, N, K, split_k))
+
+
+def ozaki_workspace_size(M, N, K, nslices=7, max_diag=8, split_k=1) -> int:
+    return int(load().detgemm_ozaki_workspace_size(M, N, K, nslices, max_diag, split_k))
+
+
+def w8a8(A, W, ea, ew, split_k: int = 1, out=None, ws=None, stream=None) -> torch.Tensor:
+    """C = rne_bf16((A W^T) * 2^(ea_i + ew_j)); A int8 [M,K], W int8 [N,K], ea/ew int32.
+    Returns a torch.bfloat16 tensor [M, N] (or writes ``out``)."""
+    lib = load()
+    _req(A, torch.int8, "A"); _req(W, torch.int8, "W")
+    _req(ea, torch.int32, "ea"); _req(ew, torch.int32, "ew")
+    M, K = A.shape
+    N = W.shape[0]
+    if W.shape[1] != K or ea.shape != (M,) or ew.shape != (N,):
+        raise ValueError("shape mismatch")
+    if out is None:
+        out = empty2d(M, N, torch.bfloat16, A.device)
+    _req(out, torch.bfloat16, "out")
+    wsb, wsn = _workspace(w8a8_workspace_size(M, N, K, split_k), A.device, ws)
+    st = lib.detgemm_w8a8(A.data_ptr(), _ld(A), W.data_ptr(), _ld(W), ea.data_ptr(), ew.data_ptr(),
+                          out.data_ptr(), _ld(out), M, N, K, split_k,
+                          wsb.data_ptr() if wsb is not None else None, wsn, _stream(stream))
+    _check(st, "detgemm_w8a8")
+    return out
+
+
+def gemm_s8_i32(A, W, split_k: int = 1, out=None, ws=None, stream=None) -> torch.Tensor:
+    """Exact int32 accumulator C = A W^T."""
+    lib = load()
+    _req(A, torch.int8, "A"); _req(W, torch.int8, "W")
+    M, K = A.shape
+    N = W.shape[0]
+    if W.shape[1] != K:
+        raise ValueError("shape mismatch")
+    if out is None:
+        out = empty2d(M, N, torch.int32, A.device)
+    _req(out, torch.int32, "out")
+    wsb, wsn = _workspace(w8a8_workspace_size(M, N, K, split_k), A.device, ws)
+    st = lib.detgemm_gemm_s8_i32(A.data_ptr(), _ld(A), W.data_ptr(), _ld(W), out.data_ptr(), _ld(out),
+                                 M, N, K, split_k, wsb.data_ptr() if wsb is not None else None, wsn,
+                                 _stream(stream))
+    _check(st, "detgemm_gemm_s8_i32")
+    return out
+
+
+def quantize_pow2(X, mode: int = POW2_NEAREST, stream=None):
+    """Per-row pow2 quantization of a bf16 or fp32 [rows, cols] tensor -> (Q int8, e int32)."""
+    lib = load()
+    if X.dtype == torch.bfloat16:
+        dt = DTYPE_BF16
+    elif X.dtype == torch.float32:
+        dt = DTYPE_F32
+    else:
+        raise TypeError("X must be bfloat16 or float32")
+    _req(X, X.dtype, "X")
+    rows, cols = X.shape
+    Q = empty2d(rows, cols, torch.int8, X.device)
+    e = torch.empty((rows,), dtype=torch.int32, device=X.device)
+    st = lib.detgemm_quantize_pow2(X.data_ptr(), dt, _ld(X), rows, cols, mode, Q.data_ptr(), _ld(Q),
+                                   e.data_ptr(), _stream(stream))
+    _check(st, "detgemm_quantize_pow2")
+    return Q, e
+
+
+def slice_f32(X, axis: int = AXIS_ROWS, nslices: int = 7, stream=None):
+    """Ozaki digits of fp32 X: (S int8 [nslices, rows, cols] or [nslices, cols, rows], e int32)."""
+    lib = load()
+    _req(X, torch.float32, "X")
+    rows, cols = X.shape
+    shape = (nslices, rows, cols) if axis == AXIS_ROWS else (nslices, cols, rows)
+    S = torch.empty(shape, dtype=torch.int8, device=X.device)
+    e = torch.empty((rows if axis == AXIS_ROWS else cols,), dtype=torch.int32, device=X.device)
+    st = lib.detgemm_slice_f32(X.data_ptr(), _ld(X), rows, cols, axis, nslices, S.data_ptr(), e.data_ptr(),
+                               _stream(stream))
+    _check(st, "detgemm_slice_f32")
+    return S, e
+
+
+def ozaki_f32(A, B, nslices: int = 7, max_diag: int = 8, split_k: int = 1, out=None, ws=None,
+              stream=None) -> torch.Tensor:
+    """Ozaki-scheme fp32 GEMM C = A B (A [M,K], B [K,N] fp32 row-major)."""
+    lib = load()
+    _req(A, torch.float32, "A"); _req(B, torch.float32, "B")
+    M, K = A.shape
+    K2, N = B.shape
+    if K2 != K:
+        raise ValueError("shape mismatch")
+    if out is None:
+        out = empty2d(M, N, torch.float32, A.device)
+    _req(out, torch.float32, "out")
+    need = ozaki_workspace_size(M, N, K, nslices, max_diag, split_k)
+    wsb, wsn = _workspace(need, A.device, ws)
+    st = lib.detgemm_ozaki_f32(A.data_ptr(), _ld(A), B.data_ptr(), _ld(B), out.data_ptr(), _ld(out),
+                               M, N, K, nslices, max_diag, split_k,
+                               wsb.data_ptr() if wsb is not None else None, wsn, _stream(stream))
+    _check(st, "detgemm_ozaki_f32")
+    return out
+
+
+def device_status(stream=None) -> int:
+    """Synchronize the stream; return and clear the device status (OK, ERR_NONFINITE, ERR_TIMEOUT)."""
+    return int(load().detgemm_get_device_status(_stream(stream)))

@@ -1,0 +1,266 @@
+// C ABI of libdetgemm (declared in include/detgemm.h): argument validation, workspace
+// layout and kernel dispatch. Every argument/alignment/precondition check runs on the
+// host before any CUDA call, so a rejected call has no effect and launches nothing.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "../../include/detgemm.h"
+#include "common.cuh"
+#include "internal.h"
+
+namespace detgemm {
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_dev_mutex;
+int g_dev_cc[kMaxDevices];  // 0 = unknown, else 10 * major + minor
+
+detgemm_status check_device() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return DETGEMM_ERR_UNSUPPORTED_DEVICE;
+    if (dev < 0 || dev >= kMaxDevices) return DETGEMM_ERR_UNSUPPORTED_DEVICE;
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    if (g_dev_cc[dev] == 0) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+            return DETGEMM_ERR_UNSUPPORTED_DEVICE;
+        g_dev_cc[dev] = 10 * major + minor;
+    }
+    return g_dev_cc[dev] == 103 ? DETGEMM_OK : DETGEMM_ERR_UNSUPPORTED_DEVICE;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+detgemm_status from_cuda(cudaError_t e) { return e == cudaSuccess ? DETGEMM_OK : DETGEMM_ERR_CUDA; }
+
+// Shared validation of the integer GEMM entry points.
+detgemm_status validate_igemm(const void* A, int64_t lda, const void* W, int64_t ldw, const void* C, int64_t ldc,
+                              int c_elem, int M, int N, int K, int split_k, const void* ws, size_t ws_bytes) {
+    if (M < 0 || N < 0 || K < 1) return DETGEMM_ERR_INVALID_ARG;
+    if (K > DETGEMM_MAX_K) return DETGEMM_ERR_PRECONDITION;
+    int nkb = (K + 63) / 64;
+    if (split_k < 1 || split_k > nkb) return DETGEMM_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return DETGEMM_OK;
+    if (!A || !W || !C) return DETGEMM_ERR_INVALID_ARG;
+    if (lda < K || ldw < K || ldc < N) return DETGEMM_ERR_INVALID_ARG;
+    if (!aligned16(A) || !aligned16(W) || !aligned16(C)) return DETGEMM_ERR_ALIGNMENT;
+    if ((lda % 16) != 0 || (ldw % 16) != 0 || ((ldc * c_elem) % 16) != 0) return DETGEMM_ERR_ALIGNMENT;
+    size_t need = detgemm_w8a8_workspace_size(M, N, K, split_k);
+    if (need > 0 && (ws == nullptr || ws_bytes < need)) return DETGEMM_ERR_WORKSPACE;
+    if (need > 0 && !aligned16(ws)) return DETGEMM_ERR_ALIGNMENT;
+    return DETGEMM_OK;
+}
+
+// Ozaki workspace layout (each piece 256-byte aligned):
+//   DA  int8 [nslices][M][Kp]   DB int8 [nslices][N][Kp]   (Kp = K rounded up to 16)
+//   e   int32 [M]               f  int32 [N]
+//   T   int32 [max_diag - 1][M][ldT]  (ldT = N rounded up to 4: 16-byte rows)
+//   igemm split-K scratch (split_k > 1)
+struct OzakiLayout {
+    size_t da, db, e, f, T, gemm, total;
+    int64_t Kp, ldT;
+};
+
+OzakiLayout ozaki_layout(int M, int N, int K, int nslices, int max_diag, int split_k) {
+    OzakiLayout L;
+    L.Kp = ((int64_t)K + 15) / 16 * 16;
+    L.ldT = ((int64_t)N + 3) / 4 * 4;
+    size_t off = 0;
+    L.da = off; off += align256((size_t)nslices * M * L.Kp);
+    L.db = off; off += align256((size_t)nslices * N * L.Kp);
+    L.e = off; off += align256((size_t)M * 4);
+    L.f = off; off += align256((size_t)N * 4);
+    L.T = off; off += align256((size_t)(max_diag - 1) * M * L.ldT * 4);
+    L.gemm = off; off += align256(igemm_workspace_bytes(M, N, split_k));
+    L.total = off;
+    return L;
+}
+
+}  // namespace
+}  // namespace detgemm
+
+using namespace detgemm;
+
+extern "C" {
+
+const char* detgemm_status_string(detgemm_status s) {
+    switch (s) {
+        case DETGEMM_OK: return "DETGEMM_OK";
+        case DETGEMM_ERR_INVALID_ARG: return "DETGEMM_ERR_INVALID_ARG";
+        case DETGEMM_ERR_ALIGNMENT: return "DETGEMM_ERR_ALIGNMENT";
+        case DETGEMM_ERR_PRECONDITION: return "DETGEMM_ERR_PRECONDITION";
+        case DETGEMM_ERR_WORKSPACE: return "DETGEMM_ERR_WORKSPACE";
+        case DETGEMM_ERR_UNSUPPORTED_DEVICE: return "DETGEMM_ERR_UNSUPPORTED_DEVICE";
+        case DETGEMM_ERR_CUDA: return "DETGEMM_ERR_CUDA";
+        case DETGEMM_ERR_TIMEOUT: return "DETGEMM_ERR_TIMEOUT";
+        case DETGEMM_ERR_NONFINITE: return "DETGEMM_ERR_NONFINITE";
+    }
+    return "DETGEMM_ERR_UNKNOWN";
+}
+
+int detgemm_version(void) { return 100; }
+
+size_t detgemm_w8a8_workspace_size(int M, int N, int K, int split_k) {
+    (void)K;
+    if (M <= 0 || N <= 0) return 0;
+    return igemm_workspace_bytes(M, N, split_k);
+}
+
+static detgemm_status run_igemm(const int8_t* A, int64_t lda, const int8_t* W, int64_t ldw, const int32_t* ea,
+                                const int32_t* ew, void* C, int64_t ldc, int mode, int M, int N, int K, int split_k,
+                                void* ws, cudaStream_t stream) {
+    IGemmArgs a = {};
+    a.seg[0] = Seg{A, W};
+    a.nseg = 1;
+    a.lda = lda;
+    a.ldw = ldw;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.split = split_k;
+    a.mode = mode;
+    a.ea = ea;
+    a.ew = ew;
+    a.C = C;
+    a.ldc = ldc;
+    return from_cuda(igemm_launch(a, ws, stream));
+}
+
+detgemm_status detgemm_w8a8(const int8_t* A, int64_t lda, const int8_t* W, int64_t ldw, const int32_t* ea,
+                            const int32_t* ew, uint16_t* C, int64_t ldc, int M, int N, int K, int split_k, void* ws,
+                            size_t ws_bytes, detgemm_stream_t stream) {
+    detgemm_status st = validate_igemm(A, lda, W, ldw, C, ldc, 2, M, N, K, split_k, ws, ws_bytes);
+    if (st != DETGEMM_OK) return st;
+    if (M == 0 || N == 0) return DETGEMM_OK;
+    if (!ea || !ew) return DETGEMM_ERR_INVALID_ARG;
+    if (!aligned4(ea) || !aligned4(ew)) return DETGEMM_ERR_ALIGNMENT;
+    if ((st = check_device()) != DETGEMM_OK) return st;
+    return run_igemm(A, lda, W, ldw, ea, ew, C, ldc, EPI_BF16_POW2, M, N, K, split_k, ws,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+detgemm_status detgemm_gemm_s8_i32(const int8_t* A, int64_t lda, const int8_t* W, int64_t ldw, int32_t* C,
+                                   int64_t ldc, int M, int N, int K, int split_k, void* ws, size_t ws_bytes,
+                                   detgemm_stream_t stream) {
+    detgemm_status st = validate_igemm(A, lda, W, ldw, C, ldc, 4, M, N, K, split_k, ws, ws_bytes);
+    if (st != DETGEMM_OK) return st;
+    if (M == 0 || N == 0) return DETGEMM_OK;
+    if ((st = check_device()) != DETGEMM_OK) return st;
+    return run_igemm(A, lda, W, ldw, nullptr, nullptr, C, ldc, EPI_STORE_I32, M, N, K, split_k, ws,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+detgemm_status detgemm_quantize_pow2(const void* X, int x_dtype, int64_t ldx, int rows, int cols, int mode,
+                                     int8_t* Q, int64_t ldq, int32_t* e, detgemm_stream_t stream) {
+    if (rows < 0 || cols < 0) return DETGEMM_ERR_INVALID_ARG;
+    if (x_dtype != DETGEMM_DTYPE_BF16 && x_dtype != DETGEMM_DTYPE_F32) return DETGEMM_ERR_INVALID_ARG;
+    if (mode != DETGEMM_POW2_NEAREST && mode != DETGEMM_POW2_CEIL) return DETGEMM_ERR_INVALID_ARG;
+    if (rows == 0) return DETGEMM_OK;
+    if (!X || !Q || !e) return DETGEMM_ERR_INVALID_ARG;
+    if (ldx < cols || ldq < cols) return DETGEMM_ERR_INVALID_ARG;
+    const int xs = x_dtype == DETGEMM_DTYPE_BF16 ? 2 : 4;
+    if (!aligned16(X) || !aligned16(Q) || !aligned4(e)) return DETGEMM_ERR_ALIGNMENT;
+    if ((ldx * xs) % 16 != 0 || ldq % 16 != 0) return DETGEMM_ERR_ALIGNMENT;
+    detgemm_status st = check_device();
+    if (st != DETGEMM_OK) return st;
+    return from_cuda(quantize_pow2_launch(X, x_dtype, ldx, rows, cols, mode, Q, ldq, e,
+                                          reinterpret_cast<cudaStream_t>(stream)));
+}
+
+detgemm_status detgemm_slice_f32(const float* X, int64_t ldx, int rows, int cols, int axis, int nslices, int8_t* S,
+                                 int32_t* e, detgemm_stream_t stream) {
+    if (rows < 0 || cols < 0) return DETGEMM_ERR_INVALID_ARG;
+    if (axis != DETGEMM_AXIS_ROWS && axis != DETGEMM_AXIS_COLS) return DETGEMM_ERR_INVALID_ARG;
+    if (nslices < 1 || nslices > 9) return DETGEMM_ERR_INVALID_ARG;
+    if (rows == 0 || cols == 0) {
+        if ((axis == DETGEMM_AXIS_ROWS ? rows : cols) == 0) return DETGEMM_OK;
+    }
+    if (!X || !S || !e) return DETGEMM_ERR_INVALID_ARG;
+    if (ldx < cols) return DETGEMM_ERR_INVALID_ARG;
+    if (!aligned16(X) || !aligned16(S) || !aligned4(e)) return DETGEMM_ERR_ALIGNMENT;
+    if ((ldx * 4) % 16 != 0) return DETGEMM_ERR_ALIGNMENT;
+    detgemm_status st = check_device();
+    if (st != DETGEMM_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (axis == DETGEMM_AXIS_ROWS) return from_cuda(slice_rows_launch(X, ldx, rows, cols, nslices, S, cols, e, s));
+    return from_cuda(slice_cols_launch(X, ldx, rows, cols, nslices, S, rows, e, s));
+}
+
+size_t detgemm_ozaki_workspace_size(int M, int N, int K, int nslices, int max_diag, int split_k) {
+    if (M <= 0 || N <= 0 || K <= 0 || nslices < 1 || max_diag < 2) return 0;
+    return ozaki_layout(M, N, K, nslices, max_diag, split_k).total;
+}
+
+detgemm_status detgemm_ozaki_f32(const float* A, int64_t lda, const float* B, int64_t ldb, float* C, int64_t ldc,
+                                 int M, int N, int K, int nslices, int max_diag, int split_k, void* ws,
+                                 size_t ws_bytes, detgemm_stream_t stream) {
+    if (M < 0 || N < 0 || K < 1) return DETGEMM_ERR_INVALID_ARG;
+    if (nslices < 1 || nslices > 9 || max_diag < 2 || max_diag > 2 * nslices) return DETGEMM_ERR_INVALID_ARG;
+    int nkb = (K + 63) / 64;
+    if (split_k < 1 || split_k > nkb) return DETGEMM_ERR_INVALID_ARG;
+    // every diagonal sum must stay in int32: at most nslices pairs of K products of |d| <= 127
+    int pairs = max_diag - 1 < nslices ? max_diag - 1 : nslices;
+    if ((long long)pairs * K * 127 * 127 >= 2147483648LL) return DETGEMM_ERR_PRECONDITION;
+    if (M == 0 || N == 0) return DETGEMM_OK;
+    if (!A || !B || !C) return DETGEMM_ERR_INVALID_ARG;
+    if (lda < K || ldb < N || ldc < N) return DETGEMM_ERR_INVALID_ARG;
+    if (!aligned16(A) || !aligned16(B) || !aligned16(C)) return DETGEMM_ERR_ALIGNMENT;
+    if ((lda * 4) % 16 || (ldb * 4) % 16 || (ldc * 4) % 16) return DETGEMM_ERR_ALIGNMENT;
+    OzakiLayout L = ozaki_layout(M, N, K, nslices, max_diag, split_k);
+    if (ws == nullptr || ws_bytes < L.total) return DETGEMM_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return DETGEMM_ERR_ALIGNMENT;
+    detgemm_status st = check_device();
+    if (st != DETGEMM_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    char* base = reinterpret_cast<char*>(ws);
+    int8_t* DA = reinterpret_cast<int8_t*>(base + L.da);
+    int8_t* DB = reinterpret_cast<int8_t*>(base + L.db);
+    int32_t* e = reinterpret_cast<int32_t*>(base + L.e);
+    int32_t* f = reinterpret_cast<int32_t*>(base + L.f);
+    int32_t* T = reinterpret_cast<int32_t*>(base + L.T);
+    cudaError_t err = slice_rows_launch(A, lda, M, K, nslices, DA, L.Kp, e, s);
+    if (err == cudaSuccess) err = slice_cols_launch(B, ldb, K, N, nslices, DB, L.Kp, f, s);
+    const int64_t planeA = (int64_t)M * L.Kp, planeB = (int64_t)N * L.Kp;
+    for (int g = 2; g <= max_diag && err == cudaSuccess; ++g) {
+        IGemmArgs a = {};
+        a.nseg = 0;
+        for (int sA = 1; sA <= nslices; ++sA) {
+            int tB = g - sA;
+            if (tB < 1 || tB > nslices) continue;
+            a.seg[a.nseg++] = Seg{DA + (sA - 1) * planeA, DB + (tB - 1) * planeB};
+        }
+        a.lda = L.Kp;
+        a.ldw = L.Kp;
+        a.M = M;
+        a.N = N;
+        a.K = K;
+        a.split = split_k;  // <= nkb <= nkb * nseg K blocks, so no part is empty
+        a.mode = EPI_STORE_I32;
+        a.C = T + (int64_t)(g - 2) * M * L.ldT;
+        a.ldc = L.ldT;
+        err = igemm_launch(a, base + L.gemm, s);
+    }
+    if (err == cudaSuccess) err = ozaki_combine_launch(T, L.ldT, max_diag, e, f, C, ldc, M, N, s);
+    return from_cuda(err);
+}
+
+detgemm_status detgemm_get_device_status(detgemm_stream_t stream) {
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return DETGEMM_ERR_CUDA;
+    uint32_t v = 0, bits = 0;
+    if (quantize_take_status(&bits) != cudaSuccess) return DETGEMM_ERR_CUDA;
+    v |= bits;
+    if (slice_take_status(&bits) != cudaSuccess) return DETGEMM_ERR_CUDA;
+    v |= bits;
+    if (v & DEV_TIMEOUT) return DETGEMM_ERR_TIMEOUT;
+    if (v & DEV_NONFINITE) return DETGEMM_ERR_NONFINITE;
+    return DETGEMM_OK;
+}
+
+}  // extern "C"

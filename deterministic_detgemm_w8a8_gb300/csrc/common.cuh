@@ -1,0 +1,112 @@
+// Shared device helpers of libdetgemm: status word, exact epilogues, bit utilities.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/detgemm.h"
+
+namespace detgemm {
+
+// Device status bits (first error wins in the host-visible translation).
+enum : uint32_t { DEV_NONFINITE = 1u, DEV_TIMEOUT = 2u };
+
+// Device status word. Every translation unit that raises a device-side condition owns
+// one (internal linkage, so no relocatable device code is needed) and exports a host
+// accessor built with DETGEMM_STATUS_ACCESSOR; the C ABI ORs them together.
+static __device__ uint32_t g_device_status = 0;
+
+__device__ __forceinline__ void raise_status(uint32_t bit) { atomicOr(&g_device_status, bit); }
+
+// Defines `cudaError_t fn(uint32_t* bits)`: reads and clears this unit's status word on
+// the current device (synchronous; the caller has synchronized the stream).
+#define DETGEMM_STATUS_ACCESSOR(fn)                                                      \
+    cudaError_t fn(uint32_t* bits) {                                                     \
+        uint32_t zero = 0;                                                               \
+        cudaError_t e = cudaMemcpyFromSymbol(bits, g_device_status, sizeof(uint32_t));   \
+        if (e == cudaSuccess && *bits != 0)                                              \
+            e = cudaMemcpyToSymbol(g_device_status, &zero, sizeof(uint32_t));            \
+        return e;                                                                        \
+    }
+
+// ------------------------------------------------------------------------------------
+// Epilogue E1 — "Deterministic LLM Inference Across GPU Kernels: Power-of-Two INT8
+// Quantization Scales ...", §II "Pipeline and alibi": the int32 accumulator is scaled
+// by the power of two 2^(ea + ew) and rounded once to bfloat16.
+//
+// Integer-only construction of rne_bf16(acc * 2^E): no floating-point operation takes
+// part, so no intermediate rounding can occur. bf16 keeps 8 significant bits; normal
+// numbers carry the biased exponent eb = msb + E + 127, subnormals count units of
+// 2^-133. In both cases the result is base + q, where q is |acc| shifted right by sh
+// and rounded half-to-even; a carry out of q moves into the exponent field on its own,
+// and anything at or above 0x7F80 is infinity.
+// ------------------------------------------------------------------------------------
+__device__ __forceinline__ uint16_t bf16_from_acc_pow2(int32_t acc, int32_t ea, int32_t ew) {
+    if (acc == 0) return 0;
+    long long El = (long long)ea + (long long)ew;
+    int E = (int)(El > 300 ? 300 : (El < -300 ? -300 : El));
+    uint32_t sign = acc < 0 ? 0x8000u : 0u;
+    uint32_t m = acc < 0 ? (uint32_t)(-(long long)acc) : (uint32_t)acc;
+    int p = 31 - __clz(m);      // m in [2^p, 2^(p+1))
+    int eb = p + E + 127;       // biased exponent of a normal result
+    int sh;
+    uint32_t base;
+    if (eb >= 1) {
+        sh = p - 7;
+        base = (uint32_t)(eb - 1) << 7;
+    } else {
+        sh = -(E + 133);
+        base = 0;
+    }
+    uint32_t q;
+    if (sh <= 0) {
+        q = m << (-sh);  // exact (at most 8 significant bits result)
+    } else if (sh > 40) {
+        q = 0;           // |value| < 2^-31 units: rounds to zero
+    } else {
+        unsigned long long mm = m;
+        unsigned long long qq = mm >> sh;
+        unsigned long long rem = mm - (qq << sh);
+        unsigned long long half = 1ull << (sh - 1);
+        if (rem > half || (rem == half && (qq & 1ull))) qq += 1;
+        q = (uint32_t)qq;
+    }
+    uint32_t bits = base + q;
+    if (bits >= 0x7F80u) bits = 0x7F80u;
+    return (uint16_t)(sign | bits);
+}
+
+// Exact power of two as a double for |k| <= 1022.
+__device__ __forceinline__ double pow2_f64(int k) {
+    return __longlong_as_double((long long)(k + 1023) << 52);
+}
+
+// Epilogue E2 — "GPU Mechanism", §3 (a): fixed-order fp64 recombination of the exact
+// diagonal sums, then one rounding to fp32. T[g] holds the int32 diagonal sum of
+// weight 2^(-7g); the order g = max_diag .. 2 is fixed.
+__device__ __forceinline__ float ozaki_combine(const int32_t* T, int max_diag, int32_t ei, int32_t fj) {
+    double acc = 0.0;
+    for (int g = max_diag; g >= 2; --g) acc = __dadd_rn(acc, __dmul_rn((double)T[g], pow2_f64(-7 * g)));
+    int k = ei + fj;
+    k = k > 300 ? 300 : (k < -300 ? -300 : k);
+    return __double2float_rn(__dmul_rn(acc, pow2_f64(k)));
+}
+
+// |x| of an fp32 bit pattern normalised to x = M * 2^(p - 23), M in [2^23, 2^24).
+// Returns false for zero. Subnormals are normalised.
+__device__ __forceinline__ bool f32_normalise(uint32_t absbits, uint32_t& M, int& p) {
+    uint32_t ef = absbits >> 23;
+    uint32_t fr = absbits & 0x7FFFFFu;
+    if (ef == 0) {
+        if (fr == 0) return false;
+        int b = 31 - __clz(fr);          // msb of the subnormal fraction
+        M = fr << (23 - b);
+        p = b - 149;
+        return true;
+    }
+    M = fr | 0x800000u;
+    p = (int)ef - 127;
+    return true;
+}
+
+}  // namespace detgemm

@@ -1,0 +1,181 @@
+/*
+ * detgemm — batch-invariant exact GEMM for NVIDIA GB300 (sm_103a).
+ *
+ * C ABI of libdetgemm.so. Every output bit is a function of the operands alone:
+ * it does not depend on the tile shape, the split-K count, the number of rows M
+ * or the launch configuration, because every reduction is an exact integer sum
+ * and every result is rounded exactly once.
+ *
+ * Sources (page title, section):
+ *  [P4] "Deterministic LLM Inference Across GPU Kernels: Power-of-Two INT8
+ *       Quantization Scales and the Limits of Tolerance-Based Conformance",
+ *       §II "Pipeline and alibi"; §V and §V.C (power-of-two requantization).
+ *  [P3] "GPU Mechanism", §3 "Method", Interventions (a) ExactGEMM; §2 "Exact GEMM
+ *       by error-free transformation" (Ozaki scheme).
+ *  [P1] "Taming Bitwise Behavior in GPU Kernels with Tensor Core", §3.2.2
+ *       (split-K: contiguous parts of the contracted axis, summed afterwards).
+ *
+ * Conventions for every call:
+ *  - All array pointers are DEVICE pointers owned by the caller. The library
+ *    allocates no device memory on any call; scratch space is the caller's
+ *    `ws` buffer of at least the size the matching *_workspace_size() returns.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default).
+ *  - Argument, alignment and precondition errors are detected on the host before
+ *    anything is launched; the call then returns the error and has no effect.
+ *  - Conditions only the device can see (a non-finite input to the quantizer or
+ *    the slicer; a bounded wait that expired) set a per-device status word that
+ *    detgemm_get_device_status() reads and clears.
+ *  - Matrices are row-major with a leading dimension in ELEMENTS. Operands of the
+ *    integer GEMMs are K-major: A is [M x K] (lda >= K), W = B^T is [N x K]
+ *    (ldw >= K), as an nn.Linear weight is stored.
+ *  - Base pointers must be 16-byte aligned and every leading dimension times the
+ *    element size a multiple of 16 bytes (DETGEMM_ERR_ALIGNMENT otherwise).
+ *  - The library is thread-safe; it keeps only a mutex-guarded per-device cache
+ *    of device properties. It never falls back to a CPU path.
+ */
+#ifndef DETGEMM_H
+#define DETGEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define DETGEMM_API __attribute__((visibility("default")))
+#else
+#define DETGEMM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* detgemm_stream_t; /* identical to cudaStream_t */
+
+typedef enum detgemm_status {
+    DETGEMM_OK = 0,
+    DETGEMM_ERR_INVALID_ARG = 1,        /* null pointer, negative size, bad enum value */
+    DETGEMM_ERR_ALIGNMENT = 2,          /* pointer or leading dimension not 16-byte aligned */
+    DETGEMM_ERR_PRECONDITION = 3,       /* the int32 accumulator could overflow (K too large) */
+    DETGEMM_ERR_WORKSPACE = 4,          /* ws missing or smaller than *_workspace_size() */
+    DETGEMM_ERR_UNSUPPORTED_DEVICE = 5, /* current device is not compute capability 10.3 */
+    DETGEMM_ERR_CUDA = 6,               /* a CUDA runtime call or launch failed */
+    DETGEMM_ERR_TIMEOUT = 7,            /* a bounded device-side wait expired */
+    DETGEMM_ERR_NONFINITE = 8           /* inf or NaN in a floating-point input */
+} detgemm_status;
+
+enum { DETGEMM_DTYPE_BF16 = 0, DETGEMM_DTYPE_F32 = 1 };
+enum { DETGEMM_POW2_NEAREST = 0, DETGEMM_POW2_CEIL = 1 };
+enum { DETGEMM_AXIS_ROWS = 0, DETGEMM_AXIS_COLS = 1 };
+
+/* Largest K for which K * 128^2 < 2^31: below it, int8 operands of any value
+ * accumulate exactly in int32, which is the bound under which [P4] §II argues that
+ * every tiling and split of K produces the same accumulator. */
+#define DETGEMM_MAX_K 131071
+
+/* Human-readable name of a status code (static string, never NULL). */
+DETGEMM_API const char* detgemm_status_string(detgemm_status status);
+
+/* Library version as 10000*major + 100*minor + patch. */
+DETGEMM_API int detgemm_version(void);
+
+/*
+ * W8A8 linear layer [P4 §II "Pipeline and alibi"]:
+ *     acc_ij = sum_k A_ik * W_jk                      (exact, int32)
+ *     C_ij   = rne_bf16(acc_ij * 2^(ea_i + ew_j))     (one rounding, IEEE RNE,
+ *                                                      subnormals kept, overflow -> inf)
+ * The activation and weight scales are the powers of two s_a = 2^ea, s_w = 2^ew,
+ * so the scale is applied exactly and the only rounding is the final one.
+ *
+ *   A   int8  [M x K], row stride lda          ea  int32 [M]  activation exponents
+ *   W   int8  [N x K], row stride ldw (= B^T)  ew  int32 [N]  weight exponents
+ *   C   bf16 bit patterns (uint16) [M x N], row stride ldc
+ *   split_k  number of contiguous K parts computed by separate CTAs and summed
+ *            exactly ([P1] §3.2.2); 1 <= split_k <= ceil(K / 64). The output bits do
+ *            not depend on it.
+ *   ws       scratch of ws_bytes >= detgemm_w8a8_workspace_size(M, N, K, split_k).
+ * Empty problems (M == 0 or N == 0) return DETGEMM_OK and launch nothing.
+ * Errors: INVALID_ARG (K < 1, M or N < 0, split_k out of range, null pointer),
+ *         PRECONDITION (K > DETGEMM_MAX_K), ALIGNMENT, WORKSPACE, UNSUPPORTED_DEVICE, CUDA.
+ */
+DETGEMM_API detgemm_status detgemm_w8a8(const int8_t* A, int64_t lda, const int8_t* W, int64_t ldw,
+                            const int32_t* ea, const int32_t* ew, uint16_t* C, int64_t ldc,
+                            int M, int N, int K, int split_k, void* ws, size_t ws_bytes,
+                            detgemm_stream_t stream);
+
+/* Bytes of scratch detgemm_w8a8 needs for this problem (0 is a valid answer). */
+DETGEMM_API size_t detgemm_w8a8_workspace_size(int M, int N, int K, int split_k);
+
+/*
+ * The exact integer accumulator alone [P4 §II: the int32 accumulator is the same for
+ * every tiling, split of K and summation order]:  C_ij = sum_k A_ik * W_jk (int32).
+ * Same operands, layout, split_k and errors as detgemm_w8a8; C is int32 [M x N].
+ * Scratch: detgemm_w8a8_workspace_size(M, N, K, split_k).
+ */
+DETGEMM_API detgemm_status detgemm_gemm_s8_i32(const int8_t* A, int64_t lda, const int8_t* W, int64_t ldw,
+                                   int32_t* C, int64_t ldc, int M, int N, int K, int split_k,
+                                   void* ws, size_t ws_bytes, detgemm_stream_t stream);
+
+/*
+ * Power-of-two quantization of each row [P4 §V, §V.C: scales requantized to a power
+ * of two, and the int8 values requantized under that scale]:
+ *     a_i = max_j |X_ij|;   s_i = a_i / 127
+ *     mode NEAREST: e_i = the integer nearest to log2(s_i)   (may clip outliers)
+ *     mode CEIL:    e_i = the smallest integer with 2^e_i >= s_i   (never clips)
+ *     Q_ij = clamp(rne(X_ij / 2^e_i), -127, 127);   a_i == 0 gives e_i = 0, Q = 0.
+ *   X  [rows x cols], bf16 bit patterns (x_dtype BF16) or fp32 (x_dtype F32), stride ldx
+ *   Q  int8 [rows x cols], stride ldq;   e  int32 [rows]
+ * Used for activations (rows = tokens) and for weights (rows = output channels of W).
+ * A non-finite input sets DETGEMM_ERR_NONFINITE in the device status word; the
+ * affected row then gets e = 0 and Q = 0.
+ */
+DETGEMM_API detgemm_status detgemm_quantize_pow2(const void* X, int x_dtype, int64_t ldx, int rows, int cols,
+                                     int mode, int8_t* Q, int64_t ldq, int32_t* e,
+                                     detgemm_stream_t stream);
+
+/*
+ * Ozaki slicing of an fp32 matrix [P3 §3 (a): each operand becomes 7-bit integer
+ * slices under a power-of-two scale taken from frexp]. One shared exponent per row
+ * (axis ROWS) or per column (axis COLS):
+ *     e = the frexp exponent of the line's max |x|  (max|x| < 2^e; 0 for a zero line)
+ *     r = x * 2^-e in (-1, 1);  for t = 1..nslices: d_t = trunc(128 r), r = 128 r - d_t
+ * so that x = 2^e * sum_t d_t 2^(-7t) + (a remainder below 2^(e - 7 nslices)).
+ *   X  fp32 [rows x cols], stride ldx
+ *   S  int8 digit planes, packed: axis ROWS -> [nslices][rows][cols];
+ *      axis COLS -> [nslices][cols][rows] (each column contiguous, i.e. K-major for B)
+ *   e  int32 [rows] (ROWS) or [cols] (COLS);   1 <= nslices <= 9
+ * A non-finite input sets DETGEMM_ERR_NONFINITE in the device status word.
+ */
+DETGEMM_API detgemm_status detgemm_slice_f32(const float* X, int64_t ldx, int rows, int cols, int axis,
+                                 int nslices, int8_t* S, int32_t* e, detgemm_stream_t stream);
+
+/*
+ * Ozaki-scheme fp32 GEMM C = A B [P3 §3 (a) ExactGEMM]:
+ *   slice A per row (e_i, DA_s) and B per column (f_j, DB_t), s, t = 1..nslices;
+ *   T_g = sum_{s+t=g} DA_s DB_t^T                     (exact int32, g = 2..max_diag)
+ *   acc = 0.0;  for g = max_diag down to 2: acc = acc + T_g * 2^(-7g)      (fp64)
+ *   C_ij = (float)(acc * 2^(e_i + f_j))                (the one rounding, IEEE RNE)
+ *   A fp32 [M x K] (lda), B fp32 [K x N] row-major (ldb), C fp32 [M x N] (ldc)
+ *   nslices in [1, 9], max_diag in [2, 2 * nslices]; split_k >= 1 (bits independent).
+ * Precondition: every T_g stays in int32: (max_diag - 1) * K * 127^2 < 2^31.
+ * Errors as detgemm_w8a8; non-finite inputs set DETGEMM_ERR_NONFINITE on the device.
+ */
+DETGEMM_API detgemm_status detgemm_ozaki_f32(const float* A, int64_t lda, const float* B, int64_t ldb,
+                                 float* C, int64_t ldc, int M, int N, int K, int nslices,
+                                 int max_diag, int split_k, void* ws, size_t ws_bytes,
+                                 detgemm_stream_t stream);
+
+/* Bytes of scratch detgemm_ozaki_f32 needs for this problem. */
+DETGEMM_API size_t detgemm_ozaki_workspace_size(int M, int N, int K, int nslices, int max_diag, int split_k);
+
+/*
+ * Synchronizes `stream`, then returns and clears the current device's status word:
+ * DETGEMM_OK, DETGEMM_ERR_NONFINITE or DETGEMM_ERR_TIMEOUT (the first one raised
+ * since the last read), or DETGEMM_ERR_CUDA if the synchronization itself failed.
+ */
+DETGEMM_API detgemm_status detgemm_get_device_status(detgemm_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DETGEMM_H */

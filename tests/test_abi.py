@@ -1,0 +1,126 @@
+"""The C-ABI library: builds, exports every declared symbol, validates on the host.
+
+No test here launches a kernel: argument, alignment, precondition and workspace
+errors are decided on the host before any CUDA call, and an otherwise valid call on
+a machine without a GB300 stops at the device check.
+"""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "detgemm.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from deterministic_detgemm_w8a8_gb300 import build as B
+    B.build()
+    import deterministic_detgemm_w8a8_gb300 as dg
+    return dg.load()
+
+
+def _declared():
+    src = open(HEADER).read()
+    return sorted(set(re.findall(r"DETGEMM_API\s+[\w\s\*]*?\b(detgemm_\w+)\s*\(", src)))
+
+
+def test_header_declares_the_entry_points():
+    names = _declared()
+    for n in ("detgemm_w8a8", "detgemm_ozaki_f32", "detgemm_quantize_pow2", "detgemm_slice_f32",
+              "detgemm_w8a8_workspace_size", "detgemm_ozaki_workspace_size", "detgemm_get_device_status",
+              "detgemm_status_string"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    from deterministic_detgemm_w8a8_gb300 import LIB_PATH, SIGNATURES
+    out = subprocess.run(["nm", "-D", "--defined-only", LIB_PATH], capture_output=True, text=True,
+                         check=True).stdout
+    exported = set(re.findall(r"\sT\s+(detgemm_\w+)", out))
+    declared = set(_declared())
+    assert declared <= exported, declared - exported
+    # the binding knows the signature of every declared call, and nothing else
+    assert set(SIGNATURES) == declared
+    for n in declared:
+        assert hasattr(lib, n)
+
+
+def test_status_strings(lib):
+    import deterministic_detgemm_w8a8_gb300 as dg
+    for code, name in [(0, "DETGEMM_OK"), (1, "DETGEMM_ERR_INVALID_ARG"), (2, "DETGEMM_ERR_ALIGNMENT"),
+                       (3, "DETGEMM_ERR_PRECONDITION"), (4, "DETGEMM_ERR_WORKSPACE"),
+                       (5, "DETGEMM_ERR_UNSUPPORTED_DEVICE"), (6, "DETGEMM_ERR_CUDA"),
+                       (7, "DETGEMM_ERR_TIMEOUT"), (8, "DETGEMM_ERR_NONFINITE")]:
+        assert dg.status_string(code) == name
+    assert lib.detgemm_version() >= 100
+
+
+# fake, never-dereferenced device addresses
+P = 0x7f0000000000
+P1 = P + 1
+
+
+def _w8a8(lib, A=P, lda=512, W=P, ldw=512, ea=P, ew=P, C=P, ldc=256, M=64, N=256, K=512, split=1,
+          ws=None, wsb=0):
+    return lib.detgemm_w8a8(A, lda, W, ldw, ea, ew, C, ldc, M, N, K, split, ws, wsb, None)
+
+
+def test_w8a8_argument_validation(lib):
+    import deterministic_detgemm_w8a8_gb300 as dg
+    assert _w8a8(lib, K=0) == dg.ERR_INVALID_ARG
+    assert _w8a8(lib, M=-1) == dg.ERR_INVALID_ARG
+    assert _w8a8(lib, K=131072, lda=131072, ldw=131072) == dg.ERR_PRECONDITION
+    assert _w8a8(lib, split=0) == dg.ERR_INVALID_ARG
+    assert _w8a8(lib, split=9) == dg.ERR_INVALID_ARG  # K=512 has 8 blocks of 64
+    assert _w8a8(lib, A=None) == dg.ERR_INVALID_ARG
+    assert _w8a8(lib, ea=None) == dg.ERR_INVALID_ARG
+    assert _w8a8(lib, lda=500) == dg.ERR_INVALID_ARG  # lda < K
+    assert _w8a8(lib, A=P1) == dg.ERR_ALIGNMENT
+    assert _w8a8(lib, lda=520) == dg.ERR_ALIGNMENT
+    assert _w8a8(lib, ldc=260) == dg.ERR_ALIGNMENT  # 520 bytes
+    need = dg.w8a8_workspace_size(64, 256, 512, 2)
+    assert need >= 64 * 256 * 4
+    assert _w8a8(lib, split=2) == dg.ERR_WORKSPACE
+    assert _w8a8(lib, split=2, ws=P, wsb=need - 1) == dg.ERR_WORKSPACE
+    # empty problems succeed without touching the device
+    assert _w8a8(lib, M=0, A=None, C=None) == dg.OK
+    assert _w8a8(lib, N=0) == dg.OK
+
+
+def test_w8a8_valid_call_stops_at_device_check_without_gpu(lib):
+    import torch
+    import deterministic_detgemm_w8a8_gb300 as dg
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert _w8a8(lib) == dg.ERR_UNSUPPORTED_DEVICE
+
+
+def test_other_entry_points_validate(lib):
+    import deterministic_detgemm_w8a8_gb300 as dg
+    q = lib.detgemm_quantize_pow2
+    assert q(P, 2, 64, 4, 64, 0, P, 64, P, None) == dg.ERR_INVALID_ARG  # dtype
+    assert q(P, 0, 64, 4, 64, 2, P, 64, P, None) == dg.ERR_INVALID_ARG  # mode
+    assert q(P, 0, 60, 4, 60, 0, P, 64, P, None) == dg.ERR_ALIGNMENT  # 120-byte rows
+    assert q(P, 0, 64, 0, 64, 0, None, 64, None, None) == dg.OK
+    s = lib.detgemm_slice_f32
+    assert s(P, 64, 4, 64, 0, 10, P, P, None) == dg.ERR_INVALID_ARG  # nslices
+    assert s(P, 64, 4, 64, 2, 7, P, P, None) == dg.ERR_INVALID_ARG  # axis
+    assert s(P1, 64, 4, 64, 0, 7, P, P, None) == dg.ERR_ALIGNMENT
+    o = lib.detgemm_ozaki_f32
+    assert o(P, 64, P, 64, P, 64, 64, 64, 64, 7, 19, 1, P, 1 << 30, None) == dg.ERR_INVALID_ARG
+    # (max_diag - 1 pairs capped at nslices) * K * 127^2 must stay below 2^31
+    assert o(P, 19024, P, 64, P, 64, 64, 64, 19024, 7, 8, 1, P, 1 << 40, None) == dg.ERR_PRECONDITION
+    assert o(P, 64, P, 64, P, 64, 64, 64, 64, 7, 8, 1, P, 16, None) == dg.ERR_WORKSPACE
+    assert dg.ozaki_workspace_size(64, 64, 64) > 7 * 64 * 64 * 2
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    import torch
+    import deterministic_detgemm_w8a8_gb300 as dg
+    A = torch.zeros((4, 16), dtype=torch.int8)
+    with pytest.raises(ValueError):
+        dg.w8a8(A, A, torch.zeros(4, dtype=torch.int32), torch.zeros(4, dtype=torch.int32))

@@ -1,0 +1,75 @@
+"""GPU parity of the Ozaki-scheme fp32 GEMM against the CPU oracle (bit-exact), plus the
+error bound |C - C_fp64| <= 4 * 2^-24 * (|A||B|)_ij on the full-size workload."""
+import numpy as np
+import pytest
+import torch
+
+import synthetic
+from gpu_util import cuda, dg, f32_bits, padded, poison_like, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    return cuda()
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return dg()
+
+
+def run(lib, dev, A, B, split=1, nslices=7, max_diag=8, lda=None, ldb=None):
+    M, K = A.shape
+    N = B.shape[1]
+    tA = padded(A, dev, lda) if lda else to_dev(A, dev)
+    tB = padded(B, dev, ldb) if ldb else to_dev(B, dev)
+    out = poison_like((M, N), torch.float32, dev)
+    lib.ozaki_f32(tA, tB, nslices=nslices, max_diag=max_diag, split_k=split, out=out)
+    return f32_bits(out)
+
+
+@pytest.mark.parametrize("M,N,K,split,nslices,max_diag", [
+    (64, 96, 256, 1, 7, 8), (33, 17, 100, 2, 7, 8), (130, 129, 513, 3, 7, 8), (1, 1, 1, 1, 7, 8),
+    (70, 40, 300, 1, 4, 5), (20, 24, 64, 1, 7, 14), (257, 65, 1024, 4, 7, 8)])
+def test_small_bitexact(lib, dev, oracle_mod, M, N, K, split, nslices, max_diag):
+    rng = np.random.default_rng(M + 7 * N + K)
+    A = (rng.standard_normal((M, K)) * np.exp2(rng.integers(-8, 9, size=(M, K)))).astype(np.float32)
+    B = (rng.standard_normal((K, N)) * np.exp2(rng.integers(-8, 9, size=(K, N)))).astype(np.float32)
+    lda = (K + 3) // 4 * 4
+    ldb = (N + 3) // 4 * 4
+    want = oracle_mod.ozaki_f32(A, B, nslices, max_diag).view(np.uint32)
+    got = run(lib, dev, A, B, split, nslices, max_diag, lda, ldb)
+    assert (got == want).all(), int((got != want).sum())
+
+
+def test_combine_order_case(lib, dev):
+    # the hand-worked cancellation case: the defined order g = 8..2 gives +0.0
+    K = 130
+    x = np.full((1, K), 0.5, np.float32)
+    x[0, 129] = 2.0 ** -7
+    y = np.full((K, 1), -(2.0 ** -8), np.float32)
+    y[0, 0] = 0.5
+    y[129, 0] = 2.0 ** -49
+    got = run(lib, dev, x, y, lda=132, ldb=4)
+    assert got[0, 0] == 0
+
+
+def test_ozaki_workload_sampled_and_error_bound(lib, dev, oracle_mod):
+    A, B = synthetic.ozaki(4096)
+    tA, tB = to_dev(A, dev), to_dev(B, dev)
+    out = poison_like((4096, 4096), torch.float32, dev)
+    lib.ozaki_f32(tA, tB, out=out)
+    C = out.cpu().numpy()
+    rows = [0, 1, 127, 128, 2047, 4094, 4095] + np.random.default_rng(3).integers(0, 4096, 3).tolist()
+    want = oracle_mod.ozaki_f32(A, B, rows=rows)
+    assert (C[rows].view(np.uint32) == want.view(np.uint32)).all()
+    # error bound on the sampled rows, against an fp64 GEMM
+    ref = A[rows].astype(np.float64) @ B.astype(np.float64)
+    absab = np.abs(A[rows].astype(np.float64)) @ np.abs(B.astype(np.float64))
+    assert (np.abs(C[rows].astype(np.float64) - ref) <= 4 * 2.0 ** -24 * absab).all()
+    # split-K gives identical bits
+    out2 = poison_like((4096, 4096), torch.float32, dev)
+    lib.ozaki_f32(tA, tB, split_k=3, out=out2)
+    assert torch.equal(out.view(torch.int32), out2.view(torch.int32))

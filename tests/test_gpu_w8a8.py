@@ -1,0 +1,202 @@
+"""GPU parity of the W8A8 GEMM and its exact int32 accumulator against the CPU oracle.
+
+Every comparison is bit-exact (uint16 bf16 patterns / int32 values). Inputs come
+from the seeded generators of the workloads (tiny, sweep, ffn, skinny), plus ragged
+shapes, tail sentinels, the all-ones probe and the worst-case magnitude bound.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import synthetic
+from gpu_util import bf16_bits, cuda, dg, padded, poison_like, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    return cuda()
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return dg()
+
+
+def run_w8a8(lib, dev, A, W, ea, ew, split=1, lda=None, ldw=None):
+    M, K = A.shape
+    N = W.shape[0]
+    tA = padded(A, dev, lda) if lda else to_dev(A, dev)
+    tW = padded(W, dev, ldw) if ldw else to_dev(W, dev)
+    out = poison_like((M, N), torch.bfloat16, dev)
+    lib.w8a8(tA, tW, to_dev(ea, dev), to_dev(ew, dev), split_k=split, out=out)
+    return bf16_bits(out)
+
+
+def run_i32(lib, dev, A, W, split=1, lda=None, ldw=None):
+    M, K = A.shape
+    N = W.shape[0]
+    tA = padded(A, dev, lda) if lda else to_dev(A, dev)
+    tW = padded(W, dev, ldw) if ldw else to_dev(W, dev)
+    out = poison_like((M, N), torch.int32, dev)
+    lib.gemm_s8_i32(tA, tW, split_k=split, out=out)
+    return out.cpu().numpy()
+
+
+def test_tiny_workload(lib, dev, oracle_mod):
+    A, W, ea, ew = synthetic.tiny()
+    want = oracle_mod.w8a8(A, W, ea, ew)
+    assert (run_w8a8(lib, dev, A, W, ea, ew) == want).all()
+    assert (run_i32(lib, dev, A, W) == oracle_mod.gemm_s8_i32(A, W)).all()
+
+
+@pytest.mark.parametrize("M,N,K,split,lda", [
+    (1, 1, 1, 1, 16), (7, 13, 33, 1, 48), (16, 200, 100, 2, 112), (33, 257, 1000, 3, 1008),
+    (64, 130, 1001, 5, 1008), (65, 129, 64, 1, 64), (129, 131, 1000, 1, 1008),
+    (200, 300, 4100, 7, 4112), (257, 64, 130, 3, 144), (300, 17, 3, 1, 16)])
+def test_ragged_shapes(lib, dev, oracle_mod, M, N, K, split, lda):
+    rng = np.random.default_rng(M * 1000 + N + K)
+    A = rng.integers(-128, 128, size=(M, K), dtype=np.int8)
+    W = rng.integers(-128, 128, size=(N, K), dtype=np.int8)
+    ea = rng.integers(-20, -2, size=M, dtype=np.int32)
+    ew = rng.integers(-20, -2, size=N, dtype=np.int32)
+    got = run_w8a8(lib, dev, A, W, ea, ew, split=split, lda=lda, ldw=lda)
+    assert (got == oracle_mod.w8a8(A, W, ea, ew)).all()
+    got = run_i32(lib, dev, A, W, split=split, lda=lda, ldw=lda)
+    assert (got == oracle_mod.gemm_s8_i32(A, W)).all()
+
+
+def test_sweep_workload_rows_identical_across_M_and_split(lib, dev, oracle_mod):
+    A, W, ea, ew = synthetic.sweep(2048)
+    want = oracle_mod.w8a8(A, W, ea, ew)
+    tW = to_dev(W, dev)
+    tew = to_dev(ew, dev)
+    for M in (1, 7, 64, 257, 2048):
+        tA = to_dev(A[:M], dev)
+        tea = to_dev(ea[:M], dev)
+        for split in (1, 2, 4, 8):
+            out = poison_like((M, 6144), torch.bfloat16, dev)
+            lib.w8a8(tA, tW, tea, tew, split_k=split, out=out)
+            got = bf16_bits(out)
+            assert (got == want[:M]).all(), (M, split, int((got != want[:M]).sum()))
+
+
+def test_skinny_workload_deep_split(lib, dev, oracle_mod):
+    A, W, ea, ew = synthetic.skinny()
+    want = oracle_mod.w8a8(A, W, ea, ew)
+    tA, tW, tea, tew = (to_dev(x, dev) for x in (A, W, ea, ew))
+    for split in (8, 16, 32):
+        out = poison_like((16, 4096), torch.bfloat16, dev)
+        lib.w8a8(tA, tW, tea, tew, split_k=split, out=out)
+        assert (bf16_bits(out) == want).all(), split
+
+
+@pytest.mark.parametrize("which", ["gate_up", "down"])
+def test_ffn_workload_sampled_rows(lib, dev, oracle_mod, which):
+    A, W, ea, ew = synthetic.ffn_gate_up() if which == "gate_up" else synthetic.ffn_down()
+    M = A.shape[0]
+    out = poison_like((M, W.shape[0]), torch.bfloat16, dev)
+    lib.w8a8(to_dev(A, dev), to_dev(W, dev), to_dev(ea, dev), to_dev(ew, dev), out=out)
+    rows = sorted({0, 1, 127, 128, 129, 4095, 4096, M - 129, M - 128, M - 1} |
+                  set(np.random.default_rng(5).integers(0, M, 6).tolist()))
+    got = bf16_bits(out)[rows]
+    assert (got == oracle_mod.w8a8(A, W, ea, ew, rows=rows)).all()
+
+
+def test_all_ones_probe(lib, dev):
+    # all-ones operands: every accumulator equals K exactly (8648, not 8640)
+    M, N, K = 4, 8, 8648
+    A = np.ones((M, K), np.int8)
+    W = np.ones((N, K), np.int8)
+    for split in (1, 3, 8):
+        assert (run_i32(lib, dev, A, W, split=split, lda=8656, ldw=8656) == 8648).all()
+        got = run_w8a8(lib, dev, A, W, np.zeros(M, np.int32), np.zeros(N, np.int32), split=split,
+                       lda=8656, ldw=8656)
+        assert (got == 0x4607).all()
+
+
+def test_tail_sentinel_walk(lib, dev):
+    # one nonzero per row at k*, walked over block, split and tail boundaries
+    K = 1000
+    ks = [0, 1, 15, 16, 63, 64, 127, 128, 333, 500, 511, 512, 959, 960, 975, 976, 991, 992, 998, 999]
+    A = np.zeros((len(ks), K), np.int8)
+    for i, k in enumerate(ks):
+        A[i, k] = (i % 120) + 3
+    W = np.ones((24, K), np.int8)
+    W[5] = -1
+    for split in (1, 2, 5, 16):
+        C = run_i32(lib, dev, A, W, split=split, lda=1008, ldw=1008)
+        want = np.outer(np.arange(len(ks)) % 120 + 3, np.where(np.arange(24) == 5, -1, 1))
+        assert (C == want).all(), split
+
+
+def test_worst_case_magnitude_bound(lib, dev):
+    # K = 131071 is the largest K with K * 128^2 < 2^31; all -128 operands
+    K = 131071
+    A = np.full((2, K), -128, np.int8)
+    W = np.full((3, K), -128, np.int8)
+    for split in (1, 7, 64):
+        C = run_i32(lib, dev, A, W, split=split, lda=131072, ldw=131072)
+        assert (C == K * 16384).all()
+    A[1] = 127
+    C = run_i32(lib, dev, A, W, split=3, lda=131072, ldw=131072)
+    assert (C[1] == -K * 127 * 128).all()
+
+
+def _row_for_acc(acc, K):
+    """int8 rows (a, w) of length K with sum a*w == acc (|acc| <= K * 16256)."""
+    a = np.zeros(K, np.int8)
+    w = np.zeros(K, np.int8)
+    s = 1 if acc >= 0 else -1
+    big = 16384 if s > 0 else 16256  # (-128)(-128) or (-128)(127)
+    q, r = divmod(abs(acc), big)
+    a[:q] = -128
+    w[:q] = -128 if s > 0 else 127
+    i = q
+    while r > 0:
+        d = min(r, 127)
+        a[i], w[i] = d, s
+        r -= d
+        i += 1
+    return a, w
+
+
+def test_golden_epilogue_cases(lib, dev):
+    path = os.path.join(os.path.dirname(__file__), "golden", "w8a8_epilogue_cases.txt")
+    rows = []
+    for line in open(path):
+        line = line.split("#")[0].strip()
+        if line:
+            acc, e, bits = line.split()[:3]
+            rows.append((int(acc), int(e), int(bits, 16)))
+    K = 2048
+    rows = [r for r in rows if abs(r[0]) <= K * 16384]  # accumulators reachable at this K
+    assert len(rows) >= 14
+    A = np.zeros((len(rows), K), np.int8)
+    W = np.zeros((len(rows), K), np.int8)
+    for i, (acc, e, _) in enumerate(rows):
+        A[i], W[i] = _row_for_acc(acc, K)
+    ea = np.array([e for _, e, _ in rows], np.int32)
+    C = run_w8a8(lib, dev, A, W, ea, np.zeros(len(rows), np.int32))
+    got = np.diag(C)
+    want = np.array([b for _, _, b in rows], np.uint16)
+    assert (got == want).all(), [(r, hex(g)) for r, g in zip(rows, got) if g != r[2]]
+    # the exponent may sit on either operand (only ea_i + ew_j matters)
+    C2 = run_w8a8(lib, dev, A, W, np.zeros(len(rows), np.int32), ea)
+    assert (np.diag(C2) == want).all()
+
+
+def test_rows_independent_of_M_and_repeatable(lib, dev, oracle_mod):
+    rng = np.random.default_rng(9)
+    A = rng.integers(-128, 128, size=(300, 512), dtype=np.int8)
+    W = rng.integers(-128, 128, size=(192, 512), dtype=np.int8)
+    ea = rng.integers(-14, -6, size=300, dtype=np.int32)
+    ew = rng.integers(-14, -6, size=192, dtype=np.int32)
+    full = run_w8a8(lib, dev, A, W, ea, ew)
+    for M in (1, 2, 17, 64, 65, 128, 299):
+        for split in (1, 4):
+            assert (run_w8a8(lib, dev, A[:M], W, ea[:M], ew, split=split) == full[:M]).all()
+    assert (run_w8a8(lib, dev, A, W, ea, ew) == full).all()
