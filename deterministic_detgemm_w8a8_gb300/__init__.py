@@ -31,6 +31,7 @@ DTYPE_BF16, DTYPE_F32 = 0, 1
 POW2_NEAREST, POW2_CEIL = 0, 1
 AXIS_ROWS, AXIS_COLS = 0, 1
 MAX_K = 131071
+NOALLOC_SCRATCH_BYTES = 8 << 20  # scratch array size of detgemm_w8a8_noalloc
 
 # every symbol include/detgemm.h declares, with its ctypes signature
 _P, _I64, _I32, _SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
@@ -45,6 +46,7 @@ SIGNATURES = {
     "detgemm_ozaki_f32": ([_P, _I64, _P, _I64, _P, _I64, _I32, _I32, _I32, _I32, _I32, _I32, _P, _SZ, _P], _I32),
     "detgemm_ozaki_workspace_size": ([_I32, _I32, _I32, _I32, _I32, _I32], _SZ),
     "detgemm_get_device_status": ([_P], _I32),
+    "detgemm_w8a8_noalloc": ([_P, _I64, _P, _I64, _P, _P, _P, _I64, _I32, _I32, _I32, _I32, _P], _I32),
 }
 
 _lock = threading.Lock()

@@ -174,6 +174,33 @@ DETGEMM_API size_t detgemm_ozaki_workspace_size(int M, int N, int K, int nslices
  */
 DETGEMM_API detgemm_status detgemm_get_device_status(detgemm_stream_t stream);
 
+/*
+ * detgemm_w8a8 without a caller-supplied workspace. The source pages have no
+ * counterpart to this call; it exists for callers that cannot allocate device memory
+ * when they run the GEMM — for example a plugin inside an inference server that is
+ * handed only its input and output tensors, or a latency-critical serving loop that
+ * bans cudaMalloc because an allocation can synchronize the device.
+ *
+ * Same operands, layout, result bits and errors as detgemm_w8a8. The split-K scratch
+ * lives in a fixed device array of DETGEMM_NOALLOC_SCRATCH_BYTES inside the library,
+ * which every GPU that loads the library keeps until the process exits. A problem
+ * whose detgemm_w8a8_workspace_size(M, N, K, split_k) exceeds that size is refused
+ * with DETGEMM_ERR_WORKSPACE before anything is launched.
+ *  - The first call on each device looks up the array's device address (set-up done
+ *    once per device, with that device current); make that first call before any
+ *    stream capture begins.
+ *  - All calls share the one array and each clears the part it uses: calls that may
+ *    overlap on the GPU (different streams, or different host threads) race and must
+ *    be serialized by the caller.
+ *  - The call allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
+ */
+#define DETGEMM_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+DETGEMM_API detgemm_status detgemm_w8a8_noalloc(const int8_t* A, int64_t lda, const int8_t* W, int64_t ldw,
+                                                const int32_t* ea, const int32_t* ew, uint16_t* C,
+                                                int64_t ldc, int M, int N, int K, int split_k,
+                                                detgemm_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
