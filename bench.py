@@ -47,6 +47,9 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-extras", action="store_true", help="skip the extra rows")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", default=None,
+                    choices=["ffn_gate_up", "ffn_down", "skinny8", "skinny32", "ozaki", "sweep"],
+                    help="run one workload call twice (warm-up + one more) for an ncu capture, then exit")
     return ap.parse_args()
 
 
@@ -149,6 +152,8 @@ def main():
 
     if args.impl == "reference":
         return run_reference(args, world, rank)
+    if args.profile:
+        return run_profile(args.profile)
 
     import torch
     import torch.distributed as dist
@@ -336,6 +341,35 @@ def extras(dg, torch, dev, pk, flush):
     res["sweep_M2048_N6144_K2048"] = {"us": round(ms * 1e3, 1),
                                       "TOPS": round(2.0 * 2048 * 6144 * 2048 / (ms * 1e-3) / 1e12, 1)}
     return res
+
+
+def run_profile(name):
+    """One workload call, twice, for a profiler capture (-s 1 -c 1 on its kernel)."""
+    import torch
+    import synthetic
+    import deterministic_detgemm_w8a8_gb300 as dg
+    dev = torch.device("cuda:0")
+    tdev = lambda x: torch.from_numpy(x).to(dev)
+    if name.startswith("ffn") or name == "sweep" or name.startswith("skinny"):
+        if name == "ffn_gate_up":
+            args = synthetic.ffn_gate_up()
+        elif name == "ffn_down":
+            args = synthetic.ffn_down()
+        elif name == "sweep":
+            args = synthetic.sweep(2048)
+        else:
+            args = synthetic.skinny()
+        split = {"skinny8": 8, "skinny32": 32}.get(name, 1)
+        A, W, ea, ew = (tdev(x) for x in args)
+        fn = lambda: dg.w8a8(A, W, ea, ew, split_k=split)
+    else:
+        Af, Bf = (tdev(x) for x in synthetic.ozaki(4096))
+        fn = lambda: dg.ozaki_f32(Af, Bf)
+    for _ in range(2):
+        fn()
+    torch.cuda.synchronize()
+    print(f"profile case {name}: done")
+    return 0
 
 
 def run_reference(args, world, rank):
