@@ -220,7 +220,7 @@ def main():
     achieved = (ops_g + ops_d) * args.steps / ((sum(g_ms) + sum(d_ms)) * 1e-3) / 1e12
     peak = pk["bf16_tflops_sustained"]
     roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
-                "frac": round(achieved / peak, 4), "traffic": None, "kernel": "igemm_tile_kernel",
+                "frac": round(achieved / peak, 4), "traffic": None, "kernel": "tc_gemm_kernel (+ int8->fp16 widening)",
                 "peak_source": f"{pk['source']} bf16 dense (sustained) — the GB300 tensor pipe's measured peak"}
 
     out = {"metric": METRIC, "value": round(value, 2), "unit": "TOPS", "n_gpus": world, "steps": args.steps,
@@ -229,7 +229,7 @@ def main():
            "config": {"workload": WORKLOAD, "M": M_FFN, "gemms": [[N1, K1], [N2, K2]], "split_k": 1,
                       "l2": "flushed before every timed step (256 MiB write, outside the events)",
                       "parallelism": f"replicas x{world} (independent problems per rank)"},
-           "roofline": roofline, "gpu_launches": 2 * args.steps, "clocks": clk,
+           "roofline": roofline, "gpu_launches": 6 * args.steps, "clocks": clk,
            "wall_s_timed_loop": round(t_wall, 3)}
 
     if rank == 0:

@@ -107,15 +107,63 @@ const char* detgemm_status_string(detgemm_status s) {
 
 int detgemm_version(void) { return 100; }
 
+// Decode-shaped problems (M <= 64) stream W through the register-fed warp-MMA kernel;
+// everything larger runs on the tcgen05 engine over exact fp16 copies of the operands.
+static bool w8a8_uses_tc(int M) { return M > 64; }
+
+// tcgen05 path scratch: A16 [M][Kp] fp16 | W16 [N][Kp] fp16 | split-K sums and counters
+struct TcW8a8Layout {
+    int64_t Kp;
+    size_t a16, w16, split, total;
+};
+
+static TcW8a8Layout tc_w8a8_layout(int M, int N, int K, int split_k) {
+    TcW8a8Layout L;
+    L.Kp = tc_padded_k(K);
+    size_t off = 0;
+    L.a16 = off; off += align256((size_t)M * L.Kp * 2);
+    L.w16 = off; off += align256((size_t)N * L.Kp * 2);
+    L.split = off; off += align256(tc_split_bytes(1, M, N, split_k));
+    L.total = off;
+    return L;
+}
+
 size_t detgemm_w8a8_workspace_size(int M, int N, int K, int split_k) {
-    (void)K;
-    if (M <= 0 || N <= 0) return 0;
+    if (M <= 0 || N <= 0 || K <= 0) return 0;
+    if (w8a8_uses_tc(M)) return tc_w8a8_layout(M, N, K, split_k).total;
     return igemm_workspace_bytes(M, N, split_k);
+}
+
+static detgemm_status run_tc(const int8_t* A, int64_t lda, const int8_t* W, int64_t ldw, const int32_t* ea,
+                             const int32_t* ew, void* C, int64_t ldc, int mode, int M, int N, int K, int split_k,
+                             void* ws, cudaStream_t stream) {
+    const TcW8a8Layout L = tc_w8a8_layout(M, N, K, split_k);
+    char* base = reinterpret_cast<char*>(ws);
+    cudaError_t e = widen_i8_f16_launch(A, lda, M, K, base + L.a16, L.Kp, stream);
+    if (e == cudaSuccess) e = widen_i8_f16_launch(W, ldw, N, K, base + L.w16, L.Kp, stream);
+    if (e != cudaSuccess) return DETGEMM_ERR_CUDA;
+    TcArgs a = {};
+    a.M = M;
+    a.N = N;
+    a.ndiag = 1;
+    a.diag_first[0] = 0;
+    a.diag_nseg[0] = 1;
+    a.segA[0] = 0;
+    a.segB[0] = 0;
+    a.split = split_k;
+    a.mode = mode;
+    a.ea = ea;
+    a.ew = ew;
+    a.C = C;
+    a.ldc = ldc;
+    a.c_plane = 0;
+    return from_cuda(tc_gemm_launch(a, base + L.a16, 1, base + L.w16, 1, L.Kp, base + L.split, stream));
 }
 
 static detgemm_status run_igemm(const int8_t* A, int64_t lda, const int8_t* W, int64_t ldw, const int32_t* ea,
                                 const int32_t* ew, void* C, int64_t ldc, int mode, int M, int N, int K, int split_k,
                                 void* ws, cudaStream_t stream) {
+    if (w8a8_uses_tc(M)) return run_tc(A, lda, W, ldw, ea, ew, C, ldc, mode, M, N, K, split_k, ws, stream);
     IGemmArgs a = {};
     a.seg[0] = Seg{A, W};
     a.nseg = 1;
@@ -257,6 +305,8 @@ detgemm_status detgemm_get_device_status(detgemm_stream_t stream) {
     if (quantize_take_status(&bits) != cudaSuccess) return DETGEMM_ERR_CUDA;
     v |= bits;
     if (slice_take_status(&bits) != cudaSuccess) return DETGEMM_ERR_CUDA;
+    v |= bits;
+    if (tc_take_status(&bits) != cudaSuccess) return DETGEMM_ERR_CUDA;
     v |= bits;
     if (v & DEV_TIMEOUT) return DETGEMM_ERR_TIMEOUT;
     if (v & DEV_NONFINITE) return DETGEMM_ERR_NONFINITE;

@@ -46,9 +46,47 @@ cudaError_t slice_rows_launch(const float* X, int64_t ldx, int rows, int cols, i
 cudaError_t slice_cols_launch(const float* X, int64_t ldx, int rows, int cols, int nslices, int8_t* S,
                               int64_t lds, int32_t* e, cudaStream_t s);
 
+// ------------------------------------------------------------------------------------
+// tcgen05 engine (gemm_tc.cu): exact int GEMM on fp16-carried operand planes.
+// A planes: fp16 [a_planes][M][Kp], B planes: fp16 [b_planes][N][Kp] (Kp multiple of 64).
+// Plane group d (an Ozaki diagonal; 0 for W8A8) sums segments diag_first[d] ..
+// diag_first[d] + diag_nseg[d] - 1, segment s pairing A plane segA[s] with B plane segB[s].
+constexpr int kTcMaxDiag = 18;
+constexpr int kTcMaxSeg = 96;
+
+struct TcArgs {
+    int M, N;
+    int nkb;                   // 64-wide K blocks per segment (set by the launcher)
+    int ndiag;
+    int diag_first[kTcMaxDiag];
+    int diag_nseg[kTcMaxDiag];
+    int16_t segA[kTcMaxSeg];
+    int16_t segB[kTcMaxSeg];
+    int split;                 // contiguous parts of each group's flattened K-block range
+    int tiles_m, tiles_n;      // set by the launcher
+    int group_m;               // tile rows per raster group (0: default)
+    int mode;                  // EpilogueMode
+    const int32_t* ea;
+    const int32_t* ew;
+    void* C;                   // bf16 [M x ldc], or int32 planes [ndiag][c_plane]
+    int64_t ldc;
+    int64_t c_plane;           // elements between int32 output planes
+    int32_t* ws_acc;           // set by the launcher (split > 1)
+    uint32_t* ws_cnt;
+};
+
+int64_t tc_padded_k(int K);
+size_t tc_split_bytes(int ndiag, int M, int N, int split);
+cudaError_t tc_gemm_launch(const TcArgs& a, const void* A16, int a_planes, const void* B16, int b_planes,
+                           int64_t Kp, void* ws_split, cudaStream_t s);
+// exact int8 -> fp16 copy of X [rows x K] into Y [rows x Kp], zero beyond K
+cudaError_t widen_i8_f16_launch(const int8_t* X, int64_t ldx, int rows, int K, void* Y, int64_t Kp,
+                                cudaStream_t s);
+
 // Read-and-clear accessors of the per-unit device status words.
 cudaError_t quantize_take_status(uint32_t* bits);
 cudaError_t slice_take_status(uint32_t* bits);
+cudaError_t tc_take_status(uint32_t* bits);
 
 // Ozaki recombination: T [ndiag][M][ldT] int32 (diagonal g at plane g - 2) -> C fp32.
 cudaError_t ozaki_combine_launch(const int32_t* T, int64_t ldT, int max_diag, const int32_t* e, const int32_t* f,

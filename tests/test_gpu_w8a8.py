@@ -200,3 +200,14 @@ def test_rows_independent_of_M_and_repeatable(lib, dev, oracle_mod):
         for split in (1, 4):
             assert (run_w8a8(lib, dev, A[:M], W, ea[:M], ew, split=split) == full[:M]).all()
     assert (run_w8a8(lib, dev, A, W, ea, ew) == full).all()
+
+
+def test_tc_engine_chunk_boundary_worst_case(lib, dev):
+    # all -128 operands: every 1024-long fp32 chunk reaches exactly 2^24 on the
+    # tensor-core path (M > 64), the largest value the chunked accumulation must hold
+    for M, N, K, split in [(130, 260, 16384, 1), (65, 8, 131071, 1), (200, 300, 131071, 7)]:
+        A = np.full((M, K), -128, np.int8)
+        W = np.full((N, K), -128, np.int8)
+        ld = (K + 15) // 16 * 16
+        C = run_i32(lib, dev, A, W, split=split, lda=ld, ldw=ld)
+        assert (C == K * 16384).all(), (M, N, K, split)
