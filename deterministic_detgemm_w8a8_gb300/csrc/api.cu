@@ -59,26 +59,27 @@ detgemm_status validate_igemm(const void* A, int64_t lda, const void* W, int64_t
 }
 
 // Ozaki workspace layout (each piece 256-byte aligned):
-//   DA  int8 [nslices][M][Kp]   DB int8 [nslices][N][Kp]   (Kp = K rounded up to 16)
+//   DA  fp16 [nslices][M][Kp]   DB fp16 [nslices][N][Kp]   (exact digit values; Kp = K
+//                                                            rounded up to 64, zero padded)
 //   e   int32 [M]               f  int32 [N]
-//   T   int32 [max_diag - 1][M][ldT]  (ldT = N rounded up to 4: 16-byte rows)
-//   igemm split-K scratch (split_k > 1)
+//   T   int32 [max_diag - 1][M][ldT]  (plane d = diagonal max_diag - d; ldT = N rounded up to 4)
+//   split-K sums and counters of the tensor-core engine (split_k > 1)
 struct OzakiLayout {
-    size_t da, db, e, f, T, gemm, total;
+    size_t da, db, e, f, T, split, total;
     int64_t Kp, ldT;
 };
 
 OzakiLayout ozaki_layout(int M, int N, int K, int nslices, int max_diag, int split_k) {
     OzakiLayout L;
-    L.Kp = ((int64_t)K + 15) / 16 * 16;
+    L.Kp = tc_padded_k(K);
     L.ldT = ((int64_t)N + 3) / 4 * 4;
     size_t off = 0;
-    L.da = off; off += align256((size_t)nslices * M * L.Kp);
-    L.db = off; off += align256((size_t)nslices * N * L.Kp);
+    L.da = off; off += align256((size_t)nslices * M * L.Kp * 2);
+    L.db = off; off += align256((size_t)nslices * N * L.Kp * 2);
     L.e = off; off += align256((size_t)M * 4);
     L.f = off; off += align256((size_t)N * 4);
     L.T = off; off += align256((size_t)(max_diag - 1) * M * L.ldT * 4);
-    L.gemm = off; off += align256(igemm_workspace_bytes(M, N, split_k));
+    L.split = off; off += align256(tc_split_bytes(max_diag - 1, M, N, split_k));
     L.total = off;
     return L;
 }
@@ -268,33 +269,37 @@ detgemm_status detgemm_ozaki_f32(const float* A, int64_t lda, const float* B, in
     if (st != DETGEMM_OK) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     char* base = reinterpret_cast<char*>(ws);
-    int8_t* DA = reinterpret_cast<int8_t*>(base + L.da);
-    int8_t* DB = reinterpret_cast<int8_t*>(base + L.db);
     int32_t* e = reinterpret_cast<int32_t*>(base + L.e);
     int32_t* f = reinterpret_cast<int32_t*>(base + L.f);
     int32_t* T = reinterpret_cast<int32_t*>(base + L.T);
-    cudaError_t err = slice_rows_launch(A, lda, M, K, nslices, DA, L.Kp, e, s);
-    if (err == cudaSuccess) err = slice_cols_launch(B, ldb, K, N, nslices, DB, L.Kp, f, s);
-    const int64_t planeA = (int64_t)M * L.Kp, planeB = (int64_t)N * L.Kp;
-    for (int g = 2; g <= max_diag && err == cudaSuccess; ++g) {
-        IGemmArgs a = {};
-        a.nseg = 0;
+    cudaError_t err = slice_rows_f16_launch(A, lda, M, K, nslices, base + L.da, L.Kp, e, s);
+    if (err == cudaSuccess) err = slice_cols_f16_launch(B, ldb, K, N, nslices, base + L.db, L.Kp, f, s);
+    if (err != cudaSuccess) return DETGEMM_ERR_CUDA;
+    // all diagonals in one persistent launch, the largest (most slice pairs) first;
+    // group d is diagonal g = max_diag - d and pairs A slice sA with B slice g - sA
+    TcArgs a = {};
+    a.M = M;
+    a.N = N;
+    a.ndiag = max_diag - 1;
+    int nseg = 0;
+    for (int d = 0; d < a.ndiag; ++d) {
+        const int g = max_diag - d;
+        a.diag_first[d] = nseg;
         for (int sA = 1; sA <= nslices; ++sA) {
-            int tB = g - sA;
+            const int tB = g - sA;
             if (tB < 1 || tB > nslices) continue;
-            a.seg[a.nseg++] = Seg{DA + (sA - 1) * planeA, DB + (tB - 1) * planeB};
+            a.segA[nseg] = (int16_t)(sA - 1);
+            a.segB[nseg] = (int16_t)(tB - 1);
+            ++nseg;
         }
-        a.lda = L.Kp;
-        a.ldw = L.Kp;
-        a.M = M;
-        a.N = N;
-        a.K = K;
-        a.split = split_k;  // <= nkb <= nkb * nseg K blocks, so no part is empty
-        a.mode = EPI_STORE_I32;
-        a.C = T + (int64_t)(g - 2) * M * L.ldT;
-        a.ldc = L.ldT;
-        err = igemm_launch(a, base + L.gemm, s);
+        a.diag_nseg[d] = nseg - a.diag_first[d];
     }
+    a.split = split_k;  // <= ceil(K / 64) <= the K blocks of every diagonal
+    a.mode = EPI_STORE_I32;
+    a.C = T;
+    a.ldc = L.ldT;
+    a.c_plane = (int64_t)M * L.ldT;
+    err = tc_gemm_launch(a, base + L.da, nslices, base + L.db, nslices, L.Kp, base + L.split, s);
     if (err == cudaSuccess) err = ozaki_combine_launch(T, L.ldT, max_diag, e, f, C, ldc, M, N, s);
     return from_cuda(err);
 }

@@ -41,10 +41,8 @@ __device__ __forceinline__ void raise_status(uint32_t bit) { atomicOr(&g_device_
 // and rounded half-to-even; a carry out of q moves into the exponent field on its own,
 // and anything at or above 0x7F80 is infinity.
 // ------------------------------------------------------------------------------------
-__device__ __forceinline__ uint16_t bf16_from_acc_pow2(int32_t acc, int32_t ea, int32_t ew) {
-    if (acc == 0) return 0;
-    long long El = (long long)ea + (long long)ew;
-    int E = (int)(El > 300 ? 300 : (El < -300 ? -300 : El));
+// General case (any exponent): subnormal results and overflow handled explicitly.
+static __device__ __noinline__ uint16_t bf16_from_acc_pow2_general(int32_t acc, int E) {
     uint32_t sign = acc < 0 ? 0x8000u : 0u;
     uint32_t m = acc < 0 ? (uint32_t)(-(long long)acc) : (uint32_t)acc;
     int p = 31 - __clz(m);      // m in [2^p, 2^(p+1))
@@ -73,6 +71,27 @@ __device__ __forceinline__ uint16_t bf16_from_acc_pow2(int32_t acc, int32_t ea, 
     }
     uint32_t bits = base + q;
     if (bits >= 0x7F80u) bits = 0x7F80u;
+    return (uint16_t)(sign | bits);
+}
+
+// Fast path for results in the normal bf16 range: normalise |acc| so its leading one
+// sits at bit 31, keep the top 8 bits and round half-to-even on the 24 dropped bits;
+// the carry of a round-up moves into the exponent field by itself.
+__device__ __forceinline__ uint16_t bf16_from_acc_pow2(int32_t acc, int32_t ea, int32_t ew) {
+    if (acc == 0) return 0;
+    long long El = (long long)ea + (long long)ew;
+    int E = (int)(El > 300 ? 300 : (El < -300 ? -300 : El));
+    const uint32_t sign = (uint32_t)acc >> 31 << 15;
+    const uint32_t m = acc < 0 ? 0u - (uint32_t)acc : (uint32_t)acc;  // |INT_MIN| = 2^31 fits
+    const int lz = __clz(m);
+    const int eb = 31 - lz + E + 127;
+    if (eb < 1 || eb > 254) return bf16_from_acc_pow2_general(acc, E);
+    const uint32_t n = m << lz;
+    uint32_t q = n >> 24;  // 1.xxxxxxx
+    const uint32_t rem = n & 0xFFFFFFu;
+    q += (rem > 0x800000u) | ((rem == 0x800000u) & q);
+    uint32_t bits = ((uint32_t)(eb - 1) << 7) + q;
+    bits = bits >= 0x7F80u ? 0x7F80u : bits;
     return (uint16_t)(sign | bits);
 }
 

@@ -12,22 +12,25 @@
 // of tiling, chunking and split-K ("Deterministic LLM Inference Across GPU Kernels ...",
 // §II "Pipeline and alibi").
 //
-// Kernel layout (one CTA per SM, persistent over work units):
-//   warp 0   TMA producer: 128x64 A and 256x64 B fp16 boxes (128-byte swizzle) into a
-//            4-stage shared-memory ring, one mbarrier pair per stage.
-//   warp 1   TMEM owner and MMA issuer: tcgen05.mma M=128 N=256 K=16, four per 64-wide
-//            K block, into one of two 256-column fp32 TMEM buffers; one chunk per buffer.
-//   warps 2-9  epilogue: warp w reads TMEM lanes 32 (w % 4) .. +31 and column half
-//            (w - 2) / 4, converts each fp32 chunk to int32 and adds it to 128 int32
-//            registers per thread; after the unit's last chunk it applies the epilogue
-//            (bf16 pow2 rounding, or int32 store) or, under split-K, adds the partial
-//            into an int32 workspace with atomics and the last-arriving CTA finishes.
-// A work unit is (plane group d, output tile, split part). Operands are fp16 planes
-// [plane][rows][Kp] addressed through 3-D tensor maps; a unit walks a list of
-// (A plane, B plane) segments, which is one segment for W8A8 and one per slice pair for
-// an Ozaki diagonal.
+// Kernel layout: persistent clusters of two CTAs (one CTA per SM) over work units; a
+// unit is (plane group d, 256 x 256 output tile, split part).
+//   warp 0     TMA producer (both CTAs): CTA r loads A rows [256 tm + 128 r, +128) and B
+//              rows [256 tn + 128 r, +128) of each 64-wide K block, fp16 with the 128-byte
+//              swizzle, into a 6-stage ring (32 KB per stage).
+//   warp 1     TMEM owner (both CTAs; the pair allocates collectively) and, in the even
+//              CTA, the MMA issuer: tcgen05.mma.cta_group::2 M=256 N=256 K=16, four per K
+//              block, into one of two 256-column fp32 TMEM buffers, one K chunk per buffer.
+//   warps 2-9  epilogue (both CTAs): warp w reads TMEM lanes 32 (w % 4) .. +31 and column
+//              half (w - 2) / 4 of its CTA's 128 rows, converts each fp32 chunk to int32
+//              and adds it to 128 int32 registers per thread; after the unit's last chunk
+//              it rounds to bf16 (or stores int32) or, under split-K, adds the partial into
+//              an int32 workspace with atomics and the last-arriving warp finishes.
+// Operands are fp16 planes [plane][rows][Kp] addressed through 3-D tensor maps; a unit
+// walks a list of (A plane, B plane) segments: one segment for W8A8, one per slice pair
+// for an Ozaki diagonal.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -44,17 +47,11 @@ namespace {
 
 using namespace sm100;
 
-constexpr int BM = 128, BN = 256, BK = 64;
-constexpr int STAGES = 4;
-constexpr int A_BYTES = BM * BK * 2;
-constexpr int B_BYTES = BN * BK * 2;
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int BN = 256, BK = 64;
 constexpr int EPI_WARPS = 8;
 constexpr int THREADS = 64 + EPI_WARPS * 32;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int CHUNK_KB = 16;  // 16 blocks of 64 = 1024 K values per exact fp32 chunk
-constexpr uint32_t IDESC = idesc_f16_f32(BM, BN);
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*alignment slack*/ + 256 /*barriers*/;
 
 struct Unit {
     int d, tm, tn, z;
@@ -84,31 +81,78 @@ __device__ __forceinline__ void kb_range(const TcArgs& p, const Unit& u, int& f0
     f1 = (int)(((long long)(u.z + 1) * F) / p.split);
 }
 
-// Epilogue of 128 consecutive columns of one output row held by one thread.
+// rne_bf16(acc * 2^ea * 2^ew) for exponents in [-60, 40] (so that every intermediate is
+// a normal fp32 number): acc is truncated to 24 significant bits and the last kept bit is
+// set when anything was dropped (rounding to odd), the scaling by powers of two is exact,
+// and the final conversion rounds to nearest-even. Rounding to odd at 24 bits followed by
+// rounding to nearest at 8 bits equals one rounding to nearest at 8 bits, because 24 >=
+// 8 + 2; so the result is bit-identical to the integer construction of
+// bf16_from_acc_pow2, at a fraction of its instruction count.
+__device__ __forceinline__ float ro24_scaled(int32_t acc, float sa, float sw) {
+    const float x = __int2float_rz(acc);
+    const uint32_t xb = __float_as_uint(x) | (uint32_t)(__float2int_rz(x) != acc);
+    return __fmul_rn(__fmul_rn(__uint_as_float(xb), sa), sw);
+}
+
+__device__ __forceinline__ float exp2_f32(int e) { return __uint_as_float((uint32_t)(e + 127) << 23); }
+
+// Epilogue of 128 consecutive columns of one output row held by one thread. The warp's
+// 32 threads hold 32 rows of the same 128 columns, so the column exponents are loaded
+// once per warp (lane l loads columns 4l .. 4l+3, coalesced) and broadcast by shuffle.
 __device__ __forceinline__ void finish_row(const TcArgs& p, int d, int row, int col0, const int32_t (&acc)[128]) {
-    if (row >= p.M) return;
+    const int lane = threadIdx.x & 31;
     if (p.mode == EPI_BF16_POW2) {
-        const int32_t ea = p.ea[row];
+        int32_t ewv[4];
+        bool inrange = true;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int c = col0 + 4 * lane + i;
+            ewv[i] = c < p.N ? __ldg(p.ew + c) : 0;
+            inrange &= ewv[i] >= -60 && ewv[i] <= 40;
+        }
+        const int32_t ea = row < p.M ? __ldg(p.ea + row) : 0;
+        inrange &= ea >= -60 && ea <= 40;
         uint16_t* C = reinterpret_cast<uint16_t*>(p.C) + (int64_t)row * p.ldc;
+        const bool fast = __all_sync(0xffffffffu, inrange);  // warp-uniform choice
+        float swv[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) swv[i] = exp2_f32(fast ? ewv[i] : 0);
+        const float sa = exp2_f32(fast ? ea : 0);
 #pragma unroll
         for (int j = 0; j < 128; j += 8) {
-            const int col = col0 + j;
-            if (col + 8 <= p.N) {
-                uint32_t w[4];
+            uint32_t w[4];
+            if (fast) {
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    uint32_t lo = bf16_from_acc_pow2(acc[j + 2 * i], ea, __ldg(p.ew + col + 2 * i));
-                    uint32_t hi = bf16_from_acc_pow2(acc[j + 2 * i + 1], ea, __ldg(p.ew + col + 2 * i + 1));
-                    w[i] = lo | (hi << 16);
+                    const int c = j + 2 * i;
+                    const float s0 = __shfl_sync(0xffffffffu, swv[c & 3], c >> 2);
+                    const float s1 = __shfl_sync(0xffffffffu, swv[(c + 1) & 3], (c + 1) >> 2);
+                    const __nv_bfloat162 h =
+                        __floats2bfloat162_rn(ro24_scaled(acc[c], sa, s0), ro24_scaled(acc[c + 1], sa, s1));
+                    w[i] = *reinterpret_cast<const uint32_t*>(&h);
                 }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int c = j + 2 * i;
+                    const int32_t e0 = __shfl_sync(0xffffffffu, ewv[c & 3], c >> 2);
+                    const int32_t e1 = __shfl_sync(0xffffffffu, ewv[(c + 1) & 3], (c + 1) >> 2);
+                    w[i] = (uint32_t)bf16_from_acc_pow2(acc[c], ea, e0) |
+                           ((uint32_t)bf16_from_acc_pow2(acc[c + 1], ea, e1) << 16);
+                }
+            }
+            if (row >= p.M) continue;
+            const int col = col0 + j;
+            if (col + 8 <= p.N) {
                 *reinterpret_cast<uint4*>(C + col) = make_uint4(w[0], w[1], w[2], w[3]);
             } else {
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
-                    if (col + i < p.N) C[col + i] = bf16_from_acc_pow2(acc[j + i], ea, __ldg(p.ew + col + i));
+                    if (col + i < p.N) C[col + i] = (uint16_t)(w[i >> 1] >> (16 * (i & 1)));
             }
         }
     } else {
+        if (row >= p.M) return;
         int32_t* C = reinterpret_cast<int32_t*>(p.C) + (int64_t)d * p.c_plane + (int64_t)row * p.ldc;
 #pragma unroll
         for (int j = 0; j < 128; j += 4) {
@@ -124,55 +168,80 @@ __device__ __forceinline__ void finish_row(const TcArgs& p, int d, int row, int 
     }
 }
 
+// ------------------------------------------------------------------------------------
+// The kernel (tcgen05 cta_group::2): a cluster of two CTAs computes a 256 x 256
+// tile. CTA r of the pair holds A rows [256 tm + 128 r, +128) and B rows
+// [256 tn + 128 r, +128) of every K block in its own 6-stage ring (32 KB per stage); the
+// even CTA issues one M=256 N=256 K=16 MMA that reads both CTAs' halves and writes each
+// CTA's 128 rows of the accumulator into that CTA's TMEM. Per SM this halves the B
+// operand bytes each multiply-add needs compared with a single-CTA 128 x 256 tile.
+// Synchronisation across the pair:
+//   full[s]   in the even CTA: its producer arms it with both CTAs' bytes; both CTAs'
+//             TMA loads complete on it (.cta_group::2 loads may signal the peer's barrier)
+//   empty[s]  in both CTAs: the MMA commit arrives on both (multicast)
+//   tfull[b]  in both CTAs: the MMA commit arrives on both (multicast)
+//   tempty[b] in the even CTA: all 16 epilogue warps of the pair arrive on it
+// ------------------------------------------------------------------------------------
+constexpr int P_STAGES = 6;
+constexpr int P_A_BYTES = 128 * BK * 2;
+constexpr int P_B_BYTES = 128 * BK * 2;
+constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
+constexpr uint32_t P_IDESC = idesc_f16_f32(256, 256);
+constexpr int P_SMEM_BYTES = P_STAGES * P_STAGE_BYTES + 1024 /*alignment slack*/ + 256 /*barriers*/;
+
 __global__ void __launch_bounds__(THREADS, 1)
-    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ TcArgs p) {
+    tc2_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ TcArgs p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
-    uint64_t* empty = full + STAGES;
-    uint64_t* tfull = empty + STAGES;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + P_STAGES * P_STAGE_BYTES);
+    uint64_t* empty = full + P_STAGES;
+    uint64_t* tfull = empty + P_STAGES;
     uint64_t* tempty = tfull + 2;
     uint64_t* mdone = tempty + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mdone + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const int cid = (int)cluster_id_x(), ncl = (int)num_clusters_x();
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
+        for (int s = 0; s < P_STAGES; ++s) {
             mbar_init(full + s, 1);
             mbar_init(empty + s, 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(tfull + b, 1);
-            mbar_init(tempty + b, EPI_WARPS);
+            mbar_init(tempty + b, 2 * EPI_WARPS);
         }
         mbar_init(mdone, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
     if (warp == 1) {
-        tmem_alloc(tmem_slot, TMEM_COLS);
-        tmem_relinquish();
+        tmem_alloc_pair(tmem_slot, TMEM_COLS);  // collective over the pair: both CTAs issue it
+        tmem_relinquish_pair();
     }
     if (warp == 0 && lane == 0) {
         prefetch_tmap(&tmA);
         prefetch_tmap(&tmB);
     }
     tc_fence_before();
-    __syncthreads();
+    cluster_sync();  // both CTAs' barriers are initialised before any remote arrival
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const int total = p.ndiag * p.tiles_m * p.tiles_n * p.split;
+    const uint32_t full_lead = mapa(smem_addr(full), 0);
+    const uint32_t tempty_lead = mapa(smem_addr(tempty), 0);
 
     if (warp == 0) {
         if (lane == 0) {
-            // ------------------------------------------------------------ TMA producer
+            // ------------------------------------------------------------ TMA producer (both CTAs)
             int stage = 0;
             uint32_t phase = 0;
             uint32_t issued = 0;
             bool ok = true;
-            for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
+            for (int u = cid; u < total && ok; u += ncl) {
                 const Unit un = unit_of(p, u);
                 int f0, f1;
                 kb_range(p, un, f0, f1);
@@ -184,25 +253,26 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const int sidx = f / p.nkb;
                     const int seg = p.diag_first[un.d] + sidx;
                     const int kx = (f - sidx * p.nkb) * BK;
-                    uint8_t* sa = smem + stage * STAGE_BYTES;
-                    mbar_arrive_expect_tx(full + stage, STAGE_BYTES);
-                    tma_load_3d(sa, &tmA, full + stage, kx, un.tm * BM, p.segA[seg]);
-                    tma_load_3d(sa + A_BYTES, &tmB, full + stage, kx, un.tn * BN, p.segB[seg]);
+                    uint8_t* sa = smem + stage * P_STAGE_BYTES;
+                    if (rank == 0) mbar_arrive_expect_tx(full + stage, 2 * P_STAGE_BYTES);
+                    const uint32_t fb = full_lead + 8u * (uint32_t)stage;
+                    tma_load_3d_pair(sa, &tmA, fb, kx, un.tm * 256 + (int)rank * 128, p.segA[seg]);
+                    tma_load_3d_pair(sa + P_A_BYTES, &tmB, fb, kx, un.tn * 256 + (int)rank * 128, p.segB[seg]);
                     ++issued;
-                    if (++stage == STAGES) {
+                    if (++stage == P_STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
             }
-            if (!ok) {
+            if (!ok && rank == 0) {
                 // let the copies already in flight land before shared memory goes away
-                uint32_t n = issued < STAGES ? issued : STAGES;
+                uint32_t n = issued < P_STAGES ? issued : P_STAGES;
                 int s = stage;
                 uint32_t ph = phase;
                 for (uint32_t i = 0; i < n; ++i) {
                     if (--s < 0) {
-                        s = STAGES - 1;
+                        s = P_STAGES - 1;
                         ph ^= 1u;
                     }
                     mbar_wait_drain(full + s, ph);
@@ -210,14 +280,14 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
         }
     } else if (warp == 1) {
-        if (lane == 0) {
-            // ------------------------------------------------------------ MMA issuer
+        if (lane == 0 && rank == 0) {
+            // ------------------------------------------------------------ MMA issuer (even CTA)
             int stage = 0;
             uint32_t phase = 0;
             int buf = 0;
             uint32_t tphase = 0;
             bool ok = true;
-            for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
+            for (int u = cid; u < total && ok; u += ncl) {
                 const Unit un = unit_of(p, u);
                 int f0, f1;
                 kb_range(p, un, f0, f1);
@@ -235,37 +305,37 @@ __global__ void __launch_bounds__(THREADS, 1)
                             break;
                         }
                         tc_fence_after();
-                        const uint32_t sa = smem_addr(smem + stage * STAGE_BYTES);
+                        const uint32_t sa = smem_addr(smem + stage * P_STAGE_BYTES);
                         const uint64_t ad = sdesc_sw128_kmajor(sa);
-                        const uint64_t bd = sdesc_sw128_kmajor(sa + A_BYTES);
+                        const uint64_t bd = sdesc_sw128_kmajor(sa + P_A_BYTES);
 #pragma unroll
                         for (int k = 0; k < BK / 16; ++k)
-                            mma_f16(dt, ad + 2 * k, bd + 2 * k, IDESC, (f > c0 || k > 0) ? 1u : 0u);
-                        mma_commit(empty + stage);
-                        if (++stage == STAGES) {
+                            mma_f16_pair(dt, ad + 2 * k, bd + 2 * k, P_IDESC, (f > c0 || k > 0) ? 1u : 0u);
+                        mma_commit_pair_mc(empty + stage, 0x3);
+                        if (++stage == P_STAGES) {
                             stage = 0;
                             phase ^= 1u;
                         }
                     }
-                    mma_commit(tfull + buf);
+                    mma_commit_pair_mc(tfull + buf, 0x3);
                     if (++buf == 2) {
                         buf = 0;
                         tphase ^= 1u;
                     }
                 }
             }
-            mma_commit(mdone);
+            mma_commit_pair_mc(mdone, 0x1);
             mbar_wait_drain(mdone, 0);
         }
     } else {
-        // ---------------------------------------------------------------- epilogue
+        // ---------------------------------------------------------------- epilogue (both CTAs)
         const int ew = warp - 2;
-        const int q = warp & 3;        // TMEM lane quarter this warp may access
-        const int h = ew >> 2;         // column half of the 256-wide tile
+        const int q = warp & 3;
+        const int h = ew >> 2;
         int buf = 0;
         uint32_t tphase = 0;
         bool ok = true;
-        for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
+        for (int u = cid; u < total && ok; u += ncl) {
             const Unit un = unit_of(p, u);
             int f0, f1;
             kb_range(p, un, f0, f1);
@@ -273,8 +343,6 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
             for (int i = 0; i < 128; ++i) acc[i] = 0;
             for (int c0 = f0; c0 < f1; c0 += CHUNK_KB) {
-                // every lane waits, and the warp proceeds only if all saw the phase: the
-                // TMEM loads below must be executed by the whole warp or not at all
                 const bool got = mbar_wait(tfull + buf, tphase, abort_flag);
                 if (!__all_sync(0xffffffffu, got)) {
                     ok = false;
@@ -292,23 +360,19 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(tempty + buf);
+                if (lane == 0) mbar_arrive_cluster(tempty_lead + 8u * (uint32_t)buf);
                 if (++buf == 2) {
                     buf = 0;
                     tphase ^= 1u;
                 }
             }
             if (!ok) break;
-            const int row = un.tm * BM + q * 32 + lane;
+            const int row = un.tm * 256 + (int)rank * 128 + q * 32 + lane;
             const int col0 = un.tn * BN + h * 128;
             if (p.split == 1) {
                 finish_row(p, un.d, row, col0, acc);
                 continue;
             }
-            // split-K: exact int32 partial sums meet in the workspace. Each warp owns a
-            // 32-row x 128-column sub-block with its own arrival counter; the warp that
-            // arrives last (in whichever CTA) reads the full sums and finishes it. No
-            // barrier spans more than one warp, so an aborted wait cannot strand others.
             int32_t* ws = p.ws_acc + (int64_t)un.d * p.M * p.N;
             if (row < p.M) {
 #pragma unroll
@@ -319,8 +383,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             __syncwarp();
             unsigned prev = 0;
             if (lane == 0) {
-                const int tile = (un.d * p.tiles_m + un.tm) * p.tiles_n + un.tn;
-                prev = atomicAdd(p.ws_cnt + (int64_t)tile * EPI_WARPS + ew, 1u);
+                const int64_t sub = ((((int64_t)un.d * p.tiles_m + un.tm) * p.tiles_n + un.tn) * 2 + rank) * EPI_WARPS + ew;
+                prev = atomicAdd(p.ws_cnt + sub, 1u);
             }
             prev = __shfl_sync(0xffffffffu, prev, 0);
             if (prev != (unsigned)(p.split - 1)) continue;
@@ -333,10 +397,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
     }
 
+    __syncwarp();
     tc_fence_before();
-    __syncthreads();
+    cluster_sync();  // no CTA leaves while its pair may still read its smem or barriers
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
+    if (warp == 1) tmem_dealloc_pair(tmem_base, TMEM_COLS);
 }
 
 // ------------------------------------------------------------------------------------
@@ -433,22 +498,49 @@ cudaError_t widen_i8_f16_launch(const int8_t* X, int64_t ldx, int rows, int K, v
 
 size_t tc_split_bytes(int ndiag, int M, int N, int split) {
     if (split <= 1) return 0;
-    const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+    // counters for 128-row tiles, or for 256-row pair tiles x 2 CTAs (whichever is more)
+    const int tiles = 2 * ((M + 255) / 256) * ((N + BN - 1) / BN);
     size_t acc = ((size_t)ndiag * M * N * sizeof(int32_t) + 255) & ~(size_t)255;
     return acc + (size_t)ndiag * tiles * EPI_WARPS * sizeof(uint32_t);
 }
 
-cudaError_t tc_gemm_launch(const TcArgs& a_in, const void* A16, int a_planes, const void* B16, int b_planes,
-                           int64_t Kp, void* ws_split, cudaStream_t s) {
-    TcArgs a = a_in;
-    if (a.M == 0 || a.N == 0) return cudaSuccess;
-    a.tiles_m = (a.M + BM - 1) / BM;
+namespace {
+int g_max_clusters[64];
+
+int max_pair_clusters() {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) return 1;
+    std::lock_guard<std::mutex> lock(g_tc_mutex);
+    if (g_max_clusters[dev] == 0) {
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3(2 * 76, 1, 1);
+        cfg.blockDim = dim3(THREADS, 1, 1);
+        cfg.dynamicSmemBytes = P_SMEM_BYTES;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, tc2_gemm_kernel, &cfg) != cudaSuccess || n <= 0) n = 1;
+        g_max_clusters[dev] = n;
+    }
+    return g_max_clusters[dev];
+}
+}  // namespace
+
+static cudaError_t tc2_launch(TcArgs a, const void* A16, int a_planes, const void* B16, int b_planes, int64_t Kp,
+                              void* ws_split, cudaStream_t s) {
+    a.tiles_m = (a.M + 255) / 256;
     a.tiles_n = (a.N + BN - 1) / BN;
     a.nkb = (int)(Kp / BK);
     if (a.group_m <= 0) a.group_m = 8;
     CUtensorMap tmA, tmB;
-    cudaError_t e = make_map(&tmA, A16, Kp, a.M, a_planes, BM);
-    if (e == cudaSuccess) e = make_map(&tmB, B16, Kp, a.N, b_planes, BN);
+    cudaError_t e = make_map(&tmA, A16, Kp, a.M, a_planes, 128);
+    if (e == cudaSuccess) e = make_map(&tmB, B16, Kp, a.N, b_planes, 128);
     if (e != cudaSuccess) return e;
     if (a.split > 1) {
         size_t accb = (((size_t)a.ndiag * a.M * a.N * sizeof(int32_t)) + 255) & ~(size_t)255;
@@ -457,12 +549,32 @@ cudaError_t tc_gemm_launch(const TcArgs& a_in, const void* A16, int a_planes, co
         e = cudaMemsetAsync(ws_split, 0, tc_split_bytes(a.ndiag, a.M, a.N, a.split), s);
         if (e != cudaSuccess) return e;
     }
-    e = cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    e = cudaFuncSetAttribute(tc2_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const int total = a.ndiag * a.tiles_m * a.tiles_n * a.split;
-    const int grid = total < num_sms() ? total : num_sms();
-    tc_gemm_kernel<<<grid, THREADS, SMEM_BYTES, s>>>(tmA, tmB, a);
+    int clusters = max_pair_clusters();
+    if (clusters > total) clusters = total;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2 * clusters, 1, 1);
+    cfg.blockDim = dim3(THREADS, 1, 1);
+    cfg.dynamicSmemBytes = P_SMEM_BYTES;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, tc2_gemm_kernel, tmA, tmB, a);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
+}
+
+cudaError_t tc_gemm_launch(const TcArgs& a, const void* A16, int a_planes, const void* B16, int b_planes,
+                           int64_t Kp, void* ws_split, cudaStream_t s) {
+    if (a.M == 0 || a.N == 0) return cudaSuccess;
+    return tc2_launch(a, A16, a_planes, B16, b_planes, Kp, ws_split, s);
 }
 
 DETGEMM_STATUS_ACCESSOR(tc_take_status)

@@ -45,6 +45,11 @@ cudaError_t slice_rows_launch(const float* X, int64_t ldx, int rows, int cols, i
                               int64_t lds, int32_t* e, cudaStream_t s);
 cudaError_t slice_cols_launch(const float* X, int64_t ldx, int rows, int cols, int nslices, int8_t* S,
                               int64_t lds, int32_t* e, cudaStream_t s);
+// the same digits as exact fp16 values (operand planes of the tensor-core engine)
+cudaError_t slice_rows_f16_launch(const float* X, int64_t ldx, int rows, int cols, int nslices, void* S,
+                                  int64_t lds, int32_t* e, cudaStream_t s);
+cudaError_t slice_cols_f16_launch(const float* X, int64_t ldx, int rows, int cols, int nslices, void* S,
+                                  int64_t lds, int32_t* e, cudaStream_t s);
 
 // ------------------------------------------------------------------------------------
 // tcgen05 engine (gemm_tc.cu): exact int GEMM on fp16-carried operand planes.
@@ -88,7 +93,8 @@ cudaError_t quantize_take_status(uint32_t* bits);
 cudaError_t slice_take_status(uint32_t* bits);
 cudaError_t tc_take_status(uint32_t* bits);
 
-// Ozaki recombination: T [ndiag][M][ldT] int32 (diagonal g at plane g - 2) -> C fp32.
+// Ozaki recombination: T [max_diag - 1][M][ldT] int32, plane d holding diagonal
+// g = max_diag - d (largest weight index first) -> C fp32.
 cudaError_t ozaki_combine_launch(const int32_t* T, int64_t ldT, int max_diag, const int32_t* e, const int32_t* f,
                                  float* C, int64_t ldc, int M, int N, cudaStream_t s);
 

@@ -4,7 +4,8 @@
 //   acc = 0.0;  for g = max_diag .. 2:  acc = acc + T_g * 2^(-7g);
 //   C_ij = fp32_rne(acc * 2^(e_i + f_j)).
 //
-// One thread per output element; T is [max_diag - 1][M][N] int32 (plane g - 2). The
+// One thread per output element; T is [max_diag - 1][M][ldT] int32, plane d holding the
+// diagonal g = max_diag - d. The
 // loads of each plane are coalesced along N. Traffic per element: 4 (max_diag - 1) B
 // read + 4 B written; fp64 work: max_diag - 1 multiply-adds, issued as separate
 // round-to-nearest multiply and add (the multiply by a power of two is exact).
@@ -29,7 +30,7 @@ __global__ void ozaki_combine_kernel(const int32_t* __restrict__ T, int64_t ldT,
     int32_t t[19];
 #pragma unroll
     for (int g = 0; g < 19; ++g) t[g] = 0;
-    for (int g = 2; g <= max_diag; ++g) t[g] = __ldg(T + (int64_t)(g - 2) * plane + idx);
+    for (int g = 2; g <= max_diag; ++g) t[g] = __ldg(T + (int64_t)(max_diag - g) * plane + idx);
     C[(int64_t)i * ldc + j] = ozaki_combine(t, max_diag, e[i], f[j]);
 }
 

@@ -11,6 +11,7 @@
 // Rows: one CTA per row, two passes (max, then digits). Columns: a column-max kernel
 // (atomicMax over row chunks), an exponent kernel, then a 32x32 tiled transpose that
 // writes every digit plane K-major ([t][col][row]).
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -47,8 +48,22 @@ __device__ __forceinline__ int8_t digit(unsigned long long R, int t, int n, bool
     return (int8_t)(neg ? -d : d);
 }
 
+// digit planes are stored as int8 (the public slicer) or as exact fp16 values (the
+// operand planes of the tensor-core engine)
+template <typename T>
+__device__ __forceinline__ T digit_out(int8_t d);
+template <>
+__device__ __forceinline__ int8_t digit_out<int8_t>(int8_t d) {
+    return d;
+}
+template <>
+__device__ __forceinline__ __half digit_out<__half>(int8_t d) {
+    return __int2half_rn((int)d);
+}
+
+template <typename T>
 __global__ void __launch_bounds__(SROW_THREADS) slice_rows_kernel(const float* __restrict__ X, int64_t ldx, int rows,
-                                                                  int cols, int nslices, int8_t* __restrict__ S,
+                                                                  int cols, int nslices, T* __restrict__ S,
                                                                   int64_t lds, int32_t* __restrict__ e_out) {
     __shared__ uint32_t red[SROW_THREADS / 32];
     const int64_t row = blockIdx.x;
@@ -63,7 +78,7 @@ __global__ void __launch_bounds__(SROW_THREADS) slice_rows_kernel(const float* _
 #pragma unroll
     for (int w = 1; w < SROW_THREADS / 32; ++w) amax = max(amax, red[w]);
     const int64_t plane = (int64_t)rows * lds;
-    int8_t* s = S + row * lds;
+    T* s = S + row * lds;
     const bool bad = amax >= 0x7F800000u;  // inf or NaN in the row: digits written as zero
     const int e = bad ? 0 : line_exponent(amax);
     if (threadIdx.x == 0) {
@@ -74,7 +89,7 @@ __global__ void __launch_bounds__(SROW_THREADS) slice_rows_kernel(const float* _
         uint32_t xb = (j < cols && !bad) ? x[j] : 0u;
         unsigned long long R = digits_of(xb, e, nslices);
         bool neg = xb >> 31;
-        for (int t = 0; t < nslices; ++t) s[t * plane + j] = digit(R, t, nslices, neg);
+        for (int t = 0; t < nslices; ++t) s[t * plane + j] = digit_out<T>(digit(R, t, nslices, neg));
     }
 }
 
@@ -115,8 +130,9 @@ __global__ void col_exponent_kernel(const uint32_t* colmax, int cols, int32_t* e
 }
 
 // 32 x 32 tile: rows r0.., columns c0..; digits written to S[t][col][row]
+template <typename T>
 __global__ void slice_cols_kernel(const float* __restrict__ X, int64_t ldx, int rows, int cols, int nslices,
-                                  const int32_t* __restrict__ e_col, int8_t* __restrict__ S, int64_t lds) {
+                                  const int32_t* __restrict__ e_col, T* __restrict__ S, int64_t lds) {
     __shared__ int8_t tile[9][32][33];
     const int r0 = blockIdx.y * 32, c0 = blockIdx.x * 32;
     const int tx = threadIdx.x, ty = threadIdx.y;  // 32 x 8
@@ -139,7 +155,7 @@ __global__ void slice_cols_kernel(const float* __restrict__ X, int64_t ldx, int 
     for (int yy = ty; yy < 32; yy += 8) {
         int c = c0 + yy, r = r0 + tx;
         if (c < cols && r < lds)  // rows in [rows, lds) are the zero padding
-            for (int t = 0; t < nslices; ++t) S[t * plane + (int64_t)c * lds + r] = tile[t][yy][tx];
+            for (int t = 0; t < nslices; ++t) S[t * plane + (int64_t)c * lds + r] = digit_out<T>(tile[t][yy][tx]);
     }
 }
 
@@ -148,32 +164,52 @@ __global__ void fix_nonfinite_cols_kernel(int32_t* e_out, int cols) {
     if (j < cols && e_out[j] == INT32_MIN) e_out[j] = 0;
 }
 
+template <typename T>
+cudaError_t rows_launch(const float* X, int64_t ldx, int rows, int cols, int nslices, T* S, int64_t lds, int32_t* e,
+                        cudaStream_t s) {
+    if (rows == 0) return cudaSuccess;
+    slice_rows_kernel<T><<<rows, SROW_THREADS, 0, s>>>(X, ldx, rows, cols, nslices, S, lds, e);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t cols_launch(const float* X, int64_t ldx, int rows, int cols, int nslices, T* S, int64_t lds, int32_t* e,
+                        cudaStream_t s) {
+    if (cols == 0) return cudaSuccess;
+    uint32_t* colmax = reinterpret_cast<uint32_t*>(e);  // reused: max bits, then exponents
+    cudaError_t err = cudaMemsetAsync(colmax, 0, (size_t)cols * sizeof(uint32_t), s);
+    if (err != cudaSuccess) return err;
+    if (rows > 0) {
+        dim3 g1((cols + 31) / 32, (rows + CM_ROWS - 1) / CM_ROWS);
+        col_absmax_kernel<<<g1, dim3(32, 8), 0, s>>>(X, ldx, rows, cols, colmax);
+    }
+    col_exponent_kernel<<<(cols + 255) / 256, 256, 0, s>>>(colmax, cols, e);
+    dim3 g2((cols + 31) / 32, (int)((lds + 31) / 32));
+    if (lds > 0) slice_cols_kernel<T><<<g2, dim3(32, 8), 0, s>>>(X, ldx, rows, cols, nslices, e, S, lds);
+    fix_nonfinite_cols_kernel<<<(cols + 255) / 256, 256, 0, s>>>(e, cols);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t slice_rows_launch(const float* X, int64_t ldx, int rows, int cols, int nslices, int8_t* S, int64_t lds,
                               int32_t* e, cudaStream_t s) {
-    if (rows == 0) return cudaSuccess;
-    slice_rows_kernel<<<rows, SROW_THREADS, 0, s>>>(X, ldx, rows, cols, nslices, S, lds, e);
-    return cudaGetLastError();
+    return rows_launch<int8_t>(X, ldx, rows, cols, nslices, S, lds, e, s);
 }
 
 cudaError_t slice_cols_launch(const float* X, int64_t ldx, int rows, int cols, int nslices, int8_t* S, int64_t lds,
                               int32_t* e, cudaStream_t s) {
-    if (cols == 0) return cudaSuccess;
-    if (rows == 0) {
-        cudaError_t err = cudaMemsetAsync(e, 0, (size_t)cols * sizeof(int32_t), s);
-        return err;
-    }
-    uint32_t* colmax = reinterpret_cast<uint32_t*>(e);  // reused: max bits, then exponents
-    cudaError_t err = cudaMemsetAsync(colmax, 0, (size_t)cols * sizeof(uint32_t), s);
-    if (err != cudaSuccess) return err;
-    dim3 g1((cols + 31) / 32, (rows + CM_ROWS - 1) / CM_ROWS);
-    col_absmax_kernel<<<g1, dim3(32, 8), 0, s>>>(X, ldx, rows, cols, colmax);
-    col_exponent_kernel<<<(cols + 255) / 256, 256, 0, s>>>(colmax, cols, e);
-    dim3 g2((cols + 31) / 32, (int)((lds + 31) / 32));
-    slice_cols_kernel<<<g2, dim3(32, 8), 0, s>>>(X, ldx, rows, cols, nslices, e, S, lds);
-    fix_nonfinite_cols_kernel<<<(cols + 255) / 256, 256, 0, s>>>(e, cols);
-    return cudaGetLastError();
+    return cols_launch<int8_t>(X, ldx, rows, cols, nslices, S, lds, e, s);
+}
+
+cudaError_t slice_rows_f16_launch(const float* X, int64_t ldx, int rows, int cols, int nslices, void* S, int64_t lds,
+                                  int32_t* e, cudaStream_t s) {
+    return rows_launch<__half>(X, ldx, rows, cols, nslices, reinterpret_cast<__half*>(S), lds, e, s);
+}
+
+cudaError_t slice_cols_f16_launch(const float* X, int64_t ldx, int rows, int cols, int nslices, void* S, int64_t lds,
+                                  int32_t* e, cudaStream_t s) {
+    return cols_launch<__half>(X, ldx, rows, cols, nslices, reinterpret_cast<__half*>(S), lds, e, s);
 }
 
 DETGEMM_STATUS_ACCESSOR(slice_take_status)

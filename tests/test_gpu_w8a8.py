@@ -211,3 +211,50 @@ def test_tc_engine_chunk_boundary_worst_case(lib, dev):
         ld = (K + 15) // 16 * 16
         C = run_i32(lib, dev, A, W, split=split, lda=ld, ldw=ld)
         assert (C == K * 16384).all(), (M, N, K, split)
+
+
+def test_tc_epilogue_large_accumulators(lib, dev, oracle_mod):
+    # accumulators of 26-28 bits (well past fp32's 24-bit significand) with random low
+    # bits: the tensor-core epilogue's rounding must still match the oracle bit for bit
+    rng = np.random.default_rng(21)
+    M, N, K = 130, 257, 10000
+    A = rng.integers(90, 128, size=(M, K), dtype=np.int8)
+    W = rng.integers(90, 128, size=(N, K), dtype=np.int8)
+    A[::3] = -A[::3]
+    ea = rng.integers(-40, -10, size=M, dtype=np.int32)
+    ew = rng.integers(-40, -10, size=N, dtype=np.int32)
+    acc = oracle_mod.gemm_s8_i32(A, W)
+    assert np.abs(acc).max() > 2 ** 26
+    got = run_w8a8(lib, dev, A, W, ea, ew, lda=10000, ldw=10000)
+    assert (got == oracle_mod.w8a8(A, W, ea, ew)).all()
+
+
+def test_tc_epilogue_extreme_exponents(lib, dev, oracle_mod):
+    # exponents that push results into bf16 subnormals, to zero, near the largest finite
+    # value and to infinity, mixed within warps, on the tensor-core path (M > 64)
+    rng = np.random.default_rng(22)
+    M, N, K = 200, 300, 700
+    A = rng.integers(-128, 128, size=(M, K), dtype=np.int8)
+    W = rng.integers(-128, 128, size=(N, K), dtype=np.int8)
+    ea = rng.integers(-160, 130, size=M, dtype=np.int32)
+    ew = rng.integers(-40, 40, size=N, dtype=np.int32)
+    ea[:40] = rng.integers(-20, 0, size=40)  # some rows entirely in the common range
+    got = run_w8a8(lib, dev, A, W, ea, ew, lda=704, ldw=704)
+    want = oracle_mod.w8a8(A, W, ea, ew)
+    assert (got == want).all(), int((got != want).sum())
+    # golden cases on the tensor-core path: rows of the hand-worked table, repeated to M > 64
+    path = os.path.join(os.path.dirname(__file__), "golden", "w8a8_epilogue_cases.txt")
+    cases = []
+    for line in open(path):
+        line = line.split("#")[0].strip()
+        if line:
+            a, e, b = line.split()[:3]
+            cases.append((int(a), int(e), int(b, 16)))
+    cases = [c for c in cases if abs(c[0]) <= 2048 * 16256]
+    rows = (cases * 10)[:130]
+    A = np.zeros((len(rows), 2048), np.int8)
+    W = np.zeros((len(rows), 2048), np.int8)
+    for i, (acc, e, _) in enumerate(rows):
+        A[i], W[i] = _row_for_acc(acc, 2048)
+    C = run_w8a8(lib, dev, A, W, np.array([e for _, e, _ in rows], np.int32), np.zeros(len(rows), np.int32))
+    assert (np.diag(C) == np.array([b for _, _, b in rows], np.uint16)).all()
