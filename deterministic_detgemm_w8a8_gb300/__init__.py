@@ -47,6 +47,10 @@ SIGNATURES = {
     "detgemm_ozaki_workspace_size": ([_I32, _I32, _I32, _I32, _I32, _I32], _SZ),
     "detgemm_get_device_status": ([_P], _I32),
     "detgemm_w8a8_noalloc": ([_P, _I64, _P, _I64, _P, _P, _P, _I64, _I32, _I32, _I32, _I32, _P], _I32),
+    "detgemm_widen_i8_f16": ([_P, _I64, _I32, _I32, _P, _I64, _P], _I32),
+    "detgemm_w8a8_f16ops": ([_P, _I64, _P, _I64, _P, _P, _P, _I64, _I32, _I32, _I32, _I32, _P, _SZ, _P], _I32),
+    "detgemm_w8a8_f16ops_workspace_size": ([_I32, _I32, _I32, _I32], _SZ),
+    "detgemm_selftest_timeout": ([_I32, _P], _I32),
 }
 
 _lock = threading.Lock()
@@ -232,6 +236,43 @@ def ozaki_f32(A, B, nslices: int = 7, max_diag: int = 8, split_k: int = 1, out=N
                                wsb.data_ptr() if wsb is not None else None, wsn, _stream(stream))
     _check(st, "detgemm_ozaki_f32")
     return out
+
+
+def widen_i8_f16(X, stream=None) -> torch.Tensor:
+    """Exact int8 -> fp16 copy [rows, cols] (row stride padded to 16 bytes, padding zeroed)."""
+    lib = load()
+    _req(X, torch.int8, "X")
+    rows, cols = X.shape
+    Y = empty2d(rows, cols, torch.float16, X.device)
+    st = lib.detgemm_widen_i8_f16(X.data_ptr(), _ld(X), rows, cols, Y.data_ptr(), _ld(Y), _stream(stream))
+    _check(st, "detgemm_widen_i8_f16")
+    return Y
+
+
+def w8a8_f16ops(A16, W16, ea, ew, split_k: int = 1, out=None, ws=None, stream=None) -> torch.Tensor:
+    """W8A8 on operands widened by widen_i8_f16 (fp16 tensors holding int8 values)."""
+    lib = load()
+    _req(A16, torch.float16, "A16"); _req(W16, torch.float16, "W16")
+    _req(ea, torch.int32, "ea"); _req(ew, torch.int32, "ew")
+    M, K = A16.shape
+    N = W16.shape[0]
+    if W16.shape[1] != K or ea.shape != (M,) or ew.shape != (N,):
+        raise ValueError("shape mismatch")
+    if out is None:
+        out = empty2d(M, N, torch.bfloat16, A16.device)
+    _req(out, torch.bfloat16, "out")
+    need = int(lib.detgemm_w8a8_f16ops_workspace_size(M, N, K, split_k))
+    wsb, wsn = _workspace(need, A16.device, ws)
+    st = lib.detgemm_w8a8_f16ops(A16.data_ptr(), _ld(A16), W16.data_ptr(), _ld(W16), ea.data_ptr(), ew.data_ptr(),
+                                 out.data_ptr(), _ld(out), M, N, K, split_k,
+                                 wsb.data_ptr() if wsb is not None else None, wsn, _stream(stream))
+    _check(st, "detgemm_w8a8_f16ops")
+    return out
+
+
+def selftest_timeout(limit_ms: int = 100, stream=None) -> None:
+    """Launch the bounded-wait self-check (expires after limit_ms; see device_status)."""
+    _check(load().detgemm_selftest_timeout(limit_ms, _stream(stream)), "detgemm_selftest_timeout")
 
 
 def device_status(stream=None) -> int:

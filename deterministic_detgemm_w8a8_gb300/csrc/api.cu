@@ -158,7 +158,7 @@ static detgemm_status run_tc(const int8_t* A, int64_t lda, const int8_t* W, int6
     a.C = C;
     a.ldc = ldc;
     a.c_plane = 0;
-    return from_cuda(tc_gemm_launch(a, base + L.a16, 1, base + L.w16, 1, L.Kp, base + L.split, stream));
+    return from_cuda(tc_gemm_launch(a, base + L.a16, L.Kp, 1, base + L.w16, L.Kp, 1, L.Kp, base + L.split, stream));
 }
 
 static detgemm_status run_igemm(const int8_t* A, int64_t lda, const int8_t* W, int64_t ldw, const int32_t* ea,
@@ -299,9 +299,67 @@ detgemm_status detgemm_ozaki_f32(const float* A, int64_t lda, const float* B, in
     a.C = T;
     a.ldc = L.ldT;
     a.c_plane = (int64_t)M * L.ldT;
-    err = tc_gemm_launch(a, base + L.da, nslices, base + L.db, nslices, L.Kp, base + L.split, s);
+    err = tc_gemm_launch(a, base + L.da, L.Kp, nslices, base + L.db, L.Kp, nslices, L.Kp, base + L.split, s);
     if (err == cudaSuccess) err = ozaki_combine_launch(T, L.ldT, max_diag, e, f, C, ldc, M, N, s);
     return from_cuda(err);
+}
+
+detgemm_status detgemm_widen_i8_f16(const int8_t* X, int64_t ldx, int rows, int cols, uint16_t* Y, int64_t ldy,
+                                    detgemm_stream_t stream) {
+    if (rows < 0 || cols < 0) return DETGEMM_ERR_INVALID_ARG;
+    if (rows == 0 || cols == 0) return DETGEMM_OK;
+    if (!X || !Y || ldx < cols || ldy < cols) return DETGEMM_ERR_INVALID_ARG;
+    if (!aligned16(X) || !aligned16(Y) || ldx % 16 != 0 || ldy % 8 != 0) return DETGEMM_ERR_ALIGNMENT;
+    detgemm_status st = check_device();
+    if (st != DETGEMM_OK) return st;
+    // the widening kernel writes 8-element groups up to ldy rounded down to 8 (all of ldy),
+    // zero beyond cols
+    return from_cuda(widen_i8_f16_launch(X, ldx, rows, cols, Y, ldy, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t detgemm_w8a8_f16ops_workspace_size(int M, int N, int K, int split_k) {
+    (void)K;
+    if (M <= 0 || N <= 0) return 0;
+    return tc_split_bytes(1, M, N, split_k);
+}
+
+detgemm_status detgemm_w8a8_f16ops(const uint16_t* A16, int64_t lda, const uint16_t* W16, int64_t ldw,
+                                   const int32_t* ea, const int32_t* ew, uint16_t* C, int64_t ldc, int M, int N,
+                                   int K, int split_k, void* ws, size_t ws_bytes, detgemm_stream_t stream) {
+    if (M < 0 || N < 0 || K < 1) return DETGEMM_ERR_INVALID_ARG;
+    if (K > DETGEMM_MAX_K) return DETGEMM_ERR_PRECONDITION;
+    if (split_k < 1 || split_k > (K + 63) / 64) return DETGEMM_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return DETGEMM_OK;
+    if (!A16 || !W16 || !C || !ea || !ew) return DETGEMM_ERR_INVALID_ARG;
+    if (lda < K || ldw < K || ldc < N) return DETGEMM_ERR_INVALID_ARG;
+    if (!aligned16(A16) || !aligned16(W16) || !aligned16(C) || !aligned4(ea) || !aligned4(ew))
+        return DETGEMM_ERR_ALIGNMENT;
+    if (lda % 8 != 0 || ldw % 8 != 0 || ldc % 8 != 0) return DETGEMM_ERR_ALIGNMENT;
+    const size_t need = detgemm_w8a8_f16ops_workspace_size(M, N, K, split_k);
+    if (need > 0 && (ws == nullptr || ws_bytes < need)) return DETGEMM_ERR_WORKSPACE;
+    if (need > 0 && (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return DETGEMM_ERR_ALIGNMENT;
+    detgemm_status st = check_device();
+    if (st != DETGEMM_OK) return st;
+    TcArgs a = {};
+    a.M = M;
+    a.N = N;
+    a.ndiag = 1;
+    a.diag_first[0] = 0;
+    a.diag_nseg[0] = 1;
+    a.split = split_k;
+    a.mode = EPI_BF16_POW2;
+    a.ea = ea;
+    a.ew = ew;
+    a.C = C;
+    a.ldc = ldc;
+    return from_cuda(tc_gemm_launch(a, A16, lda, 1, W16, ldw, 1, K, ws, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+detgemm_status detgemm_selftest_timeout(int limit_ms, detgemm_stream_t stream) {
+    if (limit_ms < 1 || limit_ms > 2000) return DETGEMM_ERR_INVALID_ARG;
+    detgemm_status st = check_device();
+    if (st != DETGEMM_OK) return st;
+    return from_cuda(selftest_wait_launch((uint64_t)limit_ms * 1000000ull, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 detgemm_status detgemm_get_device_status(detgemm_stream_t stream) {

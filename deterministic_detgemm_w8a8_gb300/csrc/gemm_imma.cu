@@ -13,8 +13,11 @@
 //  * igemm_tile_kernel   — 128x128x64 CTA tile, 8 warps, 4-stage cp.async ring,
 //                          XOR-swizzled shared memory and ldmatrix fragments.
 //  * igemm_skinny_kernel — M <= 64: each warp streams 32 rows of W straight from
-//                          global memory with 16-byte loads into mma fragments; W is
-//                          read exactly once per split part.
+//                          global memory with 16-byte loads; the int8 values are widened
+//                          exactly to fp16 in registers for the fp16 warp MMA (fp32
+//                          partials drained to int32 every <= 1024 K). W is read exactly
+//                          once per split part.
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -271,6 +274,40 @@ __device__ __forceinline__ uint32_t u4_get(const uint4& v, int i) {
     return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
 }
 
+// fp16 warp MMA: D (fp32) += A (16x16 fp16) * B (16x8 fp16)
+__device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Exact int8x4 -> two fp16x2 (bytes 0,1 -> lo; bytes 2,3 -> hi): b + 128 is placed under
+// the fp16 exponent of 1024, giving 1024 + (b + 128), and 1152 is subtracted.
+__device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    const uint32_t x = w ^ 0x80808080u;
+    const uint32_t l = __byte_perm(x, 0x64646464u, 0x4140);
+    const uint32_t h = __byte_perm(x, 0x64646464u, 0x4342);
+    const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
+    const __half2 rl = __hsub2(*reinterpret_cast<const __half2*>(&l), bias);
+    const __half2 rh = __hsub2(*reinterpret_cast<const __half2*>(&h), bias);
+    lo = *reinterpret_cast<const uint32_t*>(&rl);
+    hi = *reinterpret_cast<const uint32_t*>(&rh);
+}
+
+// 16 int8 values (a uint4) -> 8 fp16x2 words, in k order
+__device__ __forceinline__ void i8x16_to_f16x16(const uint4& v, uint32_t (&h)[8]) {
+    i8x4_to_f16x4(v.x, h[0], h[1]);
+    i8x4_to_f16x4(v.y, h[2], h[3]);
+    i8x4_to_f16x4(v.z, h[4], h[5]);
+    i8x4_to_f16x4(v.w, h[6], h[7]);
+}
+
+// The skinny kernel runs on the fp16 warp MMA (this part's int8 warp MMA is about four
+// times slower): int8 values are widened exactly in registers, products accumulate in
+// fp32 exactly (integers below 2^24) for at most 16 blocks of 64 K values per thread,
+// and every such chunk is drained into int32 registers.
 template <int MT, int U>
 __global__ void __launch_bounds__(128) igemm_skinny_kernel(const __grid_constant__ IGemmArgs p) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -282,12 +319,18 @@ __global__ void __launch_bounds__(128) igemm_skinny_kernel(const __grid_constant
     split_range(F, p.split, blockIdx.y, f0, f1);
 
     int32_t acc[MT][4][4];
+    float accf[MT][4][4];
 #pragma unroll
     for (int a = 0; a < MT; ++a)
 #pragma unroll
         for (int b = 0; b < 4; ++b)
 #pragma unroll
-            for (int c = 0; c < 4; ++c) acc[a][b][c] = 0;
+            for (int c = 0; c < 4; ++c) {
+                acc[a][b][c] = 0;
+                accf[a][b][c] = 0.f;
+            }
+    static_assert(16 % U == 0, "a drain must fall on an iteration boundary");
+    int since = 0;  // 64-wide K blocks accumulated in accf since the last drain
 
     for (int fb = f0; fb < f1; fb += U) {
         uint4 wv[U][4], av[U][MT][2];
@@ -320,18 +363,45 @@ __global__ void __launch_bounds__(128) igemm_skinny_kernel(const __grid_constant
                 }
         }
 #pragma unroll
-        for (int u = 0; u < U; ++u)
+        for (int u = 0; u < U; ++u) {
+            uint32_t hw[4][8];
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh)
+            for (int j = 0; j < 4; ++j) i8x16_to_f16x16(wv[u][j], hw[j]);
 #pragma unroll
-                for (int mt = 0; mt < MT; ++mt) {
-                    uint32_t a[4] = {u4_get(av[u][mt][0], 2 * hh), u4_get(av[u][mt][1], 2 * hh),
-                                     u4_get(av[u][mt][0], 2 * hh + 1), u4_get(av[u][mt][1], 2 * hh + 1)};
+            for (int mt = 0; mt < MT; ++mt) {
+                uint32_t h0[8], h1[8];
+                i8x16_to_f16x16(av[u][mt][0], h0);
+                i8x16_to_f16x16(av[u][mt][1], h1);
+                // the lane's 16 k values kk .. kk+15 feed four k16 MMAs, the same k slots
+                // for A and W: logical (2t + j) <- kk + 4q + j, (2t + 8 + j) <- kk + 4q + 2 + j
 #pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        mma_s8(acc[mt][j], a, u4_get(wv[u][j], 2 * hh), u4_get(wv[u][j], 2 * hh + 1));
+                for (int q = 0; q < 4; ++q) {
+                    const uint32_t a[4] = {h0[2 * q], h1[2 * q], h0[2 * q + 1], h1[2 * q + 1]};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) mma_f16(accf[mt][j], a, hw[j][2 * q], hw[j][2 * q + 1]);
                 }
+            }
+        }
+        since += U;
+        if (since == 16) {
+#pragma unroll
+            for (int a = 0; a < MT; ++a)
+#pragma unroll
+                for (int b = 0; b < 4; ++b)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        acc[a][b][c] += __float2int_rn(accf[a][b][c]);
+                        accf[a][b][c] = 0.f;
+                    }
+            since = 0;
+        }
     }
+#pragma unroll
+    for (int a = 0; a < MT; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) acc[a][b][c] += __float2int_rn(accf[a][b][c]);
 
     if (p.split == 1) {
 #pragma unroll

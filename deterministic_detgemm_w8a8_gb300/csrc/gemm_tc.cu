@@ -467,13 +467,15 @@ int num_sms() {
     return g_num_sms[dev];
 }
 
-// 3-D map over fp16 planes [planes][rows][Kp], box {64, box_rows, 1}, 128-byte swizzle
-cudaError_t make_map(CUtensorMap* m, const void* base, int64_t Kp, int rows, int planes, int box_rows) {
+// 3-D map over fp16 planes [planes][rows][ld] of which the first kext columns are the
+// matrix (TMA fills the box beyond kext and beyond rows with zeros), box {64, box_rows, 1},
+// 128-byte swizzle
+cudaError_t make_map(CUtensorMap* m, const void* base, int64_t kext, int64_t ld, int rows, int planes, int box_rows) {
     PFN_cuTensorMapEncodeTiled_v12000 enc;
     cudaError_t e = get_encode(&enc);
     if (e != cudaSuccess) return e;
-    cuuint64_t dims[3] = {(cuuint64_t)Kp, (cuuint64_t)rows, (cuuint64_t)planes};
-    cuuint64_t strides[2] = {(cuuint64_t)Kp * 2, (cuuint64_t)Kp * 2 * (cuuint64_t)rows};
+    cuuint64_t dims[3] = {(cuuint64_t)kext, (cuuint64_t)rows, (cuuint64_t)planes};
+    cuuint64_t strides[2] = {(cuuint64_t)ld * 2, (cuuint64_t)ld * 2 * (cuuint64_t)rows};
     cuuint32_t box[3] = {(cuuint32_t)BK, (cuuint32_t)box_rows, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
@@ -532,15 +534,15 @@ int max_pair_clusters() {
 }
 }  // namespace
 
-static cudaError_t tc2_launch(TcArgs a, const void* A16, int a_planes, const void* B16, int b_planes, int64_t Kp,
-                              void* ws_split, cudaStream_t s) {
+static cudaError_t tc2_launch(TcArgs a, const void* A16, int64_t lda, int a_planes, const void* B16, int64_t ldb,
+                              int b_planes, int64_t kext, void* ws_split, cudaStream_t s) {
     a.tiles_m = (a.M + 255) / 256;
     a.tiles_n = (a.N + BN - 1) / BN;
-    a.nkb = (int)(Kp / BK);
+    a.nkb = (int)((kext + BK - 1) / BK);
     if (a.group_m <= 0) a.group_m = 8;
     CUtensorMap tmA, tmB;
-    cudaError_t e = make_map(&tmA, A16, Kp, a.M, a_planes, 128);
-    if (e == cudaSuccess) e = make_map(&tmB, B16, Kp, a.N, b_planes, 128);
+    cudaError_t e = make_map(&tmA, A16, kext, lda, a.M, a_planes, 128);
+    if (e == cudaSuccess) e = make_map(&tmB, B16, kext, ldb, a.N, b_planes, 128);
     if (e != cudaSuccess) return e;
     if (a.split > 1) {
         size_t accb = (((size_t)a.ndiag * a.M * a.N * sizeof(int32_t)) + 255) & ~(size_t)255;
@@ -571,10 +573,30 @@ static cudaError_t tc2_launch(TcArgs a, const void* A16, int a_planes, const voi
     return cudaGetLastError();
 }
 
-cudaError_t tc_gemm_launch(const TcArgs& a, const void* A16, int a_planes, const void* B16, int b_planes,
-                           int64_t Kp, void* ws_split, cudaStream_t s) {
+cudaError_t tc_gemm_launch(const TcArgs& a, const void* A16, int64_t lda, int a_planes, const void* B16, int64_t ldb,
+                           int b_planes, int64_t kext, void* ws_split, cudaStream_t s) {
     if (a.M == 0 || a.N == 0) return cudaSuccess;
-    return tc2_launch(a, A16, a_planes, B16, b_planes, Kp, ws_split, s);
+    return tc2_launch(a, A16, lda, a_planes, B16, ldb, b_planes, kext, ws_split, s);
+}
+
+// Self-check of the bounded waits: one thread waits on an mbarrier that nothing ever
+// arrives on, with the given limit; the wait expires, raises DEV_TIMEOUT in this unit's
+// status word and the kernel returns normally.
+__global__ void selftest_wait_kernel(uint64_t limit_ns) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) mbar_wait(&bar, 0, &abort_flag, limit_ns);
+}
+
+cudaError_t selftest_wait_launch(uint64_t limit_ns, cudaStream_t s) {
+    selftest_wait_kernel<<<1, 32, 0, s>>>(limit_ns);
+    return cudaGetLastError();
 }
 
 DETGEMM_STATUS_ACCESSOR(tc_take_status)

@@ -82,8 +82,12 @@ struct TcArgs {
 
 int64_t tc_padded_k(int K);
 size_t tc_split_bytes(int ndiag, int M, int N, int split);
-cudaError_t tc_gemm_launch(const TcArgs& a, const void* A16, int a_planes, const void* B16, int b_planes,
-                           int64_t Kp, void* ws_split, cudaStream_t s);
+// A planes [a_planes][M][lda], B planes [b_planes][N][ldb] (fp16, 16-byte aligned rows);
+// the first kext columns of each row are the K extent (zeros are read beyond it)
+cudaError_t tc_gemm_launch(const TcArgs& a, const void* A16, int64_t lda, int a_planes, const void* B16, int64_t ldb,
+                           int b_planes, int64_t kext, void* ws_split, cudaStream_t s);
+// one-thread kernel whose bounded wait on a never-arriving mbarrier expires (DEV_TIMEOUT)
+cudaError_t selftest_wait_launch(uint64_t limit_ns, cudaStream_t s);
 // exact int8 -> fp16 copy of X [rows x K] into Y [rows x Kp], zero beyond K
 cudaError_t widen_i8_f16_launch(const int8_t* X, int64_t ldx, int rows, int K, void* Y, int64_t Kp,
                                 cudaStream_t s);

@@ -168,6 +168,40 @@ DETGEMM_API detgemm_status detgemm_ozaki_f32(const float* A, int64_t lda, const 
 DETGEMM_API size_t detgemm_ozaki_workspace_size(int M, int N, int K, int nslices, int max_diag, int split_k);
 
 /*
+ * Exact int8 -> fp16 copy (every int8 value is an fp16 value): Y[r][k] = X[r][k] for
+ * k < cols and Y[r][k] = 0 for cols <= k < ldy, i.e. the whole row stride of Y is written.
+ * The tensor-core W8A8 path consumes operands in this form; widening a static weight
+ * once (at load time) and calling detgemm_w8a8_f16ops skips that step per call.
+ *   X int8 [rows x cols] (ldx, multiple of 16); Y fp16 bit patterns [rows x ldy]
+ *   (ldy >= cols, multiple of 8). Errors: INVALID_ARG, ALIGNMENT, UNSUPPORTED_DEVICE, CUDA.
+ */
+DETGEMM_API detgemm_status detgemm_widen_i8_f16(const int8_t* X, int64_t ldx, int rows, int cols, uint16_t* Y,
+                                                int64_t ldy, detgemm_stream_t stream);
+
+/*
+ * detgemm_w8a8 on operands already widened to fp16 by detgemm_widen_i8_f16: the same
+ * definition ([P4] §II), the same result bits. A16 [M x K] (lda) and W16 [N x K] (ldw)
+ * must hold integers in [-128, 127] — exactness rests on it; other values give
+ * unspecified results (never a fault). lda, ldw and ldc are multiples of 8 elements.
+ * Scratch: detgemm_w8a8_f16ops_workspace_size (only split-K needs any; 256-byte aligned).
+ * Errors as detgemm_w8a8.
+ */
+DETGEMM_API detgemm_status detgemm_w8a8_f16ops(const uint16_t* A16, int64_t lda, const uint16_t* W16, int64_t ldw,
+                                               const int32_t* ea, const int32_t* ew, uint16_t* C, int64_t ldc,
+                                               int M, int N, int K, int split_k, void* ws, size_t ws_bytes,
+                                               detgemm_stream_t stream);
+
+DETGEMM_API size_t detgemm_w8a8_f16ops_workspace_size(int M, int N, int K, int split_k);
+
+/*
+ * Self-check of the failure detection: launches a one-thread kernel whose bounded wait
+ * on a barrier that nothing ever arrives on expires after limit_ms (1 .. 2000). After it,
+ * detgemm_get_device_status returns DETGEMM_ERR_TIMEOUT and the CUDA context stays usable.
+ * Every wait of the GEMM engine uses the same bounded mechanism (limit 4 s).
+ */
+DETGEMM_API detgemm_status detgemm_selftest_timeout(int limit_ms, detgemm_stream_t stream);
+
+/*
  * Synchronizes `stream`, then returns and clears the current device's status word:
  * DETGEMM_OK, DETGEMM_ERR_NONFINITE or DETGEMM_ERR_TIMEOUT (the first one raised
  * since the last read), or DETGEMM_ERR_CUDA if the synchronization itself failed.

@@ -258,3 +258,19 @@ def test_tc_epilogue_extreme_exponents(lib, dev, oracle_mod):
         A[i], W[i] = _row_for_acc(acc, 2048)
     C = run_w8a8(lib, dev, A, W, np.array([e for _, e, _ in rows], np.int32), np.zeros(len(rows), np.int32))
     assert (np.diag(C) == np.array([b for _, _, b in rows], np.uint16)).all()
+
+
+@pytest.mark.parametrize("M,N,K,split", [(300, 520, 1000, 1), (64, 256, 2048, 4), (1000, 130, 70, 1)])
+def test_prewidened_operands_give_the_same_bits(lib, dev, M, N, K, split):
+    rng = np.random.default_rng(M + N + K)
+    A = rng.integers(-128, 128, size=(M, K), dtype=np.int8)
+    W = rng.integers(-128, 128, size=(N, K), dtype=np.int8)
+    ea = rng.integers(-20, -2, size=M, dtype=np.int32)
+    ew = rng.integers(-20, -2, size=N, dtype=np.int32)
+    ld = (K + 15) // 16 * 16
+    tA, tW = padded(A, dev, ld), padded(W, dev, ld)
+    A16, W16 = lib.widen_i8_f16(tA), lib.widen_i8_f16(tW)
+    assert torch.equal(A16.float().cpu(), torch.from_numpy(A).float())
+    ref = lib.w8a8(tA, tW, to_dev(ea, dev), to_dev(ew, dev), split_k=split)
+    got = lib.w8a8_f16ops(A16, W16, to_dev(ea, dev), to_dev(ew, dev), split_k=split)
+    assert torch.equal(got.view(torch.int16), ref.view(torch.int16))
