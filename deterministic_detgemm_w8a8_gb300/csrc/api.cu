@@ -371,6 +371,8 @@ detgemm_status detgemm_get_device_status(detgemm_stream_t stream) {
     v |= bits;
     if (tc_take_status(&bits) != cudaSuccess) return DETGEMM_ERR_CUDA;
     v |= bits;
+    if (skinny_take_status(&bits) != cudaSuccess) return DETGEMM_ERR_CUDA;
+    v |= bits;
     if (v & DEV_TIMEOUT) return DETGEMM_ERR_TIMEOUT;
     if (v & DEV_NONFINITE) return DETGEMM_ERR_NONFINITE;
     return DETGEMM_OK;

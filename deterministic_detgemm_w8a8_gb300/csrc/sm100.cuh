@@ -69,12 +69,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
 }
 
 // Wait without the early exit on abort (used to let in-flight copies land).
-__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) {
+constexpr uint64_t kDrainLimitNs = 50000000ull;  // 50 ms per stage when draining after an abort
+
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, uint64_t limit_ns = kWaitLimitNs) {
     const uint32_t a = smem_addr(bar);
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t i = 0;; ++i) {
         if (mbar_try_wait(a, parity)) return true;
-        if ((i & 255u) == 255u && globaltimer_ns() - t0 > kWaitLimitNs) {
+        if ((i & 255u) == 255u && globaltimer_ns() - t0 > limit_ns) {
             raise_status(DEV_TIMEOUT);
             return false;
         }

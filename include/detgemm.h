@@ -91,8 +91,11 @@ DETGEMM_API int detgemm_version(void);
  *   C   bf16 bit patterns (uint16) [M x N], row stride ldc
  *   split_k  number of contiguous K parts computed by separate CTAs and summed
  *            exactly ([P1] §3.2.2); 1 <= split_k <= ceil(K / 64). The output bits do
- *            not depend on it.
- *   ws       scratch of ws_bytes >= detgemm_w8a8_workspace_size(M, N, K, split_k).
+ *            not depend on it. For M <= 64 (decode-shaped, bound by reading W) the
+ *            kernel divides K among all SMs by itself so that every SM streams the same
+ *            number of bytes; split_k is then accepted but does not change the cut.
+ *   ws       scratch of ws_bytes >= detgemm_w8a8_workspace_size(M, N, K, split_k)
+ *            (nonzero for M <= 64 at any split_k, and for split_k > 1).
  * Empty problems (M == 0 or N == 0) return DETGEMM_OK and launch nothing.
  * Errors: INVALID_ARG (K < 1, M or N < 0, split_k out of range, null pointer),
  *         PRECONDITION (K > DETGEMM_MAX_K), ALIGNMENT, WORKSPACE, UNSUPPORTED_DEVICE, CUDA.

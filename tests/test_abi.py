@@ -65,7 +65,7 @@ P1 = P + 1
 
 
 def _w8a8(lib, A=P, lda=512, W=P, ldw=512, ea=P, ew=P, C=P, ldc=256, M=64, N=256, K=512, split=1,
-          ws=None, wsb=0):
+          ws=P, wsb=1 << 30):
     return lib.detgemm_w8a8(A, lda, W, ldw, ea, ew, C, ldc, M, N, K, split, ws, wsb, None)
 
 
@@ -84,8 +84,11 @@ def test_w8a8_argument_validation(lib):
     assert _w8a8(lib, ldc=260) == dg.ERR_ALIGNMENT  # 520 bytes
     need = dg.w8a8_workspace_size(64, 256, 512, 2)
     assert need >= 64 * 256 * 4
-    assert _w8a8(lib, split=2) == dg.ERR_WORKSPACE
+    assert _w8a8(lib, split=2, ws=None, wsb=0) == dg.ERR_WORKSPACE
     assert _w8a8(lib, split=2, ws=P, wsb=need - 1) == dg.ERR_WORKSPACE
+    # the decode-shaped path (M <= 64) needs scratch at any split; larger M only to split
+    assert dg.w8a8_workspace_size(16, 256, 512, 1) >= 16 * 256 * 4
+    assert _w8a8(lib, M=16, ws=None, wsb=0) == dg.ERR_WORKSPACE
     # empty problems succeed without touching the device
     assert _w8a8(lib, M=0, A=None, C=None) == dg.OK
     assert _w8a8(lib, N=0) == dg.OK

@@ -274,3 +274,15 @@ def test_prewidened_operands_give_the_same_bits(lib, dev, M, N, K, split):
     ref = lib.w8a8(tA, tW, to_dev(ea, dev), to_dev(ew, dev), split_k=split)
     got = lib.w8a8_f16ops(A16, W16, to_dev(ea, dev), to_dev(ew, dev), split_k=split)
     assert torch.equal(got.view(torch.int16), ref.view(torch.int16))
+
+
+def test_skinny_many_ctas_repeated(lib, dev, oracle_mod):
+    # many co-resident CTAs streaming W through the shared-memory ring: repeated runs at
+    # deep splits must all be exact (guards the stage-release ordering under load)
+    A, W, ea, ew = synthetic.skinny()
+    want = oracle_mod.gemm_s8_i32(A, W)
+    tA, tW = to_dev(A, dev), to_dev(W, dev)
+    for split in (16, 32, 64, 64, 128):
+        out = poison_like((16, 4096), torch.int32, dev)
+        lib.gemm_s8_i32(tA, tW, split_k=split, out=out)
+        assert (out.cpu().numpy() == want).all(), split
