@@ -167,6 +167,23 @@ def cpu_baseline_ffn(gate, down, budget_s=15.0):
             "sample": f"{nrows} of {M_FFN} rows of both FFN GEMMs ({dt:.1f} s, int64 triple loop, OpenMP)"}
 
 
+def reduce_step_time(ms: float, world: int, device=None) -> float:
+    """Max of the per-rank step times over all ranks (the job is as slow as its slowest
+    replica); identity on one rank."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(ops_per_step: float, ms_max: float, world: int) -> float:
+    """Whole-job throughput in T(ops)/s: every rank runs one full step per ms_max."""
+    return world * ops_per_step / (ms_max * 1e-3) / 1e12
+
+
 def main():
     args = parse()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -238,12 +255,8 @@ def main():
     g_ms = [e[0].elapsed_time(e[1]) for e in evs]
     d_ms = [e[1].elapsed_time(e[2]) for e in evs]
     step_ms = [a + b for a, b in zip(g_ms, d_ms)]
-    ms = statistics.mean(step_ms)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    value = world * OPS_STEP / (ms * 1e-3) / 1e12
+    ms = reduce_step_time(statistics.mean(step_ms), world, dev)
+    value = job_throughput(OPS_STEP, ms, world)
 
     # roofline of the dominant kernel (tc2_gemm_kernel, both GEMMs): the same two GEMMs on
     # operands widened beforehand, so the events bracket that kernel's launches alone
