@@ -140,8 +140,7 @@ static detgemm_status run_tc(const int8_t* A, int64_t lda, const int8_t* W, int6
                              void* ws, cudaStream_t stream) {
     const TcW8a8Layout L = tc_w8a8_layout(M, N, K, split_k);
     char* base = reinterpret_cast<char*>(ws);
-    cudaError_t e = widen_i8_f16_launch(A, lda, M, K, base + L.a16, L.Kp, stream);
-    if (e == cudaSuccess) e = widen_i8_f16_launch(W, ldw, N, K, base + L.w16, L.Kp, stream);
+    cudaError_t e = widen_pair_launch(A, lda, M, K, base + L.a16, L.Kp, W, ldw, N, K, base + L.w16, L.Kp, stream);
     if (e != cudaSuccess) return DETGEMM_ERR_CUDA;
     TcArgs a = {};
     a.M = M;

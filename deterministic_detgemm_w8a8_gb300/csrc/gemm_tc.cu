@@ -405,36 +405,6 @@ __global__ void __launch_bounds__(THREADS, 1)
 }
 
 // ------------------------------------------------------------------------------------
-// int8 -> fp16 widening (exact), zero-filling K up to Kp.  X [rows x K] (ldx) -> Y [rows x Kp]
-// ------------------------------------------------------------------------------------
-__global__ void widen_i8_f16_kernel(const int8_t* __restrict__ X, int64_t ldx, int rows, int K,
-                                    __half* __restrict__ Y, int64_t Kp) {
-    const int64_t nvec = Kp / 8;  // 8 outputs (16 bytes) per thread step
-    const int64_t total = (int64_t)rows * nvec;
-    for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < total; v += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t r = v / nvec;
-        const int k = (int)((v - r * nvec) * 8);
-        const int8_t* x = X + r * ldx + k;
-        int8_t b[8];
-        if (k + 8 <= K) {
-            uint2 w = *reinterpret_cast<const uint2*>(x);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                b[i] = (int8_t)(w.x >> (8 * i));
-                b[4 + i] = (int8_t)(w.y >> (8 * i));
-            }
-        } else {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) b[i] = (k + i < K) ? x[i] : (int8_t)0;
-        }
-        __half2 h[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) h[i] = __halves2half2(__int2half_rn(b[2 * i]), __int2half_rn(b[2 * i + 1]));
-        *reinterpret_cast<uint4*>(Y + r * Kp + k) = *reinterpret_cast<uint4*>(h);
-    }
-}
-
-// ------------------------------------------------------------------------------------
 // host side
 // ------------------------------------------------------------------------------------
 std::mutex g_tc_mutex;
@@ -488,15 +458,6 @@ cudaError_t make_map(CUtensorMap* m, const void* base, int64_t kext, int64_t ld,
 
 int64_t tc_padded_k(int K) { return ((int64_t)K + BK - 1) / BK * BK; }
 
-cudaError_t widen_i8_f16_launch(const int8_t* X, int64_t ldx, int rows, int K, void* Y, int64_t Kp, cudaStream_t s) {
-    if (rows == 0) return cudaSuccess;
-    const int64_t total = (int64_t)rows * (Kp / 8);
-    int blocks = (int)((total + 255) / 256);
-    const int cap = num_sms() * 8;
-    if (blocks > cap) blocks = cap;
-    widen_i8_f16_kernel<<<blocks, 256, 0, s>>>(X, ldx, rows, K, reinterpret_cast<__half*>(Y), Kp);
-    return cudaGetLastError();
-}
 
 size_t tc_split_bytes(int ndiag, int M, int N, int split) {
     if (split <= 1) return 0;

@@ -96,6 +96,11 @@ cudaError_t tc_gemm_launch(const TcArgs& a, const void* A16, int64_t lda, int a_
                            int b_planes, int64_t kext, void* ws_split, cudaStream_t s);
 // one-thread kernel whose bounded wait on a never-arriving mbarrier expires (DEV_TIMEOUT)
 cudaError_t selftest_wait_launch(uint64_t limit_ns, cudaStream_t s);
+// exact int8 -> fp16 copies of two matrices in one launch (row strides Kp0, Kp1 multiples
+// of 16, zero beyond K)
+cudaError_t widen_pair_launch(const int8_t* X0, int64_t ldx0, int rows0, int K0, void* Y0, int64_t Kp0,
+                              const int8_t* X1, int64_t ldx1, int rows1, int K1, void* Y1, int64_t Kp1,
+                              cudaStream_t s);
 // exact int8 -> fp16 copy of X [rows x K] into Y [rows x Kp], zero beyond K
 cudaError_t widen_i8_f16_launch(const int8_t* X, int64_t ldx, int rows, int K, void* Y, int64_t Kp,
                                 cudaStream_t s);

@@ -276,6 +276,19 @@ def test_prewidened_operands_give_the_same_bits(lib, dev, M, N, K, split):
     assert torch.equal(got.view(torch.int16), ref.view(torch.int16))
 
 
+@pytest.mark.parametrize("rows,cols", [(3, 256), (3, 250), (5, 200), (2, 33), (7, 1)])
+def test_widening_is_exact_and_zero_pads(lib, dev, rows, cols):
+    # every int8 value appears; the row stride (cols rounded up to 8 halves) is either a
+    # multiple of 16 (two-operand kernel) or only of 8 (the narrow kernel)
+    X = ((np.arange(rows * cols, dtype=np.int64) * 37 + 11) % 256 - 128).astype(np.int8).reshape(rows, cols)
+    tX = padded(X, dev, (cols + 15) // 16 * 16)
+    Y = lib.widen_i8_f16(tX)
+    assert torch.equal(Y.float().cpu(), torch.from_numpy(X).float())
+    full = torch.as_strided(Y, (rows, Y.stride(0)), (Y.stride(0), 1))
+    assert (full[:, cols:].float().cpu() == 0).all()
+    assert (full.view(torch.int16)[:, cols:].cpu() == 0).all()  # +0, not -0
+
+
 def test_skinny_many_ctas_repeated(lib, dev, oracle_mod):
     # many co-resident CTAs streaming W through the shared-memory ring: repeated runs at
     # deep splits must all be exact (guards the stage-release ordering under load)
