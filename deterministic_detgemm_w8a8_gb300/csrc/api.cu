@@ -132,7 +132,7 @@ static TcW8a8Layout tc_w8a8_layout(int M, int N, int K, int split_k) {
 size_t detgemm_w8a8_workspace_size(int M, int N, int K, int split_k) {
     if (M <= 0 || N <= 0 || K <= 0) return 0;
     if (w8a8_uses_tc(M)) return tc_w8a8_layout(M, N, K, split_k).total;
-    return igemm_workspace_bytes(M, N, split_k);
+    return igemm_workspace_bytes(M, N, K, split_k);
 }
 
 static detgemm_status run_tc(const int8_t* A, int64_t lda, const int8_t* W, int64_t ldw, const int32_t* ea,

@@ -245,9 +245,9 @@ int n_tiles(int M, int N) { return ((N + TBN - 1) / TBN) * ((M + TBM - 1) / TBM)
 
 }  // namespace
 
-size_t igemm_workspace_bytes(int M, int N, int split) {
+size_t igemm_workspace_bytes(int M, int N, int K, int split) {
     if (M == 0 || N == 0) return 0;
-    if (use_skinny(M)) return skinny_workspace_bytes(M, N, split);  // needed at any split
+    if (use_skinny(M)) return skinny_workspace_bytes(M, N, K, split);  // needed at any split
     if (split <= 1) return 0;
     size_t acc = (size_t)M * (size_t)N * sizeof(int32_t);
     acc = (acc + 255) & ~(size_t)255;
@@ -266,7 +266,7 @@ cudaError_t igemm_launch(const IGemmArgs& a_in, void* ws, cudaStream_t s) {
         size_t accb = (((size_t)a.M * a.N * sizeof(int32_t)) + 255) & ~(size_t)255;
         a.ws_acc = reinterpret_cast<int32_t*>(ws);
         a.ws_cnt = reinterpret_cast<uint32_t*>(reinterpret_cast<char*>(ws) + accb);
-        cudaError_t e = cudaMemsetAsync(ws, 0, igemm_workspace_bytes(a.M, a.N, a.split), s);
+        cudaError_t e = cudaMemsetAsync(ws, 0, igemm_workspace_bytes(a.M, a.N, a.K, a.split), s);
         if (e != cudaSuccess) return e;
     }
     const int smem = TSTAGES * (TBM + TBN) * TBK;

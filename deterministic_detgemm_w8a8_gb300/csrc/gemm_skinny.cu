@@ -3,19 +3,26 @@
 // acc_ij = sum_k A_ik * W_jk exactly ("Deterministic LLM Inference Across GPU Kernels
 // ...", §II "Pipeline and alibi"), then the bf16 pow2 epilogue. With M <= 64 there are
 // at most 128 multiply-adds per W byte, so the kernel is bound by reading W once from
-// HBM; its job is to keep enough bytes in flight.
+// HBM; its job is to keep enough bytes in flight and to spend few instructions per byte.
 //
-// One CTA per (128-row block of W, split part). Warp 0, lane 0, is a TMA producer: for
-// each 128-wide K block it loads the int8 boxes W[128 x 128] and A[16 MT x 128] (128-byte
-// swizzle, one full cache line per row; rows past M or N and columns past K arrive as
-// zeros) into a 6-stage ring; two CTAs per SM keep ~200 KB of W in flight per SM.
-// Warps 1-4 each own 32 rows of W: they read 16-byte fragments from shared memory, widen
-// int8 to fp16 exactly in registers and run the fp16 warp MMA (m16n8k16, fp32
-// accumulate; this part's int8 warp MMA is about four times slower). Every partial sum of
-// at most 1024 products of magnitude <= 2^14 is an integer below 2^24, so
-// the fp32 accumulators are exact; they are drained into int32 registers every 1024 K.
-// Split-K parts meet through int32 atomics; the warp that arrives last at its 32-row
-// sub-block finishes it.
+// Two launches per call:
+//   prep    zeroes the split-K workspace and writes an exact fp16 copy of A (tiny: M x K)
+//           into it, so that the main kernel converts only W;
+//   main    launched as a programmatic dependent of prep: its TMA producer starts
+//           streaming W before prep has finished and waits for prep (griddepcontrol)
+//           only before its first A load.
+// Main kernel: persistent (two CTAs per SM up to 32 tokens, else one), each CTA owning an
+// equal contiguous range of the flattened (128-row block of W, 128-wide K block) space.
+// Warp 0, lane 0, is the TMA producer: per K block it loads the int8 box W[128 x 128]
+// (evict-first L2 policy: W is read exactly once) and the fp16 boxes A[16 MT x 64] x 2
+// (128-byte swizzle; rows past M or N and columns past K arrive as zeros) into a ring of
+// stages. The consumer warps each own 128 / SK_CONSUMERS rows of W: they read 16-byte
+// fragments from shared memory, widen the int8 W bytes to fp16 exactly in registers and
+// run the fp16 warp MMA (m16n8k16, fp32 accumulate; this part's int8 warp MMA is about
+// four times slower). Every partial sum of at most 1024 products of magnitude <= 2^14 is
+// an integer below 2^24, so the fp32 accumulators are exact; they are drained into int32
+// registers every 1024 K. The CTAs meet through int32 atomics in the workspace; the warp
+// that arrives last at its row sub-block finishes it.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_fp16.h>
@@ -34,15 +41,24 @@ namespace {
 
 using namespace sm100;
 
-constexpr int SK_ROWS = 128;       // W rows per CTA
+constexpr int SK_ROWS = 128;       // W rows per row block
 constexpr int SK_BK = 128;         // K per stage: one 128-byte line per W row (128-byte swizzle)
-constexpr int SK_STAGES = 6;
-constexpr int SK_CONSUMERS = 4;
+constexpr int SK_CONSUMERS = 8;    // consumer warps per CTA
+constexpr int SK_RPW = SK_ROWS / SK_CONSUMERS;  // W rows per consumer warp
+constexpr int SK_NJ = SK_RPW / 8;               // n8 MMA column groups per consumer warp
 constexpr int SK_THREADS = 32 * (1 + SK_CONSUMERS);
 constexpr int SK_W_BYTES = SK_ROWS * SK_BK;  // 16 KB
 
-__host__ __device__ constexpr int sk_stage_bytes(int MT) { return SK_W_BYTES + 16 * MT * SK_BK; }
-__host__ __device__ constexpr int sk_smem_bytes(int MT) { return SK_STAGES * sk_stage_bytes(MT) + 1024 + 512; }
+// Up to 32 tokens two CTAs share an SM (registers and shared memory allow it); above,
+// the accumulators need the registers of one CTA per SM, which then gets a deeper ring.
+__host__ __device__ constexpr int sk_ctas_per_sm(int MT) { return MT <= 2 ? 2 : 1; }
+__host__ __device__ constexpr int sk_smem_budget(int MT) { return sk_ctas_per_sm(MT) == 2 ? 110 * 1024 : 220 * 1024; }
+__host__ __device__ constexpr int sk_a_box_bytes(int MT) { return 16 * MT * 128; }  // 16 MT rows x 64 fp16
+__host__ __device__ constexpr int sk_stage_bytes(int MT) { return SK_W_BYTES + 2 * sk_a_box_bytes(MT); }
+__host__ __device__ constexpr int sk_stages(int MT) {
+    return (sk_smem_budget(MT) - 1280) / sk_stage_bytes(MT) > 6 ? 6 : (sk_smem_budget(MT) - 1280) / sk_stage_bytes(MT);
+}
+__host__ __device__ constexpr int sk_smem_bytes(int MT) { return sk_stages(MT) * sk_stage_bytes(MT) + 1024 + 256; }
 
 struct SkArgs {
     int M, N, K;
@@ -53,8 +69,25 @@ struct SkArgs {
     int64_t ldc;
     int mode;           // EPI_BF16_POW2 or EPI_STORE_I32
     int32_t* ws_acc;    // [M x N] exact partial sums
-    uint32_t* ws_cnt;   // [n blocks x 4] arrivals
+    uint32_t* ws_cnt;   // [n blocks x consumers] arrivals
 };
+
+// Workspace: [acc: M x N int32][counters][A16: M x lda16 fp16], each part 256-byte aligned.
+struct SkLayout {
+    size_t acc, cnt, a16, total;
+    int64_t lda16;
+};
+
+SkLayout sk_layout(int M, int N, int K) {
+    auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+    SkLayout L;
+    L.lda16 = ((int64_t)K + 7) / 8 * 8;
+    L.acc = 0;
+    L.cnt = up((size_t)M * N * sizeof(int32_t));
+    L.a16 = L.cnt + up((size_t)((N + SK_ROWS - 1) / SK_ROWS) * SK_CONSUMERS * sizeof(uint32_t));
+    L.total = L.a16 + up((size_t)M * L.lda16 * 2);
+    return L;
+}
 
 // byte offset of the 16-byte chunk c of row r in a box of 128-byte rows, 128-byte swizzle
 __device__ __forceinline__ uint32_t sw128(int r, int c) { return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)); }
@@ -77,6 +110,28 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* m, uin
         "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_addr(bar)), "r"(x), "r"(y)
         : "memory");
 }
+
+// L2 policy for the W stream, which nothing re-reads: its lines are evicted first (measured
+// on GB300: a TMA stream of these boxes reaches ~5.5 TB/s with it, ~4.6 TB/s without)
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// tma_load_2d with an L2 cache policy
+__device__ __forceinline__ void tma_load_2d_hint(void* dst, const CUtensorMap* m, uint64_t* bar, int x, int y,
+                                                 uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%3, "
+        "%4}], [%2], %5;" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_addr(bar)), "r"(x), "r"(y), "l"(policy)
+        : "memory");
+}
+
+// programmatic dependent launch: let the dependent grid start / wait for the prerequisite
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 __device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
     asm volatile(
@@ -130,16 +185,49 @@ __device__ __forceinline__ void store_pair(const SkArgs& p, int row, int col, in
 // (range i is [i F / P, (i + 1) F / P))
 __device__ __forceinline__ int owner_of(long long f, long long F, long long P) { return (int)(((f + 1) * P - 1) / F); }
 
+// ---------------------------------------------------------------------------- prep
+// Zeroes `zero_words` 16-byte words at Z and writes Y[r][k] = (fp16) X[r][k] for k < K,
+// zero for K <= k < ldy (ldy a multiple of 8).
+__global__ void __launch_bounds__(256) skinny_prep_kernel(uint4* __restrict__ Z, int64_t zero_words,
+                                                          const int8_t* __restrict__ X, int64_t ldx, int rows, int K,
+                                                          __half* __restrict__ Y, int64_t ldy) {
+    pdl_launch_dependents();
+    const int64_t nt = (int64_t)gridDim.x * blockDim.x;
+    const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    for (int64_t i = tid; i < zero_words; i += nt) Z[i] = make_uint4(0, 0, 0, 0);
+    const int64_t nvec = ldy / 8;
+    for (int64_t v = tid; v < (int64_t)rows * nvec; v += nt) {
+        const int64_t r = v / nvec;
+        const int k = (int)((v - r * nvec) * 8);
+        const int8_t* x = X + r * ldx + k;
+        uint2 w;
+        if (k + 8 <= K) {
+            w = *reinterpret_cast<const uint2*>(x);
+        } else {
+            uint64_t t = 0;
+            for (int i = 0; i < 8 && k + i < K; ++i) t |= (uint64_t)(uint8_t)x[i] << (8 * i);
+            w = make_uint2((uint32_t)t, (uint32_t)(t >> 32));
+        }
+        uint4 o;
+        i8x4_to_f16x4(w.x, o.x, o.y);
+        i8x4_to_f16x4(w.y, o.z, o.w);
+        *reinterpret_cast<uint4*>(Y + r * ldy + k) = o;
+    }
+}
+
+// ---------------------------------------------------------------------------- main
 template <int MT>
-__global__ void __launch_bounds__(SK_THREADS) skinny_kernel(const __grid_constant__ CUtensorMap tmW,
-                                                            const __grid_constant__ CUtensorMap tmA,
-                                                            const __grid_constant__ SkArgs p) {
+__global__ void __launch_bounds__(SK_THREADS, sk_ctas_per_sm(MT)) skinny_kernel(const __grid_constant__ CUtensorMap tmW,
+                                                               const __grid_constant__ CUtensorMap tmA,
+                                                               const __grid_constant__ SkArgs p) {
+    constexpr int STAGES = sk_stages(MT);
+    constexpr int STAGE = sk_stage_bytes(MT);
+    constexpr int ABOX = sk_a_box_bytes(MT);
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    constexpr int STAGE = sk_stage_bytes(MT);
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + SK_STAGES * STAGE);
-    uint64_t* empty = full + SK_STAGES;
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + SK_STAGES);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE);
+    uint64_t* empty = full + STAGES;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + STAGES);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int kbr = (p.K + SK_BK - 1) / SK_BK;  // K blocks per row block
@@ -149,7 +237,7 @@ __global__ void __launch_bounds__(SK_THREADS) skinny_kernel(const __grid_constan
     const int f1 = (int)(((long long)(blockIdx.x + 1) * F) / P);
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < SK_STAGES; ++s) {
+        for (int s = 0; s < STAGES; ++s) {
             mbar_init(full + s, 1);
             mbar_init(empty + s, SK_CONSUMERS);
         }
@@ -162,11 +250,28 @@ __global__ void __launch_bounds__(SK_THREADS) skinny_kernel(const __grid_constan
         if (lane == 0) {
             prefetch_tmap(&tmW);
             prefetch_tmap(&tmA);
-            int stage = 0;
-            uint32_t phase = 0;
-            uint32_t issued = 0;
+            const uint64_t stream_policy = l2_policy_evict_first();
+            // W does not depend on the prep kernel: the first ring's worth of W boxes is
+            // issued before waiting for it, their A boxes after
+            const int pre = (f1 - f0) < STAGES ? (f1 - f0) : STAGES;
+            for (int i = 0; i < pre; ++i) {
+                const int f = f0 + i;
+                const int nb = f / kbr, kb = f - nb * kbr;
+                mbar_arrive_expect_tx(full + i, STAGE);
+                tma_load_2d_hint(smem + i * STAGE, &tmW, full + i, kb * SK_BK, nb * SK_ROWS, stream_policy);
+            }
+            pdl_wait();
+            for (int i = 0; i < pre; ++i) {
+                const int kb = (f0 + i) % kbr;
+                uint8_t* a = smem + i * STAGE + SK_W_BYTES;
+                tma_load_2d(a, &tmA, full + i, kb * SK_BK, 0);
+                tma_load_2d(a + ABOX, &tmA, full + i, kb * SK_BK + 64, 0);
+            }
+            int stage = pre == STAGES ? 0 : pre;
+            uint32_t phase = pre == STAGES ? 1u : 0u;
+            uint32_t issued = pre;
             bool ok = true;
-            for (int f = f0; f < f1; ++f) {
+            for (int f = f0 + pre; f < f1; ++f) {
                 if (!mbar_wait(empty + stage, phase ^ 1u, abort_flag)) {
                     ok = false;
                     break;
@@ -174,21 +279,22 @@ __global__ void __launch_bounds__(SK_THREADS) skinny_kernel(const __grid_constan
                 const int nb = f / kbr, kb = f - nb * kbr;
                 uint8_t* st = smem + stage * STAGE;
                 mbar_arrive_expect_tx(full + stage, STAGE);
-                tma_load_2d(st, &tmW, full + stage, kb * SK_BK, nb * SK_ROWS);
+                tma_load_2d_hint(st, &tmW, full + stage, kb * SK_BK, nb * SK_ROWS, stream_policy);
                 tma_load_2d(st + SK_W_BYTES, &tmA, full + stage, kb * SK_BK, 0);
+                tma_load_2d(st + SK_W_BYTES + ABOX, &tmA, full + stage, kb * SK_BK + 64, 0);
                 ++issued;
-                if (++stage == SK_STAGES) {
+                if (++stage == STAGES) {
                     stage = 0;
                     phase ^= 1u;
                 }
             }
             if (!ok) {
-                uint32_t n = issued < SK_STAGES ? issued : SK_STAGES;
+                uint32_t n = issued < (uint32_t)STAGES ? issued : (uint32_t)STAGES;
                 int s = stage;
                 uint32_t ph = phase;
                 for (uint32_t i = 0; i < n; ++i) {
                     if (--s < 0) {
-                        s = SK_STAGES - 1;
+                        s = STAGES - 1;
                         ph ^= 1u;
                     }
                     mbar_wait_drain(full + s, ph);
@@ -199,7 +305,8 @@ __global__ void __launch_bounds__(SK_THREADS) skinny_kernel(const __grid_constan
     }
 
     // ---------------------------------------------------------------- consumers
-    const int cw = warp - 1;         // rows [32 cw, 32 cw + 32) of the row block
+    pdl_wait();                      // the workspace is zeroed before any atomic below
+    const int cw = warp - 1;         // rows [SK_RPW cw, +SK_RPW) of the row block
     const int g = lane >> 2, t = lane & 3;
     int stage = 0;
     uint32_t phase = 0;
@@ -210,12 +317,12 @@ __global__ void __launch_bounds__(SK_THREADS) skinny_kernel(const __grid_constan
         // one segment: this CTA's K blocks inside row block nb
         const int nb = f / kbr;
         const int fend = min(f1, (nb + 1) * kbr);
-        int32_t acc[MT][4][4];
-        float accf[MT][4][4];
+        int32_t acc[MT][SK_NJ][4];
+        float accf[MT][SK_NJ][4];
 #pragma unroll
         for (int a = 0; a < MT; ++a)
 #pragma unroll
-            for (int b = 0; b < 4; ++b)
+            for (int b = 0; b < SK_NJ; ++b)
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     acc[a][b][c] = 0;
@@ -223,41 +330,38 @@ __global__ void __launch_bounds__(SK_THREADS) skinny_kernel(const __grid_constan
                 }
         int since = 0;
         for (; f < fend; ++f) {
-            // lane 0 polls; after it has seen the phase complete, every lane confirms with one
-            // try_wait of its own (the acquire that makes the TMA-written bytes visible to it)
-            bool got = lane == 0 ? mbar_wait(full + stage, phase, abort_flag) : true;
-            got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
+            // every lane waits (and so acquires the TMA-written bytes) itself
+            const bool got = __all_sync(0xffffffffu, mbar_wait(full + stage, phase, abort_flag));
             if (!got) {
                 ok = false;
                 break;
             }
-            for (int spin = 0; !mbar_try_wait(smem_addr(full + stage), phase); ++spin) {
-                if (spin > (1 << 20)) {  // cannot happen once lane 0 saw the phase; bounded anyway
-                    *abort_flag = 1;
-                    break;
-                }
-            }
             const uint32_t wb = sbase + stage * STAGE;
             const uint32_t ab = wb + SK_W_BYTES;
-            // lane (g, t) takes the 16-byte chunks t and t + 4 of each 128-byte row: 32 k values
+            // lane (g, t) takes the 16-byte W chunks t and t + 4 of each 128-byte row (16 k
+            // values each); the matching 16 k of A are the fp16 chunks 2t, 2t + 1 of A box `half`
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
                 const int c = t + 4 * half;
-                uint32_t hw[4][8];
+                uint32_t hw[SK_NJ][8];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) i8x16_to_f16x16(lds16(wb + sw128(32 * cw + 8 * j + g, c)), hw[j]);
+                for (int j = 0; j < SK_NJ; ++j) i8x16_to_f16x16(lds16(wb + sw128(SK_RPW * cw + 8 * j + g, c)), hw[j]);
 #pragma unroll
                 for (int mt = 0; mt < MT; ++mt) {
-                    uint32_t h0[8], h1[8];
-                    i8x16_to_f16x16(lds16(ab + sw128(16 * mt + g, c)), h0);
-                    i8x16_to_f16x16(lds16(ab + sw128(16 * mt + g + 8, c)), h1);
+                    const uint32_t abox = ab + half * ABOX;
+                    const uint4 x0 = lds16(abox + sw128(16 * mt + g, 2 * t));
+                    const uint4 x1 = lds16(abox + sw128(16 * mt + g, 2 * t + 1));
+                    const uint4 y0 = lds16(abox + sw128(16 * mt + g + 8, 2 * t));
+                    const uint4 y1 = lds16(abox + sw128(16 * mt + g + 8, 2 * t + 1));
+                    const uint32_t h0[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+                    const uint32_t h1[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
                     // the chunk's 16 k values feed four k16 MMAs with the same k slots for A and
                     // W: logical (2t + j) <- 4q + j, (2t + 8 + j) <- 4q + 2 + j within the chunk
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         const uint32_t a[4] = {h0[2 * q], h1[2 * q], h0[2 * q + 1], h1[2 * q + 1]};
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) mma_f16(accf[mt][j], a, hw[j][2 * q], hw[j][2 * q + 1]);
+                        for (int j = 0; j < SK_NJ; ++j) mma_f16(accf[mt][j], a, hw[j][2 * q], hw[j][2 * q + 1]);
                     }
                 }
             }
@@ -268,7 +372,7 @@ __global__ void __launch_bounds__(SK_THREADS) skinny_kernel(const __grid_constan
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             __syncwarp();
             if (lane == 0) mbar_arrive(empty + stage);
-            if (++stage == SK_STAGES) {
+            if (++stage == STAGES) {
                 stage = 0;
                 phase ^= 1u;
             }
@@ -276,7 +380,7 @@ __global__ void __launch_bounds__(SK_THREADS) skinny_kernel(const __grid_constan
 #pragma unroll
                 for (int a = 0; a < MT; ++a)
 #pragma unroll
-                    for (int b = 0; b < 4; ++b)
+                    for (int b = 0; b < SK_NJ; ++b)
 #pragma unroll
                         for (int c = 0; c < 4; ++c) {
                             acc[a][b][c] += __float2int_rn(accf[a][b][c]);
@@ -289,18 +393,18 @@ __global__ void __launch_bounds__(SK_THREADS) skinny_kernel(const __grid_constan
 #pragma unroll
         for (int a = 0; a < MT; ++a)
 #pragma unroll
-            for (int b = 0; b < 4; ++b)
+            for (int b = 0; b < SK_NJ; ++b)
 #pragma unroll
                 for (int c = 0; c < 4; ++c) acc[a][b][c] += __float2int_rn(accf[a][b][c]);
 
         // exact partial of this segment -> workspace; the warp that completes the row block's
         // count (one arrival per CTA whose range touches it) finishes it.
-        // accumulator (mt, j, e): row 16 mt + g (+8 for e >= 2), column 128 nb + 32 cw + 8 j + 2 t (+1 odd e)
-        const int nc = nb * SK_ROWS + 32 * cw;
+        // accumulator (mt, j, e): row 16 mt + g (+8 for e >= 2), column 128 nb + SK_RPW cw + 8 j + 2 t (+1 odd e)
+        const int nc = nb * SK_ROWS + SK_RPW * cw;
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
+            for (int j = 0; j < SK_NJ; ++j)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int row = 16 * mt + g + 8 * (e >> 1), col = nc + 8 * j + 2 * t + (e & 1);
@@ -317,7 +421,7 @@ __global__ void __launch_bounds__(SK_THREADS) skinny_kernel(const __grid_constan
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
+            for (int j = 0; j < SK_NJ; ++j)
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const int row = 16 * mt + g + 8 * h, col = nc + 8 * j + 2 * t;
@@ -334,10 +438,10 @@ __global__ void __launch_bounds__(SK_THREADS) skinny_kernel(const __grid_constan
         if (lane == 0) {
             int s = stage;
             uint32_t ph = phase;
-            const int n = (f1 - f0) < SK_STAGES ? (f1 - f0) : SK_STAGES;
+            const int n = (f1 - f0) < STAGES ? (f1 - f0) : STAGES;
             for (int i = 0; i < n; ++i) {
                 mbar_wait_drain(full + s, ph, kDrainLimitNs);
-                if (++s == SK_STAGES) {
+                if (++s == STAGES) {
                     s = 0;
                     ph ^= 1u;
                 }
@@ -349,7 +453,10 @@ __global__ void __launch_bounds__(SK_THREADS) skinny_kernel(const __grid_constan
 std::mutex g_sk_mutex;
 PFN_cuTensorMapEncodeTiled_v12000 g_sk_encode = nullptr;
 
-cudaError_t sk_map(CUtensorMap* m, const void* base, int K, int64_t ld, int rows, int box_rows) {
+// 2-D map over a row-major matrix [rows x cols] of `esize`-byte elements with row stride
+// `ld` elements; box {128 bytes, box_rows}, 128-byte swizzle, zero fill out of bounds
+cudaError_t sk_map(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* base, int cols, int64_t ld,
+                   int rows, int box_rows) {
     {
         std::lock_guard<std::mutex> lock(g_sk_mutex);
         if (!g_sk_encode) {
@@ -360,13 +467,13 @@ cudaError_t sk_map(CUtensorMap* m, const void* base, int K, int64_t ld, int rows
             g_sk_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
         }
     }
-    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)ld};
-    cuuint32_t box[2] = {(cuuint32_t)SK_BK, (cuuint32_t)box_rows};
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)ld * (cuuint64_t)esize};
+    cuuint32_t box[2] = {(cuuint32_t)(128 / esize), (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = g_sk_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-                             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = g_sk_encode(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
@@ -390,21 +497,34 @@ cudaError_t sk_launch_mt(const CUtensorMap& tmW, const CUtensorMap& tmA, const S
     const int smem = sk_smem_bytes(MT);
     cudaError_t e = cudaFuncSetAttribute(skinny_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    // two CTAs per SM (the shared-memory ring allows two), each streaming an equal share
+    // persistent: every CTA resident at once (sk_ctas_per_sm per SM), each streaming an equal share
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, skinny_kernel<MT>, SK_THREADS, (size_t)smem);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) return cudaErrorInvalidConfiguration;
+    if (per_sm > sk_ctas_per_sm(MT)) per_sm = sk_ctas_per_sm(MT);
     const long long blocks = (long long)a.nblocks * ((a.K + SK_BK - 1) / SK_BK);
-    long long grid = 2LL * sk_num_sms();
+    long long grid = (long long)per_sm * sk_num_sms();
     if (grid > blocks) grid = blocks;
-    skinny_kernel<MT><<<(unsigned)grid, SK_THREADS, smem, s>>>(tmW, tmA, a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(SK_THREADS);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, skinny_kernel<MT>, tmW, tmA, a);
 }
 
 }  // namespace
 
-size_t skinny_workspace_bytes(int M, int N, int split) {
+size_t skinny_workspace_bytes(int M, int N, int K, int split) {
     (void)split;
     if (M == 0 || N == 0) return 0;
-    size_t acc = ((size_t)M * N * sizeof(int32_t) + 255) & ~(size_t)255;
-    return acc + (size_t)((N + SK_ROWS - 1) / SK_ROWS) * SK_CONSUMERS * sizeof(uint32_t);
+    return sk_layout(M, N, K).total;
 }
 
 cudaError_t skinny_launch(const int8_t* A, int64_t lda, const int8_t* W, int64_t ldw, const int32_t* ea,
@@ -413,6 +533,8 @@ cudaError_t skinny_launch(const int8_t* A, int64_t lda, const int8_t* W, int64_t
     (void)split;  // the kernel divides K among the SMs itself; the bits never depend on it
     if (M == 0 || N == 0) return cudaSuccess;
     const int MT = (M + 15) / 16;
+    const SkLayout L = sk_layout(M, N, K);
+    char* base = reinterpret_cast<char*>(ws);
     SkArgs a = {};
     a.M = M;
     a.N = N;
@@ -423,14 +545,22 @@ cudaError_t skinny_launch(const int8_t* A, int64_t lda, const int8_t* W, int64_t
     a.C = reinterpret_cast<uint16_t*>(C);
     a.ldc = ldc;
     a.mode = mode;
+    a.ws_acc = reinterpret_cast<int32_t*>(base + L.acc);
+    a.ws_cnt = reinterpret_cast<uint32_t*>(base + L.cnt);
+    __half* A16 = reinterpret_cast<__half*>(base + L.a16);
     CUtensorMap tmW, tmA;
-    cudaError_t e = sk_map(&tmW, W, K, ldw, N, SK_ROWS);
-    if (e == cudaSuccess) e = sk_map(&tmA, A, K, lda, M, 16 * MT);
+    cudaError_t e = sk_map(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, W, K, ldw, N, SK_ROWS);
+    if (e == cudaSuccess) e = sk_map(&tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, A16, K, L.lda16, M, 16 * MT);
     if (e != cudaSuccess) return e;
-    size_t accb = (((size_t)M * N * sizeof(int32_t)) + 255) & ~(size_t)255;
-    a.ws_acc = reinterpret_cast<int32_t*>(ws);
-    a.ws_cnt = reinterpret_cast<uint32_t*>(reinterpret_cast<char*>(ws) + accb);
-    e = cudaMemsetAsync(ws, 0, skinny_workspace_bytes(M, N, 1), s);
+    // prep: zero [acc, counters], widen A into the workspace
+    const int64_t zero_words = (int64_t)(L.a16 / 16);
+    const int64_t work = zero_words + (int64_t)M * (L.lda16 / 8);
+    int64_t blocks = (work + 255) / 256;
+    const int64_t cap = (int64_t)sk_num_sms() * 4;
+    if (blocks > cap) blocks = cap;
+    skinny_prep_kernel<<<(unsigned)blocks, 256, 0, s>>>(reinterpret_cast<uint4*>(base), zero_words, A, lda, M, K, A16,
+                                                        L.lda16);
+    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     switch (MT) {
         case 1: return sk_launch_mt<1>(tmW, tmA, a, s);

@@ -33,7 +33,7 @@ struct IGemmArgs {
 };
 
 // Decode-shaped (M <= 64) exact int8 GEMM streaming W through a TMA ring (gemm_skinny.cu).
-size_t skinny_workspace_bytes(int M, int N, int split);
+size_t skinny_workspace_bytes(int M, int N, int K, int split);
 cudaError_t skinny_launch(const int8_t* A, int64_t lda, const int8_t* W, int64_t ldw, const int32_t* ea,
                           const int32_t* ew, void* C, int64_t ldc, int mode, int M, int N, int K, int split, void* ws,
                           cudaStream_t s);
@@ -41,7 +41,7 @@ cudaError_t skinny_take_status(uint32_t* bits);
 
 // Integer GEMM on the mma.sync int8 path (exact int32 accumulation); M <= 64 is routed to
 // skinny_launch.
-size_t igemm_workspace_bytes(int M, int N, int split);
+size_t igemm_workspace_bytes(int M, int N, int K, int split);
 cudaError_t igemm_launch(const IGemmArgs& a, void* ws, cudaStream_t s);
 
 // Pow2 quantizer and Ozaki slicer.

@@ -74,7 +74,7 @@ extern "C" DETGEMM_API detgemm_status detgemm_w8a8_noalloc(const int8_t* A, int6
     if (lda < K || ldw < K || ldc < N) return DETGEMM_ERR_INVALID_ARG;
     if (!al16(A) || !al16(W) || !al16(C) || !al4(ea) || !al4(ew)) return DETGEMM_ERR_ALIGNMENT;
     if ((lda % 16) != 0 || (ldw % 16) != 0 || ((ldc * 2) % 16) != 0) return DETGEMM_ERR_ALIGNMENT;
-    if (igemm_workspace_bytes(M, N, split_k) > (size_t)DETGEMM_NOALLOC_SCRATCH_BYTES)
+    if (igemm_workspace_bytes(M, N, K, split_k) > (size_t)DETGEMM_NOALLOC_SCRATCH_BYTES)
         return DETGEMM_ERR_WORKSPACE;  // the problem needs more scratch than the fixed array holds
     void* scratch = nullptr;
     detgemm_status st = noalloc_scratch(&scratch);
