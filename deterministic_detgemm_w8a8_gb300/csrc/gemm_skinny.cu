@@ -5,12 +5,15 @@
 // at most 128 multiply-adds per W byte, so the kernel is bound by reading W once from
 // HBM; its job is to keep enough bytes in flight and to spend few instructions per byte.
 //
-// Two launches per call:
-//   prep    zeroes the split-K workspace and writes an exact fp16 copy of A (tiny: M x K)
-//           into it, so that the main kernel converts only W;
-//   main    launched as a programmatic dependent of prep: its TMA producer starts
-//           streaming W before prep has finished and waits for prep (griddepcontrol)
-//           only before its first A load.
+// Three launches per call, chained by programmatic dependent launch (each starts while
+// its predecessor runs and waits for it with griddepcontrol.wait where it needs its data):
+//   prep    zeroes the int32 accumulator workspace and writes an exact fp16 copy of A
+//           (tiny: M x K) into it, so that the main kernel converts only W;
+//   main    streams W and adds its exact partial sums into the workspace with int32
+//           atomics; its TMA producer starts on W before prep has finished and waits for
+//           prep only before its first A load;
+//   finish  once main has completed (all partial sums performed), rounds each sum to bf16
+//           (or stores it as int32).
 // Main kernel: persistent (two CTAs per SM up to 32 tokens, else one), each CTA owning an
 // equal contiguous range of the flattened (128-row block of W, 128-wide K block) space.
 // Warp 0, lane 0, is the TMA producer: per K block it loads the int8 box W[128 x 128]
@@ -21,8 +24,8 @@
 // run the fp16 warp MMA (m16n8k16, fp32 accumulate; this part's int8 warp MMA is about
 // four times slower). Every partial sum of at most 1024 products of magnitude <= 2^14 is
 // an integer below 2^24, so the fp32 accumulators are exact; they are drained into int32
-// registers every 1024 K. The CTAs meet through int32 atomics in the workspace; the warp
-// that arrives last at its row sub-block finishes it.
+// registers every 1024 K. The CTAs meet through int32 atomics in the workspace (integer
+// addition: the order in which they land cannot change the sum).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_fp16.h>
@@ -30,6 +33,7 @@
 #include <stdint.h>
 
 #include <mutex>
+#include <utility>
 
 #include "common.cuh"
 #include "internal.h"
@@ -68,13 +72,13 @@ struct SkArgs {
     uint16_t* C;
     int64_t ldc;
     int mode;           // EPI_BF16_POW2 or EPI_STORE_I32
-    int32_t* ws_acc;    // [M x N] exact partial sums
-    uint32_t* ws_cnt;   // [n blocks x consumers] arrivals
+    int32_t* ws_acc;    // [N x M] exact sums (token-contiguous: one warp atomic covers 8
+                        // consecutive tokens of 4 columns)
 };
 
-// Workspace: [acc: M x N int32][counters][A16: M x lda16 fp16], each part 256-byte aligned.
+// Workspace: [acc: N x M int32][A16: M x lda16 fp16], each part 256-byte aligned.
 struct SkLayout {
-    size_t acc, cnt, a16, total;
+    size_t acc, a16, total;
     int64_t lda16;
 };
 
@@ -83,8 +87,7 @@ SkLayout sk_layout(int M, int N, int K) {
     SkLayout L;
     L.lda16 = ((int64_t)K + 7) / 8 * 8;
     L.acc = 0;
-    L.cnt = up((size_t)M * N * sizeof(int32_t));
-    L.a16 = L.cnt + up((size_t)((N + SK_ROWS - 1) / SK_ROWS) * SK_CONSUMERS * sizeof(uint32_t));
+    L.a16 = up((size_t)M * N * sizeof(int32_t));
     L.total = L.a16 + up((size_t)M * L.lda16 * 2);
     return L;
 }
@@ -181,9 +184,6 @@ __device__ __forceinline__ void store_pair(const SkArgs& p, int row, int col, in
     }
 }
 
-// CTA that owns flattened K block f when F blocks are cut into P equal contiguous ranges
-// (range i is [i F / P, (i + 1) F / P))
-__device__ __forceinline__ int owner_of(long long f, long long F, long long P) { return (int)(((f + 1) * P - 1) / F); }
 
 // ---------------------------------------------------------------------------- prep
 // Zeroes `zero_words` 16-byte words at Z and writes Y[r][k] = (fp16) X[r][k] for k < K,
@@ -243,6 +243,7 @@ __global__ void __launch_bounds__(SK_THREADS, sk_ctas_per_sm(MT)) skinny_kernel(
         }
         *abort_flag = 0;
         fence_mbar_init();
+        pdl_launch_dependents();  // the finish kernel may be scheduled; it waits for this grid
     }
     __syncthreads();
 
@@ -397,8 +398,7 @@ __global__ void __launch_bounds__(SK_THREADS, sk_ctas_per_sm(MT)) skinny_kernel(
 #pragma unroll
                 for (int c = 0; c < 4; ++c) acc[a][b][c] += __float2int_rn(accf[a][b][c]);
 
-        // exact partial of this segment -> workspace; the warp that completes the row block's
-        // count (one arrival per CTA whose range touches it) finishes it.
+        // exact partial of this segment -> workspace
         // accumulator (mt, j, e): row 16 mt + g (+8 for e >= 2), column 128 nb + SK_RPW cw + 8 j + 2 t (+1 odd e)
         const int nc = nb * SK_ROWS + SK_RPW * cw;
 #pragma unroll
@@ -408,29 +408,7 @@ __global__ void __launch_bounds__(SK_THREADS, sk_ctas_per_sm(MT)) skinny_kernel(
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int row = 16 * mt + g + 8 * (e >> 1), col = nc + 8 * j + 2 * t + (e & 1);
-                    if (row < p.M && col < p.N) atomicAdd(p.ws_acc + (int64_t)row * p.N + col, acc[mt][j][e]);
-                }
-        __threadfence();
-        __syncwarp();
-        const int expected = owner_of((long long)(nb + 1) * kbr - 1, F, P) - owner_of((long long)nb * kbr, F, P) + 1;
-        unsigned prev = 0;
-        if (lane == 0) prev = atomicAdd(p.ws_cnt + nb * SK_CONSUMERS + cw, 1u);
-        prev = __shfl_sync(0xffffffffu, prev, 0);
-        if (prev != (unsigned)(expected - 1)) continue;
-        __threadfence();
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-            for (int j = 0; j < SK_NJ; ++j)
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int row = 16 * mt + g + 8 * h, col = nc + 8 * j + 2 * t;
-                    int32_t v0 = 0, v1 = 0;
-                    if (row < p.M && col < p.N) {
-                        v0 = __ldcg(p.ws_acc + (int64_t)row * p.N + col);
-                        if (col + 1 < p.N) v1 = __ldcg(p.ws_acc + (int64_t)row * p.N + col + 1);
-                    }
-                    store_pair(p, row, col, v0, v1);
+                    if (row < p.M && col < p.N) atomicAdd(p.ws_acc + (int64_t)col * p.M + row, acc[mt][j][e]);
                 }
     }
     if (!ok) {
@@ -448,6 +426,37 @@ __global__ void __launch_bounds__(SK_THREADS, sk_ctas_per_sm(MT)) skinny_kernel(
             }
         }
     }
+}
+
+// ---------------------------------------------------------------------------- finish
+// C[row][col] from the exact sums, two columns per thread; waits for the main kernel.
+__global__ void __launch_bounds__(256) skinny_finish_kernel(const __grid_constant__ SkArgs p) {
+    pdl_wait();
+    const int half_n = (p.N + 1) / 2;
+    const int64_t total = (int64_t)p.M * half_n;
+    for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < total; v += (int64_t)gridDim.x * blockDim.x) {
+        const int row = (int)(v / half_n);
+        const int col = 2 * (int)(v - (int64_t)row * half_n);
+        const int32_t v0 = __ldcg(p.ws_acc + (int64_t)col * p.M + row);
+        const int32_t v1 = col + 1 < p.N ? __ldcg(p.ws_acc + (int64_t)(col + 1) * p.M + row) : 0;
+        store_pair(p, row, col, v0, v1);
+    }
+}
+
+// launch with the programmatic-stream-serialization attribute (may overlap the kernel before)
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 std::mutex g_sk_mutex;
@@ -506,17 +515,12 @@ cudaError_t sk_launch_mt(const CUtensorMap& tmW, const CUtensorMap& tmA, const S
     const long long blocks = (long long)a.nblocks * ((a.K + SK_BK - 1) / SK_BK);
     long long grid = (long long)per_sm * sk_num_sms();
     if (grid > blocks) grid = blocks;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3(SK_THREADS);
-    cfg.dynamicSmemBytes = (size_t)smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, skinny_kernel<MT>, tmW, tmA, a);
+    e = launch_pdl(skinny_kernel<MT>, dim3((unsigned)grid), dim3(SK_THREADS), (size_t)smem, s, tmW, tmA, a);
+    if (e != cudaSuccess) return e;
+    const int64_t pairs = (int64_t)a.M * ((a.N + 1) / 2);
+    int64_t fblocks = (pairs + 255) / 256;
+    if (fblocks > (int64_t)sk_num_sms()) fblocks = sk_num_sms();
+    return launch_pdl(skinny_finish_kernel, dim3((unsigned)fblocks), dim3(256), 0, s, a);
 }
 
 }  // namespace
@@ -546,13 +550,12 @@ cudaError_t skinny_launch(const int8_t* A, int64_t lda, const int8_t* W, int64_t
     a.ldc = ldc;
     a.mode = mode;
     a.ws_acc = reinterpret_cast<int32_t*>(base + L.acc);
-    a.ws_cnt = reinterpret_cast<uint32_t*>(base + L.cnt);
     __half* A16 = reinterpret_cast<__half*>(base + L.a16);
     CUtensorMap tmW, tmA;
     cudaError_t e = sk_map(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, W, K, ldw, N, SK_ROWS);
     if (e == cudaSuccess) e = sk_map(&tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, A16, K, L.lda16, M, 16 * MT);
     if (e != cudaSuccess) return e;
-    // prep: zero [acc, counters], widen A into the workspace
+    // prep: zero the accumulators, widen A into the workspace
     const int64_t zero_words = (int64_t)(L.a16 / 16);
     const int64_t work = zero_words + (int64_t)M * (L.lda16 / 8);
     int64_t blocks = (work + 255) / 256;
