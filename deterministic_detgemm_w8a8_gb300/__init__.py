@@ -13,6 +13,7 @@ Functions mirror the C entry points:
 * :func:`quantize_pow2`  per-row power-of-two scale and int8 values
 * :func:`slice_f32`      Ozaki digit planes with shared exponents
 * :func:`ozaki_f32`      Ozaki-scheme fp32 GEMM C = A B
+* :func:`ozaki_combine`  its fixed-order fp64 recombination step alone
 """
 from __future__ import annotations
 
@@ -45,6 +46,7 @@ SIGNATURES = {
     "detgemm_slice_f32": ([_P, _I64, _I32, _I32, _I32, _I32, _P, _P, _P], _I32),
     "detgemm_ozaki_f32": ([_P, _I64, _P, _I64, _P, _I64, _I32, _I32, _I32, _I32, _I32, _I32, _P, _SZ, _P], _I32),
     "detgemm_ozaki_workspace_size": ([_I32, _I32, _I32, _I32, _I32, _I32], _SZ),
+    "detgemm_ozaki_combine": ([_P, _I64, _I32, _P, _P, _P, _I64, _I32, _I32, _P], _I32),
     "detgemm_get_device_status": ([_P], _I32),
     "detgemm_w8a8_noalloc": ([_P, _I64, _P, _I64, _P, _P, _P, _I64, _I32, _I32, _I32, _I32, _P], _I32),
     "detgemm_widen_i8_f16": ([_P, _I64, _I32, _I32, _P, _I64, _P], _I32),
@@ -235,6 +237,25 @@ def ozaki_f32(A, B, nslices: int = 7, max_diag: int = 8, split_k: int = 1, out=N
                                M, N, K, nslices, max_diag, split_k,
                                wsb.data_ptr() if wsb is not None else None, wsn, _stream(stream))
     _check(st, "detgemm_ozaki_f32")
+    return out
+
+
+def ozaki_combine(T, e, f, out=None, stream=None) -> torch.Tensor:
+    """Fixed-order recombination of exact diagonal sums: T int32 [max_diag - 1, M, N]
+    (plane p holds the diagonal g = max_diag - p), e int32 [M], f int32 [N] -> fp32 [M, N]."""
+    lib = load()
+    _req(T, torch.int32, "T"); _req(e, torch.int32, "e"); _req(f, torch.int32, "f")
+    if T.dim() != 3 or T.stride(2) != 1 or T.stride(0) != T.shape[1] * T.stride(1):
+        raise ValueError("T must be [planes, M, N] with contiguous rows and planes")
+    nd, M, N = T.shape
+    if e.shape != (M,) or f.shape != (N,):
+        raise ValueError("shape mismatch")
+    if out is None:
+        out = empty2d(M, N, torch.float32, T.device)
+    _req(out, torch.float32, "out")
+    st = lib.detgemm_ozaki_combine(T.data_ptr(), T.stride(1), nd + 1, e.data_ptr(), f.data_ptr(), out.data_ptr(),
+                                   _ld(out), M, N, _stream(stream))
+    _check(st, "detgemm_ozaki_combine")
     return out
 
 

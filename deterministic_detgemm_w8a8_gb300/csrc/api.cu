@@ -303,6 +303,19 @@ detgemm_status detgemm_ozaki_f32(const float* A, int64_t lda, const float* B, in
     return from_cuda(err);
 }
 
+detgemm_status detgemm_ozaki_combine(const int32_t* T, int64_t ldT, int max_diag, const int32_t* e,
+                                     const int32_t* f, float* C, int64_t ldc, int M, int N,
+                                     detgemm_stream_t stream) {
+    if (M < 0 || N < 0 || max_diag < 2 || max_diag > 18) return DETGEMM_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return DETGEMM_OK;
+    if (!T || !e || !f || !C || ldT < N || ldc < N) return DETGEMM_ERR_INVALID_ARG;
+    if (!aligned16(T) || !aligned16(C) || !aligned4(e) || !aligned4(f)) return DETGEMM_ERR_ALIGNMENT;
+    if ((ldT * 4) % 16 || (ldc * 4) % 16) return DETGEMM_ERR_ALIGNMENT;
+    detgemm_status st = check_device();
+    if (st != DETGEMM_OK) return st;
+    return from_cuda(ozaki_combine_launch(T, ldT, max_diag, e, f, C, ldc, M, N, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 detgemm_status detgemm_widen_i8_f16(const int8_t* X, int64_t ldx, int rows, int cols, uint16_t* Y, int64_t ldy,
                                     detgemm_stream_t stream) {
     if (rows < 0 || cols < 0) return DETGEMM_ERR_INVALID_ARG;

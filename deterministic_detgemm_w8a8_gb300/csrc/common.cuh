@@ -106,9 +106,9 @@ __device__ __forceinline__ double pow2_f64(int k) {
 __device__ __forceinline__ float ozaki_combine(const int32_t* T, int max_diag, int32_t ei, int32_t fj) {
     double acc = 0.0;
     for (int g = max_diag; g >= 2; --g) acc = __dadd_rn(acc, __dmul_rn((double)T[g], pow2_f64(-7 * g)));
-    int k = ei + fj;
+    long long k = (long long)ei + (long long)fj;
     k = k > 300 ? 300 : (k < -300 ? -300 : k);
-    return __double2float_rn(__dmul_rn(acc, pow2_f64(k)));
+    return __double2float_rn(__dmul_rn(acc, pow2_f64((int)k)));
 }
 
 // |x| of an fp32 bit pattern normalised to x = M * 2^(p - 23), M in [2^23, 2^24).

@@ -1,14 +1,28 @@
 // Ozaki recombination — "GPU Mechanism", §3 "Method", Interventions (a) ExactGEMM:
 // the exact diagonal sums are recombined in a fixed order in fp64 and rounded once.
 //
-//   acc = 0.0;  for g = max_diag .. 2:  acc = acc + T_g * 2^(-7g);
+//   acc = 0.0;  for g = D .. 2:  acc = acc + T_g * 2^(-7g);      (D = max_diag; fp64, RNE)
 //   C_ij = fp32_rne(acc * 2^(e_i + f_j)).
 //
-// One thread per output element; T is [max_diag - 1][M][ldT] int32, plane d holding the
-// diagonal g = max_diag - d. The
-// loads of each plane are coalesced along N. Traffic per element: 4 (max_diag - 1) B
-// read + 4 B written; fp64 work: max_diag - 1 multiply-adds, issued as separate
-// round-to-nearest multiply and add (the multiply by a power of two is exact).
+// T is [D - 1][M][ldT] int32, plane d holding the diagonal g = D - d.
+//
+// GB300 issues fp64 arithmetic at a small fraction of its integer rate (the direct fp64
+// form of this loop made the kernel bound by its ~23 fp64 operations per element, not by
+// memory), so for D <= 13 the same roundings are reproduced with integer arithmetic:
+// every value the fp64 loop produces is an integer multiple of 2^(-7D), so at the scale
+// 2^(7D) the loop is
+//     Z = 0;  for g = D .. 2:  Z = rne53(Z + T_g * 2^(7 (D - g)))
+// where rne53 rounds an integer to 53 significant bits, half to even — exactly what one
+// fp64 addition of two exact operands does (no intermediate can be subnormal: a nonzero
+// |value| is at least 2^(-7D) >= 2^-91, and at most 2^108 < 2^127 fits a signed 128-bit
+// integer for D <= 13). The first four sums are below 2^53 and need no rounding. The
+// result Z * 2^(e_i + f_j - 7D) is then rounded once to fp32 (subnormals kept, overflow
+// to infinity) by integer construction, as the fp64 product and the fp32 conversion do:
+// the product is exact in fp64 because it stays inside fp64's normal range. For D > 13
+// the loop runs in fp64 directly.
+//
+// Traffic per element: 4 (D - 1) B read + 4 B written; each thread takes four
+// consecutive columns (16-byte loads and stores).
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -19,9 +33,119 @@ namespace detgemm {
 
 namespace {
 
-__global__ void ozaki_combine_kernel(const int32_t* __restrict__ T, int64_t ldT, int max_diag,
-                                     const int32_t* __restrict__ e, const int32_t* __restrict__ f,
-                                     float* __restrict__ C, int64_t ldc, int M, int N) {
+typedef unsigned __int128 u128;
+typedef __int128 i128;
+
+__device__ __forceinline__ int bitlen128(u128 m) {
+    const uint64_t hi = (uint64_t)(m >> 64), lo = (uint64_t)m;
+    return hi ? 128 - __clzll((long long)hi) : 64 - __clzll((long long)lo);
+}
+
+// |x| rounded to 53 significant bits, ties to even (x unchanged below 2^53)
+__device__ __forceinline__ i128 rne53(i128 x) {
+    const bool neg = x < 0;
+    const u128 m = neg ? (u128)0 - (u128)x : (u128)x;
+    const int nb = bitlen128(m);
+    if (nb <= 53) return x;
+    const int sh = nb - 53;
+    uint64_t q = (uint64_t)(m >> sh);
+    const u128 rem = m - ((u128)q << sh);
+    const u128 half = (u128)1 << (sh - 1);
+    q += (uint64_t)((rem > half) | ((rem == half) & (q & 1u)));
+    const u128 r = (u128)q << sh;
+    return neg ? -(i128)r : (i128)r;
+}
+
+// fp32 round-to-nearest-even of Z * 2^s (Z an integer, |Z| < 2^127), subnormals kept,
+// overflow to infinity; +0 for Z == 0
+__device__ __forceinline__ float f32_from_i128_pow2(i128 Z, int s) {
+    if (Z == 0) return 0.0f;
+    const uint32_t sign = Z < 0 ? 0x80000000u : 0u;
+    const u128 m = Z < 0 ? (u128)0 - (u128)Z : (u128)Z;
+    const int nb = bitlen128(m);
+    const int E = nb - 1 + s;  // exponent of the leading bit
+    if (E > 127) return __uint_as_float(sign | 0x7F800000u);
+    int sh;
+    uint32_t base;
+    if (E >= -126) {
+        sh = nb - 24;
+        base = (uint32_t)(E + 126) << 23;  // (biased exponent - 1): q carries the leading one
+    } else {
+        sh = -149 - s;                      // subnormal: units of 2^-149
+        base = 0u;
+    }
+    uint32_t q;
+    if (sh <= 0) {
+        q = (uint32_t)m << (-sh);  // m < 2^24 here
+    } else if (sh > nb) {
+        q = 0u;  // below half a unit
+    } else {
+        const u128 qq = m >> sh;
+        const u128 rem = m - (qq << sh);
+        const u128 half = (u128)1 << (sh - 1);
+        q = (uint32_t)qq + (uint32_t)((rem > half) | ((rem == half) & ((uint32_t)qq & 1u)));
+    }
+    uint32_t bits = base + q;
+    if (bits >= 0x7F800000u) bits = 0x7F800000u;
+    return __uint_as_float(sign | bits);
+}
+
+// the fixed-order combine of one element; t[d] = T_(D - d)
+template <int D>
+__device__ __forceinline__ float combine_int(const int32_t (&t)[D - 1], int32_t ei, int32_t fj) {
+    long long x = 0;
+    constexpr int EXACT = D - 1 < 4 ? D - 1 : 4;
+#pragma unroll
+    for (int d = 0; d < EXACT; ++d) x += (long long)t[d] * (1ll << (7 * d));  // |x| < 2^53: no rounding
+    i128 Z = x;
+#pragma unroll
+    for (int d = EXACT; d < D - 1; ++d) Z = rne53(Z + (i128)((u128)(i128)t[d] << (7 * d)));
+    long long k = (long long)ei + (long long)fj;
+    k = k > 300 ? 300 : (k < -300 ? -300 : k);
+    return f32_from_i128_pow2(Z, (int)k - 7 * D);
+}
+
+template <int D>
+__global__ void __launch_bounds__(256) ozaki_combine_int_kernel(const int32_t* __restrict__ T, int64_t ldT,
+                                                                const int32_t* __restrict__ e,
+                                                                const int32_t* __restrict__ f, float* __restrict__ C,
+                                                                int64_t ldc, int M, int N) {
+    const int j0 = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
+    const int i = blockIdx.y;
+    if (j0 >= N || i >= M) return;
+    const int64_t plane = (int64_t)M * ldT;
+    const int64_t idx = (int64_t)i * ldT + j0;
+    const int32_t ei = __ldg(e + i);
+    float* c = C + (int64_t)i * ldc + j0;
+    if (j0 + 4 <= N) {
+        int4 v[D - 1];
+#pragma unroll
+        for (int d = 0; d < D - 1; ++d) v[d] = __ldcs(reinterpret_cast<const int4*>(T + d * plane + idx));
+        const int4 fv = __ldg(reinterpret_cast<const int4*>(f + j0));
+        float out[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            int32_t t[D - 1];
+#pragma unroll
+            for (int d = 0; d < D - 1; ++d) t[d] = q == 0 ? v[d].x : q == 1 ? v[d].y : q == 2 ? v[d].z : v[d].w;
+            const int32_t fj = q == 0 ? fv.x : q == 1 ? fv.y : q == 2 ? fv.z : fv.w;
+            out[q] = combine_int<D>(t, ei, fj);
+        }
+        __stcs(reinterpret_cast<float4*>(c), make_float4(out[0], out[1], out[2], out[3]));
+    } else {
+        for (int q = 0; j0 + q < N; ++q) {
+            int32_t t[D - 1];
+#pragma unroll
+            for (int d = 0; d < D - 1; ++d) t[d] = T[d * plane + idx + q];
+            c[q] = combine_int<D>(t, ei, f[j0 + q]);
+        }
+    }
+}
+
+// any D (up to 18): the loop in fp64 as written
+__global__ void ozaki_combine_f64_kernel(const int32_t* __restrict__ T, int64_t ldT, int max_diag,
+                                         const int32_t* __restrict__ e, const int32_t* __restrict__ f,
+                                         float* __restrict__ C, int64_t ldc, int M, int N) {
     const int j = blockIdx.x * blockDim.x + threadIdx.x;
     const int i = blockIdx.y;
     if (j >= N) return;
@@ -34,13 +158,41 @@ __global__ void ozaki_combine_kernel(const int32_t* __restrict__ T, int64_t ldT,
     C[(int64_t)i * ldc + j] = ozaki_combine(t, max_diag, e[i], f[j]);
 }
 
+template <int D>
+cudaError_t launch_int(const int32_t* T, int64_t ldT, const int32_t* e, const int32_t* f, float* C, int64_t ldc,
+                       int M, int N, cudaStream_t s) {
+    dim3 grid((unsigned)(((N + 3) / 4 + 255) / 256), (unsigned)M);
+    ozaki_combine_int_kernel<D><<<grid, 256, 0, s>>>(T, ldT, e, f, C, ldc, M, N);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t ozaki_combine_launch(const int32_t* T, int64_t ldT, int max_diag, const int32_t* e, const int32_t* f,
                                  float* C, int64_t ldc, int M, int N, cudaStream_t s) {
     if (M == 0 || N == 0) return cudaSuccess;
+    // the integer kernels use 16-byte loads of T and f and 16-byte stores of C
+    const bool vec = (ldT % 4) == 0 && (ldc % 4) == 0 && (reinterpret_cast<uintptr_t>(T) & 15u) == 0 &&
+                     (reinterpret_cast<uintptr_t>(f) & 15u) == 0 && (reinterpret_cast<uintptr_t>(C) & 15u) == 0;
+    if (vec) {
+        switch (max_diag) {
+            case 2: return launch_int<2>(T, ldT, e, f, C, ldc, M, N, s);
+            case 3: return launch_int<3>(T, ldT, e, f, C, ldc, M, N, s);
+            case 4: return launch_int<4>(T, ldT, e, f, C, ldc, M, N, s);
+            case 5: return launch_int<5>(T, ldT, e, f, C, ldc, M, N, s);
+            case 6: return launch_int<6>(T, ldT, e, f, C, ldc, M, N, s);
+            case 7: return launch_int<7>(T, ldT, e, f, C, ldc, M, N, s);
+            case 8: return launch_int<8>(T, ldT, e, f, C, ldc, M, N, s);
+            case 9: return launch_int<9>(T, ldT, e, f, C, ldc, M, N, s);
+            case 10: return launch_int<10>(T, ldT, e, f, C, ldc, M, N, s);
+            case 11: return launch_int<11>(T, ldT, e, f, C, ldc, M, N, s);
+            case 12: return launch_int<12>(T, ldT, e, f, C, ldc, M, N, s);
+            case 13: return launch_int<13>(T, ldT, e, f, C, ldc, M, N, s);
+            default: break;
+        }
+    }
     dim3 grid((N + 255) / 256, M);
-    ozaki_combine_kernel<<<grid, 256, 0, s>>>(T, ldT, max_diag, e, f, C, ldc, M, N);
+    ozaki_combine_f64_kernel<<<grid, 256, 0, s>>>(T, ldT, max_diag, e, f, C, ldc, M, N);
     return cudaGetLastError();
 }
 

@@ -8,9 +8,9 @@
 // r <- 128 r - d_t on r = x 2^-e, because truncation toward zero is sign-symmetric.
 // R is formed with integer shifts of the fp32 significand, so it is exact.
 //
-// Rows: one CTA per row, two passes (max, then digits). Columns: a column-max kernel
-// (atomicMax over row chunks), an exponent kernel, then a 32x32 tiled transpose that
-// writes every digit plane K-major ([t][col][row]).
+// Rows: one CTA per row, two passes (max, then digits), eight columns per thread.
+// Columns: a column-max kernel (atomicMax over row chunks), an exponent kernel, then a
+// 64 x 64 tiled transpose that writes every digit plane K-major ([t][col][row]).
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -61,6 +61,41 @@ __device__ __forceinline__ __half digit_out<__half>(int8_t d) {
     return __int2half_rn((int)d);
 }
 
+// Eight consecutive digits of one plane, packed for one store: int8 (8 bytes) or exact
+// fp16 values (16 bytes; d + 1152 is placed under the fp16 exponent of 1024 and 1152
+// is subtracted, both exact).
+template <typename T>
+struct Pack8;
+template <>
+struct Pack8<int8_t> {
+    typedef uint2 type;
+    static __device__ __forceinline__ uint2 make(const int8_t (&d)[8]) {
+        uint32_t lo = 0, hi = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            lo |= (uint32_t)(uint8_t)d[i] << (8 * i);
+            hi |= (uint32_t)(uint8_t)d[i + 4] << (8 * i);
+        }
+        return make_uint2(lo, hi);
+    }
+};
+template <>
+struct Pack8<__half> {
+    typedef uint4 type;
+    static __device__ __forceinline__ uint32_t two(int8_t a, int8_t b) {
+        const uint32_t w = (0x6400u | (uint32_t)(a + 128)) | ((0x6400u | (uint32_t)(b + 128)) << 16);
+        const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
+        const __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&w), bias);
+        return *reinterpret_cast<const uint32_t*>(&r);
+    }
+    static __device__ __forceinline__ uint4 make(const int8_t (&d)[8]) {
+        return make_uint4(two(d[0], d[1]), two(d[2], d[3]), two(d[4], d[5]), two(d[6], d[7]));
+    }
+};
+
+// One CTA per row, 8 consecutive columns per thread: pass 1 reduces the row's max |x|
+// (fp32 bits), pass 2 re-reads the row (cache resident) and writes each plane's eight
+// digits with one store (when the plane's row stride allows it).
 template <typename T>
 __global__ void __launch_bounds__(SROW_THREADS) slice_rows_kernel(const float* __restrict__ X, int64_t ldx, int rows,
                                                                   int cols, int nslices, T* __restrict__ S,
@@ -68,8 +103,25 @@ __global__ void __launch_bounds__(SROW_THREADS) slice_rows_kernel(const float* _
     __shared__ uint32_t red[SROW_THREADS / 32];
     const int64_t row = blockIdx.x;
     const uint32_t* x = reinterpret_cast<const uint32_t*>(X + row * ldx);
+    const bool vec_in = (ldx % 4) == 0 && (reinterpret_cast<uintptr_t>(X) & 15u) == 0;
+    auto load8 = [&](int j0, uint32_t (&v)[8]) {
+        if (vec_in && j0 + 8 <= cols) {
+            const uint4 a = __ldg(reinterpret_cast<const uint4*>(x + j0));
+            const uint4 b = __ldg(reinterpret_cast<const uint4*>(x + j0 + 4));
+            v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+            v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = j0 + i < cols ? x[j0 + i] : 0u;
+        }
+    };
     uint32_t amax = 0;
-    for (int j = threadIdx.x; j < cols; j += SROW_THREADS) amax = max(amax, x[j] & 0x7FFFFFFFu);
+    for (int j0 = threadIdx.x * 8; j0 < cols; j0 += SROW_THREADS * 8) {
+        uint32_t v[8];
+        load8(j0, v);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) amax = max(amax, v[i] & 0x7FFFFFFFu);
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, o));
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
@@ -78,18 +130,33 @@ __global__ void __launch_bounds__(SROW_THREADS) slice_rows_kernel(const float* _
 #pragma unroll
     for (int w = 1; w < SROW_THREADS / 32; ++w) amax = max(amax, red[w]);
     const int64_t plane = (int64_t)rows * lds;
-    T* s = S + row * lds;
+    T* srow = S + row * lds;
     const bool bad = amax >= 0x7F800000u;  // inf or NaN in the row: digits written as zero
     const int e = bad ? 0 : line_exponent(amax);
     if (threadIdx.x == 0) {
         if (bad) raise_status(DEV_NONFINITE);
         e_out[row] = e;
     }
-    for (int j = threadIdx.x; j < lds; j += SROW_THREADS) {
-        uint32_t xb = (j < cols && !bad) ? x[j] : 0u;
-        unsigned long long R = digits_of(xb, e, nslices);
-        bool neg = xb >> 31;
-        for (int t = 0; t < nslices; ++t) s[t * plane + j] = digit_out<T>(digit(R, t, nslices, neg));
+    const bool vec_out = (lds % 8) == 0 && (reinterpret_cast<uintptr_t>(S) & 15u) == 0;
+    for (int j0 = threadIdx.x * 8; j0 < lds; j0 += SROW_THREADS * 8) {
+        uint32_t v[8];
+        load8(j0, v);  // zero beyond cols: the padding up to lds gets zero digits
+        unsigned long long R[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) R[i] = bad ? 0ull : digits_of(v[i], e, nslices);
+        for (int t = 0; t < nslices; ++t) {
+            int8_t d[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) d[i] = digit(R[i], t, nslices, v[i] >> 31);
+            T* dst = srow + t * plane + j0;
+            if (vec_out) {
+                *reinterpret_cast<typename Pack8<T>::type*>(dst) = Pack8<T>::make(d);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    if (j0 + i < lds) dst[i] = digit_out<T>(d[i]);
+            }
+        }
     }
 }
 
@@ -129,33 +196,70 @@ __global__ void col_exponent_kernel(const uint32_t* colmax, int cols, int32_t* e
     e_out[j] = line_exponent(m);
 }
 
-// 32 x 32 tile: rows r0.., columns c0..; digits written to S[t][col][row]
+// 64 x 64 tile of X (rows r0.., columns c0..), 256 threads: each thread loads four
+// columns of four rows (16-byte loads), its digits go to a shared tile [t][col][row],
+// then each plane is written K-major, S[t][col][row], eight rows per store (each
+// column's 64 rows are 128 contiguous bytes of fp16).
+constexpr int SC_TILE = 64;
+constexpr int SC_PITCH = SC_TILE + 4;  // bytes per (t, col) line of the shared tile
+
 template <typename T>
-__global__ void slice_cols_kernel(const float* __restrict__ X, int64_t ldx, int rows, int cols, int nslices,
-                                  const int32_t* __restrict__ e_col, T* __restrict__ S, int64_t lds) {
-    __shared__ int8_t tile[9][32][33];
-    const int r0 = blockIdx.y * 32, c0 = blockIdx.x * 32;
-    const int tx = threadIdx.x, ty = threadIdx.y;  // 32 x 8
-    for (int yy = ty; yy < 32; yy += 8) {
-        int r = r0 + yy, c = c0 + tx;
-        unsigned long long R = 0;
-        bool neg = false;
-        if (r < rows && c < cols) {
-            uint32_t xb = reinterpret_cast<const uint32_t*>(X)[(int64_t)r * ldx + c];
-            int e = e_col[c];
-            if (e != INT32_MIN) {
-                R = digits_of(xb, e, nslices);
-                neg = xb >> 31;
+__global__ void __launch_bounds__(256) slice_cols_kernel(const float* __restrict__ X, int64_t ldx, int rows, int cols,
+                                                         int nslices, const int32_t* __restrict__ e_col,
+                                                         T* __restrict__ S, int64_t lds) {
+    __shared__ __align__(16) int8_t tile[9][SC_TILE][SC_PITCH];
+    const int r0 = blockIdx.y * SC_TILE, c0 = blockIdx.x * SC_TILE;
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;  // 16 column quads x 16 row lanes
+    const bool vec_in = (ldx % 4) == 0 && (reinterpret_cast<uintptr_t>(X) & 15u) == 0;
+    const int cq = c0 + 4 * tx;
+    int ecol[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) ecol[q] = cq + q < cols ? e_col[cq + q] : INT32_MIN;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int rr = ty + 16 * i, r = r0 + rr;
+        uint32_t v[4] = {0u, 0u, 0u, 0u};
+        if (r < rows) {
+            const uint32_t* xr = reinterpret_cast<const uint32_t*>(X) + (int64_t)r * ldx;
+            if (vec_in && cq + 4 <= cols) {
+                const uint4 a = __ldg(reinterpret_cast<const uint4*>(xr + cq));
+                v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+            } else {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) v[q] = cq + q < cols ? xr[cq + q] : 0u;
             }
         }
-        for (int t = 0; t < nslices; ++t) tile[t][tx][yy] = digit(R, t, nslices, neg);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            // a column marked non-finite (INT32_MIN) or outside the matrix gets zero digits
+            const unsigned long long R = ecol[q] == INT32_MIN ? 0ull : digits_of(v[q], ecol[q], nslices);
+            for (int t = 0; t < nslices; ++t) tile[t][4 * tx + q][rr] = digit(R, t, nslices, v[q] >> 31);
+        }
     }
     __syncthreads();
     const int64_t plane = (int64_t)cols * lds;
-    for (int yy = ty; yy < 32; yy += 8) {
-        int c = c0 + yy, r = r0 + tx;
-        if (c < cols && r < lds)  // rows in [rows, lds) are the zero padding
-            for (int t = 0; t < nslices; ++t) S[t * plane + (int64_t)c * lds + r] = digit_out<T>(tile[t][yy][tx]);
+    const bool vec_out = (lds % 8) == 0 && (reinterpret_cast<uintptr_t>(S) & 15u) == 0;
+    const int chunks = nslices * SC_TILE * (SC_TILE / 8);  // (t, col, 8-row group)
+    for (int w = threadIdx.x; w < chunks; w += 256) {
+        const int g8 = w & 7, cc = (w >> 3) & (SC_TILE - 1), t = w >> 9;
+        const int c = c0 + cc, r = r0 + 8 * g8;
+        if (c >= cols || r >= lds) continue;  // rows in [rows, lds) are the zero padding
+        const uint32_t* src = reinterpret_cast<const uint32_t*>(&tile[t][cc][8 * g8]);
+        const uint32_t lo = src[0], hi = src[1];
+        int8_t d[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            d[i] = (int8_t)(lo >> (8 * i));
+            d[i + 4] = (int8_t)(hi >> (8 * i));
+        }
+        T* dst = S + t * plane + (int64_t)c * lds + r;
+        if (vec_out && r + 8 <= lds) {
+            *reinterpret_cast<typename Pack8<T>::type*>(dst) = Pack8<T>::make(d);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                if (r + i < lds) dst[i] = digit_out<T>(d[i]);
+        }
     }
 }
 
@@ -184,8 +288,8 @@ cudaError_t cols_launch(const float* X, int64_t ldx, int rows, int cols, int nsl
         col_absmax_kernel<<<g1, dim3(32, 8), 0, s>>>(X, ldx, rows, cols, colmax);
     }
     col_exponent_kernel<<<(cols + 255) / 256, 256, 0, s>>>(colmax, cols, e);
-    dim3 g2((cols + 31) / 32, (int)((lds + 31) / 32));
-    if (lds > 0) slice_cols_kernel<T><<<g2, dim3(32, 8), 0, s>>>(X, ldx, rows, cols, nslices, e, S, lds);
+    dim3 g2((cols + SC_TILE - 1) / SC_TILE, (int)((lds + SC_TILE - 1) / SC_TILE));
+    if (lds > 0) slice_cols_kernel<T><<<g2, 256, 0, s>>>(X, ldx, rows, cols, nslices, e, S, lds);
     fix_nonfinite_cols_kernel<<<(cols + 255) / 256, 256, 0, s>>>(e, cols);
     return cudaGetLastError();
 }

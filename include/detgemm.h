@@ -171,6 +171,24 @@ DETGEMM_API detgemm_status detgemm_ozaki_f32(const float* A, int64_t lda, const 
 DETGEMM_API size_t detgemm_ozaki_workspace_size(int M, int N, int K, int nslices, int max_diag, int split_k);
 
 /*
+ * The recombination step of detgemm_ozaki_f32 alone [P3 §3 (a): the exact slice
+ * products are recombined in a fixed order in fp64 and rounded once]:
+ *   acc = 0.0;  for g = max_diag down to 2: acc = acc + T_g * 2^(-7g)      (fp64, RNE)
+ *   C_ij = (float)(acc * 2^(e_i + f_j))                (the one rounding, IEEE RNE,
+ *                                                       subnormals kept, overflow -> inf)
+ *   T  int32 [max_diag - 1][M][ldT]: plane p holds the diagonal sum T_g with
+ *      g = max_diag - p (largest g first, the order of the loop); ldT >= N
+ *   e  int32 [M] row exponents, f int32 [N] column exponents (any values)
+ *   C  fp32 [M x N], row stride ldc;   2 <= max_diag <= 18
+ * The result bits are those of the fp64 loop as written, whichever way the library
+ * evaluates it. Errors: INVALID_ARG, ALIGNMENT (T and C 16-byte aligned, ldT and ldc
+ * multiples of 4; e and f 4-byte aligned), UNSUPPORTED_DEVICE, CUDA.
+ */
+DETGEMM_API detgemm_status detgemm_ozaki_combine(const int32_t* T, int64_t ldT, int max_diag, const int32_t* e,
+                                                 const int32_t* f, float* C, int64_t ldc, int M, int N,
+                                                 detgemm_stream_t stream);
+
+/*
  * Exact int8 -> fp16 copy (every int8 value is an fp16 value): Y[r][k] = X[r][k] for
  * k < cols and Y[r][k] = 0 for cols <= k < ldy, i.e. the whole row stride of Y is written.
  * The tensor-core W8A8 path consumes operands in this form; widening a static weight

@@ -66,8 +66,10 @@ def _load():
             lib.oracle_slice_f32.argtypes = [p, i64, i32, i32, i32, i32, p, p]
             lib.oracle_ozaki_f32.argtypes = [p, i64, p, i64, p, i64, i32, i32, i32, i32, i32, p, i32]
             lib.oracle_ozaki_diagonals.argtypes = [p, p, i32, i32, i32, i32, i32, p]
+            lib.oracle_ozaki_combine.argtypes = [p, i64, i32, p, p, p, i64, i32, i32]
             for f in (lib.oracle_w8a8, lib.oracle_gemm_s8_i32, lib.oracle_quantize_pow2,
-                      lib.oracle_slice_f32, lib.oracle_ozaki_f32, lib.oracle_ozaki_diagonals):
+                      lib.oracle_slice_f32, lib.oracle_ozaki_f32, lib.oracle_ozaki_diagonals,
+                      lib.oracle_ozaki_combine):
                 f.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -178,3 +180,15 @@ def ozaki_diagonals(DA, DB, max_diag=8):
     T = np.empty((M, N, max_diag + 1), dtype=np.int64)
     _load().oracle_ozaki_diagonals(DA.ctypes.data, DB.ctypes.data, M, N, K, ns, max_diag, T.ctypes.data)
     return T
+
+
+def ozaki_combine(T, e, f):
+    """Fixed-order fp64 recombination of diagonal sums. T int32 [max_diag - 1, M, N],
+    plane p holding the diagonal g = max_diag - p; e int32 [M], f int32 [N]. fp32 [M, N]."""
+    T = _c(T, np.int32)
+    e, f = _c(e, np.int32), _c(f, np.int32)
+    nd, M, N = T.shape
+    assert e.shape == (M,) and f.shape == (N,) and 1 <= nd <= 17
+    C = np.empty((M, N), dtype=np.float32)
+    _load().oracle_ozaki_combine(T.ctypes.data, N, nd + 1, e.ctypes.data, f.ctypes.data, C.ctypes.data, N, M, N)
+    return C

@@ -228,6 +228,36 @@ int oracle_slice_f32(const float* X, int64_t ldx, int rows, int cols, int axis, 
 }
 
 /* ------------------------------------------------------------------------------------ */
+/* Ozaki recombination of one element [P3 §3 (a): fixed-order fp64 recombination, one   */
+/* rounding]. T[g] (g = 2..max_diag) are the exact diagonal sums of weight 2^(-7g):       */
+/*   acc = 0.0;  for g = max_diag down to 2:  acc = acc + T_g * 2^(-7g)   (fp64)         */
+/*   C = (float) (acc * 2^(e + f))                 (one rounding to fp32, RNE)           */
+/* ------------------------------------------------------------------------------------ */
+static float combine_one(const int64_t* T, int max_diag, int32_t e, int32_t f) {
+    double acc = 0.0;
+    for (int g = max_diag; g >= 2; --g) acc = acc + ldexp((double)T[g], -7 * g);
+    return (float)ldexp(acc, clamp_exp((int64_t)e + (int64_t)f));
+}
+
+/* The recombination step alone: T int32 [max_diag - 1][M][ldT], plane p holding the     */
+/* diagonal g = max_diag - p; e [M], f [N]; C fp32 [M x N] (row stride ldc).              */
+int oracle_ozaki_combine(const int32_t* T, int64_t ldT, int max_diag, const int32_t* e,
+                         const int32_t* f, float* C, int64_t ldc, int M, int N) {
+    int64_t plane = (int64_t)M * ldT;
+#pragma omp parallel for schedule(static)
+    for (int i = 0; i < M; ++i) {
+        int64_t Tg[19];
+        for (int j = 0; j < N; ++j) {
+            for (int g = 0; g <= max_diag; ++g) Tg[g] = 0;
+            for (int g = 2; g <= max_diag; ++g)
+                Tg[g] = T[(int64_t)(max_diag - g) * plane + (int64_t)i * ldT + j];
+            C[(int64_t)i * ldc + j] = combine_one(Tg, max_diag, e[i], f[j]);
+        }
+    }
+    return ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------------------------ */
 /* Ozaki fp32 GEMM [P3 §3 (a)]: C = A B with A [M x K], B [K x N] fp32 row-major.         */
 /*   slice A per row (e_i, DA_s) and B per column (f_j, DB_t);                           */
 /*   T_g = sum_{s+t=g, 1<=s,t<=nslices} sum_k DA_s[i,k] * DB_t[k,j]   (exact, int64)     */
@@ -271,9 +301,7 @@ int oracle_ozaki_f32(const float* A, int64_t lda, const float* B, int64_t ldb, f
                     T[g] += acc;
                 }
             }
-            double acc = 0.0;
-            for (int g = max_diag; g >= 2; --g) acc = acc + ldexp((double)T[g], -7 * g);
-            C[(int64_t)r * ldc + j] = (float)ldexp(acc, clamp_exp((int64_t)e[r] + (int64_t)f[j]));
+            C[(int64_t)r * ldc + j] = combine_one(T, max_diag, e[r], f[j]);
         }
         free(T);
     }

@@ -119,6 +119,13 @@ def test_other_entry_points_validate(lib):
     assert o(P, 19024, P, 64, P, 64, 64, 64, 19024, 7, 8, 1, P, 1 << 40, None) == dg.ERR_PRECONDITION
     assert o(P, 64, P, 64, P, 64, 64, 64, 64, 7, 8, 1, P, 16, None) == dg.ERR_WORKSPACE
     assert dg.ozaki_workspace_size(64, 64, 64) > 7 * 64 * 64 * 2
+    c = lib.detgemm_ozaki_combine
+    assert c(P, 64, 1, P, P, P, 64, 4, 64, None) == dg.ERR_INVALID_ARG  # max_diag < 2
+    assert c(P, 64, 19, P, P, P, 64, 4, 64, None) == dg.ERR_INVALID_ARG  # max_diag > 18
+    assert c(P, 60, 8, P, P, P, 64, 4, 64, None) == dg.ERR_INVALID_ARG  # ldT < N
+    assert c(P, 66, 8, P, P, P, 64, 4, 64, None) == dg.ERR_ALIGNMENT  # 264-byte rows
+    assert c(P1, 64, 8, P, P, P, 64, 4, 64, None) == dg.ERR_ALIGNMENT
+    assert c(None, 64, 8, None, None, None, 64, 0, 64, None) == dg.OK  # empty
 
 
 def test_binding_refuses_cpu_tensors(lib):

@@ -73,3 +73,37 @@ def test_ozaki_workload_sampled_and_error_bound(lib, dev, oracle_mod):
     out2 = poison_like((4096, 4096), torch.float32, dev)
     lib.ozaki_f32(tA, tB, split_k=3, out=out2)
     assert torch.equal(out.view(torch.int32), out2.view(torch.int32))
+
+
+def _diagonals(rng, nd, M, N):
+    # full-range, small, and trailing-zero-heavy sums: every rounding of the combine,
+    # including exact ties at the 53-bit boundary, is reached
+    full = rng.integers(-2 ** 31 + 1, 2 ** 31, size=(nd, M, N), dtype=np.int64)
+    small = rng.integers(-3000, 3001, size=(nd, M, N), dtype=np.int64)
+    shifted = rng.integers(-2 ** 10, 2 ** 10, size=(nd, M, N), dtype=np.int64) << rng.integers(0, 20, size=(nd, M, N))
+    pick = rng.integers(0, 3, size=(nd, M, N))
+    T = np.where(pick == 0, full, np.where(pick == 1, small, shifted))
+    return np.clip(T, -2 ** 31 + 1, 2 ** 31 - 1).astype(np.int32)
+
+
+@pytest.mark.parametrize("max_diag", [2, 3, 5, 8, 9, 13, 14, 18])
+def test_combine_step_bitexact(lib, dev, oracle_mod, max_diag):
+    """detgemm_ozaki_combine against the oracle's fp64 loop, element by element: ragged N
+    (the scalar tail), a padded row stride, and exponents reaching fp32 subnormals and
+    overflow."""
+    rng = np.random.default_rng(100 + max_diag)
+    M, N, ldT = 37, 1003, 1012
+    T = _diagonals(rng, max_diag - 1, M, N)
+    e = rng.integers(-40, 41, size=M).astype(np.int32)
+    f = rng.integers(-40, 41, size=N).astype(np.int32)
+    e[:4] = [-150, -120, 100, 140]
+    f[:6] = [-160, -60, 0, 60, 130, 2 ** 31 - 1]
+    f[6] = -2 ** 31
+    tT = torch.zeros((max_diag - 1, M, ldT), dtype=torch.int32, device=dev)[:, :, :N]
+    tT.copy_(torch.from_numpy(T))
+    out = poison_like((M, N), torch.float32, dev)
+    lib.ozaki_combine(tT, to_dev(e, dev), to_dev(f, dev), out=out)
+    got = f32_bits(out)
+    want = oracle_mod.ozaki_combine(T, e, f).view(np.uint32)
+    assert (got == want).all(), int((got != want).sum())
+    assert lib.device_status() == lib.OK

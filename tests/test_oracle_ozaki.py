@@ -162,3 +162,61 @@ def test_nonfinite_reported(oracle_mod):
     A = np.array([[1.0, np.inf]], np.float32)
     with pytest.raises(oracle_mod.OracleError):
         oracle_mod.ozaki_f32(A, np.ones((2, 2), np.float32))
+
+
+def _random_diagonals(rng, nd, M, N):
+    """Diagonal sums drawn to exercise every rounding of the fp64 combine: full-range
+    int32 values (the late sums then drop up to ~20 bits, and ties occur), small values,
+    and values with many trailing zero bits (exact ties at the 53-bit boundary)."""
+    full = rng.integers(-2 ** 31 + 1, 2 ** 31, size=(nd, M, N), dtype=np.int64)
+    small = rng.integers(-3000, 3001, size=(nd, M, N), dtype=np.int64)
+    shifted = rng.integers(-2 ** 10, 2 ** 10, size=(nd, M, N), dtype=np.int64) << rng.integers(0, 20, size=(nd, M, N))
+    pick = rng.integers(0, 3, size=(nd, M, N))
+    T = np.where(pick == 0, full, np.where(pick == 1, small, shifted))
+    return np.clip(T, -2 ** 31 + 1, 2 ** 31 - 1).astype(np.int32)
+
+
+def _brute_combine(Tcol, max_diag, e, f):
+    """IEEE binary64 (Python float, round to nearest even) on exact conversions of
+    T_g 2^(-7g) in the order g = max_diag..2, then the exact-rational fp32 rounding."""
+    acc = 0.0
+    for p in range(max_diag - 1):
+        g = max_diag - p
+        acc = acc + float(Fraction(int(Tcol[p])) * pow2(-7 * g))
+    return rne_f32_exact(Fraction(acc) * pow2(int(e) + int(f)))
+
+
+@pytest.mark.parametrize("max_diag", [2, 5, 8, 13, 18])
+def test_combine_step_bruteforce(oracle_mod, max_diag):
+    rng = np.random.default_rng(50 + max_diag)
+    M, N = 6, 40
+    T = _random_diagonals(rng, max_diag - 1, M, N)
+    e = rng.integers(-40, 41, size=M).astype(np.int32)
+    f = rng.integers(-40, 41, size=N).astype(np.int32)
+    C = oracle_mod.ozaki_combine(T, e, f)
+    for i in range(M):
+        for j in range(N):
+            want = _brute_combine(T[:, i, j], max_diag, e[i], f[j])
+            assert C[i, j].view(np.uint32) == np.float32(want).view(np.uint32), (i, j)
+
+
+def test_combine_step_hand_worked_order(oracle_mod):
+    # T_8 = 1, T_3 = -524288, T_2 = 4096 (the cancellation case above): g = 8..2 gives +0
+    T = np.zeros((7, 1, 1), np.int32)
+    T[0, 0, 0] = 1        # plane 0: g = 8
+    T[5, 0, 0] = -524288  # plane 5: g = 3
+    T[6, 0, 0] = 4096     # plane 6: g = 2
+    C = oracle_mod.ozaki_combine(T, np.zeros(1, np.int32), np.zeros(1, np.int32))
+    assert C.view(np.uint32)[0, 0] == 0
+
+
+def test_combine_step_matches_full_gemm(oracle_mod):
+    rng = np.random.default_rng(6)
+    A = (rng.standard_normal((5, 33)) * np.exp2(rng.integers(-8, 9, size=(5, 33)))).astype(np.float32)
+    B = (rng.standard_normal((33, 9)) * np.exp2(rng.integers(-8, 9, size=(33, 9)))).astype(np.float32)
+    DA, e = oracle_mod.slice_f32(A, 0, 7)
+    DB, f = oracle_mod.slice_f32(B, 1, 7)
+    T = oracle_mod.ozaki_diagonals(DA, DB, 8)                       # [M, N, g]
+    planes = np.stack([T[:, :, g] for g in range(8, 1, -1)]).astype(np.int32)
+    C = oracle_mod.ozaki_combine(planes, e, f)
+    assert (C.view(np.uint32) == oracle_mod.ozaki_f32(A, B).view(np.uint32)).all()
