@@ -8,8 +8,8 @@ INT8 TOPS (2 M N K per GEMM / time) with the dominant kernel's roofline fraction
 
 The same JSON line carries extra measurements of the other hot-path rows: the skinny
 decode-shaped GEMM (M=16, N=4096, K=65536, split-K 8/16/32) in GB/s against the HBM
-roofline, the Ozaki fp32 GEMM (4096^3) in effective fp32 TFLOP/s, and the sweep
-linear (M=2048, K=2048, N=6144).
+roofline, the Ozaki fp32 GEMM (4096^3) in effective fp32 TFLOP/s, the fused linear layer
+on bf16 activations at the FFN gate/up size, and the sweep linear (M=2048, K=2048, N=6144).
 
 Timing: W warm-up steps, then K timed steps; L2 is flushed before every timed step,
 outside the timed events, by a 256 MiB write followed by a 256 MiB read of another buffer
@@ -431,6 +431,33 @@ def extras(dg, torch, dev, pk, flush):
     res["ozaki_f32_4096"] = {"ms": round(ms, 3), "effective_fp32_TFLOPs": round(2 * 4096 ** 3 / (ms * 1e-3) / 1e12, 2),
                              "slice_TOPS": round(28 * 2 * 4096 ** 3 / (ms * 1e-3) / 1e12, 1)}
     del Af, Bf, Cf, ws
+    # fused linear layer on bf16 activations at the FFN gate/up size: quantize + GEMM in one
+    # call, against the same two steps as separate calls
+    M, K, N = 8192, 4096, 12288
+    X = (torch.from_numpy(synthetic.normal_f32(21, 0, (M, K), 2.0)).to(dev)).to(torch.bfloat16)
+    W = tdev(synthetic.normal_i8(2, 1, (N, K), 30.0))
+    ew = tdev(synthetic.uniform_i32(2, 3, (N,), -14, -6))
+    C = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    W16 = dg.widen_i8_f16(W)
+    ws = torch.empty(max(dg.load().detgemm_linear_w8a8_workspace_size(M, N, K, 1, 0), 1), dtype=torch.uint8,
+                     device=dev)
+    ws16 = torch.empty(max(dg.load().detgemm_linear_w8a8_workspace_size(M, N, K, 1, 1), 1), dtype=torch.uint8,
+                       device=dev)
+    wsw = torch.empty(max(dg.w8a8_workspace_size(M, N, K), 1), dtype=torch.uint8, device=dev)
+    ops = 2.0 * M * N * K
+    ms_f = _time(torch, lambda: dg.linear_w8a8(X, W, ew, out=C, ws=ws), flush)
+    ms_f16 = _time(torch, lambda: dg.linear_w8a8(X, W, ew, W16=W16, out=C, ws=ws16), flush)
+
+    def two_calls():
+        Q, ea = dg.quantize_pow2(X)
+        dg.w8a8(Q, W, ea, ew, out=C, ws=wsw)
+    ms_2 = _time(torch, two_calls, flush)
+    res["linear_bf16_M8192_N12288_K4096"] = {
+        "fused_us": round(ms_f * 1e3, 1), "fused_TOPS": round(ops / (ms_f * 1e-3) / 1e12, 1),
+        "fused_prewidened_weight_us": round(ms_f16 * 1e3, 1),
+        "fused_prewidened_weight_TOPS": round(ops / (ms_f16 * 1e-3) / 1e12, 1),
+        "quantize_then_w8a8_us": round(ms_2 * 1e3, 1)}
+    del X, W, W16, ws, ws16, wsw, C
     # sweep linear at M = 2048
     A, W, ea, ew = (tdev(x) for x in synthetic.sweep(2048))
     C = torch.empty((2048, 6144), dtype=torch.bfloat16, device=dev)

@@ -11,6 +11,7 @@ Functions mirror the C entry points:
 * :func:`w8a8`           C = rne_bf16((A W^T) * 2^(ea_i + ew_j))      (bf16 out)
 * :func:`gemm_s8_i32`    C = A W^T, exact int32
 * :func:`quantize_pow2`  per-row power-of-two scale and int8 values
+* :func:`linear_w8a8`    quantize_pow2 of bf16/fp32 activations + w8a8, fused
 * :func:`slice_f32`      Ozaki digit planes with shared exponents
 * :func:`ozaki_f32`      Ozaki-scheme fp32 GEMM C = A B
 * :func:`ozaki_combine`  its fixed-order fp64 recombination step alone
@@ -47,6 +48,9 @@ SIGNATURES = {
     "detgemm_ozaki_f32": ([_P, _I64, _P, _I64, _P, _I64, _I32, _I32, _I32, _I32, _I32, _I32, _P, _SZ, _P], _I32),
     "detgemm_ozaki_workspace_size": ([_I32, _I32, _I32, _I32, _I32, _I32], _SZ),
     "detgemm_ozaki_combine": ([_P, _I64, _I32, _P, _P, _P, _I64, _I32, _I32, _P], _I32),
+    "detgemm_linear_w8a8": ([_P, _I32, _I64, _I32, _P, _I64, _P, _I64, _P, _P, _I64, _P, _I32, _I32, _I32, _I32,
+                             _P, _SZ, _P], _I32),
+    "detgemm_linear_w8a8_workspace_size": ([_I32, _I32, _I32, _I32, _I32], _SZ),
     "detgemm_get_device_status": ([_P], _I32),
     "detgemm_w8a8_noalloc": ([_P, _I64, _P, _I64, _P, _P, _P, _I64, _I32, _I32, _I32, _I32, _P], _I32),
     "detgemm_widen_i8_f16": ([_P, _I64, _I32, _I32, _P, _I64, _P], _I32),
@@ -203,6 +207,46 @@ def quantize_pow2(X, mode: int = POW2_NEAREST, stream=None):
                                    e.data_ptr(), _stream(stream))
     _check(st, "detgemm_quantize_pow2")
     return Q, e
+
+
+def linear_w8a8(X, W, ew, mode: int = POW2_NEAREST, W16=None, split_k: int = 1, out=None, ea_out=None, ws=None,
+                stream=None) -> torch.Tensor:
+    """W8A8 linear layer on bf16/fp32 activations X [M, K]: per-row pow2 quantization of X
+    fused with the exact GEMM against int8 W [N, K] (ew int32 [N]); bf16 [M, N] out.
+    W16 (optional) is W widened once by widen_i8_f16; ea_out (optional) int32 [M] receives
+    the activation exponents."""
+    lib = load()
+    if X.dtype == torch.bfloat16:
+        dt = DTYPE_BF16
+    elif X.dtype == torch.float32:
+        dt = DTYPE_F32
+    else:
+        raise TypeError("X must be bfloat16 or float32")
+    _req(X, X.dtype, "X"); _req(W, torch.int8, "W"); _req(ew, torch.int32, "ew")
+    M, K = X.shape
+    N = W.shape[0]
+    if W.shape[1] != K or ew.shape != (N,):
+        raise ValueError("shape mismatch")
+    if W16 is not None:
+        _req(W16, torch.float16, "W16")
+        if W16.shape != (N, K):
+            raise ValueError("W16 shape mismatch")
+    if ea_out is not None:
+        _req(ea_out, torch.int32, "ea_out")
+        if ea_out.shape != (M,):
+            raise ValueError("ea_out shape mismatch")
+    if out is None:
+        out = empty2d(M, N, torch.bfloat16, X.device)
+    _req(out, torch.bfloat16, "out")
+    need = int(lib.detgemm_linear_w8a8_workspace_size(M, N, K, split_k, 1 if W16 is not None else 0))
+    wsb, wsn = _workspace(need, X.device, ws)
+    st = lib.detgemm_linear_w8a8(X.data_ptr(), dt, _ld(X), mode, W.data_ptr(), _ld(W),
+                                 W16.data_ptr() if W16 is not None else None, _ld(W16) if W16 is not None else 0,
+                                 ew.data_ptr(), out.data_ptr(), _ld(out),
+                                 ea_out.data_ptr() if ea_out is not None else None, M, N, K, split_k,
+                                 wsb.data_ptr() if wsb is not None else None, wsn, _stream(stream))
+    _check(st, "detgemm_linear_w8a8")
+    return out
 
 
 def slice_f32(X, axis: int = AXIS_ROWS, nslices: int = 7, stream=None):

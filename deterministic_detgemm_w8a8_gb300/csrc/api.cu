@@ -205,6 +205,101 @@ detgemm_status detgemm_gemm_s8_i32(const int8_t* A, int64_t lda, const int8_t* W
                      reinterpret_cast<cudaStream_t>(stream));
 }
 
+// Fused linear layer scratch. M > 64: A16 [M][Kp] fp16 | W16 [N][Kp] fp16 (only when no
+// widened weight is given) | ea [M] | split-K sums and counters. M <= 64: Q int8 [M][K16]
+// | ea [M] | the decode-shaped GEMM's scratch.
+struct LinearLayout {
+    int64_t Kp, K16;
+    size_t a, w16, ea, gemm, total;
+};
+
+static LinearLayout linear_layout(int M, int N, int K, int split_k, bool have_w16) {
+    LinearLayout L;
+    L.Kp = tc_padded_k(K);
+    L.K16 = ((int64_t)K + 15) / 16 * 16;
+    size_t off = 0;
+    if (w8a8_uses_tc(M)) {
+        L.a = off; off += align256((size_t)M * L.Kp * 2);
+        L.w16 = off; off += have_w16 ? 0 : align256((size_t)N * L.Kp * 2);
+        L.ea = off; off += align256((size_t)M * 4);
+        L.gemm = off; off += align256(tc_split_bytes(1, M, N, split_k));
+    } else {
+        L.a = off; off += align256((size_t)M * L.K16);
+        L.w16 = off;
+        L.ea = off; off += align256((size_t)M * 4);
+        L.gemm = off; off += align256(igemm_workspace_bytes(M, N, K, split_k));
+    }
+    L.total = off;
+    return L;
+}
+
+size_t detgemm_linear_w8a8_workspace_size(int M, int N, int K, int split_k, int have_w16) {
+    if (M <= 0 || N <= 0 || K <= 0) return 0;
+    return linear_layout(M, N, K, split_k, have_w16 != 0).total;
+}
+
+detgemm_status detgemm_linear_w8a8(const void* X, int x_dtype, int64_t ldx, int mode, const int8_t* W, int64_t ldw,
+                                   const uint16_t* W16, int64_t ldw16, const int32_t* ew, uint16_t* C, int64_t ldc,
+                                   int32_t* ea_out, int M, int N, int K, int split_k, void* ws, size_t ws_bytes,
+                                   detgemm_stream_t stream) {
+    if (M < 0 || N < 0 || K < 1) return DETGEMM_ERR_INVALID_ARG;
+    if (x_dtype != DETGEMM_DTYPE_BF16 && x_dtype != DETGEMM_DTYPE_F32) return DETGEMM_ERR_INVALID_ARG;
+    if (mode != DETGEMM_POW2_NEAREST && mode != DETGEMM_POW2_CEIL) return DETGEMM_ERR_INVALID_ARG;
+    if (K > DETGEMM_MAX_K) return DETGEMM_ERR_PRECONDITION;
+    if (split_k < 1 || split_k > (K + 63) / 64) return DETGEMM_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return DETGEMM_OK;
+    if (!X || !W || !ew || !C || ldx < K || ldw < K || ldc < N) return DETGEMM_ERR_INVALID_ARG;
+    if (W16 && ldw16 < K) return DETGEMM_ERR_INVALID_ARG;
+    const int xs = x_dtype == DETGEMM_DTYPE_BF16 ? 2 : 4;
+    if (!aligned16(X) || !aligned16(W) || !aligned16(C) || !aligned4(ew) || (ea_out && !aligned4(ea_out)))
+        return DETGEMM_ERR_ALIGNMENT;
+    if ((ldx * xs) % 16 || ldw % 16 || (ldc * 2) % 16) return DETGEMM_ERR_ALIGNMENT;
+    if (W16 && (!aligned16(W16) || ldw16 % 8)) return DETGEMM_ERR_ALIGNMENT;
+    const bool tc = w8a8_uses_tc(M);
+    const bool use_w16 = tc && W16 != nullptr;
+    const LinearLayout L = linear_layout(M, N, K, split_k, use_w16);
+    if (ws == nullptr || ws_bytes < L.total) return DETGEMM_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return DETGEMM_ERR_ALIGNMENT;
+    detgemm_status st = check_device();
+    if (st != DETGEMM_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    char* base = reinterpret_cast<char*>(ws);
+    int32_t* ea = ea_out ? ea_out : reinterpret_cast<int32_t*>(base + L.ea);
+    cudaError_t err;
+    if (!tc) {
+        // decode-shaped: int8 rows, then the W-streaming kernel on them
+        int8_t* Q = reinterpret_cast<int8_t*>(base + L.a);
+        err = quantize_pow2_launch(X, x_dtype, ldx, M, K, mode, Q, L.K16, ea, s);
+        if (err != cudaSuccess) return DETGEMM_ERR_CUDA;
+        return run_igemm(Q, L.K16, W, ldw, ea, ew, C, ldc, EPI_BF16_POW2, M, N, K, split_k, base + L.gemm, s);
+    }
+    // tensor-core path: the quantizer writes the activation operand directly in its fp16
+    // carrier form (no int8 copy, no widening pass over it)
+    err = quantize_pow2_f16_launch(X, x_dtype, ldx, M, K, mode, base + L.a, L.Kp, ea, s);
+    if (err != cudaSuccess) return DETGEMM_ERR_CUDA;
+    const void* wop = W16;
+    int64_t ldwop = ldw16;
+    if (!use_w16) {
+        err = widen_i8_f16_launch(W, ldw, N, K, base + L.w16, L.Kp, s);
+        if (err != cudaSuccess) return DETGEMM_ERR_CUDA;
+        wop = base + L.w16;
+        ldwop = L.Kp;
+    }
+    TcArgs a = {};
+    a.M = M;
+    a.N = N;
+    a.ndiag = 1;
+    a.diag_first[0] = 0;
+    a.diag_nseg[0] = 1;
+    a.split = split_k;
+    a.mode = EPI_BF16_POW2;
+    a.ea = ea;
+    a.ew = ew;
+    a.C = C;
+    a.ldc = ldc;
+    return from_cuda(tc_gemm_launch(a, base + L.a, L.Kp, 1, wop, ldwop, 1, K, base + L.gemm, s));
+}
+
 detgemm_status detgemm_quantize_pow2(const void* X, int x_dtype, int64_t ldx, int rows, int cols, int mode,
                                      int8_t* Q, int64_t ldq, int32_t* e, detgemm_stream_t stream) {
     if (rows < 0 || cols < 0) return DETGEMM_ERR_INVALID_ARG;

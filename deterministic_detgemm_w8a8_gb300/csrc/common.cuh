@@ -1,6 +1,7 @@
 // Shared device helpers of libdetgemm: status word, exact epilogues, bit utilities.
 #pragma once
 
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -127,5 +128,39 @@ __device__ __forceinline__ bool f32_normalise(uint32_t absbits, uint32_t& M, int
     p = (int)ef - 127;
     return true;
 }
+
+// Eight consecutive small integers (int8 range), packed for one store: as int8 (8 bytes)
+// or as exact fp16 values (16 bytes; d + 1152 is placed under the fp16 exponent of 1024
+// and 1152 is subtracted, both exact).
+template <typename T>
+struct Pack8;
+template <>
+struct Pack8<int8_t> {
+    typedef uint2 type;
+    static __device__ __forceinline__ int8_t one(int8_t d) { return d; }
+    static __device__ __forceinline__ uint2 make(const int8_t (&d)[8]) {
+        uint32_t lo = 0, hi = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            lo |= (uint32_t)(uint8_t)d[i] << (8 * i);
+            hi |= (uint32_t)(uint8_t)d[i + 4] << (8 * i);
+        }
+        return make_uint2(lo, hi);
+    }
+};
+template <>
+struct Pack8<__half> {
+    typedef uint4 type;
+    static __device__ __forceinline__ __half one(int8_t d) { return __short_as_half((short)(two(d, 0) & 0xFFFFu)); }
+    static __device__ __forceinline__ uint32_t two(int8_t a, int8_t b) {
+        const uint32_t w = (0x6400u | (uint32_t)(a + 128)) | ((0x6400u | (uint32_t)(b + 128)) << 16);
+        const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
+        const __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&w), bias);
+        return *reinterpret_cast<const uint32_t*>(&r);
+    }
+    static __device__ __forceinline__ uint4 make(const int8_t (&d)[8]) {
+        return make_uint4(two(d[0], d[1]), two(d[2], d[3]), two(d[4], d[5]), two(d[6], d[7]));
+    }
+};
 
 }  // namespace detgemm

@@ -47,6 +47,10 @@ cudaError_t igemm_launch(const IGemmArgs& a, void* ws, cudaStream_t s);
 // Pow2 quantizer and Ozaki slicer.
 cudaError_t quantize_pow2_launch(const void* X, int x_dtype, int64_t ldx, int rows, int cols, int mode,
                                  int8_t* Q, int64_t ldq, int32_t* e, cudaStream_t s);
+// the same integers as exact fp16 values, zero for cols <= j < ldq (the padded operand of
+// the tensor-core engine; ldq a multiple of 8)
+cudaError_t quantize_pow2_f16_launch(const void* X, int x_dtype, int64_t ldx, int rows, int cols, int mode,
+                                     void* Q16, int64_t ldq, int32_t* e, cudaStream_t s);
 // Digit planes: ROWS -> S[t][row][j] with row stride lds >= cols; COLS -> S[t][col][r] with
 // column stride lds >= rows. Padding bytes up to lds are written as zero.
 cudaError_t slice_rows_launch(const float* X, int64_t ldx, int rows, int cols, int nslices, int8_t* S,

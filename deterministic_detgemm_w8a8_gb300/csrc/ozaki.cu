@@ -17,9 +17,8 @@
 // |value| is at least 2^(-7D) >= 2^-91, and at most 2^108 < 2^127 fits a signed 128-bit
 // integer for D <= 13). The first four sums are below 2^53 and need no rounding. The
 // result Z * 2^(e_i + f_j - 7D) is then rounded once to fp32 (subnormals kept, overflow
-// to infinity) by integer construction, as the fp64 product and the fp32 conversion do:
-// the product is exact in fp64 because it stays inside fp64's normal range. For D > 13
-// the loop runs in fp64 directly.
+// to infinity), as the fp64 product and the fp32 conversion do: the product is exact in
+// fp64 because it stays inside fp64's normal range. For D > 13 the loop runs in fp64.
 //
 // Traffic per element: 4 (D - 1) B read + 4 B written; each thread takes four
 // consecutive columns (16-byte loads and stores).
@@ -41,24 +40,41 @@ __device__ __forceinline__ int bitlen128(u128 m) {
     return hi ? 128 - __clzll((long long)hi) : 64 - __clzll((long long)lo);
 }
 
-// |x| rounded to 53 significant bits, ties to even (x unchanged below 2^53)
-__device__ __forceinline__ i128 rne53(i128 x) {
-    const bool neg = x < 0;
-    const u128 m = neg ? (u128)0 - (u128)x : (u128)x;
-    const int nb = bitlen128(m);
-    if (nb <= 53) return x;
+// x (|x| < 2^127) rounded to 53 significant bits, ties to even, returned as q * 2^sh
+// with q an int64. Works on the two's complement words directly: the shift is a floor,
+// rem = x - q 2^sh is in [0, 2^sh), and rounding up on rem > half (or on a tie with q
+// odd) is round-half-even for either sign. The bit length of |x| is taken from x ^ sign
+// (= -x - 1 for x < 0), which differs from |x| only when |x| is a power of two, which
+// needs no rounding either way. Here |x| < 2^109, so 1 <= sh <= 56.
+__device__ __forceinline__ long long rne53(i128 x, int& sh_out) {
+    const uint64_t lo = (uint64_t)x;
+    const int64_t hi = (int64_t)(x >> 64);
+    const int64_t sm = hi >> 63;
+    const uint64_t yhi = (uint64_t)(hi ^ sm), ylo = lo ^ (uint64_t)sm;
+    const int nb = yhi ? 128 - __clzll((long long)yhi) : 64 - __clzll((long long)ylo);
+    if (nb <= 53) {  // |x| <= 2^53: exact, and it fits the low word
+        sh_out = 0;
+        return (long long)lo;
+    }
     const int sh = nb - 53;
-    uint64_t q = (uint64_t)(m >> sh);
-    const u128 rem = m - ((u128)q << sh);
-    const u128 half = (u128)1 << (sh - 1);
-    q += (uint64_t)((rem > half) | ((rem == half) & (q & 1u)));
-    const u128 r = (u128)q << sh;
-    return neg ? -(i128)r : (i128)r;
+    long long q = (long long)((lo >> sh) | ((uint64_t)hi << (64 - sh)));
+    const uint64_t rem = lo & ((1ull << sh) - 1ull);
+    const uint64_t half = 1ull << (sh - 1);
+    q += (long long)((rem > half) | ((rem == half) & ((uint64_t)q & 1ull)));
+    sh_out = sh;
+    return q;
+}
+
+// q * 2^sh as a 128-bit integer (0 <= sh <= 63)
+__device__ __forceinline__ i128 widen_shifted(long long q, int sh) {
+    const uint64_t lo = (uint64_t)q << sh;
+    const int64_t hi = sh ? (q >> (64 - sh)) : (q >> 63);
+    return (i128)(((u128)(uint64_t)hi << 64) | (u128)lo);
 }
 
 // fp32 round-to-nearest-even of Z * 2^s (Z an integer, |Z| < 2^127), subnormals kept,
 // overflow to infinity; +0 for Z == 0
-__device__ __forceinline__ float f32_from_i128_pow2(i128 Z, int s) {
+__device__ __noinline__ float f32_from_i128_pow2(i128 Z, int s) {
     if (Z == 0) return 0.0f;
     const uint32_t sign = Z < 0 ? 0x80000000u : 0u;
     const u128 m = Z < 0 ? (u128)0 - (u128)Z : (u128)Z;
@@ -90,19 +106,34 @@ __device__ __forceinline__ float f32_from_i128_pow2(i128 Z, int s) {
     return __uint_as_float(sign | bits);
 }
 
+// fp32 round-to-nearest-even of q * 2^t. When the result is a normal number the
+// hardware conversion rounds q to 24 bits (exactly the same rounding, as scaling by a
+// power of two commutes with rounding there) and t is added to the exponent field;
+// subnormal and overflowing results take the integer construction.
+__device__ __forceinline__ float f32_from_q(long long q, int t) {
+    if (q == 0) return 0.0f;
+    const uint64_t a = q < 0 ? 0ull - (uint64_t)q : (uint64_t)q;
+    const int E = 63 - __clzll((long long)a) + t;  // exponent of the leading bit
+    if (E >= -126 && E <= 126) {                   // stays normal after a round-up
+        const float f = __ll2float_rn(q);
+        return __uint_as_float(__float_as_uint(f) + ((uint32_t)t << 23));
+    }
+    return f32_from_i128_pow2((i128)q, t);
+}
+
 // the fixed-order combine of one element; t[d] = T_(D - d)
 template <int D>
 __device__ __forceinline__ float combine_int(const int32_t (&t)[D - 1], int32_t ei, int32_t fj) {
-    long long x = 0;
+    long long q = 0;
     constexpr int EXACT = D - 1 < 4 ? D - 1 : 4;
 #pragma unroll
-    for (int d = 0; d < EXACT; ++d) x += (long long)t[d] * (1ll << (7 * d));  // |x| < 2^53: no rounding
-    i128 Z = x;
+    for (int d = 0; d < EXACT; ++d) q += (long long)t[d] * (1ll << (7 * d));  // |q| < 2^53: no rounding
+    int sh = 0;
 #pragma unroll
-    for (int d = EXACT; d < D - 1; ++d) Z = rne53(Z + (i128)((u128)(i128)t[d] << (7 * d)));
+    for (int d = EXACT; d < D - 1; ++d) q = rne53(widen_shifted(q, sh) + (i128)((u128)(i128)t[d] << (7 * d)), sh);
     long long k = (long long)ei + (long long)fj;
     k = k > 300 ? 300 : (k < -300 ? -300 : k);
-    return f32_from_i128_pow2(Z, (int)k - 7 * D);
+    return f32_from_q(q, sh + (int)k - 7 * D);
 }
 
 template <int D>

@@ -136,6 +136,34 @@ DETGEMM_API detgemm_status detgemm_quantize_pow2(const void* X, int x_dtype, int
                                      detgemm_stream_t stream);
 
 /*
+ * W8A8 linear layer on floating-point activations [P4 §II "Pipeline and alibi" with
+ * the activation side quantized under a power-of-two scale as in §V]: the two calls
+ * detgemm_quantize_pow2 + detgemm_w8a8 in one, with the same result bits:
+ *     (Q, ea) = quantize_pow2(X, mode)                   (per row, as detgemm_quantize_pow2)
+ *     C_ij    = rne_bf16((sum_k Q_ik W_jk) * 2^(ea_i + ew_j))
+ * For M > 64 the quantizer writes the activation operand directly in the tensor
+ * cores' exact fp16 carrier form, so no int8 copy of it is written or widened.
+ *   X      [M x K] bf16 bit patterns (x_dtype BF16) or fp32 (x_dtype F32), stride ldx
+ *   mode   DETGEMM_POW2_NEAREST or DETGEMM_POW2_CEIL
+ *   W      int8 [N x K] (ldw), ew int32 [N]
+ *   W16    optional (may be NULL): the same weight widened once by detgemm_widen_i8_f16
+ *          (fp16 [N x ldw16], ldw16 a multiple of 8); when given and M > 64 it is read
+ *          instead of widening W on every call (a static weight widened at load time)
+ *   C      bf16 bit patterns [M x N] (ldc)
+ *   ea_out optional (may be NULL): int32 [M] receives the activation exponents
+ *   split_k, errors: as detgemm_w8a8; a non-finite row of X raises
+ *          DETGEMM_ERR_NONFINITE in the device status word (that row is quantized to 0)
+ *   ws     scratch of at least detgemm_linear_w8a8_workspace_size(M, N, K, split_k,
+ *          W16 != NULL) bytes, 256-byte aligned
+ */
+DETGEMM_API detgemm_status detgemm_linear_w8a8(const void* X, int x_dtype, int64_t ldx, int mode, const int8_t* W,
+                                               int64_t ldw, const uint16_t* W16, int64_t ldw16, const int32_t* ew,
+                                               uint16_t* C, int64_t ldc, int32_t* ea_out, int M, int N, int K,
+                                               int split_k, void* ws, size_t ws_bytes, detgemm_stream_t stream);
+
+DETGEMM_API size_t detgemm_linear_w8a8_workspace_size(int M, int N, int K, int split_k, int have_w16);
+
+/*
  * Ozaki slicing of an fp32 matrix [P3 §3 (a): each operand becomes 7-bit integer
  * slices under a power-of-two scale taken from frexp]. One shared exponent per row
  * (axis ROWS) or per column (axis COLS):

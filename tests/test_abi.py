@@ -119,6 +119,18 @@ def test_other_entry_points_validate(lib):
     assert o(P, 19024, P, 64, P, 64, 64, 64, 19024, 7, 8, 1, P, 1 << 40, None) == dg.ERR_PRECONDITION
     assert o(P, 64, P, 64, P, 64, 64, 64, 64, 7, 8, 1, P, 16, None) == dg.ERR_WORKSPACE
     assert dg.ozaki_workspace_size(64, 64, 64) > 7 * 64 * 64 * 2
+    li = lib.detgemm_linear_w8a8
+    # X, dtype, ldx, mode, W, ldw, W16, ldw16, ew, C, ldc, ea_out, M, N, K, split, ws, ws_bytes
+    assert li(P, 2, 64, 0, P, 64, None, 0, P, P, 64, None, 4, 64, 64, 1, P, 1 << 30, None) == dg.ERR_INVALID_ARG
+    assert li(P, 0, 64, 2, P, 64, None, 0, P, P, 64, None, 4, 64, 64, 1, P, 1 << 30, None) == dg.ERR_INVALID_ARG
+    assert li(P, 0, 131072, 0, P, 131072, None, 0, P, P, 64, None, 4, 64, 131072, 1, P, 1 << 30,
+              None) == dg.ERR_PRECONDITION
+    assert li(P, 0, 60, 0, P, 64, None, 0, P, P, 64, None, 4, 64, 60, 1, P, 1 << 30, None) == dg.ERR_ALIGNMENT
+    assert li(P, 0, 64, 0, P, 64, P1, 64, P, P, 64, None, 100, 64, 64, 1, P, 1 << 30, None) == dg.ERR_ALIGNMENT
+    assert li(P, 0, 64, 0, P, 64, None, 0, P, P, 64, None, 100, 64, 64, 1, P, 16, None) == dg.ERR_WORKSPACE
+    assert li(P, 0, 64, 0, P, 64, None, 0, P, P, 64, None, 0, 64, 64, 1, None, 0, None) == dg.OK
+    assert lib.detgemm_linear_w8a8_workspace_size(100, 64, 64, 1, 0) > lib.detgemm_linear_w8a8_workspace_size(
+        100, 64, 64, 1, 1)
     c = lib.detgemm_ozaki_combine
     assert c(P, 64, 1, P, P, P, 64, 4, 64, None) == dg.ERR_INVALID_ARG  # max_diag < 2
     assert c(P, 64, 19, P, P, P, 64, 4, 64, None) == dg.ERR_INVALID_ARG  # max_diag > 18
