@@ -67,9 +67,13 @@ def _load():
             lib.oracle_ozaki_f32.argtypes = [p, i64, p, i64, p, i64, i32, i32, i32, i32, i32, p, i32]
             lib.oracle_ozaki_diagonals.argtypes = [p, p, i32, i32, i32, i32, i32, p]
             lib.oracle_ozaki_combine.argtypes = [p, i64, i32, p, p, p, i64, i32, i32]
+            lib.oracle_ozaki_combine_f64.argtypes = [p, i64, i32, p, p, p, i64, i32, i32]
+            lib.oracle_slice_f64.argtypes = [p, i64, i32, i32, i32, i32, p, p]
+            lib.oracle_ozaki_f64.argtypes = [p, i64, p, i64, p, i64, i32, i32, i32, i32, i32, p, i32]
             for f in (lib.oracle_w8a8, lib.oracle_gemm_s8_i32, lib.oracle_quantize_pow2,
                       lib.oracle_slice_f32, lib.oracle_ozaki_f32, lib.oracle_ozaki_diagonals,
-                      lib.oracle_ozaki_combine):
+                      lib.oracle_ozaki_combine, lib.oracle_ozaki_combine_f64, lib.oracle_slice_f64,
+                      lib.oracle_ozaki_f64):
                 f.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -156,6 +160,19 @@ def slice_f32(X, axis=ROWS, nslices=7, check=True):
     return S, e
 
 
+def slice_f64(X, axis=ROWS, nslices=8, check=True):
+    """Ozaki digits of an fp64 matrix (same layout as slice_f32)."""
+    X = _c(X, np.float64)
+    rows, cols = X.shape
+    S = np.empty((nslices, rows, cols) if axis == ROWS else (nslices, cols, rows), dtype=np.int8)
+    e = np.empty((rows if axis == ROWS else cols,), dtype=np.int32)
+    st = _load().oracle_slice_f64(X.ctypes.data, cols, rows, cols, axis, nslices, S.ctypes.data,
+                                  e.ctypes.data)
+    if check and st != OK:
+        raise OracleError(f"oracle_slice_f64 status {st}")
+    return S, e
+
+
 def ozaki_f32(A, B, nslices=7, max_diag=8, rows=None, check=True):
     """Ozaki-scheme fp32 GEMM C = A B (fp32 [rows x N])."""
     A, B = _c(A, np.float32), _c(B, np.float32)
@@ -168,6 +185,21 @@ def ozaki_f32(A, B, nslices=7, max_diag=8, rows=None, check=True):
                                   nslices, max_diag, r.ctypes.data if r is not None else None, nr)
     if check and st != OK:
         raise OracleError(f"oracle_ozaki_f32 status {st}")
+    return C
+
+
+def ozaki_f64(A, B, nslices=8, max_diag=9, rows=None, check=True):
+    """fp64-target Ozaki-scheme GEMM C = A B (fp64 [rows x N])."""
+    A, B = _c(A, np.float64), _c(B, np.float64)
+    M, K = A.shape
+    K2, N = B.shape
+    assert K == K2
+    r, nr = _rows(rows)
+    C = np.empty((nr if r is not None else M, N), dtype=np.float64)
+    st = _load().oracle_ozaki_f64(A.ctypes.data, K, B.ctypes.data, N, C.ctypes.data, N, M, N, K,
+                                  nslices, max_diag, r.ctypes.data if r is not None else None, nr)
+    if check and st != OK:
+        raise OracleError(f"oracle_ozaki_f64 status {st}")
     return C
 
 
@@ -191,4 +223,15 @@ def ozaki_combine(T, e, f):
     assert e.shape == (M,) and f.shape == (N,) and 1 <= nd <= 17
     C = np.empty((M, N), dtype=np.float32)
     _load().oracle_ozaki_combine(T.ctypes.data, N, nd + 1, e.ctypes.data, f.ctypes.data, C.ctypes.data, N, M, N)
+    return C
+
+
+def ozaki_combine_f64(T, e, f):
+    """The fp64-target recombination: as ozaki_combine, result rounded to fp64 [M, N]."""
+    T = _c(T, np.int32)
+    e, f = _c(e, np.int32), _c(f, np.int32)
+    nd, M, N = T.shape
+    assert e.shape == (M,) and f.shape == (N,) and 1 <= nd <= 17
+    C = np.empty((M, N), dtype=np.float64)
+    _load().oracle_ozaki_combine_f64(T.ctypes.data, N, nd + 1, e.ctypes.data, f.ctypes.data, C.ctypes.data, N, M, N)
     return C

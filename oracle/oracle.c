@@ -181,11 +181,15 @@ int oracle_quantize_pow2(const void* X, int x_dtype, int64_t ldx, int rows, int 
 /* All steps are exact in fp64. Output planes S[t-1]:                                    */
 /*   axis 0: [rows x cols] row-major;  axis 1: [cols x rows] (each column contiguous).   */
 /* ------------------------------------------------------------------------------------ */
-static void slice_line(const float* X, int64_t stride, int len, int nslices, int8_t* S,
+static double load_line(const void* X, int f64, int64_t idx) {
+    return f64 ? ((const double*)X)[idx] : (double)((const float*)X)[idx];
+}
+
+static void slice_line(const void* X, int f64, int64_t stride, int len, int nslices, int8_t* S,
                        int64_t plane, int64_t sstride, int32_t* e_out, int* bad) {
     double a = 0.0;
     for (int k = 0; k < len; ++k) {
-        double x = X[(int64_t)k * stride];
+        double x = load_line(X, f64, (int64_t)k * stride);
         if (!isfinite(x)) *bad = 1;
         if (fabs(x) > a) a = fabs(x);
     }
@@ -193,7 +197,7 @@ static void slice_line(const float* X, int64_t stride, int len, int nslices, int
     if (a > 0.0 && isfinite(a)) frexp(a, &e);
     *e_out = e;
     for (int k = 0; k < len; ++k) {
-        double r = ldexp((double)X[(int64_t)k * stride], -e);
+        double r = ldexp(load_line(X, f64, (int64_t)k * stride), -e);
         if (!isfinite(r)) r = 0.0;
         for (int t = 0; t < nslices; ++t) {
             double v = r * 128.0;
@@ -204,27 +208,40 @@ static void slice_line(const float* X, int64_t stride, int len, int nslices, int
     }
 }
 
-int oracle_slice_f32(const float* X, int64_t ldx, int rows, int cols, int axis, int nslices,
+static int slice_any(const void* X, int f64, int64_t ldx, int rows, int cols, int axis, int nslices,
                      int8_t* S, int32_t* e_out) {
     int bad = 0;
     int64_t plane = (int64_t)rows * cols;
+    const size_t es = f64 ? sizeof(double) : sizeof(float);
     if (axis == 0) {
 #pragma omp parallel for schedule(dynamic, 16) reduction(| : bad)
         for (int i = 0; i < rows; ++i) {
             int b = 0;
-            slice_line(X + (int64_t)i * ldx, 1, cols, nslices, S + (int64_t)i * cols, plane, 1,
-                       e_out + i, &b);
+            slice_line((const char*)X + (size_t)i * (size_t)ldx * es, f64, 1, cols, nslices,
+                       S + (int64_t)i * cols, plane, 1, e_out + i, &b);
             bad |= b;
         }
     } else {
 #pragma omp parallel for schedule(dynamic, 16) reduction(| : bad)
         for (int j = 0; j < cols; ++j) {
             int b = 0;
-            slice_line(X + j, ldx, rows, nslices, S + (int64_t)j * rows, plane, 1, e_out + j, &b);
+            slice_line((const char*)X + (size_t)j * es, f64, ldx, rows, nslices, S + (int64_t)j * rows,
+                       plane, 1, e_out + j, &b);
             bad |= b;
         }
     }
     return bad ? ORACLE_ERR_NONFINITE : ORACLE_OK;
+}
+
+int oracle_slice_f32(const float* X, int64_t ldx, int rows, int cols, int axis, int nslices,
+                     int8_t* S, int32_t* e_out) {
+    return slice_any(X, 0, ldx, rows, cols, axis, nslices, S, e_out);
+}
+
+/* The same slicing of an fp64 matrix (every step is still exact in fp64). */
+int oracle_slice_f64(const double* X, int64_t ldx, int rows, int cols, int axis, int nslices,
+                     int8_t* S, int32_t* e_out) {
+    return slice_any(X, 1, ldx, rows, cols, axis, nslices, S, e_out);
 }
 
 /* ------------------------------------------------------------------------------------ */
@@ -237,6 +254,18 @@ static float combine_one(const int64_t* T, int max_diag, int32_t e, int32_t f) {
     double acc = 0.0;
     for (int g = max_diag; g >= 2; --g) acc = acc + ldexp((double)T[g], -7 * g);
     return (float)ldexp(acc, clamp_exp((int64_t)e + (int64_t)f));
+}
+
+/* The fp64-target form: the same loop, then C = acc * 2^(e + f) rounded to fp64 (exact   */
+/* unless the result is subnormal or overflows). |acc| lies in [2^-126, 2^144), so        */
+/* exponents beyond +-2200 give 0 or inf either way.                                      */
+static double combine_one_f64(const int64_t* T, int max_diag, int32_t e, int32_t f) {
+    double acc = 0.0;
+    for (int g = max_diag; g >= 2; --g) acc = acc + ldexp((double)T[g], -7 * g);
+    int64_t k = (int64_t)e + (int64_t)f;
+    if (k > 2200) k = 2200;
+    if (k < -2200) k = -2200;
+    return ldexp(acc, (int)k);
 }
 
 /* The recombination step alone: T int32 [max_diag - 1][M][ldT], plane p holding the     */
@@ -257,6 +286,22 @@ int oracle_ozaki_combine(const int32_t* T, int64_t ldT, int max_diag, const int3
     return ORACLE_OK;
 }
 
+int oracle_ozaki_combine_f64(const int32_t* T, int64_t ldT, int max_diag, const int32_t* e,
+                             const int32_t* f, double* C, int64_t ldc, int M, int N) {
+    int64_t plane = (int64_t)M * ldT;
+#pragma omp parallel for schedule(static)
+    for (int i = 0; i < M; ++i) {
+        int64_t Tg[19];
+        for (int j = 0; j < N; ++j) {
+            for (int g = 0; g <= max_diag; ++g) Tg[g] = 0;
+            for (int g = 2; g <= max_diag; ++g)
+                Tg[g] = T[(int64_t)(max_diag - g) * plane + (int64_t)i * ldT + j];
+            C[(int64_t)i * ldc + j] = combine_one_f64(Tg, max_diag, e[i], f[j]);
+        }
+    }
+    return ORACLE_OK;
+}
+
 /* ------------------------------------------------------------------------------------ */
 /* Ozaki fp32 GEMM [P3 §3 (a)]: C = A B with A [M x K], B [K x N] fp32 row-major.         */
 /*   slice A per row (e_i, DA_s) and B per column (f_j, DB_t);                           */
@@ -265,23 +310,24 @@ int oracle_ozaki_combine(const int32_t* T, int64_t ldT, int max_diag, const int3
 /*   C_ij = (float) (acc * 2^(e_i + f_j))          (one rounding to fp32, RNE)           */
 /* rows == NULL: all rows; else output row r is A-row rows[r].                           */
 /* ------------------------------------------------------------------------------------ */
-int oracle_ozaki_f32(const float* A, int64_t lda, const float* B, int64_t ldb, float* C,
-                     int64_t ldc, int M, int N, int K, int nslices, int max_diag,
-                     const int32_t* rows, int nrows) {
+static int ozaki_any(const void* A, int64_t lda, const void* B, int64_t ldb, void* C, int64_t ldc,
+                     int f64, int M, int N, int K, int nslices, int max_diag, const int32_t* rows,
+                     int nrows) {
     int n_out = rows ? nrows : M;
+    const size_t es = f64 ? sizeof(double) : sizeof(float);
     int8_t* DB = (int8_t*)malloc((size_t)nslices * N * K);
     int32_t* f = (int32_t*)malloc(sizeof(int32_t) * N);
     int8_t* DA = (int8_t*)malloc((size_t)nslices * n_out * K);
     int32_t* e = (int32_t*)malloc(sizeof(int32_t) * n_out);
     if (!DB || !f || !DA || !e) { free(DB); free(f); free(DA); free(e); return 1; }
-    int bad = oracle_slice_f32(B, ldb, K, N, 1, nslices, DB, f) != 0;
+    int bad = slice_any(B, f64, ldb, K, N, 1, nslices, DB, f) != 0;
     /* slice the requested rows of A */
     int bad_rows = 0;
     for (int r = 0; r < n_out; ++r) {
         int i = rows ? rows[r] : r;
         int b = 0;
-        slice_line(A + (int64_t)i * lda, 1, K, nslices, DA + (int64_t)r * K, (int64_t)n_out * K, 1,
-                   e + r, &b);
+        slice_line((const char*)A + (size_t)i * (size_t)lda * es, f64, 1, K, nslices, DA + (int64_t)r * K,
+                   (int64_t)n_out * K, 1, e + r, &b);
         bad_rows |= b;
     }
     int64_t planeA = (int64_t)n_out * K, planeB = (int64_t)N * K;
@@ -301,12 +347,30 @@ int oracle_ozaki_f32(const float* A, int64_t lda, const float* B, int64_t ldb, f
                     T[g] += acc;
                 }
             }
-            C[(int64_t)r * ldc + j] = combine_one(T, max_diag, e[r], f[j]);
+            if (f64)
+                ((double*)C)[(int64_t)r * ldc + j] = combine_one_f64(T, max_diag, e[r], f[j]);
+            else
+                ((float*)C)[(int64_t)r * ldc + j] = combine_one(T, max_diag, e[r], f[j]);
         }
         free(T);
     }
     free(DB); free(f); free(DA); free(e);
     return (bad || bad_rows) ? ORACLE_ERR_NONFINITE : ORACLE_OK;
+}
+
+int oracle_ozaki_f32(const float* A, int64_t lda, const float* B, int64_t ldb, float* C,
+                     int64_t ldc, int M, int N, int K, int nslices, int max_diag,
+                     const int32_t* rows, int nrows) {
+    return ozaki_any(A, lda, B, ldb, C, ldc, 0, M, N, K, nslices, max_diag, rows, nrows);
+}
+
+/* fp64-target Ozaki GEMM: the same slicing of fp64 operands (nslices digits of 7 bits),  */
+/* the same exact diagonal sums and fixed-order fp64 combine, and the result              */
+/* C_ij = acc * 2^(e_i + f_j) rounded to fp64.                                            */
+int oracle_ozaki_f64(const double* A, int64_t lda, const double* B, int64_t ldb, double* C,
+                     int64_t ldc, int M, int N, int K, int nslices, int max_diag,
+                     const int32_t* rows, int nrows) {
+    return ozaki_any(A, lda, B, ldb, C, ldc, 1, M, N, K, nslices, max_diag, rows, nrows);
 }
 
 /* Per-diagonal exact sums T_g (int64) for one output element set, for tests of the     */

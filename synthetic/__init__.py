@@ -61,8 +61,9 @@ def _load():
             lib.gen_normal_i8.argtypes = [u64, u64, i64, dbl, i32, ptr]
             lib.gen_normal_pow2_f32.argtypes = [u64, u64, i64, i32, i32, ptr]
             lib.gen_normal_f32.argtypes = [u64, u64, i64, dbl, ptr]
+            lib.gen_normal_pow2_f64.argtypes = [u64, u64, i64, i32, i32, ptr]
             for f in (lib.gen_uniform_i8, lib.gen_uniform_i32, lib.gen_normal_i8,
-                      lib.gen_normal_pow2_f32, lib.gen_normal_f32):
+                      lib.gen_normal_pow2_f32, lib.gen_normal_f32, lib.gen_normal_pow2_f64):
                 f.restype = None
             _lib = lib
     return _lib
@@ -96,6 +97,12 @@ def normal_i8(seed, stream, shape, sigma, clip=127, out=None):
 def normal_pow2_f32(seed, stream, shape, ulo=-8, uhi=8, out=None):
     out = _out(shape, np.float32, out)
     _load().gen_normal_pow2_f32(seed, stream, out.size, ulo, uhi, out.ctypes.data)
+    return out
+
+
+def normal_pow2_f64(seed, stream, shape, ulo=0, uhi=0, out=None):
+    out = _out(shape, np.float64, out)
+    _load().gen_normal_pow2_f64(seed, stream, out.size, ulo, uhi, out.ctypes.data)
     return out
 
 
@@ -157,4 +164,11 @@ def ozaki(n=4096, seed=4):
     """fp32 A, B (n x n, row-major) with entries N(0,1) * 2^U, U in [-8, 8]."""
     A = normal_pow2_f32(seed, 0, (n, n), -8, 8)
     B = normal_pow2_f32(seed, 1, (n, n), -8, 8)
+    return A, B
+
+
+def ozaki_f64(n=4096, seed=5, ulo=0, uhi=0):
+    """fp64 A, B (n x n, row-major) with entries N(0,1) * 2^U, U uniform in [ulo, uhi]."""
+    A = normal_pow2_f64(seed, 0, (n, n), ulo, uhi)
+    B = normal_pow2_f64(seed, 1, (n, n), ulo, uhi)
     return A, B

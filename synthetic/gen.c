@@ -85,6 +85,17 @@ void gen_normal_pow2_f32(uint64_t seed, uint64_t stream, int64_t n, int ulo, int
     }
 }
 
+/* N(0, 1) * 2^U as fp64 (U uniform in [ulo, uhi], exponent draws on stream + 1000). */
+void gen_normal_pow2_f64(uint64_t seed, uint64_t stream, int64_t n, int ulo, int uhi, double* out) {
+    uint64_t key = stream_key(seed, stream);
+    uint64_t ukey = stream_key(seed, stream + 1000);
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i) {
+        int u = (int)uniform_int(draw(ukey, (uint64_t)i), ulo, uhi);
+        out[i] = ldexp(std_normal(key, (uint64_t)i), u);
+    }
+}
+
 /* sigma * N(0, 1) as fp32 (activation-like inputs for the quantizer). */
 void gen_normal_f32(uint64_t seed, uint64_t stream, int64_t n, double sigma, float* out) {
     uint64_t key = stream_key(seed, stream);

@@ -78,3 +78,15 @@ def rne_f32_exact(v: Fraction) -> np.float32:
 
 def pow2(e: int) -> Fraction:
     return Fraction(2) ** e if e >= 0 else Fraction(1, 2 ** (-e))
+
+
+def rne_f64_exact(v: Fraction) -> float:
+    """fp64 nearest to v (ties to even; subnormals kept; overflow to +-inf). Python's
+    int/Fraction to float conversion is correctly rounded; only its overflow needs care."""
+    v = Fraction(v)
+    if v == 0:
+        return 0.0
+    big = Fraction(2) ** 1024 - Fraction(2) ** (1024 - 54)  # halfway between max finite and 2^1024
+    if abs(v) >= big:
+        return float("inf") if v > 0 else float("-inf")
+    return float(v)
