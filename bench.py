@@ -8,7 +8,8 @@ INT8 TOPS (2 M N K per GEMM / time) with the dominant kernel's roofline fraction
 
 The same JSON line carries extra measurements of the other hot-path rows: the skinny
 decode-shaped GEMM (M=16, N=4096, K=65536, split-K 8/16/32) in GB/s against the HBM
-roofline, the Ozaki fp32 GEMM (4096^3) in effective fp32 TFLOP/s, the fused linear layer
+roofline, the Ozaki fp32 GEMM (4096^3) in effective fp32 TFLOP/s, the fp64-target Ozaki
+GEMM (4096^3) next to the library fp64 GEMM, the fused linear layer
 on bf16 activations at the FFN gate/up size, and the sweep linear (M=2048, K=2048, N=6144).
 
 Timing: W warm-up steps, then K timed steps; L2 is flushed before every timed step,
@@ -76,7 +77,7 @@ def parse():
     ap.add_argument("--no-extras", action="store_true", help="skip the extra rows")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", default=None,
-                    choices=["ffn_gate_up", "ffn_down", "skinny8", "skinny32", "ozaki", "sweep"],
+                    choices=["ffn_gate_up", "ffn_down", "skinny8", "skinny32", "ozaki", "ozaki_f64", "sweep"],
                     help="run one workload call twice (warm-up + one more) for an ncu capture, then exit")
     return ap.parse_args()
 
@@ -431,6 +432,18 @@ def extras(dg, torch, dev, pk, flush):
     res["ozaki_f32_4096"] = {"ms": round(ms, 3), "effective_fp32_TFLOPs": round(2 * 4096 ** 3 / (ms * 1e-3) / 1e12, 2),
                              "slice_TOPS": round(28 * 2 * 4096 ** 3 / (ms * 1e-3) / 1e12, 1)}
     del Af, Bf, Cf, ws
+    # fp64-target Ozaki GEMM 4096^3 (8 slices, 36 slice pairs), next to the fp64 GEMM of the
+    # vendor library on the same operands (context: GB300's fp64 rate)
+    Ad, Bd = (tdev(x) for x in synthetic.ozaki_f64(4096))
+    Cd = torch.empty((4096, 4096), dtype=torch.float64, device=dev)
+    ws = torch.empty(dg.ozaki_f64_workspace_size(4096, 4096, 4096), dtype=torch.uint8, device=dev)
+    ms = _time(torch, lambda: dg.ozaki_f64(Ad, Bd, out=Cd, ws=ws), flush, reps=3, warm=1)
+    ms_lib = _time(torch, lambda: torch.matmul(Ad, Bd, out=Cd), flush, reps=3, warm=1)
+    res["ozaki_f64_4096"] = {"ms": round(ms, 3), "effective_fp64_TFLOPs": round(2 * 4096 ** 3 / (ms * 1e-3) / 1e12, 2),
+                             "slice_TOPS": round(36 * 2 * 4096 ** 3 / (ms * 1e-3) / 1e12, 1),
+                             "library_dgemm_ms": round(ms_lib, 3),
+                             "library_dgemm_TFLOPs": round(2 * 4096 ** 3 / (ms_lib * 1e-3) / 1e12, 2)}
+    del Ad, Bd, Cd, ws
     # fused linear layer on bf16 activations at the FFN gate/up size: quantize + GEMM in one
     # call, against the same two steps as separate calls
     M, K, N = 8192, 4096, 12288
@@ -486,6 +499,9 @@ def run_profile(name):
         split = {"skinny8": 8, "skinny32": 32}.get(name, 1)
         A, W, ea, ew = (tdev(x) for x in args)
         fn = lambda: dg.w8a8(A, W, ea, ew, split_k=split)
+    elif name == "ozaki_f64":
+        Ad, Bd = (tdev(x) for x in synthetic.ozaki_f64(4096))
+        fn = lambda: dg.ozaki_f64(Ad, Bd)
     else:
         Af, Bf = (tdev(x) for x in synthetic.ozaki(4096))
         fn = lambda: dg.ozaki_f32(Af, Bf)

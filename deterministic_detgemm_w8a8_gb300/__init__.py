@@ -15,6 +15,7 @@ Functions mirror the C entry points:
 * :func:`slice_f32`      Ozaki digit planes with shared exponents
 * :func:`ozaki_f32`      Ozaki-scheme fp32 GEMM C = A B
 * :func:`ozaki_combine`  its fixed-order fp64 recombination step alone
+* :func:`ozaki_f64`      the fp64-target Ozaki GEMM (DGEMM emulation), :func:`slice_f64`
 """
 from __future__ import annotations
 
@@ -29,7 +30,7 @@ LIB_PATH = os.path.join(_HERE, "libdetgemm.so")
 
 OK, ERR_INVALID_ARG, ERR_ALIGNMENT, ERR_PRECONDITION, ERR_WORKSPACE = 0, 1, 2, 3, 4
 ERR_UNSUPPORTED_DEVICE, ERR_CUDA, ERR_TIMEOUT, ERR_NONFINITE = 5, 6, 7, 8
-DTYPE_BF16, DTYPE_F32 = 0, 1
+DTYPE_BF16, DTYPE_F32, DTYPE_F64 = 0, 1, 2
 POW2_NEAREST, POW2_CEIL = 0, 1
 AXIS_ROWS, AXIS_COLS = 0, 1
 MAX_K = 131071
@@ -47,7 +48,10 @@ SIGNATURES = {
     "detgemm_slice_f32": ([_P, _I64, _I32, _I32, _I32, _I32, _P, _P, _P], _I32),
     "detgemm_ozaki_f32": ([_P, _I64, _P, _I64, _P, _I64, _I32, _I32, _I32, _I32, _I32, _I32, _P, _SZ, _P], _I32),
     "detgemm_ozaki_workspace_size": ([_I32, _I32, _I32, _I32, _I32, _I32], _SZ),
-    "detgemm_ozaki_combine": ([_P, _I64, _I32, _P, _P, _P, _I64, _I32, _I32, _P], _I32),
+    "detgemm_ozaki_combine": ([_P, _I64, _I32, _P, _P, _P, _I32, _I64, _I32, _I32, _P], _I32),
+    "detgemm_slice_f64": ([_P, _I64, _I32, _I32, _I32, _I32, _P, _P, _P], _I32),
+    "detgemm_ozaki_f64": ([_P, _I64, _P, _I64, _P, _I64, _I32, _I32, _I32, _I32, _I32, _I32, _P, _SZ, _P], _I32),
+    "detgemm_ozaki_f64_workspace_size": ([_I32, _I32, _I32, _I32, _I32, _I32], _SZ),
     "detgemm_linear_w8a8": ([_P, _I32, _I64, _I32, _P, _I64, _P, _I64, _P, _P, _I64, _P, _I32, _I32, _I32, _I32,
                              _P, _SZ, _P], _I32),
     "detgemm_linear_w8a8_workspace_size": ([_I32, _I32, _I32, _I32, _I32], _SZ),
@@ -284,9 +288,10 @@ def ozaki_f32(A, B, nslices: int = 7, max_diag: int = 8, split_k: int = 1, out=N
     return out
 
 
-def ozaki_combine(T, e, f, out=None, stream=None) -> torch.Tensor:
+def ozaki_combine(T, e, f, out=None, dtype=torch.float32, stream=None) -> torch.Tensor:
     """Fixed-order recombination of exact diagonal sums: T int32 [max_diag - 1, M, N]
-    (plane p holds the diagonal g = max_diag - p), e int32 [M], f int32 [N] -> fp32 [M, N]."""
+    (plane p holds the diagonal g = max_diag - p), e int32 [M], f int32 [N] -> fp32 or
+    fp64 [M, N] (``dtype``)."""
     lib = load()
     _req(T, torch.int32, "T"); _req(e, torch.int32, "e"); _req(f, torch.int32, "f")
     if T.dim() != 3 or T.stride(2) != 1 or T.stride(0) != T.shape[1] * T.stride(1):
@@ -294,12 +299,54 @@ def ozaki_combine(T, e, f, out=None, stream=None) -> torch.Tensor:
     nd, M, N = T.shape
     if e.shape != (M,) or f.shape != (N,):
         raise ValueError("shape mismatch")
+    if dtype not in (torch.float32, torch.float64):
+        raise TypeError("dtype must be float32 or float64")
     if out is None:
-        out = empty2d(M, N, torch.float32, T.device)
-    _req(out, torch.float32, "out")
+        out = empty2d(M, N, dtype, T.device)
+    _req(out, dtype, "out")
+    cdt = DTYPE_F64 if dtype == torch.float64 else DTYPE_F32
     st = lib.detgemm_ozaki_combine(T.data_ptr(), T.stride(1), nd + 1, e.data_ptr(), f.data_ptr(), out.data_ptr(),
-                                   _ld(out), M, N, _stream(stream))
+                                   cdt, _ld(out), M, N, _stream(stream))
     _check(st, "detgemm_ozaki_combine")
+    return out
+
+
+def slice_f64(X, axis: int = AXIS_ROWS, nslices: int = 8, stream=None):
+    """Ozaki digits of fp64 X: (S int8 [nslices, rows, cols] or [nslices, cols, rows], e int32)."""
+    lib = load()
+    _req(X, torch.float64, "X")
+    rows, cols = X.shape
+    shape = (nslices, rows, cols) if axis == AXIS_ROWS else (nslices, cols, rows)
+    S = torch.empty(shape, dtype=torch.int8, device=X.device)
+    e = torch.empty((rows if axis == AXIS_ROWS else cols,), dtype=torch.int32, device=X.device)
+    st = lib.detgemm_slice_f64(X.data_ptr(), _ld(X), rows, cols, axis, nslices, S.data_ptr(), e.data_ptr(),
+                               _stream(stream))
+    _check(st, "detgemm_slice_f64")
+    return S, e
+
+
+def ozaki_f64_workspace_size(M, N, K, nslices=8, max_diag=9, split_k=1) -> int:
+    return int(load().detgemm_ozaki_f64_workspace_size(M, N, K, nslices, max_diag, split_k))
+
+
+def ozaki_f64(A, B, nslices: int = 8, max_diag: int = 9, split_k: int = 1, out=None, ws=None,
+              stream=None) -> torch.Tensor:
+    """fp64-target Ozaki-scheme GEMM C = A B (A [M,K], B [K,N] fp64 row-major)."""
+    lib = load()
+    _req(A, torch.float64, "A"); _req(B, torch.float64, "B")
+    M, K = A.shape
+    K2, N = B.shape
+    if K2 != K:
+        raise ValueError("shape mismatch")
+    if out is None:
+        out = empty2d(M, N, torch.float64, A.device)
+    _req(out, torch.float64, "out")
+    need = ozaki_f64_workspace_size(M, N, K, nslices, max_diag, split_k)
+    wsb, wsn = _workspace(need, A.device, ws)
+    st = lib.detgemm_ozaki_f64(A.data_ptr(), _ld(A), B.data_ptr(), _ld(B), out.data_ptr(), _ld(out),
+                               M, N, K, nslices, max_diag, split_k,
+                               wsb.data_ptr() if wsb is not None else None, wsn, _stream(stream))
+    _check(st, "detgemm_ozaki_f64")
     return out
 
 

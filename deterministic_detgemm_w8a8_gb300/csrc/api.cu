@@ -336,26 +336,51 @@ detgemm_status detgemm_slice_f32(const float* X, int64_t ldx, int rows, int cols
     return from_cuda(slice_cols_launch(X, ldx, rows, cols, nslices, S, rows, e, s));
 }
 
+detgemm_status detgemm_slice_f64(const double* X, int64_t ldx, int rows, int cols, int axis, int nslices, int8_t* S,
+                                 int32_t* e, detgemm_stream_t stream) {
+    if (rows < 0 || cols < 0) return DETGEMM_ERR_INVALID_ARG;
+    if (nslices < 1 || nslices > 12) return DETGEMM_ERR_INVALID_ARG;
+    if (axis != DETGEMM_AXIS_ROWS && axis != DETGEMM_AXIS_COLS) return DETGEMM_ERR_INVALID_ARG;
+    if (rows == 0 || cols == 0) return DETGEMM_OK;
+    if (!X || !S || !e || ldx < cols) return DETGEMM_ERR_INVALID_ARG;
+    if (!aligned16(X) || !aligned16(S) || !aligned4(e) || (ldx * 8) % 16) return DETGEMM_ERR_ALIGNMENT;
+    detgemm_status st = check_device();
+    if (st != DETGEMM_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    return from_cuda(slice_f64_launch(X, ldx, rows, cols, axis, nslices, S, axis == DETGEMM_AXIS_ROWS ? cols : rows,
+                                      e, s));
+}
+
 size_t detgemm_ozaki_workspace_size(int M, int N, int K, int nslices, int max_diag, int split_k) {
     if (M <= 0 || N <= 0 || K <= 0 || nslices < 1 || max_diag < 2) return 0;
     return ozaki_layout(M, N, K, nslices, max_diag, split_k).total;
 }
 
-detgemm_status detgemm_ozaki_f32(const float* A, int64_t lda, const float* B, int64_t ldb, float* C, int64_t ldc,
-                                 int M, int N, int K, int nslices, int max_diag, int split_k, void* ws,
-                                 size_t ws_bytes, detgemm_stream_t stream) {
+// Shared Ozaki driver: slice A per row and B per column into fp16 digit planes, all
+// diagonals' exact slice products in one tensor-core launch (largest first; group d is
+// diagonal g = max_diag - d and pairs A slice sA with B slice g - sA), then the combine.
+static detgemm_status ozaki_run(const void* A, int64_t lda, const void* B, int64_t ldb, void* C, int64_t ldc,
+                                bool f64, int M, int N, int K, int nslices, int max_diag, int split_k, void* ws,
+                                size_t ws_bytes, detgemm_stream_t stream) {
     if (M < 0 || N < 0 || K < 1) return DETGEMM_ERR_INVALID_ARG;
-    if (nslices < 1 || nslices > 9 || max_diag < 2 || max_diag > 2 * nslices) return DETGEMM_ERR_INVALID_ARG;
+    const int max_slices = f64 ? 12 : 9;
+    if (nslices < 1 || nslices > max_slices || max_diag < 2 || max_diag > 2 * nslices || max_diag > kTcMaxDiag)
+        return DETGEMM_ERR_INVALID_ARG;
     int nkb = (K + 63) / 64;
     if (split_k < 1 || split_k > nkb) return DETGEMM_ERR_INVALID_ARG;
-    // every diagonal sum must stay in int32: at most nslices pairs of K products of |d| <= 127
+    // every diagonal sum must stay in int32: at most min(g - 1, nslices) pairs of K products of |d| <= 127
     int pairs = max_diag - 1 < nslices ? max_diag - 1 : nslices;
     if ((long long)pairs * K * 127 * 127 >= 2147483648LL) return DETGEMM_ERR_PRECONDITION;
+    int total_pairs = 0;
+    for (int g = 2; g <= max_diag; ++g)
+        for (int sA = 1; sA <= nslices; ++sA) total_pairs += (g - sA >= 1 && g - sA <= nslices) ? 1 : 0;
+    if (total_pairs > kTcMaxSeg) return DETGEMM_ERR_INVALID_ARG;
     if (M == 0 || N == 0) return DETGEMM_OK;
     if (!A || !B || !C) return DETGEMM_ERR_INVALID_ARG;
     if (lda < K || ldb < N || ldc < N) return DETGEMM_ERR_INVALID_ARG;
+    const int es = f64 ? 8 : 4;
     if (!aligned16(A) || !aligned16(B) || !aligned16(C)) return DETGEMM_ERR_ALIGNMENT;
-    if ((lda * 4) % 16 || (ldb * 4) % 16 || (ldc * 4) % 16) return DETGEMM_ERR_ALIGNMENT;
+    if ((lda * es) % 16 || (ldb * es) % 16 || (ldc * es) % 16) return DETGEMM_ERR_ALIGNMENT;
     OzakiLayout L = ozaki_layout(M, N, K, nslices, max_diag, split_k);
     if (ws == nullptr || ws_bytes < L.total) return DETGEMM_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return DETGEMM_ERR_ALIGNMENT;
@@ -366,11 +391,17 @@ detgemm_status detgemm_ozaki_f32(const float* A, int64_t lda, const float* B, in
     int32_t* e = reinterpret_cast<int32_t*>(base + L.e);
     int32_t* f = reinterpret_cast<int32_t*>(base + L.f);
     int32_t* T = reinterpret_cast<int32_t*>(base + L.T);
-    cudaError_t err = slice_rows_f16_launch(A, lda, M, K, nslices, base + L.da, L.Kp, e, s);
-    if (err == cudaSuccess) err = slice_cols_f16_launch(B, ldb, K, N, nslices, base + L.db, L.Kp, f, s);
+    cudaError_t err;
+    if (f64) {
+        err = slice_f64_f16_launch(static_cast<const double*>(A), lda, M, K, 0, nslices, base + L.da, L.Kp, e, s);
+        if (err == cudaSuccess)
+            err = slice_f64_f16_launch(static_cast<const double*>(B), ldb, K, N, 1, nslices, base + L.db, L.Kp, f, s);
+    } else {
+        err = slice_rows_f16_launch(static_cast<const float*>(A), lda, M, K, nslices, base + L.da, L.Kp, e, s);
+        if (err == cudaSuccess)
+            err = slice_cols_f16_launch(static_cast<const float*>(B), ldb, K, N, nslices, base + L.db, L.Kp, f, s);
+    }
     if (err != cudaSuccess) return DETGEMM_ERR_CUDA;
-    // all diagonals in one persistent launch, the largest (most slice pairs) first;
-    // group d is diagonal g = max_diag - d and pairs A slice sA with B slice g - sA
     TcArgs a = {};
     a.M = M;
     a.N = N;
@@ -394,21 +425,44 @@ detgemm_status detgemm_ozaki_f32(const float* A, int64_t lda, const float* B, in
     a.ldc = L.ldT;
     a.c_plane = (int64_t)M * L.ldT;
     err = tc_gemm_launch(a, base + L.da, L.Kp, nslices, base + L.db, L.Kp, nslices, L.Kp, base + L.split, s);
-    if (err == cudaSuccess) err = ozaki_combine_launch(T, L.ldT, max_diag, e, f, C, ldc, M, N, s);
+    if (err == cudaSuccess)
+        err = f64 ? ozaki_combine_f64out_launch(T, L.ldT, max_diag, e, f, static_cast<double*>(C), ldc, M, N, s)
+                  : ozaki_combine_launch(T, L.ldT, max_diag, e, f, static_cast<float*>(C), ldc, M, N, s);
     return from_cuda(err);
 }
 
+detgemm_status detgemm_ozaki_f32(const float* A, int64_t lda, const float* B, int64_t ldb, float* C, int64_t ldc,
+                                 int M, int N, int K, int nslices, int max_diag, int split_k, void* ws,
+                                 size_t ws_bytes, detgemm_stream_t stream) {
+    return ozaki_run(A, lda, B, ldb, C, ldc, false, M, N, K, nslices, max_diag, split_k, ws, ws_bytes, stream);
+}
+
+detgemm_status detgemm_ozaki_f64(const double* A, int64_t lda, const double* B, int64_t ldb, double* C, int64_t ldc,
+                                 int M, int N, int K, int nslices, int max_diag, int split_k, void* ws,
+                                 size_t ws_bytes, detgemm_stream_t stream) {
+    return ozaki_run(A, lda, B, ldb, C, ldc, true, M, N, K, nslices, max_diag, split_k, ws, ws_bytes, stream);
+}
+
+size_t detgemm_ozaki_f64_workspace_size(int M, int N, int K, int nslices, int max_diag, int split_k) {
+    return detgemm_ozaki_workspace_size(M, N, K, nslices, max_diag, split_k);
+}
+
 detgemm_status detgemm_ozaki_combine(const int32_t* T, int64_t ldT, int max_diag, const int32_t* e,
-                                     const int32_t* f, float* C, int64_t ldc, int M, int N,
+                                     const int32_t* f, void* C, int c_dtype, int64_t ldc, int M, int N,
                                      detgemm_stream_t stream) {
     if (M < 0 || N < 0 || max_diag < 2 || max_diag > 18) return DETGEMM_ERR_INVALID_ARG;
+    if (c_dtype != DETGEMM_DTYPE_F32 && c_dtype != DETGEMM_DTYPE_F64) return DETGEMM_ERR_INVALID_ARG;
     if (M == 0 || N == 0) return DETGEMM_OK;
     if (!T || !e || !f || !C || ldT < N || ldc < N) return DETGEMM_ERR_INVALID_ARG;
+    const int cs = c_dtype == DETGEMM_DTYPE_F64 ? 8 : 4;
     if (!aligned16(T) || !aligned16(C) || !aligned4(e) || !aligned4(f)) return DETGEMM_ERR_ALIGNMENT;
-    if ((ldT * 4) % 16 || (ldc * 4) % 16) return DETGEMM_ERR_ALIGNMENT;
+    if ((ldT * 4) % 16 || (ldc * cs) % 16) return DETGEMM_ERR_ALIGNMENT;
     detgemm_status st = check_device();
     if (st != DETGEMM_OK) return st;
-    return from_cuda(ozaki_combine_launch(T, ldT, max_diag, e, f, C, ldc, M, N, reinterpret_cast<cudaStream_t>(stream)));
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (c_dtype == DETGEMM_DTYPE_F64)
+        return from_cuda(ozaki_combine_f64out_launch(T, ldT, max_diag, e, f, static_cast<double*>(C), ldc, M, N, s));
+    return from_cuda(ozaki_combine_launch(T, ldT, max_diag, e, f, static_cast<float*>(C), ldc, M, N, s));
 }
 
 detgemm_status detgemm_widen_i8_f16(const int8_t* X, int64_t ldx, int rows, int cols, uint16_t* Y, int64_t ldy,

@@ -101,17 +101,6 @@ __device__ __forceinline__ double pow2_f64(int k) {
     return __longlong_as_double((long long)(k + 1023) << 52);
 }
 
-// Epilogue E2 — "GPU Mechanism", §3 (a): fixed-order fp64 recombination of the exact
-// diagonal sums, then one rounding to fp32. T[g] holds the int32 diagonal sum of
-// weight 2^(-7g); the order g = max_diag .. 2 is fixed.
-__device__ __forceinline__ float ozaki_combine(const int32_t* T, int max_diag, int32_t ei, int32_t fj) {
-    double acc = 0.0;
-    for (int g = max_diag; g >= 2; --g) acc = __dadd_rn(acc, __dmul_rn((double)T[g], pow2_f64(-7 * g)));
-    long long k = (long long)ei + (long long)fj;
-    k = k > 300 ? 300 : (k < -300 ? -300 : k);
-    return __double2float_rn(__dmul_rn(acc, pow2_f64((int)k)));
-}
-
 // |x| of an fp32 bit pattern normalised to x = M * 2^(p - 23), M in [2^23, 2^24).
 // Returns false for zero. Subnormals are normalised.
 __device__ __forceinline__ bool f32_normalise(uint32_t absbits, uint32_t& M, int& p) {

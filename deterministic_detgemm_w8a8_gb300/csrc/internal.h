@@ -62,6 +62,11 @@ cudaError_t slice_rows_f16_launch(const float* X, int64_t ldx, int rows, int col
                                   int64_t lds, int32_t* e, cudaStream_t s);
 cudaError_t slice_cols_f16_launch(const float* X, int64_t ldx, int rows, int cols, int nslices, void* S,
                                   int64_t lds, int32_t* e, cudaStream_t s);
+// fp64 operands: axis 0 = rows, 1 = columns; int8 digits or exact fp16 digit values
+cudaError_t slice_f64_launch(const double* X, int64_t ldx, int rows, int cols, int axis, int nslices, int8_t* S,
+                             int64_t lds, int32_t* e, cudaStream_t s);
+cudaError_t slice_f64_f16_launch(const double* X, int64_t ldx, int rows, int cols, int axis, int nslices, void* S,
+                                 int64_t lds, int32_t* e, cudaStream_t s);
 
 // ------------------------------------------------------------------------------------
 // tcgen05 engine (gemm_tc.cu): exact int GEMM on fp16-carried operand planes.
@@ -118,5 +123,8 @@ cudaError_t tc_take_status(uint32_t* bits);
 // g = max_diag - d (largest weight index first) -> C fp32.
 cudaError_t ozaki_combine_launch(const int32_t* T, int64_t ldT, int max_diag, const int32_t* e, const int32_t* f,
                                  float* C, int64_t ldc, int M, int N, cudaStream_t s);
+// the same with the result rounded to fp64 (the fp64-target scheme)
+cudaError_t ozaki_combine_f64out_launch(const int32_t* T, int64_t ldT, int max_diag, const int32_t* e,
+                                        const int32_t* f, double* C, int64_t ldc, int M, int N, cudaStream_t s);
 
 }  // namespace detgemm

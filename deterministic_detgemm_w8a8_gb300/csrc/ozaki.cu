@@ -121,9 +121,54 @@ __device__ __forceinline__ float f32_from_q(long long q, int t) {
     return f32_from_i128_pow2((i128)q, t);
 }
 
+// fp64 round-to-nearest-even of q * 2^t (|q| <= 2^53): exact for normal results (q has at
+// most 53 significant bits), rounded at 2^-1074 for subnormal ones, infinity on overflow
+__device__ __forceinline__ double f64_from_q(long long q, int t) {
+    if (q == 0) return 0.0;
+    const uint64_t sign = q < 0 ? 0x8000000000000000ull : 0ull;
+    const uint64_t a = q < 0 ? 0ull - (uint64_t)q : (uint64_t)q;
+    const int nb = 64 - __clzll((long long)a);
+    const int E = nb - 1 + t;
+    if (E > 1023) return __longlong_as_double((long long)(sign | 0x7FF0000000000000ull));
+    uint64_t bits;
+    if (E >= -1022) {
+        const uint64_t m = nb <= 53 ? a << (53 - nb) : a >> (nb - 53);  // a = 2^53 drops a zero
+        bits = ((uint64_t)(E + 1023) << 52) | (m & 0x000FFFFFFFFFFFFFull);
+    } else {
+        const int up = t + 1074;  // value in units of 2^-1074 is a * 2^up
+        if (up >= 0) {
+            bits = a << up;  // < 2^52: exact
+        } else {
+            const int sh = -up;
+            if (sh > nb) {
+                bits = 0;  // below half a unit
+            } else {
+                const uint64_t qq = sh >= 64 ? 0ull : a >> sh;
+                const uint64_t rem = a - (sh >= 64 ? 0ull : qq << sh);
+                const uint64_t half = 1ull << (sh - 1);
+                bits = qq + (uint64_t)((rem > half) | ((rem == half) & (qq & 1ull)));
+            }
+        }
+    }
+    return __longlong_as_double((long long)(sign | bits));
+}
+
+template <typename OutT>
+struct Out;
+template <>
+struct Out<float> {
+    static constexpr int KMAX = 300;  // |acc| in [2^-91, 2^109): beyond, 0 or inf either way
+    static __device__ __forceinline__ float from_q(long long q, int t) { return f32_from_q(q, t); }
+};
+template <>
+struct Out<double> {
+    static constexpr int KMAX = 2200;
+    static __device__ __forceinline__ double from_q(long long q, int t) { return f64_from_q(q, t); }
+};
+
 // the fixed-order combine of one element; t[d] = T_(D - d)
-template <int D>
-__device__ __forceinline__ float combine_int(const int32_t (&t)[D - 1], int32_t ei, int32_t fj) {
+template <int D, typename OutT>
+__device__ __forceinline__ OutT combine_int(const int32_t (&t)[D - 1], int32_t ei, int32_t fj) {
     long long q = 0;
     constexpr int EXACT = D - 1 < 4 ? D - 1 : 4;
 #pragma unroll
@@ -132,14 +177,14 @@ __device__ __forceinline__ float combine_int(const int32_t (&t)[D - 1], int32_t 
 #pragma unroll
     for (int d = EXACT; d < D - 1; ++d) q = rne53(widen_shifted(q, sh) + (i128)((u128)(i128)t[d] << (7 * d)), sh);
     long long k = (long long)ei + (long long)fj;
-    k = k > 300 ? 300 : (k < -300 ? -300 : k);
-    return f32_from_q(q, sh + (int)k - 7 * D);
+    k = k > Out<OutT>::KMAX ? Out<OutT>::KMAX : (k < -Out<OutT>::KMAX ? -Out<OutT>::KMAX : k);
+    return Out<OutT>::from_q(q, sh + (int)k - 7 * D);
 }
 
-template <int D>
+template <int D, typename OutT>
 __global__ void __launch_bounds__(256) ozaki_combine_int_kernel(const int32_t* __restrict__ T, int64_t ldT,
                                                                 const int32_t* __restrict__ e,
-                                                                const int32_t* __restrict__ f, float* __restrict__ C,
+                                                                const int32_t* __restrict__ f, OutT* __restrict__ C,
                                                                 int64_t ldc, int M, int N) {
     const int j0 = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
     const int i = blockIdx.y;
@@ -147,64 +192,82 @@ __global__ void __launch_bounds__(256) ozaki_combine_int_kernel(const int32_t* _
     const int64_t plane = (int64_t)M * ldT;
     const int64_t idx = (int64_t)i * ldT + j0;
     const int32_t ei = __ldg(e + i);
-    float* c = C + (int64_t)i * ldc + j0;
+    OutT* c = C + (int64_t)i * ldc + j0;
     if (j0 + 4 <= N) {
         int4 v[D - 1];
 #pragma unroll
         for (int d = 0; d < D - 1; ++d) v[d] = __ldcs(reinterpret_cast<const int4*>(T + d * plane + idx));
         const int4 fv = __ldg(reinterpret_cast<const int4*>(f + j0));
-        float out[4];
+        OutT out[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             int32_t t[D - 1];
 #pragma unroll
             for (int d = 0; d < D - 1; ++d) t[d] = q == 0 ? v[d].x : q == 1 ? v[d].y : q == 2 ? v[d].z : v[d].w;
             const int32_t fj = q == 0 ? fv.x : q == 1 ? fv.y : q == 2 ? fv.z : fv.w;
-            out[q] = combine_int<D>(t, ei, fj);
+            out[q] = combine_int<D, OutT>(t, ei, fj);
         }
-        __stcs(reinterpret_cast<float4*>(c), make_float4(out[0], out[1], out[2], out[3]));
+        if (sizeof(OutT) == 4) {
+            __stcs(reinterpret_cast<float4*>(c), *reinterpret_cast<const float4*>(out));
+        } else {
+            __stcs(reinterpret_cast<double2*>(c), *reinterpret_cast<const double2*>(out));
+            __stcs(reinterpret_cast<double2*>(c) + 1, *(reinterpret_cast<const double2*>(out) + 1));
+        }
     } else {
         for (int q = 0; j0 + q < N; ++q) {
             int32_t t[D - 1];
 #pragma unroll
             for (int d = 0; d < D - 1; ++d) t[d] = T[d * plane + idx + q];
-            c[q] = combine_int<D>(t, ei, f[j0 + q]);
+            c[q] = combine_int<D, OutT>(t, ei, f[j0 + q]);
         }
     }
 }
 
-// any D (up to 18): the loop in fp64 as written
+// any D (up to 18): the loop in fp64 as written; for fp64 output the final scaling is one
+// exact multiply that keeps acc normal and one that rounds (|acc| in [2^-126, 2^144))
+__device__ __forceinline__ float scale_out(double acc, long long k, float*) {
+    k = k > 300 ? 300 : (k < -300 ? -300 : k);
+    return __double2float_rn(__dmul_rn(acc, pow2_f64((int)k)));
+}
+__device__ __forceinline__ double scale_out(double acc, long long k, double*) {
+    k = k > 2200 ? 2200 : (k < -2200 ? -2200 : k);
+    const long long k1 = k > 800 ? 800 : (k < -800 ? -800 : k);
+    long long k2 = k - k1;
+    k2 = k2 > 1000 ? 1000 : (k2 < -1000 ? -1000 : k2);  // beyond: 0 or inf either way
+    return __dmul_rn(__dmul_rn(acc, pow2_f64((int)k1)), pow2_f64((int)k2));
+}
+
+template <typename OutT>
 __global__ void ozaki_combine_f64_kernel(const int32_t* __restrict__ T, int64_t ldT, int max_diag,
                                          const int32_t* __restrict__ e, const int32_t* __restrict__ f,
-                                         float* __restrict__ C, int64_t ldc, int M, int N) {
+                                         OutT* __restrict__ C, int64_t ldc, int M, int N) {
     const int j = blockIdx.x * blockDim.x + threadIdx.x;
     const int i = blockIdx.y;
     if (j >= N) return;
     const int64_t plane = (int64_t)M * ldT;
     const int64_t idx = (int64_t)i * ldT + j;
-    int32_t t[19];
-#pragma unroll
-    for (int g = 0; g < 19; ++g) t[g] = 0;
-    for (int g = 2; g <= max_diag; ++g) t[g] = __ldg(T + (int64_t)(max_diag - g) * plane + idx);
-    C[(int64_t)i * ldc + j] = ozaki_combine(t, max_diag, e[i], f[j]);
+    double acc = 0.0;
+    for (int g = max_diag; g >= 2; --g)
+        acc = __dadd_rn(acc, __dmul_rn((double)__ldg(T + (int64_t)(max_diag - g) * plane + idx), pow2_f64(-7 * g)));
+    C[(int64_t)i * ldc + j] = scale_out(acc, (long long)e[i] + (long long)f[j], (OutT*)nullptr);
 }
 
-template <int D>
-cudaError_t launch_int(const int32_t* T, int64_t ldT, const int32_t* e, const int32_t* f, float* C, int64_t ldc,
+template <int D, typename OutT>
+cudaError_t launch_int(const int32_t* T, int64_t ldT, const int32_t* e, const int32_t* f, OutT* C, int64_t ldc,
                        int M, int N, cudaStream_t s) {
     dim3 grid((unsigned)(((N + 3) / 4 + 255) / 256), (unsigned)M);
-    ozaki_combine_int_kernel<D><<<grid, 256, 0, s>>>(T, ldT, e, f, C, ldc, M, N);
+    ozaki_combine_int_kernel<D, OutT><<<grid, 256, 0, s>>>(T, ldT, e, f, C, ldc, M, N);
     return cudaGetLastError();
 }
 
-}  // namespace
-
-cudaError_t ozaki_combine_launch(const int32_t* T, int64_t ldT, int max_diag, const int32_t* e, const int32_t* f,
-                                 float* C, int64_t ldc, int M, int N, cudaStream_t s) {
+template <typename OutT>
+cudaError_t combine_launch(const int32_t* T, int64_t ldT, int max_diag, const int32_t* e, const int32_t* f, OutT* C,
+                           int64_t ldc, int M, int N, cudaStream_t s) {
     if (M == 0 || N == 0) return cudaSuccess;
     // the integer kernels use 16-byte loads of T and f and 16-byte stores of C
-    const bool vec = (ldT % 4) == 0 && (ldc % 4) == 0 && (reinterpret_cast<uintptr_t>(T) & 15u) == 0 &&
-                     (reinterpret_cast<uintptr_t>(f) & 15u) == 0 && (reinterpret_cast<uintptr_t>(C) & 15u) == 0;
+    const bool vec = (ldT % 4) == 0 && ((ldc * (int64_t)sizeof(OutT)) % 16) == 0 &&
+                     (reinterpret_cast<uintptr_t>(T) & 15u) == 0 && (reinterpret_cast<uintptr_t>(f) & 15u) == 0 &&
+                     (reinterpret_cast<uintptr_t>(C) & 15u) == 0;
     if (vec) {
         switch (max_diag) {
             case 2: return launch_int<2>(T, ldT, e, f, C, ldc, M, N, s);
@@ -223,8 +286,20 @@ cudaError_t ozaki_combine_launch(const int32_t* T, int64_t ldT, int max_diag, co
         }
     }
     dim3 grid((N + 255) / 256, M);
-    ozaki_combine_f64_kernel<<<grid, 256, 0, s>>>(T, ldT, max_diag, e, f, C, ldc, M, N);
+    ozaki_combine_f64_kernel<OutT><<<grid, 256, 0, s>>>(T, ldT, max_diag, e, f, C, ldc, M, N);
     return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t ozaki_combine_launch(const int32_t* T, int64_t ldT, int max_diag, const int32_t* e, const int32_t* f,
+                                 float* C, int64_t ldc, int M, int N, cudaStream_t s) {
+    return combine_launch<float>(T, ldT, max_diag, e, f, C, ldc, M, N, s);
+}
+
+cudaError_t ozaki_combine_f64out_launch(const int32_t* T, int64_t ldT, int max_diag, const int32_t* e,
+                                        const int32_t* f, double* C, int64_t ldc, int M, int N, cudaStream_t s) {
+    return combine_launch<double>(T, ldT, max_diag, e, f, C, ldc, M, N, s);
 }
 
 }  // namespace detgemm

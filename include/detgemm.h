@@ -63,7 +63,7 @@ typedef enum detgemm_status {
     DETGEMM_ERR_NONFINITE = 8           /* inf or NaN in a floating-point input */
 } detgemm_status;
 
-enum { DETGEMM_DTYPE_BF16 = 0, DETGEMM_DTYPE_F32 = 1 };
+enum { DETGEMM_DTYPE_BF16 = 0, DETGEMM_DTYPE_F32 = 1, DETGEMM_DTYPE_F64 = 2 };
 enum { DETGEMM_POW2_NEAREST = 0, DETGEMM_POW2_CEIL = 1 };
 enum { DETGEMM_AXIS_ROWS = 0, DETGEMM_AXIS_COLS = 1 };
 
@@ -199,22 +199,55 @@ DETGEMM_API detgemm_status detgemm_ozaki_f32(const float* A, int64_t lda, const 
 DETGEMM_API size_t detgemm_ozaki_workspace_size(int M, int N, int K, int nslices, int max_diag, int split_k);
 
 /*
- * The recombination step of detgemm_ozaki_f32 alone [P3 §3 (a): the exact slice
- * products are recombined in a fixed order in fp64 and rounded once]:
+ * The recombination step of the Ozaki GEMMs alone [P3 §3 (a): the exact slice products
+ * are recombined in a fixed order in fp64 and rounded once]:
  *   acc = 0.0;  for g = max_diag down to 2: acc = acc + T_g * 2^(-7g)      (fp64, RNE)
- *   C_ij = (float)(acc * 2^(e_i + f_j))                (the one rounding, IEEE RNE,
- *                                                       subnormals kept, overflow -> inf)
+ *   C_ij = acc * 2^(e_i + f_j) rounded once to the output type           (IEEE RNE,
+ *          c_dtype DETGEMM_DTYPE_F32 as detgemm_ozaki_f32,                 subnormals kept,
+ *          or DETGEMM_DTYPE_F64 as detgemm_ozaki_f64)                      overflow -> inf)
  *   T  int32 [max_diag - 1][M][ldT]: plane p holds the diagonal sum T_g with
  *      g = max_diag - p (largest g first, the order of the loop); ldT >= N
  *   e  int32 [M] row exponents, f int32 [N] column exponents (any values)
- *   C  fp32 [M x N], row stride ldc;   2 <= max_diag <= 18
+ *   C  fp32 or fp64 [M x N], row stride ldc;   2 <= max_diag <= 18
  * The result bits are those of the fp64 loop as written, whichever way the library
- * evaluates it. Errors: INVALID_ARG, ALIGNMENT (T and C 16-byte aligned, ldT and ldc
- * multiples of 4; e and f 4-byte aligned), UNSUPPORTED_DEVICE, CUDA.
+ * evaluates it. Errors: INVALID_ARG, ALIGNMENT (T and C 16-byte aligned, ldT a multiple
+ * of 4, ldc times the element size a multiple of 16; e and f 4-byte aligned),
+ * UNSUPPORTED_DEVICE, CUDA.
  */
 DETGEMM_API detgemm_status detgemm_ozaki_combine(const int32_t* T, int64_t ldT, int max_diag, const int32_t* e,
-                                                 const int32_t* f, float* C, int64_t ldc, int M, int N,
+                                                 const int32_t* f, void* C, int c_dtype, int64_t ldc, int M, int N,
                                                  detgemm_stream_t stream);
+
+/*
+ * Ozaki slicing of an fp64 matrix: detgemm_slice_f32's definition applied to fp64
+ * values (every step is exact), 1 <= nslices <= 12 (84 bits; 8 cover fp64's 53-bit
+ * significand with 3 bits of headroom below the line's largest element).
+ */
+DETGEMM_API detgemm_status detgemm_slice_f64(const double* X, int64_t ldx, int rows, int cols, int axis,
+                                             int nslices, int8_t* S, int32_t* e, detgemm_stream_t stream);
+
+/*
+ * Ozaki-scheme fp64 GEMM C = A B (DGEMM emulation on exact integer slice products) —
+ * [P3 §3 (a)] applied to fp64 operands:
+ *   slice A per row (e_i, DA_s) and B per column (f_j, DB_t), s, t = 1..nslices;
+ *   T_g = sum_{s+t=g} DA_s DB_t^T                     (exact int32, g = 2..max_diag)
+ *   acc = 0.0;  for g = max_diag down to 2: acc = acc + T_g * 2^(-7g)      (fp64)
+ *   C_ij = acc * 2^(e_i + f_j) rounded to fp64        (exact unless subnormal / overflow)
+ *   A fp64 [M x K] (lda), B fp64 [K x N] row-major (ldb), C fp64 [M x N] (ldc)
+ *   1 <= nslices <= 12, 2 <= max_diag <= min(2 nslices, 18); the usual choice is
+ *   nslices = 8, max_diag = 9 (36 slice pairs). Accuracy is relative to the lines'
+ *   largest elements: |C - AB|_ij <= 2^-53 |C_ij| + 10 K 2^(e_i + f_j - 53) for
+ *   nslices = 8, max_diag = 9 (more slices for operands that span many binades).
+ * Precondition: min(max_diag - 1, nslices) * K * 127^2 < 2^31 (K <= 16644 for 8 slices).
+ * Errors as detgemm_ozaki_f32; non-finite inputs set DETGEMM_ERR_NONFINITE on the device.
+ */
+DETGEMM_API detgemm_status detgemm_ozaki_f64(const double* A, int64_t lda, const double* B, int64_t ldb,
+                                             double* C, int64_t ldc, int M, int N, int K, int nslices,
+                                             int max_diag, int split_k, void* ws, size_t ws_bytes,
+                                             detgemm_stream_t stream);
+
+/* Bytes of scratch detgemm_ozaki_f64 needs for this problem. */
+DETGEMM_API size_t detgemm_ozaki_f64_workspace_size(int M, int N, int K, int nslices, int max_diag, int split_k);
 
 /*
  * Exact int8 -> fp16 copy (every int8 value is an fp16 value): Y[r][k] = X[r][k] for

@@ -132,12 +132,24 @@ def test_other_entry_points_validate(lib):
     assert lib.detgemm_linear_w8a8_workspace_size(100, 64, 64, 1, 0) > lib.detgemm_linear_w8a8_workspace_size(
         100, 64, 64, 1, 1)
     c = lib.detgemm_ozaki_combine
-    assert c(P, 64, 1, P, P, P, 64, 4, 64, None) == dg.ERR_INVALID_ARG  # max_diag < 2
-    assert c(P, 64, 19, P, P, P, 64, 4, 64, None) == dg.ERR_INVALID_ARG  # max_diag > 18
-    assert c(P, 60, 8, P, P, P, 64, 4, 64, None) == dg.ERR_INVALID_ARG  # ldT < N
-    assert c(P, 66, 8, P, P, P, 64, 4, 64, None) == dg.ERR_ALIGNMENT  # 264-byte rows
-    assert c(P1, 64, 8, P, P, P, 64, 4, 64, None) == dg.ERR_ALIGNMENT
-    assert c(None, 64, 8, None, None, None, 64, 0, 64, None) == dg.OK  # empty
+    assert c(P, 64, 1, P, P, P, 1, 64, 4, 64, None) == dg.ERR_INVALID_ARG  # max_diag < 2
+    assert c(P, 64, 19, P, P, P, 1, 64, 4, 64, None) == dg.ERR_INVALID_ARG  # max_diag > 18
+    assert c(P, 64, 8, P, P, P, 0, 64, 4, 64, None) == dg.ERR_INVALID_ARG  # bf16 output
+    assert c(P, 60, 8, P, P, P, 1, 64, 4, 64, None) == dg.ERR_INVALID_ARG  # ldT < N
+    assert c(P, 66, 8, P, P, P, 1, 64, 4, 64, None) == dg.ERR_ALIGNMENT  # 264-byte rows
+    assert c(P, 64, 8, P, P, P, 2, 65, 4, 64, None) == dg.ERR_ALIGNMENT  # fp64 rows of 520 bytes
+    assert c(P1, 64, 8, P, P, P, 1, 64, 4, 64, None) == dg.ERR_ALIGNMENT
+    assert c(None, 64, 8, None, None, None, 1, 64, 0, 64, None) == dg.OK  # empty
+    s64 = lib.detgemm_slice_f64
+    assert s64(P, 64, 4, 64, 0, 13, P, P, None) == dg.ERR_INVALID_ARG  # nslices
+    assert s64(P, 63, 4, 63, 0, 8, P, P, None) == dg.ERR_ALIGNMENT  # 504-byte rows
+    o64 = lib.detgemm_ozaki_f64
+    assert o64(P, 64, P, 64, P, 64, 64, 64, 64, 8, 17, 1, P, 1 << 30, None) == dg.ERR_INVALID_ARG
+    assert o64(P, 64, P, 64, P, 64, 64, 64, 64, 13, 9, 1, P, 1 << 30, None) == dg.ERR_INVALID_ARG
+    # 8 pairs * K * 127^2 must stay below 2^31: K = 16644 passes the bound, 16646 does not
+    assert o64(P, 16646, P, 64, P, 64, 64, 64, 16646, 8, 9, 1, P, 1 << 40, None) == dg.ERR_PRECONDITION
+    assert o64(P, 64, P, 64, P, 64, 64, 64, 64, 8, 9, 1, P, 16, None) == dg.ERR_WORKSPACE
+    assert dg.ozaki_f64_workspace_size(64, 64, 64) > 8 * 64 * 64 * 2
 
 
 def test_binding_refuses_cpu_tensors(lib):
