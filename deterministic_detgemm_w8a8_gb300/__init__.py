@@ -9,6 +9,7 @@ built, importing works but every call raises ``DetGemmError``.
 Functions mirror the C entry points:
 
 * :func:`w8a8`           C = rne_bf16((A W^T) * 2^(ea_i + ew_j))      (bf16 out)
+* :func:`w8a8_host`      the same on host (pinned) tensors, copies overlapped with compute
 * :func:`gemm_s8_i32`    C = A W^T, exact int32
 * :func:`quantize_pow2`  per-row power-of-two scale and int8 values
 * :func:`linear_w8a8`    quantize_pow2 of bf16/fp32 activations + w8a8, fused
@@ -52,6 +53,8 @@ SIGNATURES = {
     "detgemm_slice_f64": ([_P, _I64, _I32, _I32, _I32, _I32, _P, _P, _P], _I32),
     "detgemm_ozaki_f64": ([_P, _I64, _P, _I64, _P, _I64, _I32, _I32, _I32, _I32, _I32, _I32, _P, _SZ, _P], _I32),
     "detgemm_ozaki_f64_workspace_size": ([_I32, _I32, _I32, _I32, _I32, _I32], _SZ),
+    "detgemm_w8a8_host": ([_P, _I64, _P, _I64, _P, _P, _P, _I64, _I32, _I32, _I32, _P, _SZ, _P], _I32),
+    "detgemm_w8a8_host_buffer_size": ([_I32, _I32, _I32], _SZ),
     "detgemm_linear_w8a8": ([_P, _I32, _I64, _I32, _P, _I64, _P, _I64, _P, _P, _I64, _P, _I32, _I32, _I32, _I32,
                              _P, _SZ, _P], _I32),
     "detgemm_linear_w8a8_workspace_size": ([_I32, _I32, _I32, _I32, _I32], _SZ),
@@ -172,6 +175,53 @@ def w8a8(A, W, ea, ew, split_k: int = 1, out=None, ws=None, stream=None) -> torc
                           out.data_ptr(), _ld(out), M, N, K, split_k,
                           wsb.data_ptr() if wsb is not None else None, wsn, _stream(stream))
     _check(st, "detgemm_w8a8")
+    return out
+
+
+def _req_host(t: torch.Tensor, dtype, name):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.is_cuda:
+        raise ValueError(f"{name} must be a host (CPU) tensor")
+    if (t.dim() == 2 and t.stride(1) != 1) or (t.dim() == 1 and not t.is_contiguous()):
+        raise ValueError(f"{name} must have unit stride along its last dimension")
+
+
+def w8a8_host_buffer_size(M: int, N: int, K: int) -> int:
+    return int(load().detgemm_w8a8_host_buffer_size(M, N, K))
+
+
+def w8a8_host(A, W, ea, ew, out=None, buf=None, stream=None, sync: bool = True) -> torch.Tensor:
+    """w8a8 on HOST tensors (pin them for overlap): A int8 [M,K], W int8 [N,K], ea/ew int32;
+    returns a host bfloat16 tensor [M, N] (or writes ``out``). The host-to-device copies,
+    the computation and the copy back are pipelined over chunks of rows on the current
+    CUDA device; ``buf`` is the device scratch (allocated here if None). With sync=False
+    the result is valid only after the stream has been synchronized."""
+    lib = load()
+    _req_host(A, torch.int8, "A"); _req_host(W, torch.int8, "W")
+    _req_host(ea, torch.int32, "ea"); _req_host(ew, torch.int32, "ew")
+    M, K = A.shape
+    N = W.shape[0]
+    if W.shape[1] != K or ea.shape != (M,) or ew.shape != (N,):
+        raise ValueError("shape mismatch")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, pin_memory=A.is_pinned())
+    _req_host(out, torch.bfloat16, "out")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    need = w8a8_host_buffer_size(M, N, K)
+    if buf is None:
+        buf = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    if buf.numel() * buf.element_size() < need:
+        raise ValueError(f"buffer too small: need {need} bytes")
+    s = stream if stream is not None else torch.cuda.current_stream()
+    st = lib.detgemm_w8a8_host(A.data_ptr(), A.stride(0) if M > 1 else K, W.data_ptr(), W.stride(0) if N > 1 else K,
+                               ea.data_ptr(), ew.data_ptr(), out.data_ptr(), out.stride(0) if M > 1 else N,
+                               M, N, K, buf.data_ptr(), buf.numel() * buf.element_size(), s.cuda_stream)
+    _check(st, "detgemm_w8a8_host")
+    if sync:
+        s.synchronize()
     return out
 
 

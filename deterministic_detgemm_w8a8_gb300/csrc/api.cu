@@ -18,7 +18,7 @@ constexpr int kMaxDevices = 64;
 std::mutex g_dev_mutex;
 int g_dev_cc[kMaxDevices];  // 0 = unknown, else 10 * major + minor
 
-detgemm_status check_device() {
+detgemm_status check_device_impl() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return DETGEMM_ERR_UNSUPPORTED_DEVICE;
     if (dev < 0 || dev >= kMaxDevices) return DETGEMM_ERR_UNSUPPORTED_DEVICE;
@@ -32,6 +32,8 @@ detgemm_status check_device() {
     }
     return g_dev_cc[dev] == 103 ? DETGEMM_OK : DETGEMM_ERR_UNSUPPORTED_DEVICE;
 }
+
+detgemm_status check_device() { return check_device_impl(); }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
@@ -85,6 +87,9 @@ OzakiLayout ozaki_layout(int M, int N, int K, int nslices, int max_diag, int spl
 }
 
 }  // namespace
+
+int device_is_supported() { return check_device_impl() == DETGEMM_OK; }
+
 }  // namespace detgemm
 
 using namespace detgemm;

@@ -114,6 +114,9 @@ cudaError_t widen_pair_launch(const int8_t* X0, int64_t ldx0, int rows0, int K0,
 cudaError_t widen_i8_f16_launch(const int8_t* X, int64_t ldx, int rows, int K, void* Y, int64_t Kp,
                                 cudaStream_t s);
 
+// 1 when the current device is a compute-capability 10.3 GPU (checked once per device).
+int device_is_supported();
+
 // Read-and-clear accessors of the per-unit device status words.
 cudaError_t quantize_take_status(uint32_t* bits);
 cudaError_t slice_take_status(uint32_t* bits);

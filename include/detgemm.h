@@ -276,6 +276,30 @@ DETGEMM_API detgemm_status detgemm_w8a8_f16ops(const uint16_t* A16, int64_t lda,
 DETGEMM_API size_t detgemm_w8a8_f16ops_workspace_size(int M, int N, int K, int split_k);
 
 /*
+ * detgemm_w8a8 on operands in HOST memory [P4 §II: a row's int32 accumulator, and so
+ * its bf16 result, does not depend on which rows are computed with it]: the rows of A
+ * are cut into chunks, and each chunk's host-to-device copy, its computation (the same
+ * exact path as detgemm_w8a8) and the copy of its result back to host memory overlap
+ * with those of its neighbours. The result bits are those of detgemm_w8a8.
+ *   A int8 [M x K] (lda), W int8 [N x K] (ldw), ea int32 [M], ew int32 [N],
+ *   C bf16 bit patterns [M x N] (ldc): all HOST pointers, no alignment rule; page-locked
+ *   (pinned) memory lets the copies run asynchronously and overlap (pageable memory
+ *   works, without the overlap).
+ *   buf  DEVICE scratch of buf_bytes >= detgemm_w8a8_host_buffer_size(M, N, K),
+ *        256-byte aligned; it holds the weight, its fp16 copy and two chunks.
+ * Asynchronous on `stream`: C is complete when the stream has been synchronized. The
+ * library creates two copy streams and a few events once per device (no device memory).
+ * Errors: INVALID_ARG, PRECONDITION (K > DETGEMM_MAX_K), WORKSPACE, ALIGNMENT (buf),
+ *         UNSUPPORTED_DEVICE, CUDA.
+ */
+DETGEMM_API detgemm_status detgemm_w8a8_host(const int8_t* A, int64_t lda, const int8_t* W, int64_t ldw,
+                                             const int32_t* ea, const int32_t* ew, uint16_t* C, int64_t ldc,
+                                             int M, int N, int K, void* buf, size_t buf_bytes,
+                                             detgemm_stream_t stream);
+
+DETGEMM_API size_t detgemm_w8a8_host_buffer_size(int M, int N, int K);
+
+/*
  * Self-check of the failure detection: launches a one-thread kernel whose bounded wait
  * on a barrier that nothing ever arrives on expires after limit_ms (1 .. 2000). After it,
  * detgemm_get_device_status returns DETGEMM_ERR_TIMEOUT and the CUDA context stays usable.

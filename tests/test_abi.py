@@ -131,6 +131,13 @@ def test_other_entry_points_validate(lib):
     assert li(P, 0, 64, 0, P, 64, None, 0, P, P, 64, None, 0, 64, 64, 1, None, 0, None) == dg.OK
     assert lib.detgemm_linear_w8a8_workspace_size(100, 64, 64, 1, 0) > lib.detgemm_linear_w8a8_workspace_size(
         100, 64, 64, 1, 1)
+    h = lib.detgemm_w8a8_host
+    assert h(P, 64, P, 64, P, P, P, 64, 100, 64, 131072, P, 1 << 40, None) == dg.ERR_PRECONDITION
+    assert h(P, 60, P, 64, P, P, P, 64, 100, 64, 64, P, 1 << 40, None) == dg.ERR_INVALID_ARG  # lda < K
+    assert h(P, 64, P, 64, P, P, P, 64, 100, 64, 64, P, 16, None) == dg.ERR_WORKSPACE
+    assert h(P, 64, P, 64, P, P, P, 64, 100, 64, 64, P + 16, 1 << 40, None) == dg.ERR_ALIGNMENT
+    assert h(None, 64, None, 64, None, None, None, 64, 0, 64, 64, None, 0, None) == dg.OK
+    assert lib.detgemm_w8a8_host_buffer_size(8192, 4096, 12288) > 4096 * 12288 * 3
     c = lib.detgemm_ozaki_combine
     assert c(P, 64, 1, P, P, P, 1, 64, 4, 64, None) == dg.ERR_INVALID_ARG  # max_diag < 2
     assert c(P, 64, 19, P, P, P, 1, 64, 4, 64, None) == dg.ERR_INVALID_ARG  # max_diag > 18
