@@ -429,6 +429,17 @@ def extras(dg, torch, dev, pk, flush):
     res["ozaki_f32_4096"] = {"ms": round(ms, 3), "effective_fp32_TFLOPs": round(2 * 4096 ** 3 / (ms * 1e-3) / 1e12, 2),
                              "slice_TOPS": round(28 * 2 * 4096 ** 3 / (ms * 1e-3) / 1e12, 1)}
     del Af, Bf, Cf, ws
+    # context for the tensor-core roofline: the vendor library's fp16 GEMM (fp32 accumulate)
+    # on the FFN shapes, operands resident, L2 flushed
+    lib_ffn = {}
+    for name, (m, n, k) in (("gate_up", (M_FFN, N1, K1)), ("down", (M_FFN, N2, K2))):
+        a16 = torch.randn((m, k), device=dev).to(torch.float16)
+        b16 = torch.randn((k, n), device=dev).to(torch.float16)
+        c16 = torch.empty((m, n), dtype=torch.float16, device=dev)
+        ms = _time(torch, lambda: torch.matmul(a16, b16, out=c16), flush)
+        lib_ffn[name] = {"us": round(ms * 1e3, 1), "TFLOPs": round(2.0 * m * n * k / (ms * 1e-3) / 1e12, 1)}
+        del a16, b16, c16
+    res["library_fp16_gemm_ffn_shapes"] = lib_ffn
     # fp64-target Ozaki GEMM 4096^3 (8 slices, 36 slice pairs), next to the fp64 GEMM of the
     # vendor library on the same operands (context: GB300's fp64 rate)
     Ad, Bd = (tdev(x) for x in synthetic.ozaki_f64(4096))
