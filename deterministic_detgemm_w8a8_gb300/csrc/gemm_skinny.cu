@@ -501,17 +501,31 @@ int sk_num_sms() {
     return g_sk_sms[dev];
 }
 
+int g_sk_per_sm[64][5];  // resident CTAs per SM of skinny_kernel<MT>, per device (0 = not set up)
+
 template <int MT>
 cudaError_t sk_launch_mt(const CUtensorMap& tmW, const CUtensorMap& tmA, const SkArgs& a, cudaStream_t s) {
     const int smem = sk_smem_bytes(MT);
-    cudaError_t e = cudaFuncSetAttribute(skinny_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    // persistent: every CTA resident at once (sk_ctas_per_sm per SM), each streaming an equal share
-    int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, skinny_kernel<MT>, SK_THREADS, (size_t)smem);
-    if (e != cudaSuccess) return e;
-    if (per_sm < 1) return cudaErrorInvalidConfiguration;
-    if (per_sm > sk_ctas_per_sm(MT)) per_sm = sk_ctas_per_sm(MT);
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    int per_sm;
+    {
+        // set up once per device: the shared-memory opt-in and the resident CTAs per SM
+        std::lock_guard<std::mutex> lock(g_sk_mutex);
+        per_sm = g_sk_per_sm[dev][MT];
+        if (per_sm == 0) {
+            e = cudaFuncSetAttribute(skinny_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+            if (e != cudaSuccess) return e;
+            // persistent: every CTA resident at once (sk_ctas_per_sm per SM), each streaming an equal share
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, skinny_kernel<MT>, SK_THREADS, (size_t)smem);
+            if (e != cudaSuccess) return e;
+            if (per_sm < 1) return cudaErrorInvalidConfiguration;
+            if (per_sm > sk_ctas_per_sm(MT)) per_sm = sk_ctas_per_sm(MT);
+            g_sk_per_sm[dev][MT] = per_sm;
+        }
+    }
     const long long blocks = (long long)a.nblocks * ((a.K + SK_BK - 1) / SK_BK);
     long long grid = (long long)per_sm * sk_num_sms();
     if (grid > blocks) grid = blocks;

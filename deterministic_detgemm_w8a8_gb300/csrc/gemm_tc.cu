@@ -23,8 +23,9 @@
 //   warps 2-9  epilogue (both CTAs): warp w reads TMEM lanes 32 (w % 4) .. +31 and column
 //              half (w - 2) / 4 of its CTA's 128 rows, converts each fp32 chunk to int32
 //              and adds it to 128 int32 registers per thread; after the unit's last chunk
-//              it rounds to bf16 (or stores int32) or, under split-K, adds the partial into
-//              an int32 workspace with atomics and the last-arriving warp finishes.
+//              it rounds to bf16 (or keeps int32), stages its 32 x 128 block in a 4 KB
+//              shared-memory slot and writes it with TMA stores or, under split-K, adds the
+//              partial into an int32 workspace with atomics and the last-arriving warp finishes.
 // Operands are fp16 planes [plane][rows][Kp] addressed through 3-D tensor maps; a unit
 // walks a list of (A plane, B plane) segments: one segment for W8A8, one per slice pair
 // for an Ozaki diagonal.
@@ -96,11 +97,42 @@ __device__ __forceinline__ float ro24_scaled(int32_t acc, float sa, float sw) {
 
 __device__ __forceinline__ float exp2_f32(int e) { return __uint_as_float((uint32_t)(e + 127) << 23); }
 
-// Epilogue of 128 consecutive columns of one output row held by one thread. The warp's
-// 32 threads hold 32 rows of the same 128 columns, so the column exponents are loaded
-// once per warp (lane l loads columns 4l .. 4l+3, coalesced) and broadcast by shuffle.
-__device__ __forceinline__ void finish_row(const TcArgs& p, int d, int row, int col0, const int32_t (&acc)[128]) {
+// Epilogue of a warp's 32 rows x 128 columns: lane l holds row row0 + l. The results go
+// through the warp's 4 KB shared-memory slot, 32 rows x 128 bytes with the 128-byte
+// swizzle (16-byte chunk c of row r at c ^ (r % 8), so the eight lanes of each store phase
+// hit eight different bank groups), and from there to global memory with one TMA store per
+// piece (64 bf16 or 32 int32 columns); the TMA clips rows past M and columns past N. Before
+// a piece overwrites the slot, the warp's previous store must have finished reading it.
+// The column exponents are loaded once per warp (lane l loads columns 4l .. 4l+3,
+// coalesced) and broadcast by shuffle.
+__device__ __forceinline__ void slot_acquire(bool& pending) {
+    if (pending) {
+        if ((threadIdx.x & 31) == 0) bulk_wait_read_all();
+        __syncwarp();
+    }
+}
+
+__device__ __forceinline__ void slot_release(const CUtensorMap* tmC, uint8_t* slot, int x, int y, int z, bool live,
+                                             bool& pending) {
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (live && (threadIdx.x & 31) == 0) {  // a piece wholly past M or N is not stored
+        tma_store_3d(tmC, slot, x, y, z);
+        bulk_commit();
+    }
+    pending = true;
+}
+
+__device__ __forceinline__ void st_shared16(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+__device__ __forceinline__ void finish_rows(const TcArgs& p, const CUtensorMap* tmC, uint8_t* slot, int d, int row0,
+                                            int col0, const int32_t (&acc)[128], bool& pending) {
     const int lane = threadIdx.x & 31;
+    const int row = row0 + lane;
+    const uint32_t sbase = smem_addr(slot) + (uint32_t)lane * 128u;
+    const int sw = lane & 7;
     if (p.mode == EPI_BF16_POW2) {
         int32_t ewv[4];
         bool inrange = true;
@@ -112,58 +144,53 @@ __device__ __forceinline__ void finish_row(const TcArgs& p, int d, int row, int 
         }
         const int32_t ea = row < p.M ? __ldg(p.ea + row) : 0;
         inrange &= ea >= -60 && ea <= 40;
-        uint16_t* C = reinterpret_cast<uint16_t*>(p.C) + (int64_t)row * p.ldc;
         const bool fast = __all_sync(0xffffffffu, inrange);  // warp-uniform choice
         float swv[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) swv[i] = exp2_f32(fast ? ewv[i] : 0);
         const float sa = exp2_f32(fast ? ea : 0);
 #pragma unroll
-        for (int j = 0; j < 128; j += 8) {
-            uint32_t w[4];
-            if (fast) {
+        for (int hh = 0; hh < 2; ++hh) {
+            slot_acquire(pending);
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int c = j + 2 * i;
-                    const float s0 = __shfl_sync(0xffffffffu, swv[c & 3], c >> 2);
-                    const float s1 = __shfl_sync(0xffffffffu, swv[(c + 1) & 3], (c + 1) >> 2);
-                    const __nv_bfloat162 h =
-                        __floats2bfloat162_rn(ro24_scaled(acc[c], sa, s0), ro24_scaled(acc[c + 1], sa, s1));
-                    w[i] = *reinterpret_cast<const uint32_t*>(&h);
+            for (int jj = 0; jj < 8; ++jj) {
+                const int j = 64 * hh + 8 * jj;
+                uint32_t w[4];
+                if (fast) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int c = j + 2 * i;
+                        const float s0 = __shfl_sync(0xffffffffu, swv[c & 3], c >> 2);
+                        const float s1 = __shfl_sync(0xffffffffu, swv[(c + 1) & 3], (c + 1) >> 2);
+                        const __nv_bfloat162 h =
+                            __floats2bfloat162_rn(ro24_scaled(acc[c], sa, s0), ro24_scaled(acc[c + 1], sa, s1));
+                        w[i] = *reinterpret_cast<const uint32_t*>(&h);
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int c = j + 2 * i;
+                        const int32_t e0 = __shfl_sync(0xffffffffu, ewv[c & 3], c >> 2);
+                        const int32_t e1 = __shfl_sync(0xffffffffu, ewv[(c + 1) & 3], (c + 1) >> 2);
+                        w[i] = (uint32_t)bf16_from_acc_pow2(acc[c], ea, e0) |
+                               ((uint32_t)bf16_from_acc_pow2(acc[c + 1], ea, e1) << 16);
+                    }
                 }
-            } else {
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int c = j + 2 * i;
-                    const int32_t e0 = __shfl_sync(0xffffffffu, ewv[c & 3], c >> 2);
-                    const int32_t e1 = __shfl_sync(0xffffffffu, ewv[(c + 1) & 3], (c + 1) >> 2);
-                    w[i] = (uint32_t)bf16_from_acc_pow2(acc[c], ea, e0) |
-                           ((uint32_t)bf16_from_acc_pow2(acc[c + 1], ea, e1) << 16);
-                }
+                st_shared16(sbase + (uint32_t)((jj ^ sw) << 4), w[0], w[1], w[2], w[3]);
             }
-            if (row >= p.M) continue;
-            const int col = col0 + j;
-            if (col + 8 <= p.N) {
-                *reinterpret_cast<uint4*>(C + col) = make_uint4(w[0], w[1], w[2], w[3]);
-            } else {
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    if (col + i < p.N) C[col + i] = (uint16_t)(w[i >> 1] >> (16 * (i & 1)));
-            }
+            slot_release(tmC, slot, col0 + 64 * hh, row0, 0, row0 < p.M && col0 + 64 * hh < p.N, pending);
         }
     } else {
-        if (row >= p.M) return;
-        int32_t* C = reinterpret_cast<int32_t*>(p.C) + (int64_t)d * p.c_plane + (int64_t)row * p.ldc;
 #pragma unroll
-        for (int j = 0; j < 128; j += 4) {
-            const int col = col0 + j;
-            if (col + 4 <= p.N) {
-                *reinterpret_cast<int4*>(C + col) = make_int4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
-            } else {
+        for (int pc = 0; pc < 4; ++pc) {
+            slot_acquire(pending);
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    if (col + i < p.N) C[col + i] = acc[j + i];
+            for (int jj = 0; jj < 8; ++jj) {
+                const int j = 32 * pc + 4 * jj;
+                st_shared16(sbase + (uint32_t)((jj ^ sw) << 4), (uint32_t)acc[j], (uint32_t)acc[j + 1],
+                            (uint32_t)acc[j + 2], (uint32_t)acc[j + 3]);
             }
+            slot_release(tmC, slot, col0 + 32 * pc, row0, d, row0 < p.M && col0 + 32 * pc < p.N, pending);
         }
     }
 }
@@ -187,14 +214,17 @@ constexpr int P_A_BYTES = 128 * BK * 2;
 constexpr int P_B_BYTES = 128 * BK * 2;
 constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
 constexpr uint32_t P_IDESC = idesc_f16_f32(256, 256);
-constexpr int P_SMEM_BYTES = P_STAGES * P_STAGE_BYTES + 1024 /*alignment slack*/ + 256 /*barriers*/;
+constexpr int P_SLOT_BYTES = 32 * 128;  // one epilogue warp's staging slot
+constexpr int P_SMEM_BYTES =
+    P_STAGES * P_STAGE_BYTES + EPI_WARPS * P_SLOT_BYTES + 1024 /*alignment slack*/ + 256 /*barriers*/;
 
 __global__ void __launch_bounds__(THREADS, 1)
     tc2_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                    const __grid_constant__ TcArgs p) {
+                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ TcArgs p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + P_STAGES * P_STAGE_BYTES);
+    uint8_t* slots = smem + P_STAGES * P_STAGE_BYTES;  // epilogue staging, 1024-byte aligned
+    uint64_t* full = reinterpret_cast<uint64_t*>(slots + EPI_WARPS * P_SLOT_BYTES);
     uint64_t* empty = full + P_STAGES;
     uint64_t* tfull = empty + P_STAGES;
     uint64_t* tempty = tfull + 2;
@@ -332,6 +362,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int ew = warp - 2;
         const int q = warp & 3;
         const int h = ew >> 2;
+        uint8_t* slot = slots + ew * P_SLOT_BYTES;
+        bool pending = false;  // a TMA store from this warp's slot may still be in flight
         int buf = 0;
         uint32_t tphase = 0;
         bool ok = true;
@@ -370,7 +402,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             const int row = un.tm * 256 + (int)rank * 128 + q * 32 + lane;
             const int col0 = un.tn * BN + h * 128;
             if (p.split == 1) {
-                finish_row(p, un.d, row, col0, acc);
+                finish_rows(p, &tmC, slot, un.d, row - lane, col0, acc, pending);
                 continue;
             }
             int32_t* ws = p.ws_acc + (int64_t)un.d * p.M * p.N;
@@ -393,8 +425,10 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                 for (int i = 0; i < 128; ++i) acc[i] = (col0 + i < p.N) ? __ldcg(ws + (int64_t)row * p.N + col0 + i) : 0;
             }
-            finish_row(p, un.d, row, col0, acc);
+            finish_rows(p, &tmC, slot, un.d, row - lane, col0, acc, pending);
         }
+        // the slot's last stores complete before the CTA's shared memory goes away
+        if (pending && lane == 0) bulk_wait_all();
     }
 
     __syncwarp();
@@ -454,6 +488,27 @@ cudaError_t make_map(CUtensorMap* m, const void* base, int64_t kext, int64_t ld,
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// 3-D map over the output: bf16 [1][M][ldc] (box 64 x 32) or int32 planes [ndiag][M][ldc]
+// spaced c_plane elements apart (box 32 x 32); 128-byte swizzle, the epilogue's slot layout
+cudaError_t make_out_map(CUtensorMap* m, const TcArgs& a) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc;
+    cudaError_t e = get_encode(&enc);
+    if (e != cudaSuccess) return e;
+    const bool bf = a.mode == EPI_BF16_POW2;
+    const cuuint64_t es = bf ? 2 : 4;
+    const int planes = bf ? 1 : a.ndiag;
+    const cuuint64_t row_bytes = (cuuint64_t)a.ldc * es;
+    const cuuint64_t plane_bytes = (planes > 1 ? (cuuint64_t)a.c_plane : (cuuint64_t)a.ldc * (cuuint64_t)a.M) * es;
+    cuuint64_t dims[3] = {(cuuint64_t)a.N, (cuuint64_t)a.M, (cuuint64_t)planes};
+    cuuint64_t strides[2] = {row_bytes, plane_bytes};
+    cuuint32_t box[3] = {(cuuint32_t)(128 / es), 32, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(m, bf ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_INT32, 3, a.C, dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 }  // namespace
 
 int64_t tc_padded_k(int K) { return ((int64_t)K + BK - 1) / BK * BK; }
@@ -501,9 +556,10 @@ static cudaError_t tc2_launch(TcArgs a, const void* A16, int64_t lda, int a_plan
     a.tiles_n = (a.N + BN - 1) / BN;
     a.nkb = (int)((kext + BK - 1) / BK);
     if (a.group_m <= 0) a.group_m = 8;
-    CUtensorMap tmA, tmB;
+    CUtensorMap tmA, tmB, tmC;
     cudaError_t e = make_map(&tmA, A16, kext, lda, a.M, a_planes, 128);
     if (e == cudaSuccess) e = make_map(&tmB, B16, kext, ldb, a.N, b_planes, 128);
+    if (e == cudaSuccess) e = make_out_map(&tmC, a);
     if (e != cudaSuccess) return e;
     if (a.split > 1) {
         size_t accb = (((size_t)a.ndiag * a.M * a.N * sizeof(int32_t)) + 255) & ~(size_t)255;
@@ -529,7 +585,7 @@ static cudaError_t tc2_launch(TcArgs a, const void* A16, int64_t lda, int a_plan
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, tc2_gemm_kernel, tmA, tmB, a);
+    e = cudaLaunchKernelEx(&cfg, tc2_gemm_kernel, tmA, tmB, tmC, a);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
