@@ -382,13 +382,15 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 tc_fence_after();
                 const uint32_t ta = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN + h * 128);
+                // 16 columns per load: the 128 accumulators plus one load's registers stay
+                // within the thread's register budget
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    uint32_t r[32];
-                    tmem_ld32(ta + 32 * j, r);
+                for (int j = 0; j < 8; ++j) {
+                    uint32_t r[16];
+                    tmem_ld16(ta + 16 * j, r);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) acc[32 * j + i] += __float2int_rn(__uint_as_float(r[i]));
+                    for (int i = 0; i < 16; ++i) acc[16 * j + i] += __float2int_rn(__uint_as_float(r[i]));
                 }
                 tc_fence_before();
                 __syncwarp();
