@@ -10,7 +10,8 @@ The same JSON line carries extra measurements of the other hot-path rows: the sk
 decode-shaped GEMM (M=16, N=4096, K=65536, split-K 8/16/32) in GB/s against the HBM
 roofline, the Ozaki fp32 GEMM (4096^3) in effective fp32 TFLOP/s, the fp64-target Ozaki
 GEMM (4096^3) next to the library fp64 GEMM, the fused linear layer
-on bf16 activations at the FFN gate/up size, and the sweep linear (M=2048, K=2048, N=6144).
+on bf16 activations at the FFN gate/up size, the sweep linear (K=2048, N=6144) at
+M = 1, 7, 64, 257, 2048, and the tiny workload's latency.
 
 Timing: W warm-up steps, then K timed steps; L2 is flushed before every timed step,
 outside the timed events, by a 256 MiB write followed by a 256 MiB read of another buffer
@@ -46,7 +47,7 @@ OPS_STEP = 2.0 * M_FFN * (N1 * K1 + N2 * K2)
 # FFN GEMMs (profiles/tc2_gemm_kernel_ffn_gate_up.md, profiles/launches_ffn_tc2.md), keyed
 # by a digest of the engine source so that a changed kernel reports null, not stale counters
 PROFILED_TRAFFIC = {
-    "381de61248af2299": {"gate_up": 479849216 + 183604736, "down": 901412608 + 67719680},
+    "e72208fb4969efb8": {"gate_up": 478702336 + 182116352, "down": 897767936 + 63704064},
 }
 
 
@@ -479,12 +480,23 @@ def extras(dg, torch, dev, pk, flush):
         "fused_prewidened_weight_TOPS": round(ops / (ms_f16 * 1e-3) / 1e12, 1),
         "quantize_then_w8a8_us": round(ms_2 * 1e3, 1)}
     del X, W, W16, ws, ws16, wsw, C
-    # sweep linear at M = 2048
+    # the batch-invariance sweep linear (K=2048, N=6144) at every M of the sweep, split 1;
+    # W (12.6 MB) dominates the bytes up to M = 64, the tensor pipe at M = 2048
     A, W, ea, ew = (tdev(x) for x in synthetic.sweep(2048))
-    C = torch.empty((2048, 6144), dtype=torch.bfloat16, device=dev)
+    sweep = {}
+    for m in (1, 7, 64, 257, 2048):
+        Am, eam = A[:m].contiguous(), ea[:m].contiguous()
+        C = torch.empty((m, 6144), dtype=torch.bfloat16, device=dev)
+        ms = _time(torch, lambda: dg.w8a8(Am, W, eam, ew, out=C), flush)
+        nbytes = m * 2048 + 6144 * 2048 + m * 6144 * 2
+        sweep[str(m)] = {"us": round(ms * 1e3, 1), "TOPS": round(2.0 * m * 6144 * 2048 / (ms * 1e-3) / 1e12, 1),
+                         "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1)}
+    res["sweep_N6144_K2048"] = sweep
+    # the tiny workload (64 x 256 x 512): launch-latency bound
+    A, W, ea, ew = (tdev(x) for x in synthetic.tiny())
+    C = torch.empty((64, 256), dtype=torch.bfloat16, device=dev)
     ms = _time(torch, lambda: dg.w8a8(A, W, ea, ew, out=C), flush)
-    res["sweep_M2048_N6144_K2048"] = {"us": round(ms * 1e3, 1),
-                                      "TOPS": round(2.0 * 2048 * 6144 * 2048 / (ms * 1e-3) / 1e12, 1)}
+    res["tiny_M64_N256_K512"] = {"us": round(ms * 1e3, 1)}
     return res
 
 
