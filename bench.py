@@ -47,15 +47,20 @@ OPS_STEP = 2.0 * M_FFN * (N1 * K1 + N2 * K2)
 # FFN GEMMs (profiles/tc2_gemm_kernel_ffn_gate_up.md, profiles/launches_ffn_tc2.md), keyed
 # by a digest of the engine source so that a changed kernel reports null, not stale counters
 PROFILED_TRAFFIC = {
-    "e72208fb4969efb8": {"gate_up": 478702336 + 182116352, "down": 897767936 + 63704064},
+    "1f98568956c65c6d": {"gate_up": 478702336 + 182116352, "down": 897767936 + 63704064},
 }
 
 
 def _engine_digest():
+    """Digest of the engine's device code: gemm_tc.cu up to its host-side section, sm100.cuh
+    and common.cuh (host-side launch changes do not change the counters)."""
     import hashlib
     h = hashlib.sha256()
     for f in ("gemm_tc.cu", "sm100.cuh", "common.cuh"):
-        h.update(open(os.path.join(ROOT, "deterministic_detgemm_w8a8_gb300", "csrc", f), "rb").read())
+        src = open(os.path.join(ROOT, "deterministic_detgemm_w8a8_gb300", "csrc", f), "rb").read()
+        if f == "gemm_tc.cu":
+            src = src.split(b"// host side")[0]
+        h.update(src)
     return h.hexdigest()[:16]
 
 
@@ -78,7 +83,8 @@ def parse():
     ap.add_argument("--no-extras", action="store_true", help="skip the extra rows")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", default=None,
-                    choices=["ffn_gate_up", "ffn_down", "skinny8", "skinny32", "ozaki", "ozaki_f64", "sweep"],
+                    choices=["ffn_gate_up", "ffn_down", "skinny8", "skinny32", "ozaki", "ozaki_f64", "sweep",
+                             "sweep1", "sweep64"],
                     help="run one workload call twice (warm-up + one more) for an ncu capture, then exit")
     return ap.parse_args()
 
@@ -429,6 +435,20 @@ def extras(dg, torch, dev, pk, flush):
     ms = _time(torch, lambda: dg.ozaki_f32(Af, Bf, out=Cf, ws=ws), flush, reps=3, warm=1)
     res["ozaki_f32_4096"] = {"ms": round(ms, 3), "effective_fp32_TFLOPs": round(2 * 4096 ** 3 / (ms * 1e-3) / 1e12, 2),
                              "slice_TOPS": round(28 * 2 * 4096 ** 3 / (ms * 1e-3) / 1e12, 1)}
+    # the page's own configuration of the scheme: 4 slices, diagonals g <= 5 (10 slice pairs),
+    # with its error against an fp64 GEMM relative to (|A||B|)_ij on 64 sampled rows
+    ws4 = torch.empty(dg.ozaki_workspace_size(4096, 4096, 4096, 4, 5), dtype=torch.uint8, device=dev)
+    ms4 = _time(torch, lambda: dg.ozaki_f32(Af, Bf, nslices=4, max_diag=5, out=Cf, ws=ws4), flush, reps=3, warm=1)
+    rows = torch.arange(0, 4096, 64, device=dev)
+    Ad, Bd = Af[rows].double(), Bf.double()
+    rel = lambda C: float(((C[rows].double() - Ad @ Bd).abs() / (Ad.abs() @ Bd.abs())).max())
+    rel4 = rel(Cf)
+    dg.ozaki_f32(Af, Bf, out=Cf, ws=ws)
+    res["ozaki_f32_4096"]["max_err_over_absAabsB_sampled"] = rel(Cf)
+    res["ozaki_f32_4096_4slices"] = {"ms": round(ms4, 3),
+                                     "effective_fp32_TFLOPs": round(2 * 4096 ** 3 / (ms4 * 1e-3) / 1e12, 2),
+                                     "max_err_over_absAabsB_sampled": rel4}
+    del ws4, Ad, Bd
     del Af, Bf, Cf, ws
     # context for the tensor-core roofline: the vendor library's fp16 GEMM (fp32 accumulate)
     # on the FFN shapes, operands resident, L2 flushed
@@ -512,8 +532,8 @@ def run_profile(name):
             args = synthetic.ffn_gate_up()
         elif name == "ffn_down":
             args = synthetic.ffn_down()
-        elif name == "sweep":
-            args = synthetic.sweep(2048)
+        elif name.startswith("sweep"):
+            args = synthetic.sweep({"sweep": 2048, "sweep1": 1, "sweep64": 64}[name])
         else:
             args = synthetic.skinny()
         split = {"skinny8": 8, "skinny32": 32}.get(name, 1)

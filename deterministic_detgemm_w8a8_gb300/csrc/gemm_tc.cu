@@ -533,6 +533,9 @@ int max_pair_clusters() {
     if (dev < 0 || dev >= 64) return 1;
     std::lock_guard<std::mutex> lock(g_tc_mutex);
     if (g_max_clusters[dev] == 0) {
+        if (cudaFuncSetAttribute(tc2_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM_BYTES) !=
+            cudaSuccess)
+            return 0;
         cudaLaunchConfig_t cfg = {};
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -570,10 +573,9 @@ static cudaError_t tc2_launch(TcArgs a, const void* A16, int64_t lda, int a_plan
         e = cudaMemsetAsync(ws_split, 0, tc_split_bytes(a.ndiag, a.M, a.N, a.split), s);
         if (e != cudaSuccess) return e;
     }
-    e = cudaFuncSetAttribute(tc2_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM_BYTES);
-    if (e != cudaSuccess) return e;
     const int total = a.ndiag * a.tiles_m * a.tiles_n * a.split;
-    int clusters = max_pair_clusters();
+    int clusters = max_pair_clusters();  // also opts the kernel into its shared memory (once per device)
+    if (clusters <= 0) return cudaErrorInvalidConfiguration;
     if (clusters > total) clusters = total;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
