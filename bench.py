@@ -527,7 +527,7 @@ def run_profile(name):
     import deterministic_detgemm_w8a8_gb300 as dg
     dev = torch.device("cuda:0")
     tdev = lambda x: torch.from_numpy(x).to(dev)
-    if name.startswith("ffn") or name == "sweep" or name.startswith("skinny"):
+    if name.startswith("ffn") or name.startswith("sweep") or name.startswith("skinny"):
         if name == "ffn_gate_up":
             args = synthetic.ffn_gate_up()
         elif name == "ffn_down":

@@ -429,17 +429,28 @@ __global__ void __launch_bounds__(SK_THREADS, sk_ctas_per_sm(MT)) skinny_kernel(
 }
 
 // ---------------------------------------------------------------------------- finish
-// C[row][col] from the exact sums, two columns per thread; waits for the main kernel.
+// C from the exact sums once the main kernel has completed. A block takes 32 columns: their
+// sums are 32 M consecutive words of the token-contiguous workspace (read coalesced into
+// shared memory), then each thread rounds two columns of one row (written coalesced).
+constexpr int SKF_COLS = 32;
+
 __global__ void __launch_bounds__(256) skinny_finish_kernel(const __grid_constant__ SkArgs p) {
+    __shared__ int32_t tile[SKF_COLS][64 + 1];  // [column][token], M <= 64
     pdl_wait();
-    const int half_n = (p.N + 1) / 2;
-    const int64_t total = (int64_t)p.M * half_n;
-    for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < total; v += (int64_t)gridDim.x * blockDim.x) {
-        const int row = (int)(v / half_n);
-        const int col = 2 * (int)(v - (int64_t)row * half_n);
-        const int32_t v0 = __ldcg(p.ws_acc + (int64_t)col * p.M + row);
-        const int32_t v1 = col + 1 < p.N ? __ldcg(p.ws_acc + (int64_t)(col + 1) * p.M + row) : 0;
-        store_pair(p, row, col, v0, v1);
+    const int c0 = blockIdx.x * SKF_COLS;
+    const int ncols = min(SKF_COLS, p.N - c0);
+    const int words = ncols * p.M;
+    const int32_t* src = p.ws_acc + (int64_t)c0 * p.M;
+    for (int i = threadIdx.x; i < words; i += blockDim.x) {
+        const int c = i / p.M;
+        tile[c][i - c * p.M] = __ldcg(src + i);
+    }
+    __syncthreads();
+    const int pairs = SKF_COLS / 2;
+    for (int i = threadIdx.x; i < p.M * pairs; i += blockDim.x) {
+        const int row = i / pairs;
+        const int c = 2 * (i - row * pairs);
+        if (c < ncols) store_pair(p, row, c0 + c, tile[c][row], c + 1 < ncols ? tile[c + 1][row] : 0);
     }
 }
 
@@ -531,10 +542,8 @@ cudaError_t sk_launch_mt(const CUtensorMap& tmW, const CUtensorMap& tmA, const S
     if (grid > blocks) grid = blocks;
     e = launch_pdl(skinny_kernel<MT>, dim3((unsigned)grid), dim3(SK_THREADS), (size_t)smem, s, tmW, tmA, a);
     if (e != cudaSuccess) return e;
-    const int64_t pairs = (int64_t)a.M * ((a.N + 1) / 2);
-    int64_t fblocks = (pairs + 255) / 256;
-    if (fblocks > (int64_t)sk_num_sms()) fblocks = sk_num_sms();
-    return launch_pdl(skinny_finish_kernel, dim3((unsigned)fblocks), dim3(256), 0, s, a);
+    const unsigned fblocks = (unsigned)((a.N + SKF_COLS - 1) / SKF_COLS);
+    return launch_pdl(skinny_finish_kernel, dim3(fblocks), dim3(256), 0, s, a);
 }
 
 }  // namespace
