@@ -57,3 +57,30 @@ def test_host_async_then_sync(lib, dev):
     s.synchronize()
     want = lib.w8a8(*(torch.from_numpy(x).to(dev) for x in (A, W, ea, ew)))
     assert (out.view(torch.int16).numpy().view(np.uint16) == bf16_bits(want)).all()
+
+
+def test_host_two_streams_share_copy_streams(lib, dev):
+    """Two independent problems issued on two streams go through the same library copy
+    streams and events (re-recorded by the second call); every step's results equal those
+    of the calls made one after the other."""
+    probs = [synthetic.w8a8_normal(11, 1500, 640, 1024, 25.0, 35.0, -14, -6),
+             synthetic.w8a8_normal(12, 700, 256, 2560, 25.0, 35.0, -14, -6)]
+    want = [bf16_bits(lib.w8a8(*(torch.from_numpy(x).to(dev) for x in p))) for p in probs]
+    hosts = [[torch.from_numpy(x).pin_memory() for x in p] for p in probs]
+    outs = [torch.empty((p[0].shape[0], p[1].shape[0]), dtype=torch.bfloat16).pin_memory() for p in probs]
+    bufs = [torch.empty(lib.w8a8_host_buffer_size(p[0].shape[0], p[1].shape[0], p[0].shape[1]),
+                        dtype=torch.uint8, device=dev) for p in probs]
+    main = torch.cuda.current_stream()
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    for step in range(3):
+        for o in outs:
+            o.view(torch.int16).fill_(-1)
+        for s in streams:
+            s.wait_stream(main)
+        for h, o, b, s in zip(hosts, outs, bufs, streams):
+            lib.w8a8_host(*h, out=o, buf=b, stream=s, sync=False)
+        for s in streams:
+            main.wait_stream(s)
+        main.synchronize()
+        for o, w in zip(outs, want):
+            assert (o.view(torch.int16).numpy().view(np.uint16) == w).all(), step
