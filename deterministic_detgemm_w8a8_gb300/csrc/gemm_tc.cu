@@ -25,7 +25,8 @@
 //              and adds it to 128 int32 registers per thread; after the unit's last chunk
 //              it rounds to bf16 (or keeps int32), stages its 32 x 128 block in a 4 KB
 //              shared-memory slot and writes it with TMA stores or, under split-K, adds the
-//              partial into an int32 workspace with atomics and the last-arriving warp finishes.
+//              partial into the tile's int32 slot of the split workspace with TMA reductions;
+//              the last-arriving warp reads the sums back and finishes.
 // Operands are fp16 planes [plane][rows][Kp] addressed through 3-D tensor maps; a unit
 // walks a list of (A plane, B plane) segments: one segment for W8A8, one per slice pair
 // for an Ozaki diagonal.
@@ -36,6 +37,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <cstring>
 #include <mutex>
 
 #include "common.cuh"
@@ -55,24 +57,31 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr int CHUNK_KB = 16;  // 16 blocks of 64 = 1024 K values per exact fp32 chunk
 
 struct Unit {
-    int d, tm, tn, z;
+    int d, tm, tn, z;  // plane group, tile row, tile column, K part
 };
 
-__device__ __forceinline__ Unit unit_of(const TcArgs& p, int u) {
-    Unit r;
-    const int per_d = p.tiles_m * p.tiles_n * p.split;
-    r.d = u / per_d;
-    int rem = u - r.d * per_d;
-    int t = rem / p.split;
-    r.z = rem - t * p.split;
+// tile unit j -> (plane group, tile row, tile column)
+__device__ __forceinline__ void tile_of(const TcArgs& p, int j, int& d, int& tm, int& tn) {
+    const int per_d = p.tiles_m * p.tiles_n;
+    d = j / per_d;
+    const int t = j - d * per_d;
     // grouped raster: p.group_m tile rows walk together across N for L2 reuse of B
     const int per_group = p.group_m * p.tiles_n;
     const int g = t / per_group;
     const int first_m = g * p.group_m;
     const int gsize = min(p.tiles_m - first_m, p.group_m);
     const int in = t - g * per_group;
-    r.tm = first_m + in % gsize;
-    r.tn = in / gsize;
+    tm = first_m + in % gsize;
+    tn = in / gsize;
+}
+
+// unit u -> tile unit u / split (plane group major; its slot in the split workspace),
+// K part u % split
+__device__ __forceinline__ Unit unit_of(const TcArgs& p, int u) {
+    Unit r;
+    const int j = u / p.split;
+    r.z = u - j * p.split;
+    tile_of(p, j, r.d, r.tm, r.tn);
     return r;
 }
 
@@ -195,6 +204,33 @@ __device__ __forceinline__ void finish_rows(const TcArgs& p, const CUtensorMap* 
     }
 }
 
+// A warp's 32 x 128 int32 partial into the split workspace (int32 [tile units x 256][256],
+// row-major): four 32 x 32 pieces staged in the warp's slot (128-byte swizzle) and added
+// to global memory by TMA reductions.
+__device__ __forceinline__ void reduce_rows(const CUtensorMap* tmS, uint8_t* slot, int wrow, int wcol,
+                                            const int32_t (&acc)[128], bool& pending) {
+    const int lane = threadIdx.x & 31;
+    const uint32_t sbase = smem_addr(slot) + (uint32_t)lane * 128u;
+    const int sw = lane & 7;
+#pragma unroll
+    for (int pc = 0; pc < 4; ++pc) {
+        slot_acquire(pending);
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+            const int j = 32 * pc + 4 * jj;
+            st_shared16(sbase + (uint32_t)((jj ^ sw) << 4), (uint32_t)acc[j], (uint32_t)acc[j + 1],
+                        (uint32_t)acc[j + 2], (uint32_t)acc[j + 3]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            tma_reduce_add_2d(tmS, slot, wcol + 32 * pc, wrow);
+            bulk_commit();
+        }
+        pending = true;
+    }
+}
+
 // ------------------------------------------------------------------------------------
 // The kernel (tcgen05 cta_group::2): a cluster of two CTAs computes a 256 x 256
 // tile. CTA r of the pair holds A rows [256 tm + 128 r, +128) and B rows
@@ -218,9 +254,13 @@ constexpr int P_SLOT_BYTES = 32 * 128;  // one epilogue warp's staging slot
 constexpr int P_SMEM_BYTES =
     P_STAGES * P_STAGE_BYTES + EPI_WARPS * P_SLOT_BYTES + 1024 /*alignment slack*/ + 256 /*barriers*/;
 
+// kSplit: the instantiation for split > 1 (the split epilogue's registers stay out of the
+// other one)
+template <bool kSplit>
 __global__ void __launch_bounds__(THREADS, 1)
     tc2_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ TcArgs p) {
+                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmS,
+                    const __grid_constant__ TcArgs p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* slots = smem + P_STAGES * P_STAGE_BYTES;  // epilogue staging, 1024-byte aligned
@@ -403,29 +443,39 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (!ok) break;
             const int row = un.tm * 256 + (int)rank * 128 + q * 32 + lane;
             const int col0 = un.tn * BN + h * 128;
-            if (p.split == 1) {
+            if constexpr (!kSplit) {
                 finish_rows(p, &tmC, slot, un.d, row - lane, col0, acc, pending);
                 continue;
             }
-            int32_t* ws = p.ws_acc + (int64_t)un.d * p.M * p.N;
-            if (row < p.M) {
-#pragma unroll
-                for (int i = 0; i < 128; ++i)
-                    if (col0 + i < p.N) atomicAdd(ws + (int64_t)row * p.N + col0 + i, acc[i]);
-            }
-            __threadfence();
-            __syncwarp();
+            // a K part: add the exact partial into the tile's slot of the split workspace with
+            // TMA reductions (integer addition in L2: order-free), then count the arrival; the
+            // warp that arrives last reads the complete sums back
+            const int sidx = u / p.split;
+            const int wrow = sidx * 256 + (int)rank * 128 + q * 32;
+            reduce_rows(&tmS, slot, wrow, h * 128, acc, pending);
             unsigned prev = 0;
             if (lane == 0) {
-                const int64_t sub = ((((int64_t)un.d * p.tiles_m + un.tm) * p.tiles_n + un.tn) * 2 + rank) * EPI_WARPS + ew;
-                prev = atomicAdd(p.ws_cnt + sub, 1u);
+                bulk_wait_all();             // the reductions have been performed
+                fence_proxy_async_global();  // ... before the arrival below
+                __threadfence();
+                prev = atomicAdd(p.ws_cnt + ((int64_t)sidx * 2 + rank) * EPI_WARPS + ew, 1u);
             }
+            pending = false;
             prev = __shfl_sync(0xffffffffu, prev, 0);
             if (prev != (unsigned)(p.split - 1)) continue;
             __threadfence();
-            if (row < p.M) {
+            // lane l's row: 32 independent 16-byte loads. They go through L1, which holds no
+            // copy of these lines (no one reads a slot before its sums are complete, and L1 starts
+            // each launch empty), so that the four 16-byte pieces of each 128-byte line that a
+            // lane reads in turn come from one L2 request.
+            const int4* src = reinterpret_cast<const int4*>(p.ws_acc + (int64_t)(wrow + lane) * 256 + h * 128);
 #pragma unroll
-                for (int i = 0; i < 128; ++i) acc[i] = (col0 + i < p.N) ? __ldcg(ws + (int64_t)row * p.N + col0 + i) : 0;
+            for (int i = 0; i < 32; ++i) {
+                const int4 v = __ldca(src + i);
+                acc[4 * i] = v.x;
+                acc[4 * i + 1] = v.y;
+                acc[4 * i + 2] = v.z;
+                acc[4 * i + 3] = v.w;
             }
             finish_rows(p, &tmC, slot, un.d, row - lane, col0, acc, pending);
         }
@@ -516,12 +566,34 @@ cudaError_t make_out_map(CUtensorMap* m, const TcArgs& a) {
 int64_t tc_padded_k(int K) { return ((int64_t)K + BK - 1) / BK * BK; }
 
 
+// Split workspace: one 256 x 256 int32 slot per tile unit, then an arrival counter per tile
+// unit, CTA and epilogue warp; zeroed by a memset before the engine starts.
+constexpr size_t kSlotBytes = (size_t)256 * 256 * sizeof(int32_t);
+
+static size_t split_ws_bytes(int cut) {
+    if (cut <= 0) return 0;
+    return (size_t)cut * kSlotBytes + (((size_t)cut * 2 * EPI_WARPS * sizeof(uint32_t) + 255) & ~(size_t)255);
+}
+
 size_t tc_split_bytes(int ndiag, int M, int N, int split) {
     if (split <= 1) return 0;
-    // counters for 128-row tiles, or for 256-row pair tiles x 2 CTAs (whichever is more)
-    const int tiles = 2 * ((M + 255) / 256) * ((N + BN - 1) / BN);
-    size_t acc = ((size_t)ndiag * M * N * sizeof(int32_t) + 255) & ~(size_t)255;
-    return acc + (size_t)ndiag * tiles * EPI_WARPS * sizeof(uint32_t);
+    return split_ws_bytes(ndiag * ((M + 255) / 256) * ((N + BN - 1) / BN));
+}
+
+// 2-D map over the split workspace's slots: int32 [units x 256][256], box 32 x 32, the
+// epilogue's slot layout (128-byte swizzle)
+static cudaError_t make_ws_map(CUtensorMap* m, void* base, int cut) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc;
+    cudaError_t e = get_encode(&enc);
+    if (e != cudaSuccess) return e;
+    cuuint64_t dims[2] = {256, (cuuint64_t)cut * 256};
+    cuuint64_t strides[1] = {256 * sizeof(int32_t)};
+    cuuint32_t box[2] = {32, 32};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_INT32, 2, base, dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
 namespace {
@@ -533,8 +605,10 @@ int max_pair_clusters() {
     if (dev < 0 || dev >= 64) return 1;
     std::lock_guard<std::mutex> lock(g_tc_mutex);
     if (g_max_clusters[dev] == 0) {
-        if (cudaFuncSetAttribute(tc2_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM_BYTES) !=
-            cudaSuccess)
+        if (cudaFuncSetAttribute(tc2_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM_BYTES) !=
+                cudaSuccess ||
+            cudaFuncSetAttribute(tc2_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM_BYTES) !=
+                cudaSuccess)
             return 0;
         cudaLaunchConfig_t cfg = {};
         cudaLaunchAttribute attr[1];
@@ -548,34 +622,44 @@ int max_pair_clusters() {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, tc2_gemm_kernel, &cfg) != cudaSuccess || n <= 0) n = 1;
+        if (cudaOccupancyMaxActiveClusters(&n, tc2_gemm_kernel<false>, &cfg) != cudaSuccess || n <= 0) n = 1;
         g_max_clusters[dev] = n;
     }
     return g_max_clusters[dev];
 }
 }  // namespace
 
-static cudaError_t tc2_launch(TcArgs a, const void* A16, int64_t lda, int a_planes, const void* B16, int64_t ldb,
-                              int b_planes, int64_t kext, void* ws_split, cudaStream_t s) {
+static void set_tiles(TcArgs& a, int64_t kext) {
     a.tiles_m = (a.M + 255) / 256;
     a.tiles_n = (a.N + BN - 1) / BN;
     a.nkb = (int)((kext + BK - 1) / BK);
     if (a.group_m <= 0) a.group_m = 8;
+}
+
+cudaError_t tc_gemm_launch(const TcArgs& a0, const void* A16, int64_t lda, int a_planes, const void* B16,
+                           int64_t ldb, int b_planes, int64_t kext, void* ws_split, cudaStream_t s) {
+    if (a0.M == 0 || a0.N == 0) return cudaSuccess;
+    TcArgs a = a0;
+    set_tiles(a, kext);
     CUtensorMap tmA, tmB, tmC;
     cudaError_t e = make_map(&tmA, A16, kext, lda, a.M, a_planes, 128);
     if (e == cudaSuccess) e = make_map(&tmB, B16, kext, ldb, a.N, b_planes, 128);
     if (e == cudaSuccess) e = make_out_map(&tmC, a);
     if (e != cudaSuccess) return e;
-    if (a.split > 1) {
-        size_t accb = (((size_t)a.ndiag * a.M * a.N * sizeof(int32_t)) + 255) & ~(size_t)255;
-        a.ws_acc = reinterpret_cast<int32_t*>(ws_split);
-        a.ws_cnt = reinterpret_cast<uint32_t*>(reinterpret_cast<char*>(ws_split) + accb);
-        e = cudaMemsetAsync(ws_split, 0, tc_split_bytes(a.ndiag, a.M, a.N, a.split), s);
-        if (e != cudaSuccess) return e;
-    }
-    const int total = a.ndiag * a.tiles_m * a.tiles_n * a.split;
     int clusters = max_pair_clusters();  // also opts the kernel into its shared memory (once per device)
     if (clusters <= 0) return cudaErrorInvalidConfiguration;
+    const int total = a.ndiag * a.tiles_m * a.tiles_n * a.split;
+    CUtensorMap tmS;
+    memset(&tmS, 0, sizeof(tmS));
+    if (a.split > 1) {  // every tile unit in `split` K parts, one slot each
+        const int cut = a.ndiag * a.tiles_m * a.tiles_n;
+        a.ws_acc = reinterpret_cast<int32_t*>(ws_split);
+        a.ws_cnt = reinterpret_cast<uint32_t*>(reinterpret_cast<char*>(ws_split) + (size_t)cut * kSlotBytes);
+        e = make_ws_map(&tmS, ws_split, cut);
+        if (e != cudaSuccess) return e;
+        e = cudaMemsetAsync(ws_split, 0, split_ws_bytes(cut), s);
+        if (e != cudaSuccess) return e;
+    }
     if (clusters > total) clusters = total;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -589,15 +673,10 @@ static cudaError_t tc2_launch(TcArgs a, const void* A16, int64_t lda, int a_plan
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, tc2_gemm_kernel, tmA, tmB, tmC, a);
+    e = a.split > 1 ? cudaLaunchKernelEx(&cfg, tc2_gemm_kernel<true>, tmA, tmB, tmC, tmS, a)
+                    : cudaLaunchKernelEx(&cfg, tc2_gemm_kernel<false>, tmA, tmB, tmC, tmS, a);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
-}
-
-cudaError_t tc_gemm_launch(const TcArgs& a, const void* A16, int64_t lda, int a_planes, const void* B16, int64_t ldb,
-                           int b_planes, int64_t kext, void* ws_split, cudaStream_t s) {
-    if (a.M == 0 || a.N == 0) return cudaSuccess;
-    return tc2_launch(a, A16, lda, a_planes, B16, ldb, b_planes, kext, ws_split, s);
 }
 
 // Self-check of the bounded waits: one thread waits on an mbarrier that nothing ever

@@ -84,7 +84,10 @@ struct TcArgs {
     int diag_nseg[kTcMaxDiag];
     int16_t segA[kTcMaxSeg];
     int16_t segB[kTcMaxSeg];
-    int split;                 // contiguous parts of each group's flattened K-block range
+    int split;                 // contiguous parts of each group's flattened K-block range; with
+                               // split > 1 the parts' exact int32 partials meet in the split
+                               // workspace (one 256 x 256 slot per tile unit) and the warp that
+                               // arrives last at its counter rounds the sums
     int tiles_m, tiles_n;      // set by the launcher
     int group_m;               // tile rows per raster group (0: default)
     int mode;                  // EpilogueMode
@@ -93,8 +96,8 @@ struct TcArgs {
     void* C;                   // bf16 [M x ldc], or int32 planes [ndiag][c_plane]
     int64_t ldc;
     int64_t c_plane;           // elements between int32 output planes
-    int32_t* ws_acc;           // set by the launcher (split > 1)
-    uint32_t* ws_cnt;
+    int32_t* ws_acc;           // set by the launcher (split > 1): [tile units][256][256] sums
+    uint32_t* ws_cnt;          // [tile units][2 CTAs][epilogue warps] arrival counters
 };
 
 int64_t tc_padded_k(int K);

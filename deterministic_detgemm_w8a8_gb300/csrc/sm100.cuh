@@ -104,6 +104,17 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* m, const void* s
                  "r"(x), "r"(y), "r"(z), "r"(smem_addr(src))
                  : "memory");
 }
+// 2-D tiled reduction of the box at (x, y): global += shared, element-wise, with the
+// tensor map's element type (int32 here: exact integer addition performed in L2)
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* m, const void* src, int x, int y) {
+    asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     reinterpret_cast<uint64_t>(m)),
+                 "r"(x), "r"(y), "r"(smem_addr(src))
+                 : "memory");
+}
+// orders this thread's completed async-proxy global writes (bulk stores / reductions)
+// before its later generic-proxy memory operations
+__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // the bulk stores committed so far have finished reading shared memory
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
