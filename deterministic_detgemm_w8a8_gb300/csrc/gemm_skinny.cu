@@ -454,6 +454,178 @@ __global__ void __launch_bounds__(256) skinny_finish_kernel(const __grid_constan
     }
 }
 
+// ---------------------------------------------------------------------------- whole K
+// Decode-shaped problems with a short K (one launch, no workspace): CTA b owns W rows
+// [32 b, 32 b + 32) over the whole of K, so its sums are complete inside the CTA. Warp 0,
+// lane 0, streams per 128-wide K block one int8 box W[32 x 128] (evict-first) and one int8
+// box A[16 MT x 128] (128-byte swizzle, zero fill past M, N and K) into a ring of
+// wk_stages(MT) stages (16 for up to 16 tokens: the whole of a K = 2048 problem in flight). The eight consumer warps are two row groups (16 W rows each) times four K groups:
+// K group kg takes the K blocks kb = kg mod 4 (their stages, kb mod WK_STAGES, are released
+// by its two warps). Both operands are widened to fp16 in registers and multiplied with the
+// fp16 warp MMA into fp32 accumulators. With K <= WK_MAX_K = 4096 a warp's K blocks hold at
+// most 1024 k values, so every partial sum is an integer of magnitude <= 2^24, exact in fp32,
+// and no int32 drain is needed on the way. At the end the four K groups' partials, converted
+// to int32, meet in shared memory (integer sums, exact) and each row group's first warp
+// rounds and stores them.
+constexpr int WK_ROWS = 32;
+constexpr int WK_KG = 4;
+constexpr int WK_CONSUMERS = 2 * WK_KG;
+constexpr int WK_THREADS = 32 * (1 + WK_CONSUMERS);
+constexpr int WK_MAX_K = WK_KG * 1024;  // longer K goes to the split kernel (all SMs share K)
+
+__host__ __device__ constexpr int wk_w_bytes() { return WK_ROWS * 128; }
+__host__ __device__ constexpr int wk_a_bytes(int MT) { return 16 * MT * 128; }
+__host__ __device__ constexpr int wk_stage_bytes(int MT) { return wk_w_bytes() + wk_a_bytes(MT); }
+// a multiple of WK_KG, so that stage s is always released by K group s mod WK_KG
+// (at most 96 KB of ring: two CTAs per SM)
+__host__ __device__ constexpr int wk_stages(int MT) { return MT == 1 ? 16 : (MT == 2 ? 12 : 8); }
+// the ring, reused for the partial sums at the end: WK_CONSUMERS x 32 lanes x 8 MT words
+__host__ __device__ constexpr int wk_smem_bytes(int MT) {
+    return (wk_stages(MT) * wk_stage_bytes(MT) > WK_CONSUMERS * 32 * 8 * MT * 4 ? wk_stages(MT) * wk_stage_bytes(MT)
+                                                                                  : WK_CONSUMERS * 32 * 8 * MT * 4) +
+           1024 + 512;
+}
+
+__device__ __forceinline__ void consumer_bar() { asm volatile("bar.sync 1, %0;" ::"n"(WK_CONSUMERS * 32) : "memory"); }
+
+template <int MT>
+__global__ void __launch_bounds__(WK_THREADS, 2) skinny_wk_kernel(const __grid_constant__ CUtensorMap tmW,
+                                                                  const __grid_constant__ CUtensorMap tmA,
+                                                                  const __grid_constant__ SkArgs p) {
+    constexpr int STAGE = wk_stage_bytes(MT);
+    constexpr int WK_STAGES = wk_stages(MT);
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + (wk_smem_bytes(MT) - 1024 - 512));
+    uint64_t* empty = full + WK_STAGES;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + WK_STAGES);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nkb = (p.K + 127) / 128;
+    const int row0 = blockIdx.x * WK_ROWS;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < WK_STAGES; ++s) {
+            mbar_init(full + s, 1);
+            mbar_init(empty + s, 2);  // the two row-group warps of the stage's K group
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == 0) {
+        if (lane == 0) {
+            prefetch_tmap(&tmW);
+            prefetch_tmap(&tmA);
+            const uint64_t stream_policy = l2_policy_evict_first();
+            bool ok = true;
+            int kb = 0;
+            for (; kb < nkb; ++kb) {
+                const int st = kb % WK_STAGES;
+                if (kb >= WK_STAGES && !mbar_wait(empty + st, ((kb / WK_STAGES) - 1) & 1u, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                uint8_t* d = smem + st * STAGE;
+                mbar_arrive_expect_tx(full + st, STAGE);
+                tma_load_2d_hint(d, &tmW, full + st, kb * 128, row0, stream_policy);
+                tma_load_2d(d + wk_w_bytes(), &tmA, full + st, kb * 128, 0);
+            }
+            if (!ok) {
+                // let the loads already issued land before the CTA's shared memory goes away
+                for (int i = kb - 1; i >= 0 && i >= kb - WK_STAGES; --i)
+                    mbar_wait_drain(full + i % WK_STAGES, (i / WK_STAGES) & 1u, kDrainLimitNs);
+            }
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------------- consumers
+    const int cw = warp - 1;
+    const int rg = cw & 1, kg = cw >> 1;
+    const int g = lane >> 2, t = lane & 3;
+    // the epilogue's exponents: fetched into L1 now, read after the main loop
+    if (cw == 0 && lane < 3) {
+        const void* a = lane == 0 ? (const void*)(p.ew + min(row0, p.N - 1))
+                                  : (const void*)(p.ea + min(32 * (lane - 1), p.M - 1));
+        asm volatile("prefetch.global.L1 [%0];" ::"l"(a));
+    }
+    const uint32_t sbase = smem_addr(smem);
+    float accf[MT][2][4];
+#pragma unroll
+    for (int a = 0; a < MT; ++a)
+#pragma unroll
+        for (int b = 0; b < 2; ++b)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) accf[a][b][c] = 0.f;
+    bool ok = true;
+    for (int kb = kg; kb < nkb; kb += WK_KG) {
+        const int st = kb % WK_STAGES;
+        const bool got = __all_sync(0xffffffffu, mbar_wait(full + st, (kb / WK_STAGES) & 1u, abort_flag));
+        if (!got) {
+            ok = false;
+            break;
+        }
+        const uint32_t wb = sbase + st * STAGE;
+        const uint32_t ab = wb + wk_w_bytes();
+        // lane (g, t) takes the 16-byte chunks t and t + 4 of each 128-byte row (16 k values
+        // each) of W and of A alike, so both operands see the same k order
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            const int c = t + 4 * half;
+            uint32_t hw[2][8];
+#pragma unroll
+            for (int j = 0; j < 2; ++j) i8x16_to_f16x16(lds16(wb + sw128(16 * rg + 8 * j + g, c)), hw[j]);
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+                uint32_t h0[8], h1[8];
+                i8x16_to_f16x16(lds16(ab + sw128(16 * mt + g, c)), h0);
+                i8x16_to_f16x16(lds16(ab + sw128(16 * mt + g + 8, c)), h1);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint32_t a[4] = {h0[2 * q], h1[2 * q], h0[2 * q + 1], h1[2 * q + 1]};
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) mma_f16(accf[mt][j], a, hw[j][2 * q], hw[j][2 * q + 1]);
+                }
+            }
+        }
+        // generic-proxy reads of the stage ordered before its release to the TMA refill
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty + st);
+    }
+
+    // The K groups' partials meet in the ring: every consumer is past its last stage, so
+    // every load into it has landed (unless a wait gave up, which raised the abort flag and
+    // the device status; then nothing is stored). Layout [warp][element][lane].
+    consumer_bar();
+    int32_t* red = reinterpret_cast<int32_t*>(smem);
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                red[(cw * (MT * 8) + (mt * 2 + j) * 4 + c) * 32 + lane] = __float2int_rn(accf[mt][j][c]);
+    consumer_bar();
+    if (kg != 0 || !ok || *abort_flag) return;
+    // accumulator (mt, j, c): token 16 mt + g (+8 for c >= 2), W row 16 rg + 8 j + 2 t (+1 odd c)
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            int32_t v[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int e = (mt * 2 + j) * 4 + c;
+                v[c] = red[((rg + 0) * (MT * 8) + e) * 32 + lane] + red[((rg + 2) * (MT * 8) + e) * 32 + lane] +
+                       red[((rg + 4) * (MT * 8) + e) * 32 + lane] + red[((rg + 6) * (MT * 8) + e) * 32 + lane];
+            }
+            const int col = row0 + 16 * rg + 8 * j + 2 * t;
+            store_pair(p, 16 * mt + g, col, v[0], v[1]);
+            store_pair(p, 16 * mt + g + 8, col, v[2], v[3]);
+        }
+}
 // launch with the programmatic-stream-serialization attribute (may overlap the kernel before)
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args&&... args) {
@@ -546,6 +718,27 @@ cudaError_t sk_launch_mt(const CUtensorMap& tmW, const CUtensorMap& tmA, const S
     return launch_pdl(skinny_finish_kernel, dim3(fblocks), dim3(256), 0, s, a);
 }
 
+int g_wk_set[64][5];  // skinny_wk_kernel<MT> opted into its shared memory, per device
+
+template <int MT>
+cudaError_t wk_launch_mt(const CUtensorMap& tmW, const CUtensorMap& tmA, const SkArgs& a, cudaStream_t s) {
+    const int smem = wk_smem_bytes(MT);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    {
+        std::lock_guard<std::mutex> lock(g_sk_mutex);
+        if (!g_wk_set[dev][MT]) {
+            e = cudaFuncSetAttribute(skinny_wk_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+            if (e != cudaSuccess) return e;
+            g_wk_set[dev][MT] = 1;
+        }
+    }
+    skinny_wk_kernel<MT><<<(unsigned)((a.N + WK_ROWS - 1) / WK_ROWS), WK_THREADS, smem, s>>>(tmW, tmA, a);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 size_t skinny_workspace_bytes(int M, int N, int K, int split) {
@@ -560,6 +753,28 @@ cudaError_t skinny_launch(const int8_t* A, int64_t lda, const int8_t* W, int64_t
     (void)split;  // the kernel divides K among the SMs itself; the bits never depend on it
     if (M == 0 || N == 0) return cudaSuccess;
     const int MT = (M + 15) / 16;
+    if (K <= WK_MAX_K) {
+        // short K: one CTA per 32 W rows over the whole of K, int8 A read directly
+        SkArgs a = {};
+        a.M = M;
+        a.N = N;
+        a.K = K;
+        a.ea = ea;
+        a.ew = ew;
+        a.C = reinterpret_cast<uint16_t*>(C);
+        a.ldc = ldc;
+        a.mode = mode;
+        CUtensorMap tmW, tmA;
+        cudaError_t e = sk_map(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, W, K, ldw, N, WK_ROWS);
+        if (e == cudaSuccess) e = sk_map(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A, K, lda, M, 16 * MT);
+        if (e != cudaSuccess) return e;
+        switch (MT) {
+            case 1: return wk_launch_mt<1>(tmW, tmA, a, s);
+            case 2: return wk_launch_mt<2>(tmW, tmA, a, s);
+            case 3: return wk_launch_mt<3>(tmW, tmA, a, s);
+            default: return wk_launch_mt<4>(tmW, tmA, a, s);
+        }
+    }
     const SkLayout L = sk_layout(M, N, K);
     char* base = reinterpret_cast<char*>(ws);
     SkArgs a = {};

@@ -299,3 +299,21 @@ def test_skinny_many_ctas_repeated(lib, dev, oracle_mod):
         out = poison_like((16, 4096), torch.int32, dev)
         lib.gemm_s8_i32(tA, tW, split_k=split, out=out)
         assert (out.cpu().numpy() == want).all(), split
+
+
+@pytest.mark.parametrize("M,N,K", [(64, 40, 4096), (17, 100, 4096), (1, 33, 4097), (48, 70, 3969), (64, 96, 5000)])
+def test_decode_short_and_long_k(lib, dev, oracle_mod, M, N, K):
+    # up to K = 4096 the decode path keeps whole rows of W per CTA (each warp's fp32 partials
+    # hold at most 1024 products); longer K splits K over the SMs. Worst case first: every
+    # product 128^2, so each warp's partial sums reach 2^24 exactly.
+    ld = (K + 15) // 16 * 16
+    A = np.full((M, K), -128, np.int8)
+    W = np.full((N, K), -128, np.int8)
+    assert (run_i32(lib, dev, A, W, lda=ld, ldw=ld) == K * 16384).all()
+    rng = np.random.default_rng(M * 7 + N + K)
+    A = rng.integers(-128, 128, size=(M, K), dtype=np.int8)
+    W = rng.integers(-128, 128, size=(N, K), dtype=np.int8)
+    ea = rng.integers(-24, -2, size=M, dtype=np.int32)
+    ew = rng.integers(-24, -2, size=N, dtype=np.int32)
+    assert (run_w8a8(lib, dev, A, W, ea, ew, lda=ld, ldw=ld) == oracle_mod.w8a8(A, W, ea, ew)).all()
+    assert (run_i32(lib, dev, A, W, lda=ld, ldw=ld) == oracle_mod.gemm_s8_i32(A, W)).all()
