@@ -113,9 +113,10 @@ const char* detgemm_status_string(detgemm_status s) {
 
 int detgemm_version(void) { return 100; }
 
-// Decode-shaped problems (M <= 64) stream W through the register-fed warp-MMA kernel;
-// everything larger runs on the tcgen05 engine over exact fp16 copies of the operands.
-static bool w8a8_uses_tc(int M) { return M > 64; }
+// Decode-shaped problems (decode_path: M <= 64) stream W
+// through the register-fed warp-MMA kernels; everything larger runs on the tcgen05 engine
+// over exact fp16 copies of the operands.
+static bool w8a8_uses_tc(int M, int K) { return !decode_path(M, K); }
 
 // tcgen05 path scratch: A16 [M][Kp] fp16 | W16 [N][Kp] fp16 | split-K sums and counters
 struct TcW8a8Layout {
@@ -136,7 +137,7 @@ static TcW8a8Layout tc_w8a8_layout(int M, int N, int K, int split_k) {
 
 size_t detgemm_w8a8_workspace_size(int M, int N, int K, int split_k) {
     if (M <= 0 || N <= 0 || K <= 0) return 0;
-    if (w8a8_uses_tc(M)) return tc_w8a8_layout(M, N, K, split_k).total;
+    if (w8a8_uses_tc(M, K)) return tc_w8a8_layout(M, N, K, split_k).total;
     return igemm_workspace_bytes(M, N, K, split_k);
 }
 
@@ -168,7 +169,7 @@ static detgemm_status run_tc(const int8_t* A, int64_t lda, const int8_t* W, int6
 static detgemm_status run_igemm(const int8_t* A, int64_t lda, const int8_t* W, int64_t ldw, const int32_t* ea,
                                 const int32_t* ew, void* C, int64_t ldc, int mode, int M, int N, int K, int split_k,
                                 void* ws, cudaStream_t stream) {
-    if (w8a8_uses_tc(M)) return run_tc(A, lda, W, ldw, ea, ew, C, ldc, mode, M, N, K, split_k, ws, stream);
+    if (w8a8_uses_tc(M, K)) return run_tc(A, lda, W, ldw, ea, ew, C, ldc, mode, M, N, K, split_k, ws, stream);
     IGemmArgs a = {};
     a.seg[0] = Seg{A, W};
     a.nseg = 1;
@@ -210,9 +211,9 @@ detgemm_status detgemm_gemm_s8_i32(const int8_t* A, int64_t lda, const int8_t* W
                      reinterpret_cast<cudaStream_t>(stream));
 }
 
-// Fused linear layer scratch. M > 64: A16 [M][Kp] fp16 | W16 [N][Kp] fp16 (only when no
-// widened weight is given) | ea [M] | split-K sums and counters. M <= 64: Q int8 [M][K16]
-// | ea [M] | the decode-shaped GEMM's scratch.
+// Fused linear layer scratch. Tensor-core path: A16 [M][Kp] fp16 | W16 [N][Kp] fp16 (only
+// when no widened weight is given) | ea [M] | split-K sums and counters. Decode-shaped
+// path: Q int8 [M][K16] | ea [M] | the decode-shaped GEMM's scratch.
 struct LinearLayout {
     int64_t Kp, K16;
     size_t a, w16, ea, gemm, total;
@@ -223,7 +224,7 @@ static LinearLayout linear_layout(int M, int N, int K, int split_k, bool have_w1
     L.Kp = tc_padded_k(K);
     L.K16 = ((int64_t)K + 15) / 16 * 16;
     size_t off = 0;
-    if (w8a8_uses_tc(M)) {
+    if (w8a8_uses_tc(M, K)) {
         L.a = off; off += align256((size_t)M * L.Kp * 2);
         L.w16 = off; off += have_w16 ? 0 : align256((size_t)N * L.Kp * 2);
         L.ea = off; off += align256((size_t)M * 4);
@@ -260,7 +261,7 @@ detgemm_status detgemm_linear_w8a8(const void* X, int x_dtype, int64_t ldx, int 
         return DETGEMM_ERR_ALIGNMENT;
     if ((ldx * xs) % 16 || ldw % 16 || (ldc * 2) % 16) return DETGEMM_ERR_ALIGNMENT;
     if (W16 && (!aligned16(W16) || ldw16 % 8)) return DETGEMM_ERR_ALIGNMENT;
-    const bool tc = w8a8_uses_tc(M);
+    const bool tc = w8a8_uses_tc(M, K);
     const bool use_w16 = tc && W16 != nullptr;
     const LinearLayout L = linear_layout(M, N, K, split_k, use_w16);
     if (ws == nullptr || ws_bytes < L.total) return DETGEMM_ERR_WORKSPACE;

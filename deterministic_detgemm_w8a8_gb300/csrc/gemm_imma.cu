@@ -12,7 +12,7 @@
 // Two kernels:
 //  * igemm_tile_kernel   — 128x128x64 CTA tile, 8 warps, 4-stage cp.async ring,
 //                          XOR-swizzled shared memory and ldmatrix fragments.
-//  (problems with M <= 64 go to the TMA-fed skinny kernel in gemm_skinny.cu)
+//  (decode-shaped problems, decode_path(M, K), go to the TMA-fed kernels in gemm_skinny.cu)
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -239,7 +239,7 @@ __global__ void __launch_bounds__(TTHREADS) igemm_tile_kernel(const __grid_const
         }
 }
 
-bool use_skinny(int M) { return M <= 64; }
+bool use_skinny(int M, int K) { return decode_path(M, K); }
 
 int n_tiles(int M, int N) { return ((N + TBN - 1) / TBN) * ((M + TBM - 1) / TBM); }
 
@@ -247,7 +247,7 @@ int n_tiles(int M, int N) { return ((N + TBN - 1) / TBN) * ((M + TBM - 1) / TBM)
 
 size_t igemm_workspace_bytes(int M, int N, int K, int split) {
     if (M == 0 || N == 0) return 0;
-    if (use_skinny(M)) return skinny_workspace_bytes(M, N, K, split);  // needed at any split
+    if (use_skinny(M, K)) return skinny_workspace_bytes(M, N, K, split);  // needed at any split
     if (split <= 1) return 0;
     size_t acc = (size_t)M * (size_t)N * sizeof(int32_t);
     acc = (acc + 255) & ~(size_t)255;
@@ -257,7 +257,7 @@ size_t igemm_workspace_bytes(int M, int N, int K, int split) {
 cudaError_t igemm_launch(const IGemmArgs& a_in, void* ws, cudaStream_t s) {
     IGemmArgs a = a_in;
     if (a.M == 0 || a.N == 0) return cudaSuccess;
-    if (use_skinny(a.M)) {
+    if (use_skinny(a.M, a.K)) {
         if (a.nseg != 1) return cudaErrorInvalidValue;
         return skinny_launch(a.seg[0].A, a.lda, a.seg[0].W, a.ldw, a.ea, a.ew, a.C, a.ldc, a.mode, a.M, a.N, a.K,
                              a.split, ws, s);

@@ -4,6 +4,8 @@
 // ...", §II "Pipeline and alibi"), then the bf16 pow2 epilogue. With M <= 64 there are
 // at most 128 multiply-adds per W byte, so the kernel is bound by reading W once from
 // HBM; its job is to keep enough bytes in flight and to spend few instructions per byte.
+// K <= 4096 runs in one launch (skinny_wk_kernel, below: whole rows of W per CTA); longer K
+// takes the split form:
 //
 // Three launches per call, chained by programmatic dependent launch (each starts while
 // its predecessor runs and waits for it with griddepcontrol.wait where it needs its data):
@@ -741,6 +743,11 @@ cudaError_t wk_launch_mt(const CUtensorMap& tmW, const CUtensorMap& tmA, const S
 
 }  // namespace
 
+bool decode_path(int M, int K) {
+    (void)K;
+    return M <= 64;
+}
+
 size_t skinny_workspace_bytes(int M, int N, int K, int split) {
     (void)split;
     if (M == 0 || N == 0) return 0;
@@ -752,6 +759,7 @@ cudaError_t skinny_launch(const int8_t* A, int64_t lda, const int8_t* W, int64_t
                           cudaStream_t s) {
     (void)split;  // the kernel divides K among the SMs itself; the bits never depend on it
     if (M == 0 || N == 0) return cudaSuccess;
+    if (!decode_path(M, K)) return cudaErrorInvalidValue;
     const int MT = (M + 15) / 16;
     if (K <= WK_MAX_K) {
         // short K: one CTA per 32 W rows over the whole of K, int8 A read directly

@@ -64,7 +64,7 @@ size_t up256(size_t x) { return (x + 255) & ~(size_t)255; }
 // Buffer layout. Rows are stored with 16-byte aligned strides: int8 rows of K16 bytes,
 // fp16 rows of Kp elements (the tensor-core engine's padded K), bf16 results of N8.
 struct HostLayout {
-    bool tc;        // tensor-core path (M > 64) or the decode-shaped path
+    bool tc;        // tensor-core path, or the decode-shaped path (decode_path(M, K))
     int R;          // rows per chunk
     int64_t K16, Kp, N8;
     size_t w, ew, w16, ws;
@@ -74,7 +74,7 @@ struct HostLayout {
 
 HostLayout host_layout(int M, int N, int K) {
     HostLayout L = {};
-    L.tc = M > 64;
+    L.tc = !decode_path(M, K);
     L.K16 = ((int64_t)K + 15) / 16 * 16;
     L.Kp = tc_padded_k(K);
     L.N8 = ((int64_t)N + 7) / 8 * 8;

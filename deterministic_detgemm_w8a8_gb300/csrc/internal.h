@@ -32,15 +32,17 @@ struct IGemmArgs {
     uint32_t* ws_cnt;     // one arrival counter per output tile, zero on entry (split > 1)
 };
 
-// Decode-shaped (M <= 64) exact int8 GEMM streaming W through a TMA ring (gemm_skinny.cu).
+// Decode-shaped exact int8 GEMM streaming W through a TMA ring (gemm_skinny.cu), for the
+// problems decode_path accepts (M <= 64); everything else runs on the tensor-core engine.
+bool decode_path(int M, int K);
 size_t skinny_workspace_bytes(int M, int N, int K, int split);
 cudaError_t skinny_launch(const int8_t* A, int64_t lda, const int8_t* W, int64_t ldw, const int32_t* ea,
                           const int32_t* ew, void* C, int64_t ldc, int mode, int M, int N, int K, int split, void* ws,
                           cudaStream_t s);
 cudaError_t skinny_take_status(uint32_t* bits);
 
-// Integer GEMM on the mma.sync int8 path (exact int32 accumulation); M <= 64 is routed to
-// skinny_launch.
+// Integer GEMM on the mma.sync int8 path (exact int32 accumulation); decode_path problems
+// are routed to skinny_launch.
 size_t igemm_workspace_bytes(int M, int N, int K, int split);
 cudaError_t igemm_launch(const IGemmArgs& a, void* ws, cudaStream_t s);
 

@@ -91,11 +91,12 @@ DETGEMM_API int detgemm_version(void);
  *   C   bf16 bit patterns (uint16) [M x N], row stride ldc
  *   split_k  number of contiguous K parts computed by separate CTAs and summed
  *            exactly ([P1] §3.2.2); 1 <= split_k <= ceil(K / 64). The output bits do
- *            not depend on it. For M <= 64 (decode-shaped, bound by reading W) the
- *            kernel divides K among all SMs by itself so that every SM streams the same
+ *            not depend on it. Decode-shaped problems (M <= 64, bound by reading W)
+ *            choose their own cut: K <= 4096 gives each CTA whole rows of W over all of
+ *            K, longer K is divided among all SMs so that every SM streams the same
  *            number of bytes; split_k is then accepted but does not change the cut.
  *   ws       scratch of ws_bytes >= detgemm_w8a8_workspace_size(M, N, K, split_k)
- *            (nonzero for M <= 64 at any split_k, and for split_k > 1).
+ *            (nonzero for decode-shaped problems at any split_k, and for split_k > 1).
  * Empty problems (M == 0 or N == 0) return DETGEMM_OK and launch nothing.
  * Errors: INVALID_ARG (K < 1, M or N < 0, split_k out of range, null pointer),
  *         PRECONDITION (K > DETGEMM_MAX_K), ALIGNMENT, WORKSPACE, UNSUPPORTED_DEVICE, CUDA.
@@ -141,14 +142,16 @@ DETGEMM_API detgemm_status detgemm_quantize_pow2(const void* X, int x_dtype, int
  * detgemm_quantize_pow2 + detgemm_w8a8 in one, with the same result bits:
  *     (Q, ea) = quantize_pow2(X, mode)                   (per row, as detgemm_quantize_pow2)
  *     C_ij    = rne_bf16((sum_k Q_ik W_jk) * 2^(ea_i + ew_j))
- * For M > 64 the quantizer writes the activation operand directly in the tensor
- * cores' exact fp16 carrier form, so no int8 copy of it is written or widened.
+ * Outside the decode-shaped problems (M <= 64) the quantizer writes the activation
+ * operand directly in the tensor cores' exact fp16 carrier form, so no int8 copy of it is
+ * written or widened.
  *   X      [M x K] bf16 bit patterns (x_dtype BF16) or fp32 (x_dtype F32), stride ldx
  *   mode   DETGEMM_POW2_NEAREST or DETGEMM_POW2_CEIL
  *   W      int8 [N x K] (ldw), ew int32 [N]
  *   W16    optional (may be NULL): the same weight widened once by detgemm_widen_i8_f16
- *          (fp16 [N x ldw16], ldw16 a multiple of 8); when given and M > 64 it is read
- *          instead of widening W on every call (a static weight widened at load time)
+ *          (fp16 [N x ldw16], ldw16 a multiple of 8); when given, the tensor-core path
+ *          reads it instead of widening W on every call (a static weight widened at
+ *          load time); the decode-shaped path reads the int8 W
  *   C      bf16 bit patterns [M x N] (ldc)
  *   ea_out optional (may be NULL): int32 [M] receives the activation exponents
  *   split_k, errors: as detgemm_w8a8; a non-finite row of X raises

@@ -48,6 +48,8 @@ def _dev_x(X, tdt, dev, ld):
     (7, 200, 1000, 2, "f32", 1, False),
     (64, 256, 4096, 4, "bf16", 0, False),
     (65, 130, 1000, 1, "bf16", 0, False),
+    (100, 200, 2048, 1, "bf16", 0, True),
+    (128, 96, 4096, 2, "f32", 1, False),
     (257, 300, 2048, 2, "f32", 0, True),
     (300, 256, 777, 1, "bf16", 1, True),
     (512, 512, 4096, 3, "bf16", 0, False),
