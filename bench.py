@@ -465,6 +465,14 @@ def extras(dg, torch, dev, pk, flush):
     res["ozaki_f32_4096_4slices"] = {"ms": round(ms4, 3),
                                      "effective_fp32_TFLOPs": round(2 * 4096 ** 3 / (ms4 * 1e-3) / 1e12, 2),
                                      "max_err_over_absAabsB_sampled": rel4}
+    # context: the vendor library's fp32 GEMM on the same operands (fp32 arithmetic, no TF32;
+    # its bits depend on the library's reduction order) and its error on the same rows
+    tf32 = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = False
+    ms_s = _time(torch, lambda: torch.matmul(Af, Bf, out=Cf), flush, reps=3, warm=1)
+    torch.backends.cuda.matmul.allow_tf32 = tf32
+    res["library_fp32_gemm_4096"] = {"ms": round(ms_s, 3), "TFLOPs": round(2 * 4096 ** 3 / (ms_s * 1e-3) / 1e12, 2),
+                                     "max_err_over_absAabsB_sampled": rel(Cf)}
     del ws4, Ad, Bd
     del Af, Bf, Cf, ws
     # context for the tensor-core roofline: the vendor library's fp16 GEMM (fp32 accumulate)

@@ -299,6 +299,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     tc_fence_before();
     cluster_sync();  // both CTAs' barriers are initialised before any remote arrival
     tc_fence_after();
+    // Launched as a programmatic dependent of the kernel before it on the stream: the setup
+    // above overlaps that kernel's tail; every thread waits for its completion (and the
+    // visibility of its writes: the operands, the exponents) before touching global memory.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const uint32_t tmem_base = *tmem_slot;
     const int total = p.ndiag * p.tiles_m * p.tiles_n * p.split;
     const uint32_t full_lead = mapa(smem_addr(full), 0);
@@ -484,6 +488,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
 
     __syncwarp();
+    // the next kernel on the stream may be scheduled once every CTA is here (not earlier:
+    // its blocks would wait beside this kernel's and take issue slots)
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     tc_fence_before();
     cluster_sync();  // no CTA leaves while its pair may still read its smem or barriers
     tc_fence_after();
@@ -662,17 +669,19 @@ cudaError_t tc_gemm_launch(const TcArgs& a0, const void* A16, int64_t lda, int a
     }
     if (clusters > total) clusters = total;
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see griddepcontrol.wait
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.gridDim = dim3(2 * clusters, 1, 1);
     cfg.blockDim = dim3(THREADS, 1, 1);
     cfg.dynamicSmemBytes = P_SMEM_BYTES;
     cfg.stream = s;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     e = a.split > 1 ? cudaLaunchKernelEx(&cfg, tc2_gemm_kernel<true>, tmA, tmB, tmC, tmS, a)
                     : cudaLaunchKernelEx(&cfg, tc2_gemm_kernel<false>, tmA, tmB, tmC, tmS, a);
     if (e != cudaSuccess) return e;

@@ -81,7 +81,18 @@ __device__ __forceinline__ void widen_store32(uint4* y, uint4 w) {
     y[1] = o1;
 }
 
+// Both kernels are launched as programmatic dependents of the kernel before them on the
+// stream: they wait for its completion (which may have produced X) before reading, then let
+// the next kernel (the GEMM, which waits for them in turn) be scheduled at once: its blocks
+// need an SM's shared memory, so they start as these blocks leave, with their setup done
+// by the time the widened operands are complete.
+__device__ __forceinline__ void pdl_enter() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __global__ void __launch_bounds__(256) widen_pair_kernel(const __grid_constant__ WidenPair p) {
+    pdl_enter();
     const int64_t nv0 = (int64_t)p.rows[0] * (p.Kp[0] / 16);
     const int64_t total = nv0 + (int64_t)p.rows[1] * (p.Kp[1] / 16);
     const int64_t nt = (int64_t)gridDim.x * blockDim.x;
@@ -105,6 +116,7 @@ __global__ void __launch_bounds__(256) widen_pair_kernel(const __grid_constant__
 // One matrix whose output row stride is a multiple of 8 (not of 16): 8 int8 per step.
 __global__ void __launch_bounds__(256) widen8_kernel(const int8_t* __restrict__ X, int64_t ldx, int rows, int K,
                                                      __half* __restrict__ Y, int64_t Kp) {
+    pdl_enter();
     const int64_t nvec = Kp / 8;
     const int64_t total = (int64_t)rows * nvec;
     for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < total; v += (int64_t)gridDim.x * blockDim.x) {
@@ -142,6 +154,21 @@ int widen_num_sms() {
     return g_widen_sms[dev];
 }
 
+// 256-thread launch with the programmatic-stream-serialization attribute
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), unsigned blocks, cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(blocks, 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 unsigned widen_blocks(int64_t total, int per_sm) {
     int64_t blocks = (total + 255) / 256;
     const int64_t cap = (int64_t)widen_num_sms() * per_sm;
@@ -158,16 +185,15 @@ cudaError_t widen_pair_launch(const int8_t* X0, int64_t ldx0, int rows0, int K0,
     p.X[1] = X1; p.ldx[1] = ldx1; p.rows[1] = rows1; p.K[1] = K1; p.Y[1] = reinterpret_cast<__half*>(Y1); p.Kp[1] = Kp1;
     const int64_t total = (int64_t)rows0 * (Kp0 / 16) + (int64_t)rows1 * (Kp1 / 16);
     if (total == 0) return cudaSuccess;
-    widen_pair_kernel<<<widen_blocks(total, 3), 256, 0, s>>>(p);  // 3 blocks per SM measured fastest (2, 4, 6, 8 slower)
-    return cudaGetLastError();
+    // 3 blocks per SM measured fastest (2, 4, 6, 8 slower)
+    return launch_dependent(widen_pair_kernel, widen_blocks(total, 3), s, p);
 }
 
 cudaError_t widen_i8_f16_launch(const int8_t* X, int64_t ldx, int rows, int K, void* Y, int64_t Kp, cudaStream_t s) {
     if (rows == 0) return cudaSuccess;
     if (Kp % 16 == 0) return widen_pair_launch(X, ldx, rows, K, Y, Kp, nullptr, 0, 0, 0, nullptr, 0, s);
-    widen8_kernel<<<widen_blocks((int64_t)rows * (Kp / 8), 8), 256, 0, s>>>(X, ldx, rows, K, reinterpret_cast<__half*>(Y),
-                                                                         Kp);
-    return cudaGetLastError();
+    return launch_dependent(widen8_kernel, widen_blocks((int64_t)rows * (Kp / 8), 8), s, X, ldx, rows, K,
+                            reinterpret_cast<__half*>(Y), Kp);
 }
 
 }  // namespace detgemm
