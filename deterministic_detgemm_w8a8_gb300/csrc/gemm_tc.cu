@@ -13,20 +13,22 @@
 // §II "Pipeline and alibi").
 //
 // Kernel layout: persistent clusters of two CTAs (one CTA per SM) over work units; a
-// unit is (plane group d, 256 x 256 output tile, split part).
+// unit is (plane group d, 256 x BN output tile, split part), BN = 256, or 192 for an
+// unsplit one-plane problem whose tiles all fit in one round of the clusters.
 //   warp 0     TMA producer (both CTAs): CTA r loads A rows [256 tm + 128 r, +128) and B
-//              rows [256 tn + 128 r, +128) of each 64-wide K block, fp16 with the 128-byte
-//              swizzle, into a 6-stage ring (32 KB per stage).
+//              rows [BN tn + BN/2 r, +BN/2) of each 64-wide K block, fp16 with the 128-byte
+//              swizzle, into a 6-stage ring (32 KB or 28 KB per stage).
 //   warp 1     TMEM owner (both CTAs; the pair allocates collectively) and, in the even
-//              CTA, the MMA issuer: tcgen05.mma.cta_group::2 M=256 N=256 K=16, four per K
-//              block, into one of two 256-column fp32 TMEM buffers, one K chunk per buffer.
-//   warps 2-9  epilogue (both CTAs): warp w reads TMEM lanes 32 (w % 4) .. +31 and column
-//              half (w - 2) / 4 of its CTA's 128 rows, converts each fp32 chunk to int32
-//              and adds it to 128 int32 registers per thread; after the unit's last chunk
-//              it rounds to bf16 (or keeps int32), stages its 32 x 128 block in a 4 KB
-//              shared-memory slot and writes it with TMA stores or, under split-K, adds the
-//              partial into the tile's int32 slot of the split workspace with TMA reductions;
-//              the last-arriving warp reads the sums back and finishes.
+//              CTA, the MMA issuer: tcgen05.mma.cta_group::2 M=256 N=BN K=16, four per K
+//              block, into one of two BN-column fp32 TMEM buffers, one K chunk per buffer.
+//   warps 2..  epilogue (both CTAs; 8 warps of 128 columns for BN = 256, 12 of 64 for 192):
+//              warp w reads TMEM lanes 32 (w % 4) .. +31 and column group (w - 2) / 4 of its
+//              CTA's 128 rows, converts each fp32 chunk to int32 and adds it to its int32
+//              registers; after the unit's last chunk it rounds to bf16 (or keeps int32),
+//              stages its block in a 4 KB shared-memory slot and writes it with TMA stores or,
+//              under split-K, adds the partial into the tile's int32 slot of the split
+//              workspace with TMA reductions; the last-arriving warp reads the sums back and
+//              finishes.
 // Operands are fp16 planes [plane][rows][Kp] addressed through 3-D tensor maps; a unit
 // walks a list of (A plane, B plane) segments: one segment for W8A8, one per slice pair
 // for an Ozaki diagonal.
@@ -50,9 +52,8 @@ namespace {
 
 using namespace sm100;
 
-constexpr int BN = 256, BK = 64;
-constexpr int EPI_WARPS = 8;
-constexpr int THREADS = 64 + EPI_WARPS * 32;
+constexpr int BK = 64;
+constexpr int SPLIT_BN = 256;  // tile width of split-K launches (and of every multi-plane launch)
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int CHUNK_KB = 16;  // 16 blocks of 64 = 1024 K values per exact fp32 chunk
 
@@ -106,14 +107,14 @@ __device__ __forceinline__ float ro24_scaled(int32_t acc, float sa, float sw) {
 
 __device__ __forceinline__ float exp2_f32(int e) { return __uint_as_float((uint32_t)(e + 127) << 23); }
 
-// Epilogue of a warp's 32 rows x 128 columns: lane l holds row row0 + l. The results go
+// Epilogue of a warp's 32 rows x COLS columns (COLS = 128 or 64): lane l holds row row0 + l. The results go
 // through the warp's 4 KB shared-memory slot, 32 rows x 128 bytes with the 128-byte
 // swizzle (16-byte chunk c of row r at c ^ (r % 8), so the eight lanes of each store phase
 // hit eight different bank groups), and from there to global memory with one TMA store per
 // piece (64 bf16 or 32 int32 columns); the TMA clips rows past M and columns past N. Before
 // a piece overwrites the slot, the warp's previous store must have finished reading it.
-// The column exponents are loaded once per warp (lane l loads columns 4l .. 4l+3,
-// coalesced) and broadcast by shuffle.
+// The column exponents are loaded once per warp (lane l loads columns PER l .. PER l + PER - 1,
+// PER = COLS / 32, coalesced) and broadcast by shuffle.
 __device__ __forceinline__ void slot_acquire(bool& pending) {
     if (pending) {
         if ((threadIdx.x & 31) == 0) bulk_wait_read_all();
@@ -136,30 +137,32 @@ __device__ __forceinline__ void st_shared16(uint32_t addr, uint32_t a, uint32_t 
     asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
+template <int COLS>
 __device__ __forceinline__ void finish_rows(const TcArgs& p, const CUtensorMap* tmC, uint8_t* slot, int d, int row0,
-                                            int col0, const int32_t (&acc)[128], bool& pending) {
+                                            int col0, const int32_t (&acc)[COLS], bool& pending) {
+    constexpr int PER = COLS / 32;
     const int lane = threadIdx.x & 31;
     const int row = row0 + lane;
     const uint32_t sbase = smem_addr(slot) + (uint32_t)lane * 128u;
     const int sw = lane & 7;
     if (p.mode == EPI_BF16_POW2) {
-        int32_t ewv[4];
+        int32_t ewv[PER];
         bool inrange = true;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int c = col0 + 4 * lane + i;
+        for (int i = 0; i < PER; ++i) {
+            const int c = col0 + PER * lane + i;
             ewv[i] = c < p.N ? __ldg(p.ew + c) : 0;
             inrange &= ewv[i] >= -60 && ewv[i] <= 40;
         }
         const int32_t ea = row < p.M ? __ldg(p.ea + row) : 0;
         inrange &= ea >= -60 && ea <= 40;
         const bool fast = __all_sync(0xffffffffu, inrange);  // warp-uniform choice
-        float swv[4];
+        float swv[PER];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) swv[i] = exp2_f32(fast ? ewv[i] : 0);
+        for (int i = 0; i < PER; ++i) swv[i] = exp2_f32(fast ? ewv[i] : 0);
         const float sa = exp2_f32(fast ? ea : 0);
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
+        for (int hh = 0; hh < COLS / 64; ++hh) {
             slot_acquire(pending);
 #pragma unroll
             for (int jj = 0; jj < 8; ++jj) {
@@ -169,8 +172,8 @@ __device__ __forceinline__ void finish_rows(const TcArgs& p, const CUtensorMap* 
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         const int c = j + 2 * i;
-                        const float s0 = __shfl_sync(0xffffffffu, swv[c & 3], c >> 2);
-                        const float s1 = __shfl_sync(0xffffffffu, swv[(c + 1) & 3], (c + 1) >> 2);
+                        const float s0 = __shfl_sync(0xffffffffu, swv[c % PER], c / PER);
+                        const float s1 = __shfl_sync(0xffffffffu, swv[(c + 1) % PER], (c + 1) / PER);
                         const __nv_bfloat162 h =
                             __floats2bfloat162_rn(ro24_scaled(acc[c], sa, s0), ro24_scaled(acc[c + 1], sa, s1));
                         w[i] = *reinterpret_cast<const uint32_t*>(&h);
@@ -179,8 +182,8 @@ __device__ __forceinline__ void finish_rows(const TcArgs& p, const CUtensorMap* 
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         const int c = j + 2 * i;
-                        const int32_t e0 = __shfl_sync(0xffffffffu, ewv[c & 3], c >> 2);
-                        const int32_t e1 = __shfl_sync(0xffffffffu, ewv[(c + 1) & 3], (c + 1) >> 2);
+                        const int32_t e0 = __shfl_sync(0xffffffffu, ewv[c % PER], c / PER);
+                        const int32_t e1 = __shfl_sync(0xffffffffu, ewv[(c + 1) % PER], (c + 1) / PER);
                         w[i] = (uint32_t)bf16_from_acc_pow2(acc[c], ea, e0) |
                                ((uint32_t)bf16_from_acc_pow2(acc[c + 1], ea, e1) << 16);
                     }
@@ -191,7 +194,7 @@ __device__ __forceinline__ void finish_rows(const TcArgs& p, const CUtensorMap* 
         }
     } else {
 #pragma unroll
-        for (int pc = 0; pc < 4; ++pc) {
+        for (int pc = 0; pc < COLS / 32; ++pc) {
             slot_acquire(pending);
 #pragma unroll
             for (int jj = 0; jj < 8; ++jj) {
@@ -204,16 +207,17 @@ __device__ __forceinline__ void finish_rows(const TcArgs& p, const CUtensorMap* 
     }
 }
 
-// A warp's 32 x 128 int32 partial into the split workspace (int32 [tile units x 256][256],
-// row-major): four 32 x 32 pieces staged in the warp's slot (128-byte swizzle) and added
-// to global memory by TMA reductions.
+// A warp's 32 x COLS int32 partial into the split workspace (int32 [tile units x 256][256],
+// row-major): 32 x 32 pieces staged in the warp's slot (128-byte swizzle) and added to
+// global memory by TMA reductions.
+template <int COLS>
 __device__ __forceinline__ void reduce_rows(const CUtensorMap* tmS, uint8_t* slot, int wrow, int wcol,
-                                            const int32_t (&acc)[128], bool& pending) {
+                                            const int32_t (&acc)[COLS], bool& pending) {
     const int lane = threadIdx.x & 31;
     const uint32_t sbase = smem_addr(slot) + (uint32_t)lane * 128u;
     const int sw = lane & 7;
 #pragma unroll
-    for (int pc = 0; pc < 4; ++pc) {
+    for (int pc = 0; pc < COLS / 32; ++pc) {
         slot_acquire(pending);
 #pragma unroll
         for (int jj = 0; jj < 8; ++jj) {
@@ -245,22 +249,37 @@ __device__ __forceinline__ void reduce_rows(const CUtensorMap* tmS, uint8_t* slo
 //   tfull[b]  in both CTAs: the MMA commit arrives on both (multicast)
 //   tempty[b] in the even CTA: all 16 epilogue warps of the pair arrive on it
 // ------------------------------------------------------------------------------------
-constexpr int P_STAGES = 6;
-constexpr int P_A_BYTES = 128 * BK * 2;
-constexpr int P_B_BYTES = 128 * BK * 2;
-constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
-constexpr uint32_t P_IDESC = idesc_f16_f32(256, 256);
-constexpr int P_SLOT_BYTES = 32 * 128;  // one epilogue warp's staging slot
-constexpr int P_SMEM_BYTES =
-    P_STAGES * P_STAGE_BYTES + EPI_WARPS * P_SLOT_BYTES + 1024 /*alignment slack*/ + 256 /*barriers*/;
+// Tile geometry by tile width BN: 256 (eight epilogue warps of 32 rows x 128 columns) or
+// 192 (twelve of 32 x 64), chosen by choose_bn; B rows per CTA are BN / 2.
+template <int BNT>
+struct Geo {
+    static constexpr int BN = BNT;
+    static constexpr int COLS = BNT == 256 ? 128 : 64;  // columns per epilogue warp
+    static constexpr int EPI_WARPS = 4 * BNT / COLS;
+    static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+    static constexpr int STAGES = 6;
+    static constexpr int A_BYTES = 128 * BK * 2;
+    static constexpr int B_BYTES = (BNT / 2) * BK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr uint32_t IDESC = idesc_f16_f32(256, BNT);
+    static constexpr int SLOT_BYTES = 32 * 128;  // one epilogue warp's staging slot
+    static constexpr int SMEM_BYTES =
+        STAGES * STAGE_BYTES + EPI_WARPS * SLOT_BYTES + 1024 /*alignment slack*/ + 256 /*barriers*/;
+};
+static_assert(Geo<256>::SMEM_BYTES <= 227 * 1024 && Geo<192>::SMEM_BYTES <= 227 * 1024, "shared memory");
+static_assert(2 * 256 <= 512 && 2 * 192 <= 512, "two accumulator buffers in TMEM");
 
 // kSplit: the instantiation for split > 1 (the split epilogue's registers stay out of the
 // other one)
-template <bool kSplit>
-__global__ void __launch_bounds__(THREADS, 1)
+template <int BNT, bool kSplit>
+__global__ void __launch_bounds__(Geo<BNT>::THREADS, 1)
     tc2_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmS,
                     const __grid_constant__ TcArgs p) {
+    typedef Geo<BNT> G;
+    constexpr int BN = G::BN, COLS = G::COLS, EPI_WARPS = G::EPI_WARPS, P_STAGES = G::STAGES;
+    constexpr int P_A_BYTES = G::A_BYTES, P_STAGE_BYTES = G::STAGE_BYTES, P_SLOT_BYTES = G::SLOT_BYTES;
+    constexpr uint32_t P_IDESC = G::IDESC;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* slots = smem + P_STAGES * P_STAGE_BYTES;  // epilogue staging, 1024-byte aligned
@@ -331,7 +350,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     if (rank == 0) mbar_arrive_expect_tx(full + stage, 2 * P_STAGE_BYTES);
                     const uint32_t fb = full_lead + 8u * (uint32_t)stage;
                     tma_load_3d_pair(sa, &tmA, fb, kx, un.tm * 256 + (int)rank * 128, p.segA[seg]);
-                    tma_load_3d_pair(sa + P_A_BYTES, &tmB, fb, kx, un.tn * 256 + (int)rank * 128, p.segB[seg]);
+                    tma_load_3d_pair(sa + P_A_BYTES, &tmB, fb, kx, un.tn * BN + (int)rank * (BN / 2), p.segB[seg]);
                     ++issued;
                     if (++stage == P_STAGES) {
                         stage = 0;
@@ -415,9 +434,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             const Unit un = unit_of(p, u);
             int f0, f1;
             kb_range(p, un, f0, f1);
-            int32_t acc[128];
+            int32_t acc[COLS];
 #pragma unroll
-            for (int i = 0; i < 128; ++i) acc[i] = 0;
+            for (int i = 0; i < COLS; ++i) acc[i] = 0;
             for (int c0 = f0; c0 < f1; c0 += CHUNK_KB) {
                 const bool got = mbar_wait(tfull + buf, tphase, abort_flag);
                 if (!__all_sync(0xffffffffu, got)) {
@@ -425,11 +444,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t ta = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN + h * 128);
-                // 16 columns per load: the 128 accumulators plus one load's registers stay
-                // within the thread's register budget
+                const uint32_t ta = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN + h * COLS);
+                // 16 columns per load: the accumulators plus one load's registers stay within
+                // the thread's register budget
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
+                for (int j = 0; j < COLS / 16; ++j) {
                     uint32_t r[16];
                     tmem_ld16(ta + 16 * j, r);
                     tmem_wait_ld();
@@ -446,7 +465,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             if (!ok) break;
             const int row = un.tm * 256 + (int)rank * 128 + q * 32 + lane;
-            const int col0 = un.tn * BN + h * 128;
+            const int col0 = un.tn * BN + h * COLS;
             if constexpr (!kSplit) {
                 finish_rows(p, &tmC, slot, un.d, row - lane, col0, acc, pending);
                 continue;
@@ -456,7 +475,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             // warp that arrives last reads the complete sums back
             const int sidx = u / p.split;
             const int wrow = sidx * 256 + (int)rank * 128 + q * 32;
-            reduce_rows(&tmS, slot, wrow, h * 128, acc, pending);
+            reduce_rows<COLS>(&tmS, slot, wrow, h * COLS, acc, pending);
             unsigned prev = 0;
             if (lane == 0) {
                 bulk_wait_all();             // the reductions have been performed
@@ -472,9 +491,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             // copy of these lines (no one reads a slot before its sums are complete, and L1 starts
             // each launch empty), so that the four 16-byte pieces of each 128-byte line that a
             // lane reads in turn come from one L2 request.
-            const int4* src = reinterpret_cast<const int4*>(p.ws_acc + (int64_t)(wrow + lane) * 256 + h * 128);
+            const int4* src = reinterpret_cast<const int4*>(p.ws_acc + (int64_t)(wrow + lane) * BN + h * COLS);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
+            for (int i = 0; i < COLS / 4; ++i) {
                 const int4 v = __ldca(src + i);
                 acc[4 * i] = v.x;
                 acc[4 * i + 1] = v.y;
@@ -574,17 +593,19 @@ int64_t tc_padded_k(int K) { return ((int64_t)K + BK - 1) / BK * BK; }
 
 
 // Split workspace: one 256 x 256 int32 slot per tile unit, then an arrival counter per tile
-// unit, CTA and epilogue warp; zeroed by a memset before the engine starts.
-constexpr size_t kSlotBytes = (size_t)256 * 256 * sizeof(int32_t);
+// unit, CTA and epilogue warp; zeroed by a memset before the engine starts. Split launches
+// use 256 x 256 tiles.
+constexpr size_t kSlotBytes = (size_t)256 * SPLIT_BN * sizeof(int32_t);
 
 static size_t split_ws_bytes(int cut) {
     if (cut <= 0) return 0;
-    return (size_t)cut * kSlotBytes + (((size_t)cut * 2 * EPI_WARPS * sizeof(uint32_t) + 255) & ~(size_t)255);
+    return (size_t)cut * kSlotBytes +
+           (((size_t)cut * 2 * Geo<SPLIT_BN>::EPI_WARPS * sizeof(uint32_t) + 255) & ~(size_t)255);
 }
 
 size_t tc_split_bytes(int ndiag, int M, int N, int split) {
     if (split <= 1) return 0;
-    return split_ws_bytes(ndiag * ((M + 255) / 256) * ((N + BN - 1) / BN));
+    return split_ws_bytes(ndiag * ((M + 255) / 256) * ((N + SPLIT_BN - 1) / SPLIT_BN));
 }
 
 // 2-D map over the split workspace's slots: int32 [units x 256][256], box 32 x 32, the
@@ -593,8 +614,8 @@ static cudaError_t make_ws_map(CUtensorMap* m, void* base, int cut) {
     PFN_cuTensorMapEncodeTiled_v12000 enc;
     cudaError_t e = get_encode(&enc);
     if (e != cudaSuccess) return e;
-    cuuint64_t dims[2] = {256, (cuuint64_t)cut * 256};
-    cuuint64_t strides[1] = {256 * sizeof(int32_t)};
+    cuuint64_t dims[2] = {SPLIT_BN, (cuuint64_t)cut * 256};
+    cuuint64_t strides[1] = {SPLIT_BN * sizeof(int32_t)};
     cuuint32_t box[2] = {32, 32};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_INT32, 2, base, dims, strides, box, estr,
@@ -604,56 +625,108 @@ static cudaError_t make_ws_map(CUtensorMap* m, void* base, int cut) {
 }
 
 namespace {
-int g_max_clusters[64];
+int g_max_clusters[64][2];  // per device: 256-wide, 192-wide tiles
 
-int max_pair_clusters() {
+template <int BNT, bool kSplit>
+cudaError_t opt_in() {
+    return cudaFuncSetAttribute(tc2_gemm_kernel<BNT, kSplit>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                Geo<BNT>::SMEM_BYTES);
+}
+
+template <int BNT>
+int occupancy_clusters() {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2 * 76, 1, 1);
+    cfg.blockDim = dim3(Geo<BNT>::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = Geo<BNT>::SMEM_BYTES;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, tc2_gemm_kernel<BNT, false>, &cfg) != cudaSuccess || n <= 0) n = 1;
+    return n;
+}
+
+// CTA pairs resident at once for tile width bn (256 or 192); also opts the kernels into
+// their shared memory, once per device
+int max_pair_clusters(int bn) {
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) return 1;
     std::lock_guard<std::mutex> lock(g_tc_mutex);
-    if (g_max_clusters[dev] == 0) {
-        if (cudaFuncSetAttribute(tc2_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM_BYTES) !=
-                cudaSuccess ||
-            cudaFuncSetAttribute(tc2_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM_BYTES) !=
-                cudaSuccess)
+    if (g_max_clusters[dev][0] == 0) {
+        if (opt_in<256, false>() != cudaSuccess || opt_in<256, true>() != cudaSuccess ||
+            opt_in<192, false>() != cudaSuccess)
             return 0;
-        cudaLaunchConfig_t cfg = {};
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.gridDim = dim3(2 * 76, 1, 1);
-        cfg.blockDim = dim3(THREADS, 1, 1);
-        cfg.dynamicSmemBytes = P_SMEM_BYTES;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, tc2_gemm_kernel<false>, &cfg) != cudaSuccess || n <= 0) n = 1;
-        g_max_clusters[dev] = n;
+        g_max_clusters[dev][0] = occupancy_clusters<256>();
+        g_max_clusters[dev][1] = occupancy_clusters<192>();
     }
-    return g_max_clusters[dev];
+    return g_max_clusters[dev][bn == 256 ? 0 : 1];
 }
 }  // namespace
 
-static void set_tiles(TcArgs& a, int64_t kext) {
+static void set_tiles(TcArgs& a, int64_t kext, int bn) {
     a.tiles_m = (a.M + 255) / 256;
-    a.tiles_n = (a.N + BN - 1) / BN;
+    a.tiles_n = (a.N + bn - 1) / bn;
     a.nkb = (int)((kext + BK - 1) / BK);
     if (a.group_m <= 0) a.group_m = 8;
+}
+
+// Tile width of an unsplit one-plane launch. When every tile fits in one round of the
+// clusters, the call takes about one tile's time, which 256 x 192 tiles cut by a quarter if
+// they still fit in one round (the 257 x 6144 x 2048 sweep GEMM: 64 tiles of 192 columns on
+// 76 pairs, 31 us against 41 us for 48 tiles of 256). Over several rounds the narrower tile
+// is no help: on the 8192 x 12288 x 4096 FFN GEMM (27 rounds of 192-wide tiles against 21 of
+// 256) it took 581 us against 461, the tensor pipe busy 59% of the time against 74%.
+static int choose_bn(const TcArgs& a) {
+    if (a.split > 1 || a.ndiag != 1) return 256;
+    const int c256 = max_pair_clusters(256), c192 = max_pair_clusters(192);
+    if (c256 <= 0 || c192 <= 0) return 256;
+    const long long tm = (a.M + 255) / 256;
+    const bool one256 = tm * ((a.N + 255) / 256) <= c256;
+    const bool one192 = tm * ((a.N + 191) / 192) <= c192;
+    return one256 && one192 ? 192 : 256;
+}
+
+template <int BNT, bool kSplit>
+static cudaError_t launch_engine(const TcArgs& a, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                                 const CUtensorMap& tmC, const CUtensorMap& tmS, int clusters, cudaStream_t s) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see griddepcontrol.wait
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(2 * clusters, 1, 1);
+    cfg.blockDim = dim3(Geo<BNT>::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = Geo<BNT>::SMEM_BYTES;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, tc2_gemm_kernel<BNT, kSplit>, tmA, tmB, tmC, tmS, a);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
 }
 
 cudaError_t tc_gemm_launch(const TcArgs& a0, const void* A16, int64_t lda, int a_planes, const void* B16,
                            int64_t ldb, int b_planes, int64_t kext, void* ws_split, cudaStream_t s) {
     if (a0.M == 0 || a0.N == 0) return cudaSuccess;
     TcArgs a = a0;
-    set_tiles(a, kext);
+    if (max_pair_clusters(256) <= 0) return cudaErrorInvalidConfiguration;
+    const int bn = choose_bn(a);
+    set_tiles(a, kext, bn);
     CUtensorMap tmA, tmB, tmC;
     cudaError_t e = make_map(&tmA, A16, kext, lda, a.M, a_planes, 128);
-    if (e == cudaSuccess) e = make_map(&tmB, B16, kext, ldb, a.N, b_planes, 128);
+    if (e == cudaSuccess) e = make_map(&tmB, B16, kext, ldb, a.N, b_planes, bn / 2);
     if (e == cudaSuccess) e = make_out_map(&tmC, a);
     if (e != cudaSuccess) return e;
-    int clusters = max_pair_clusters();  // also opts the kernel into its shared memory (once per device)
+    int clusters = max_pair_clusters(bn);
     if (clusters <= 0) return cudaErrorInvalidConfiguration;
     const int total = a.ndiag * a.tiles_m * a.tiles_n * a.split;
     CUtensorMap tmS;
@@ -668,24 +741,9 @@ cudaError_t tc_gemm_launch(const TcArgs& a0, const void* A16, int64_t lda, int a
         if (e != cudaSuccess) return e;
     }
     if (clusters > total) clusters = total;
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see griddepcontrol.wait
-    attr[1].val.programmaticStreamSerializationAllowed = 1;
-    cfg.gridDim = dim3(2 * clusters, 1, 1);
-    cfg.blockDim = dim3(THREADS, 1, 1);
-    cfg.dynamicSmemBytes = P_SMEM_BYTES;
-    cfg.stream = s;
-    cfg.attrs = attr;
-    cfg.numAttrs = 2;
-    e = a.split > 1 ? cudaLaunchKernelEx(&cfg, tc2_gemm_kernel<true>, tmA, tmB, tmC, tmS, a)
-                    : cudaLaunchKernelEx(&cfg, tc2_gemm_kernel<false>, tmA, tmB, tmC, tmS, a);
-    if (e != cudaSuccess) return e;
-    return cudaGetLastError();
+    if (a.split > 1) return launch_engine<256, true>(a, tmA, tmB, tmC, tmS, clusters, s);
+    if (bn == 192) return launch_engine<192, false>(a, tmA, tmB, tmC, tmS, clusters, s);
+    return launch_engine<256, false>(a, tmA, tmB, tmC, tmS, clusters, s);
 }
 
 // Self-check of the bounded waits: one thread waits on an mbarrier that nothing ever
