@@ -65,6 +65,23 @@ __device__ __forceinline__ long long rne53(i128 x, int& sh_out) {
     return q;
 }
 
+// X (|X| < 2^63) rounded to 53 significant bits, ties to even, as q * 2^s (|q| <= 2^53):
+// the same rounding as rne53 for a value that fits a 64-bit word, on its magnitude
+__device__ __forceinline__ long long rne53_i64(long long X, int& s) {
+    const uint64_t a = X < 0 ? 0ull - (uint64_t)X : (uint64_t)X;
+    const int nb = 64 - __clzll((long long)a);
+    if (nb <= 53) {
+        s = 0;
+        return X;
+    }
+    s = nb - 53;
+    uint64_t qq = a >> s;
+    const uint64_t rem = a & ((1ull << s) - 1ull);
+    const uint64_t half = 1ull << (s - 1);
+    qq += (uint64_t)((rem > half) | ((rem == half) & (qq & 1ull)));
+    return X < 0 ? -(long long)qq : (long long)qq;
+}
+
 // q * 2^sh as a 128-bit integer (0 <= sh <= 63)
 __device__ __forceinline__ i128 widen_shifted(long long q, int sh) {
     const uint64_t lo = (uint64_t)q << sh;
@@ -174,8 +191,26 @@ __device__ __forceinline__ OutT combine_int(const int32_t (&t)[D - 1], int32_t e
 #pragma unroll
     for (int d = 0; d < EXACT; ++d) q += (long long)t[d] * (1ll << (7 * d));  // |q| < 2^53: no rounding
     int sh = 0;
+    // Each rounding step forms Z * 2^sh + T * 2^(7d) and rounds it to 53 bits. While the sum,
+    // taken in units of 2^sh, fits a 64-bit word (|q| <= 2^53 and |T| 2^(7d - sh) < 2^62),
+    // it is formed and rounded in int64 — the same value and the same rounding; otherwise in
+    // 128 bits from there on.
+    bool fast = true;
 #pragma unroll
-    for (int d = EXACT; d < D - 1; ++d) q = rne53(widen_shifted(q, sh) + (i128)((u128)(i128)t[d] << (7 * d)), sh);
+    for (int d = EXACT; d < D - 1; ++d) {
+        if (fast) {
+            const int k = 7 * d - sh;
+            const uint32_t at = t[d] < 0 ? 0u - (uint32_t)t[d] : (uint32_t)t[d];
+            if (k >= 0 && 32 - __clz(at) + k <= 62) {
+                int s2;
+                q = rne53_i64(q + (long long)t[d] * (1ll << k), s2);
+                sh += s2;
+                continue;
+            }
+            fast = false;
+        }
+        q = rne53(widen_shifted(q, sh) + (i128)((u128)(i128)t[d] << (7 * d)), sh);
+    }
     long long k = (long long)ei + (long long)fj;
     k = k > Out<OutT>::KMAX ? Out<OutT>::KMAX : (k < -Out<OutT>::KMAX ? -Out<OutT>::KMAX : k);
     return Out<OutT>::from_q(q, sh + (int)k - 7 * D);
