@@ -242,7 +242,8 @@ __global__ void col_key_kernel(const X* __restrict__ Xm, int64_t ldx, int rows, 
 }
 
 // 64 x 64 tile of X (rows r0.., columns c0..), 256 threads: each thread loads four
-// columns of four rows, its digits go to a shared tile [t][col][row], then each plane is
+// columns of four consecutive rows, its digits go to a shared tile [t][col][row] (four rows
+// per 32-bit store), then each plane is
 // written K-major, S[t][col][row], eight rows per store (each column's 64 rows are 128
 // contiguous bytes of fp16).
 constexpr int SC_TILE = 64;
@@ -263,9 +264,14 @@ __global__ void __launch_bounds__(256) slice_cols_kernel(const X* __restrict__ X
 #pragma unroll
     for (int q = 0; q < 4; ++q) ecol[q] = cq + q < cols ? keys[cq + q] : KEY_ZERO;
 #pragma unroll
+    // rows 4 ty .. 4 ty + 3 of columns cq .. cq + 3: all four rows are loaded first, then each
+    // (plane, column) gets its four row digits in one 32-bit shared-memory store
+    B v[4][4];
+#pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const int rr = ty + 16 * i, r = r0 + rr;
-        B v[4] = {0, 0, 0, 0};
+        const int r = r0 + 4 * ty + i;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) v[i][q] = 0;
         if (r < rows) {
             const X* xr = Xm + (int64_t)r * ldx;
             if (vec_in && cq + 4 <= cols) {
@@ -275,19 +281,26 @@ __global__ void __launch_bounds__(256) slice_cols_kernel(const X* __restrict__ X
                     const uint4 a = __ldg(qp + h);
                     const B* w = reinterpret_cast<const B*>(&a);
 #pragma unroll
-                    for (int k = 0; k < PER; ++k) v[h * PER + k] = w[k];
+                    for (int k = 0; k < PER; ++k) v[i][h * PER + k] = w[k];
                 }
             } else {
 #pragma unroll
-                for (int q = 0; q < 4; ++q) v[q] = cq + q < cols ? bits_of<X>(xr[cq + q]) : (B)0;
+                for (int q = 0; q < 4; ++q) v[i][q] = cq + q < cols ? bits_of<X>(xr[cq + q]) : (B)0;
             }
         }
+    }
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            // a column marked non-finite or all-zero (or outside the matrix) gets zero digits
-            const bool live = ecol[q] != KEY_NONFINITE && ecol[q] != KEY_ZERO;
-            const Digits g = prep_digits<X>(live ? v[q] : (B)0, live ? ecol[q] : 0, nslices);
-            for (int t = 0; t < nslices; ++t) tile[(t * SC_TILE + 4 * tx + q) * SC_PITCH + rr] = digit_at(g, t, nslices);
+    for (int q = 0; q < 4; ++q) {
+        // a column marked non-finite or all-zero (or outside the matrix) gets zero digits
+        const bool live = ecol[q] != KEY_NONFINITE && ecol[q] != KEY_ZERO;
+        Digits g[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) g[i] = prep_digits<X>(live ? v[i][q] : (B)0, live ? ecol[q] : 0, nslices);
+        for (int t = 0; t < nslices; ++t) {
+            uint32_t w = 0;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) w |= (uint32_t)(uint8_t)digit_at(g[i], t, nslices) << (8 * i);
+            *reinterpret_cast<uint32_t*>(&tile[(t * SC_TILE + 4 * tx + q) * SC_PITCH + 4 * ty]) = w;
         }
     }
     __syncthreads();
