@@ -86,6 +86,27 @@ __device__ __forceinline__ Unit unit_of(const TcArgs& p, int u) {
     return r;
 }
 
+// The i-th unit u of CTA pair cid (false past its last): each plane group in turn, its base
+// units, then its leftover unit if it has one (see TcArgs::extra_of). Recomputed from i
+// (one step per plane group) so that a role's loop carries one counter.
+__device__ __forceinline__ bool unit_at(const TcArgs& p, int cid, int ncl, int i, int& u) {
+    const int per_d = p.tiles_m * p.tiles_n * p.split;
+    const int nb = per_d / ncl;
+    for (int d = 0; d < p.ndiag; ++d) {
+        const int x = p.extra_of[d][cid];
+        if (i < nb) {
+            u = d * per_d + cid + ncl * i;
+            return true;
+        }
+        if (i == nb && x >= 0) {
+            u = d * per_d + nb * ncl + x;
+            return true;
+        }
+        i -= nb + (x >= 0);
+    }
+    return false;
+}
+
 __device__ __forceinline__ void kb_range(const TcArgs& p, const Unit& u, int& f0, int& f1) {
     const int F = p.diag_nseg[u.d] * p.nkb;
     f0 = (int)(((long long)u.z * F) / p.split);
@@ -270,8 +291,9 @@ static_assert(Geo<256>::SMEM_BYTES <= 227 * 1024 && Geo<192>::SMEM_BYTES <= 227 
 static_assert(2 * 256 <= 512 && 2 * 192 <= 512, "two accumulator buffers in TMEM");
 
 // kSplit: the instantiation for split > 1 (the split epilogue's registers stay out of the
-// other one)
-template <int BNT, bool kSplit>
+// other one); kGroups: several plane groups (the Ozaki diagonals), units assigned through
+// TcArgs::extra_of (one group: plain round-robin, with no table walk in the loops)
+template <int BNT, bool kSplit, bool kGroups>
 __global__ void __launch_bounds__(Geo<BNT>::THREADS, 1)
     tc2_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmS,
@@ -323,7 +345,7 @@ __global__ void __launch_bounds__(Geo<BNT>::THREADS, 1)
     // visibility of its writes: the operands, the exponents) before touching global memory.
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const uint32_t tmem_base = *tmem_slot;
-    const int total = p.ndiag * p.tiles_m * p.tiles_n * p.split;
+    const int total = p.ndiag * p.tiles_m * p.tiles_n * p.split;  // one plane group: units cid, cid + ncl, ...
     const uint32_t full_lead = mapa(smem_addr(full), 0);
     const uint32_t tempty_lead = mapa(smem_addr(tempty), 0);
 
@@ -334,7 +356,7 @@ __global__ void __launch_bounds__(Geo<BNT>::THREADS, 1)
             uint32_t phase = 0;
             uint32_t issued = 0;
             bool ok = true;
-            for (int u = cid; u < total && ok; u += ncl) {
+            for (int i = 0, u = cid; ok && (kGroups ? unit_at(p, cid, ncl, i, u) : u < total); ++i, u += ncl) {
                 const Unit un = unit_of(p, u);
                 int f0, f1;
                 kb_range(p, un, f0, f1);
@@ -380,7 +402,7 @@ __global__ void __launch_bounds__(Geo<BNT>::THREADS, 1)
             int buf = 0;
             uint32_t tphase = 0;
             bool ok = true;
-            for (int u = cid; u < total && ok; u += ncl) {
+            for (int i = 0, u = cid; ok && (kGroups ? unit_at(p, cid, ncl, i, u) : u < total); ++i, u += ncl) {
                 const Unit un = unit_of(p, u);
                 int f0, f1;
                 kb_range(p, un, f0, f1);
@@ -430,7 +452,7 @@ __global__ void __launch_bounds__(Geo<BNT>::THREADS, 1)
         int buf = 0;
         uint32_t tphase = 0;
         bool ok = true;
-        for (int u = cid; u < total && ok; u += ncl) {
+        for (int i = 0, u = cid; ok && (kGroups ? unit_at(p, cid, ncl, i, u) : u < total); ++i, u += ncl) {
             const Unit un = unit_of(p, u);
             int f0, f1;
             kb_range(p, un, f0, f1);
@@ -627,9 +649,9 @@ static cudaError_t make_ws_map(CUtensorMap* m, void* base, int cut) {
 namespace {
 int g_max_clusters[64][2];  // per device: 256-wide, 192-wide tiles
 
-template <int BNT, bool kSplit>
+template <int BNT, bool kSplit, bool kGroups>
 cudaError_t opt_in() {
-    return cudaFuncSetAttribute(tc2_gemm_kernel<BNT, kSplit>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    return cudaFuncSetAttribute(tc2_gemm_kernel<BNT, kSplit, kGroups>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 Geo<BNT>::SMEM_BYTES);
 }
 
@@ -647,7 +669,7 @@ int occupancy_clusters() {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, tc2_gemm_kernel<BNT, false>, &cfg) != cudaSuccess || n <= 0) n = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, tc2_gemm_kernel<BNT, false, false>, &cfg) != cudaSuccess || n <= 0) n = 1;
     return n;
 }
 
@@ -659,8 +681,8 @@ int max_pair_clusters(int bn) {
     if (dev < 0 || dev >= 64) return 1;
     std::lock_guard<std::mutex> lock(g_tc_mutex);
     if (g_max_clusters[dev][0] == 0) {
-        if (opt_in<256, false>() != cudaSuccess || opt_in<256, true>() != cudaSuccess ||
-            opt_in<192, false>() != cudaSuccess)
+        if (opt_in<256, false, false>() != cudaSuccess || opt_in<256, false, true>() != cudaSuccess ||
+            opt_in<256, true, true>() != cudaSuccess || opt_in<192, false, false>() != cudaSuccess)
             return 0;
         g_max_clusters[dev][0] = occupancy_clusters<256>();
         g_max_clusters[dev][1] = occupancy_clusters<192>();
@@ -692,7 +714,31 @@ static int choose_bn(const TcArgs& a) {
     return one256 && one192 ? 192 : 256;
 }
 
-template <int BNT, bool kSplit>
+// Leftover units of each plane group (per_d mod C of them) to CTA pairs: the groups in
+// order (the Ozaki diagonals come heaviest first), each leftover to the pair with the least
+// work so far (ties: the lowest index), at most one per pair and group. Work is counted in
+// segments (a unit of group d reads diag_nseg[d] plane pairs). For a single group this is
+// leftover k -> pair k, a plain round-robin.
+static void assign_leftovers(TcArgs& a, int C) {
+    memset(a.extra_of, -1, sizeof(a.extra_of));
+    const int per_d = a.tiles_m * a.tiles_n * a.split;
+    const int nb = per_d / C, nx = per_d % C;
+    long long load[kTcMaxClusters];
+    for (int c = 0; c < C; ++c) load[c] = 0;
+    for (int d = 0; d < a.ndiag; ++d) {
+        const long long w = a.diag_nseg[d];
+        for (int c = 0; c < C; ++c) load[c] += (long long)nb * w;
+        for (int k = 0; k < nx; ++k) {
+            int best = -1;
+            for (int c = 0; c < C; ++c)
+                if (a.extra_of[d][c] < 0 && (best < 0 || load[c] < load[best])) best = c;
+            a.extra_of[d][best] = (int8_t)k;
+            load[best] += w;
+        }
+    }
+}
+
+template <int BNT, bool kSplit, bool kGroups>
 static cudaError_t launch_engine(const TcArgs& a, const CUtensorMap& tmA, const CUtensorMap& tmB,
                                  const CUtensorMap& tmC, const CUtensorMap& tmS, int clusters, cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};
@@ -709,7 +755,7 @@ static cudaError_t launch_engine(const TcArgs& a, const CUtensorMap& tmA, const 
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, tc2_gemm_kernel<BNT, kSplit>, tmA, tmB, tmC, tmS, a);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, tc2_gemm_kernel<BNT, kSplit, kGroups>, tmA, tmB, tmC, tmS, a);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -741,9 +787,14 @@ cudaError_t tc_gemm_launch(const TcArgs& a0, const void* A16, int64_t lda, int a
         if (e != cudaSuccess) return e;
     }
     if (clusters > total) clusters = total;
-    if (a.split > 1) return launch_engine<256, true>(a, tmA, tmB, tmC, tmS, clusters, s);
-    if (bn == 192) return launch_engine<192, false>(a, tmA, tmB, tmC, tmS, clusters, s);
-    return launch_engine<256, false>(a, tmA, tmB, tmC, tmS, clusters, s);
+    if (clusters > kTcMaxClusters) clusters = kTcMaxClusters;
+    assign_leftovers(a, clusters);
+    // split launches (and every multi-group launch) walk the assignment table; the one-group
+    // unsplit ones keep a plain round-robin (the table walk's registers would spill there)
+    if (a.split > 1) return launch_engine<256, true, true>(a, tmA, tmB, tmC, tmS, clusters, s);
+    if (a.ndiag > 1) return launch_engine<256, false, true>(a, tmA, tmB, tmC, tmS, clusters, s);
+    if (bn == 192) return launch_engine<192, false, false>(a, tmA, tmB, tmC, tmS, clusters, s);
+    return launch_engine<256, false, false>(a, tmA, tmB, tmC, tmS, clusters, s);
 }
 
 // Self-check of the bounded waits: one thread waits on an mbarrier that nothing ever

@@ -77,6 +77,7 @@ cudaError_t slice_f64_f16_launch(const double* X, int64_t ldx, int rows, int col
 // diag_first[d] + diag_nseg[d] - 1, segment s pairing A plane segA[s] with B plane segB[s].
 constexpr int kTcMaxDiag = 18;
 constexpr int kTcMaxSeg = 96;
+constexpr int kTcMaxClusters = 128;  // CTA pairs of one launch
 
 struct TcArgs {
     int M, N;
@@ -91,6 +92,11 @@ struct TcArgs {
                                // workspace (one 256 x 256 slot per tile unit) and the warp that
                                // arrives last at its counter rounds the sums
     int tiles_m, tiles_n;      // set by the launcher
+    // Work assignment (set by the launcher): plane group d has per_d = tiles * split units;
+    // CTA pair c takes units c, c + C, ... below C * (per_d / C) (C pairs launched), and
+    // the leftover unit C * (per_d / C) + extra_of[d][c] when that is >= 0 (the leftovers of
+    // the groups, heaviest group first, go to the least-loaded pairs).
+    int8_t extra_of[kTcMaxDiag][kTcMaxClusters];
     int group_m;               // tile rows per raster group (0: default)
     int mode;                  // EpilogueMode
     const int32_t* ea;
