@@ -543,7 +543,6 @@ __global__ void __launch_bounds__(Geo<BNT>::THREADS, 1)
 // ------------------------------------------------------------------------------------
 std::mutex g_tc_mutex;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-int g_num_sms[64];
 
 cudaError_t get_encode(PFN_cuTensorMapEncodeTiled_v12000* fn) {
     std::lock_guard<std::mutex> lock(g_tc_mutex);
@@ -556,19 +555,6 @@ cudaError_t get_encode(PFN_cuTensorMapEncodeTiled_v12000* fn) {
     }
     *fn = g_encode;
     return cudaSuccess;
-}
-
-int num_sms() {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64) return 148;
-    std::lock_guard<std::mutex> lock(g_tc_mutex);
-    if (g_num_sms[dev] == 0) {
-        int n = 0;
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-        g_num_sms[dev] = n > 0 ? n : 148;
-    }
-    return g_num_sms[dev];
 }
 
 // 3-D map over fp16 planes [planes][rows][ld] of which the first kext columns are the
