@@ -8,8 +8,8 @@ INT8 TOPS (2 M N K per GEMM / time) with the dominant kernel's roofline fraction
 
 The same JSON line carries extra measurements of the other hot-path rows: the skinny
 decode-shaped GEMM (M=16, N=4096, K=65536, split-K 8/16/32) in GB/s against the HBM
-roofline, the Ozaki fp32 GEMM (4096^3) in effective fp32 TFLOP/s, the fp64-target Ozaki
-GEMM (4096^3) next to the library fp64 GEMM, the fused linear layer
+roofline, the Ozaki fp32 GEMM (4096^3) in effective fp32 TFLOP/s next to the library fp32
+GEMM, the fp64-target Ozaki GEMM (4096^3) next to the library fp64 GEMM, the fused linear layer
 on bf16 activations at the FFN gate/up size, the sweep linear (K=2048, N=6144) at
 M = 1, 7, 64, 257, 2048, and the tiny workload's latency.
 
