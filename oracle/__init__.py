@@ -61,6 +61,9 @@ def _load():
             lib.oracle_rne_bf16.argtypes = [ctypes.c_double]
             lib.oracle_rne_bf16.restype = ctypes.c_uint16
             lib.oracle_w8a8.argtypes = [p, i64, p, i64, p, p, p, i64, i32, i32, i32, p, i32]
+            lib.oracle_bias_round.argtypes = [i64, i64, ctypes.c_uint16]
+            lib.oracle_bias_round.restype = ctypes.c_uint16
+            lib.oracle_w8a8_bias.argtypes = [p, i64, p, i64, p, p, p, p, i64, i32, i32, i32, p, i32]
             lib.oracle_gemm_s8_i32.argtypes = [p, i64, p, i64, p, i64, i32, i32, i32, p, i32]
             lib.oracle_quantize_pow2.argtypes = [p, i32, i64, i32, i32, i32, p, i64, p]
             lib.oracle_slice_f32.argtypes = [p, i64, i32, i32, i32, i32, p, p]
@@ -70,7 +73,7 @@ def _load():
             lib.oracle_ozaki_combine_f64.argtypes = [p, i64, i32, p, p, p, i64, i32, i32]
             lib.oracle_slice_f64.argtypes = [p, i64, i32, i32, i32, i32, p, p]
             lib.oracle_ozaki_f64.argtypes = [p, i64, p, i64, p, i64, i32, i32, i32, i32, i32, p, i32]
-            for f in (lib.oracle_w8a8, lib.oracle_gemm_s8_i32, lib.oracle_quantize_pow2,
+            for f in (lib.oracle_w8a8, lib.oracle_w8a8_bias, lib.oracle_gemm_s8_i32, lib.oracle_quantize_pow2,
                       lib.oracle_slice_f32, lib.oracle_ozaki_f32, lib.oracle_ozaki_diagonals,
                       lib.oracle_ozaki_combine, lib.oracle_ozaki_combine_f64, lib.oracle_slice_f64,
                       lib.oracle_ozaki_f64):
@@ -110,6 +113,29 @@ def w8a8(A, W, ea, ew, rows=None, check=True):
                              C.ctypes.data, N, M, N, K, r.ctypes.data if r is not None else None, nr)
     if check and st != OK:
         raise OracleError(f"oracle_w8a8 status {st}")
+    return C
+
+
+def bias_round(acc: int, E: int, b: int) -> int:
+    """bf16 bits of rne_bf16(acc * 2^E + b) for an int64 acc and the bf16 bit pattern b."""
+    return int(_load().oracle_bias_round(int(acc), int(E), int(b)))
+
+
+def w8a8_bias(A, W, ea, ew, bias, rows=None, check=True):
+    """C = rne_bf16((A W^T) * 2^(ea_i + ew_j) + b_j) as uint16 bf16 bits [rows x N]; bias is
+    uint16 bf16 bits [N]."""
+    A, W = _c(A, np.int8), _c(W, np.int8)
+    ea, ew, bias = _c(ea, np.int32), _c(ew, np.int32), _c(bias, np.uint16)
+    M, K = A.shape
+    N = W.shape[0]
+    assert W.shape[1] == K and ea.shape == (M,) and ew.shape == (N,) and bias.shape == (N,)
+    r, nr = _rows(rows)
+    C = np.empty((nr if r is not None else M, N), dtype=np.uint16)
+    st = _load().oracle_w8a8_bias(A.ctypes.data, K, W.ctypes.data, K, ea.ctypes.data, ew.ctypes.data,
+                                  bias.ctypes.data, C.ctypes.data, N, M, N, K,
+                                  r.ctypes.data if r is not None else None, nr)
+    if check and st != OK:
+        raise OracleError(f"oracle_w8a8_bias status {st}")
     return C
 
 

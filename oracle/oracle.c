@@ -102,6 +102,66 @@ int oracle_w8a8(const int8_t* A, int64_t lda, const int8_t* W, int64_t ldw, cons
     return bad ? ORACLE_ERR_PRECONDITION : ORACLE_OK;
 }
 
+/* ------------------------------------------------------------------------------------ */
+/* W8A8 with a bias: the epilogue's one rounding [P4 §II] taken of the exact sum          */
+/*   C_ij = rne_bf16(acc_ij * 2^(ea_i + ew_j) + b_j),   b_j a bfloat16 value.             */
+/* Readings: b = +-0 leaves the W8A8 result unchanged (x + 0 = x, including the sign of   */
+/* an underflowing x); a non-finite b is returned unchanged; an exact zero sum gives +0.  */
+/* Route: x = acc * 2^E and b are exact doubles; the double sum s and its error t (the    */
+/* classical two-sum, exact without overflow) give the exact sum s + t. Rounding s to     */
+/* bf16 is right unless s lies exactly halfway between two bf16 numbers while t != 0:    */
+/* every bf16 halfway point is a double, so s and the exact sum are on the same side of   */
+/* every other one; in that case the sign of t picks the neighbour.                      */
+/* ------------------------------------------------------------------------------------ */
+static double bf16_to_double(uint16_t b) {
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return (double)f;
+}
+
+uint16_t oracle_bias_round(int64_t acc, int64_t E, uint16_t b) {
+    if ((b & 0x7F80) == 0x7F80) return b;                    /* +-inf, NaN */
+    double x = ldexp((double)acc, clamp_exp(E));
+    if ((b & 0x7FFF) == 0) return oracle_rne_bf16(x);        /* x + (+-0) = x */
+    double bv = bf16_to_double(b);
+    if (acc == 0) return oracle_rne_bf16(bv);                /* = b */
+    double s = x + bv;
+    double z = s - x;
+    double t = (x - (s - z)) + (bv - z);                     /* s + t = x + bv exactly */
+    if (s == 0.0) return 0;                                  /* exact zero sum: +0 */
+    if (isinf(s) || t == 0.0) return oracle_rne_bf16(s);
+    double a = fabs(s);
+    int k;
+    frexp(a, &k);
+    int p = k - 1;
+    int q = (p < -126) ? -133 : p - 7;                       /* log2 of the bf16 spacing at a */
+    double n = ldexp(a, -q);
+    double fl = floor(n);
+    if (n - fl != 0.5) return oracle_rne_bf16(s);            /* not a halfway point */
+    int up = (t > 0.0) == (s > 0.0);                         /* exact |sum| above a? */
+    double r = ldexp(up ? fl + 1.0 : fl, q);                 /* on the bf16 grid (or 2^128) */
+    return oracle_rne_bf16(s > 0.0 ? r : -r);
+}
+
+int oracle_w8a8_bias(const int8_t* A, int64_t lda, const int8_t* W, int64_t ldw, const int32_t* ea,
+                     const int32_t* ew, const uint16_t* bias, uint16_t* C, int64_t ldc, int M, int N,
+                     int K, const int32_t* rows, int nrows) {
+    int n_out = rows ? nrows : M;
+    int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+    for (int r = 0; r < n_out; ++r) {
+        int i = rows ? rows[r] : r;
+        for (int j = 0; j < N; ++j) {
+            int64_t acc = 0;
+            for (int k = 0; k < K; ++k) acc += (int64_t)A[(int64_t)i * lda + k] * (int64_t)W[(int64_t)j * ldw + k];
+            if (acc >= 2147483648LL || acc < -2147483648LL) bad = 1;
+            C[(int64_t)r * ldc + j] = oracle_bias_round(acc, (int64_t)ea[i] + (int64_t)ew[j], bias[j]);
+        }
+    }
+    return bad ? ORACLE_ERR_PRECONDITION : ORACLE_OK;
+}
+
 /* The exact int32 accumulator alone: C_ij = sum_k A_ik * W_jk. */
 int oracle_gemm_s8_i32(const int8_t* A, int64_t lda, const int8_t* W, int64_t ldw, int32_t* C,
                        int64_t ldc, int M, int N, int K, const int32_t* rows, int nrows) {
