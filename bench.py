@@ -47,7 +47,7 @@ OPS_STEP = 2.0 * M_FFN * (N1 * K1 + N2 * K2)
 # FFN GEMMs (profiles/tc2_gemm_kernel_ffn_gate_up.md, profiles/launches_ffn_tc2.md), keyed
 # by a digest of the engine source so that a changed kernel reports null, not stale counters
 PROFILED_TRAFFIC = {
-    "7e7918d6b904cf95": {"gate_up": 487089152 + 182165760, "down": 897474048 + 62837248},
+    "00eb2364097789cf": {"gate_up": 478853632 + 182162688, "down": 897511168 + 62855168},
 }
 
 

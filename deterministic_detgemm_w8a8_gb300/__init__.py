@@ -44,6 +44,7 @@ SIGNATURES = {
     "detgemm_version": ([], _I32),
     "detgemm_w8a8": ([_P, _I64, _P, _I64, _P, _P, _P, _I64, _I32, _I32, _I32, _I32, _P, _SZ, _P], _I32),
     "detgemm_w8a8_workspace_size": ([_I32, _I32, _I32, _I32], _SZ),
+    "detgemm_w8a8_bias": ([_P, _I64, _P, _I64, _P, _P, _P, _P, _I64, _I32, _I32, _I32, _I32, _P, _SZ, _P], _I32),
     "detgemm_gemm_s8_i32": ([_P, _I64, _P, _I64, _P, _I64, _I32, _I32, _I32, _I32, _P, _SZ, _P], _I32),
     "detgemm_quantize_pow2": ([_P, _I32, _I64, _I32, _I32, _I32, _P, _I64, _P, _P], _I32),
     "detgemm_slice_f32": ([_P, _I64, _I32, _I32, _I32, _I32, _P, _P, _P], _I32),
@@ -58,6 +59,8 @@ SIGNATURES = {
     "detgemm_linear_w8a8": ([_P, _I32, _I64, _I32, _P, _I64, _P, _I64, _P, _P, _I64, _P, _I32, _I32, _I32, _I32,
                              _P, _SZ, _P], _I32),
     "detgemm_linear_w8a8_workspace_size": ([_I32, _I32, _I32, _I32, _I32], _SZ),
+    "detgemm_linear_w8a8_bias": ([_P, _I32, _I64, _I32, _P, _I64, _P, _I64, _P, _P, _P, _I64, _P, _I32, _I32, _I32,
+                                  _I32, _P, _SZ, _P], _I32),
     "detgemm_get_device_status": ([_P], _I32),
     "detgemm_w8a8_noalloc": ([_P, _I64, _P, _I64, _P, _P, _P, _I64, _I32, _I32, _I32, _I32, _P], _I32),
     "detgemm_widen_i8_f16": ([_P, _I64, _I32, _I32, _P, _I64, _P], _I32),
@@ -157,8 +160,19 @@ def ozaki_workspace_size(M, N, K, nslices=7, max_diag=8, split_k=1) -> int:
     return int(load().detgemm_ozaki_workspace_size(M, N, K, nslices, max_diag, split_k))
 
 
-def w8a8(A, W, ea, ew, split_k: int = 1, out=None, ws=None, stream=None) -> torch.Tensor:
-    """C = rne_bf16((A W^T) * 2^(ea_i + ew_j)); A int8 [M,K], W int8 [N,K], ea/ew int32.
+def _bias_vec(bias, N, device):
+    if bias is None:
+        return None
+    if not isinstance(bias, torch.Tensor) or bias.dtype != torch.bfloat16 or bias.shape != (N,):
+        raise ValueError("bias must be a bfloat16 tensor of shape [N]")
+    if bias.device != device or not bias.is_contiguous():
+        raise ValueError("bias must be contiguous on the operands' device")
+    return bias
+
+
+def w8a8(A, W, ea, ew, split_k: int = 1, out=None, ws=None, stream=None, bias=None) -> torch.Tensor:
+    """C = rne_bf16((A W^T) * 2^(ea_i + ew_j) [+ bias_j]); A int8 [M,K], W int8 [N,K], ea/ew
+    int32, bias (optional) bfloat16 [N] added before the one rounding.
     Returns a torch.bfloat16 tensor [M, N] (or writes ``out``)."""
     lib = load()
     _req(A, torch.int8, "A"); _req(W, torch.int8, "W")
@@ -170,7 +184,14 @@ def w8a8(A, W, ea, ew, split_k: int = 1, out=None, ws=None, stream=None) -> torc
     if out is None:
         out = empty2d(M, N, torch.bfloat16, A.device)
     _req(out, torch.bfloat16, "out")
+    bias = _bias_vec(bias, N, A.device)
     wsb, wsn = _workspace(w8a8_workspace_size(M, N, K, split_k), A.device, ws)
+    if bias is not None:
+        st = lib.detgemm_w8a8_bias(A.data_ptr(), _ld(A), W.data_ptr(), _ld(W), ea.data_ptr(), ew.data_ptr(),
+                                   bias.data_ptr(), out.data_ptr(), _ld(out), M, N, K, split_k,
+                                   wsb.data_ptr() if wsb is not None else None, wsn, _stream(stream))
+        _check(st, "detgemm_w8a8_bias")
+        return out
     st = lib.detgemm_w8a8(A.data_ptr(), _ld(A), W.data_ptr(), _ld(W), ea.data_ptr(), ew.data_ptr(),
                           out.data_ptr(), _ld(out), M, N, K, split_k,
                           wsb.data_ptr() if wsb is not None else None, wsn, _stream(stream))
@@ -264,11 +285,11 @@ def quantize_pow2(X, mode: int = POW2_NEAREST, stream=None):
 
 
 def linear_w8a8(X, W, ew, mode: int = POW2_NEAREST, W16=None, split_k: int = 1, out=None, ea_out=None, ws=None,
-                stream=None) -> torch.Tensor:
+                stream=None, bias=None) -> torch.Tensor:
     """W8A8 linear layer on bf16/fp32 activations X [M, K]: per-row pow2 quantization of X
     fused with the exact GEMM against int8 W [N, K] (ew int32 [N]); bf16 [M, N] out.
     W16 (optional) is W widened once by widen_i8_f16; ea_out (optional) int32 [M] receives
-    the activation exponents."""
+    the activation exponents; bias (optional) bfloat16 [N] is added before the one rounding."""
     lib = load()
     if X.dtype == torch.bfloat16:
         dt = DTYPE_BF16
@@ -292,13 +313,21 @@ def linear_w8a8(X, W, ew, mode: int = POW2_NEAREST, W16=None, split_k: int = 1, 
     if out is None:
         out = empty2d(M, N, torch.bfloat16, X.device)
     _req(out, torch.bfloat16, "out")
+    bias = _bias_vec(bias, N, X.device)
     need = int(lib.detgemm_linear_w8a8_workspace_size(M, N, K, split_k, 1 if W16 is not None else 0))
     wsb, wsn = _workspace(need, X.device, ws)
-    st = lib.detgemm_linear_w8a8(X.data_ptr(), dt, _ld(X), mode, W.data_ptr(), _ld(W),
-                                 W16.data_ptr() if W16 is not None else None, _ld(W16) if W16 is not None else 0,
-                                 ew.data_ptr(), out.data_ptr(), _ld(out),
-                                 ea_out.data_ptr() if ea_out is not None else None, M, N, K, split_k,
-                                 wsb.data_ptr() if wsb is not None else None, wsn, _stream(stream))
+    w16p, w16ld = (W16.data_ptr(), _ld(W16)) if W16 is not None else (None, 0)
+    eap = ea_out.data_ptr() if ea_out is not None else None
+    wsp = wsb.data_ptr() if wsb is not None else None
+    if bias is not None:
+        st = lib.detgemm_linear_w8a8_bias(X.data_ptr(), dt, _ld(X), mode, W.data_ptr(), _ld(W), w16p, w16ld,
+                                          ew.data_ptr(), bias.data_ptr(), out.data_ptr(), _ld(out), eap, M, N, K,
+                                          split_k, wsp, wsn, _stream(stream))
+        _check(st, "detgemm_linear_w8a8_bias")
+        return out
+    st = lib.detgemm_linear_w8a8(X.data_ptr(), dt, _ld(X), mode, W.data_ptr(), _ld(W), w16p, w16ld,
+                                 ew.data_ptr(), out.data_ptr(), _ld(out), eap, M, N, K, split_k, wsp, wsn,
+                                 _stream(stream))
     _check(st, "detgemm_linear_w8a8")
     return out
 

@@ -37,6 +37,7 @@ detgemm_status check_device() { return check_device_impl(); }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+bool aligned2(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 1u) == 0; }
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
@@ -142,7 +143,7 @@ size_t detgemm_w8a8_workspace_size(int M, int N, int K, int split_k) {
 }
 
 static detgemm_status run_tc(const int8_t* A, int64_t lda, const int8_t* W, int64_t ldw, const int32_t* ea,
-                             const int32_t* ew, void* C, int64_t ldc, int mode, int M, int N, int K, int split_k,
+                             const int32_t* ew, const uint16_t* bias, void* C, int64_t ldc, int mode, int M, int N, int K, int split_k,
                              void* ws, cudaStream_t stream) {
     const TcW8a8Layout L = tc_w8a8_layout(M, N, K, split_k);
     char* base = reinterpret_cast<char*>(ws);
@@ -160,6 +161,7 @@ static detgemm_status run_tc(const int8_t* A, int64_t lda, const int8_t* W, int6
     a.mode = mode;
     a.ea = ea;
     a.ew = ew;
+    a.bias = bias;
     a.C = C;
     a.ldc = ldc;
     a.c_plane = 0;
@@ -167,9 +169,9 @@ static detgemm_status run_tc(const int8_t* A, int64_t lda, const int8_t* W, int6
 }
 
 static detgemm_status run_igemm(const int8_t* A, int64_t lda, const int8_t* W, int64_t ldw, const int32_t* ea,
-                                const int32_t* ew, void* C, int64_t ldc, int mode, int M, int N, int K, int split_k,
+                                const int32_t* ew, const uint16_t* bias, void* C, int64_t ldc, int mode, int M, int N, int K, int split_k,
                                 void* ws, cudaStream_t stream) {
-    if (w8a8_uses_tc(M, K)) return run_tc(A, lda, W, ldw, ea, ew, C, ldc, mode, M, N, K, split_k, ws, stream);
+    if (w8a8_uses_tc(M, K)) return run_tc(A, lda, W, ldw, ea, ew, bias, C, ldc, mode, M, N, K, split_k, ws, stream);
     IGemmArgs a = {};
     a.seg[0] = Seg{A, W};
     a.nseg = 1;
@@ -182,22 +184,37 @@ static detgemm_status run_igemm(const int8_t* A, int64_t lda, const int8_t* W, i
     a.mode = mode;
     a.ea = ea;
     a.ew = ew;
+    a.bias = bias;
     a.C = C;
     a.ldc = ldc;
     return from_cuda(igemm_launch(a, ws, stream));
 }
 
-detgemm_status detgemm_w8a8(const int8_t* A, int64_t lda, const int8_t* W, int64_t ldw, const int32_t* ea,
-                            const int32_t* ew, uint16_t* C, int64_t ldc, int M, int N, int K, int split_k, void* ws,
-                            size_t ws_bytes, detgemm_stream_t stream) {
+static detgemm_status w8a8_impl(const int8_t* A, int64_t lda, const int8_t* W, int64_t ldw, const int32_t* ea,
+                                const int32_t* ew, const uint16_t* bias, bool with_bias, uint16_t* C, int64_t ldc,
+                                int M, int N, int K, int split_k, void* ws, size_t ws_bytes,
+                                detgemm_stream_t stream) {
     detgemm_status st = validate_igemm(A, lda, W, ldw, C, ldc, 2, M, N, K, split_k, ws, ws_bytes);
     if (st != DETGEMM_OK) return st;
     if (M == 0 || N == 0) return DETGEMM_OK;
-    if (!ea || !ew) return DETGEMM_ERR_INVALID_ARG;
-    if (!aligned4(ea) || !aligned4(ew)) return DETGEMM_ERR_ALIGNMENT;
+    if (!ea || !ew || (with_bias && !bias)) return DETGEMM_ERR_INVALID_ARG;
+    if (!aligned4(ea) || !aligned4(ew) || (with_bias && !aligned2(bias))) return DETGEMM_ERR_ALIGNMENT;
     if ((st = check_device()) != DETGEMM_OK) return st;
-    return run_igemm(A, lda, W, ldw, ea, ew, C, ldc, EPI_BF16_POW2, M, N, K, split_k, ws,
+    return run_igemm(A, lda, W, ldw, ea, ew, with_bias ? bias : nullptr, C, ldc,
+                     with_bias ? EPI_BF16_POW2_BIAS : EPI_BF16_POW2, M, N, K, split_k, ws,
                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+detgemm_status detgemm_w8a8(const int8_t* A, int64_t lda, const int8_t* W, int64_t ldw, const int32_t* ea,
+                            const int32_t* ew, uint16_t* C, int64_t ldc, int M, int N, int K, int split_k, void* ws,
+                            size_t ws_bytes, detgemm_stream_t stream) {
+    return w8a8_impl(A, lda, W, ldw, ea, ew, nullptr, false, C, ldc, M, N, K, split_k, ws, ws_bytes, stream);
+}
+
+detgemm_status detgemm_w8a8_bias(const int8_t* A, int64_t lda, const int8_t* W, int64_t ldw, const int32_t* ea,
+                                 const int32_t* ew, const uint16_t* bias, uint16_t* C, int64_t ldc, int M, int N,
+                                 int K, int split_k, void* ws, size_t ws_bytes, detgemm_stream_t stream) {
+    return w8a8_impl(A, lda, W, ldw, ea, ew, bias, true, C, ldc, M, N, K, split_k, ws, ws_bytes, stream);
 }
 
 detgemm_status detgemm_gemm_s8_i32(const int8_t* A, int64_t lda, const int8_t* W, int64_t ldw, int32_t* C,
@@ -207,7 +224,7 @@ detgemm_status detgemm_gemm_s8_i32(const int8_t* A, int64_t lda, const int8_t* W
     if (st != DETGEMM_OK) return st;
     if (M == 0 || N == 0) return DETGEMM_OK;
     if ((st = check_device()) != DETGEMM_OK) return st;
-    return run_igemm(A, lda, W, ldw, nullptr, nullptr, C, ldc, EPI_STORE_I32, M, N, K, split_k, ws,
+    return run_igemm(A, lda, W, ldw, nullptr, nullptr, nullptr, C, ldc, EPI_STORE_I32, M, N, K, split_k, ws,
                      reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -244,10 +261,10 @@ size_t detgemm_linear_w8a8_workspace_size(int M, int N, int K, int split_k, int 
     return linear_layout(M, N, K, split_k, have_w16 != 0).total;
 }
 
-detgemm_status detgemm_linear_w8a8(const void* X, int x_dtype, int64_t ldx, int mode, const int8_t* W, int64_t ldw,
-                                   const uint16_t* W16, int64_t ldw16, const int32_t* ew, uint16_t* C, int64_t ldc,
-                                   int32_t* ea_out, int M, int N, int K, int split_k, void* ws, size_t ws_bytes,
-                                   detgemm_stream_t stream) {
+static detgemm_status linear_impl(const void* X, int x_dtype, int64_t ldx, int mode, const int8_t* W, int64_t ldw,
+                                  const uint16_t* W16, int64_t ldw16, const int32_t* ew, const uint16_t* bias,
+                                  bool with_bias, uint16_t* C, int64_t ldc, int32_t* ea_out, int M, int N, int K,
+                                  int split_k, void* ws, size_t ws_bytes, detgemm_stream_t stream) {
     if (M < 0 || N < 0 || K < 1) return DETGEMM_ERR_INVALID_ARG;
     if (x_dtype != DETGEMM_DTYPE_BF16 && x_dtype != DETGEMM_DTYPE_F32) return DETGEMM_ERR_INVALID_ARG;
     if (mode != DETGEMM_POW2_NEAREST && mode != DETGEMM_POW2_CEIL) return DETGEMM_ERR_INVALID_ARG;
@@ -256,6 +273,10 @@ detgemm_status detgemm_linear_w8a8(const void* X, int x_dtype, int64_t ldx, int 
     if (M == 0 || N == 0) return DETGEMM_OK;
     if (!X || !W || !ew || !C || ldx < K || ldw < K || ldc < N) return DETGEMM_ERR_INVALID_ARG;
     if (W16 && ldw16 < K) return DETGEMM_ERR_INVALID_ARG;
+    if (with_bias && !bias) return DETGEMM_ERR_INVALID_ARG;
+    if (with_bias && !aligned2(bias)) return DETGEMM_ERR_ALIGNMENT;
+    const int epi = with_bias ? EPI_BF16_POW2_BIAS : EPI_BF16_POW2;
+    if (!with_bias) bias = nullptr;
     const int xs = x_dtype == DETGEMM_DTYPE_BF16 ? 2 : 4;
     if (!aligned16(X) || !aligned16(W) || !aligned16(C) || !aligned4(ew) || (ea_out && !aligned4(ea_out)))
         return DETGEMM_ERR_ALIGNMENT;
@@ -277,7 +298,7 @@ detgemm_status detgemm_linear_w8a8(const void* X, int x_dtype, int64_t ldx, int 
         int8_t* Q = reinterpret_cast<int8_t*>(base + L.a);
         err = quantize_pow2_launch(X, x_dtype, ldx, M, K, mode, Q, L.K16, ea, s);
         if (err != cudaSuccess) return DETGEMM_ERR_CUDA;
-        return run_igemm(Q, L.K16, W, ldw, ea, ew, C, ldc, EPI_BF16_POW2, M, N, K, split_k, base + L.gemm, s);
+        return run_igemm(Q, L.K16, W, ldw, ea, ew, bias, C, ldc, epi, M, N, K, split_k, base + L.gemm, s);
     }
     // tensor-core path: the quantizer writes the activation operand directly in its fp16
     // carrier form (no int8 copy, no widening pass over it)
@@ -298,12 +319,29 @@ detgemm_status detgemm_linear_w8a8(const void* X, int x_dtype, int64_t ldx, int 
     a.diag_first[0] = 0;
     a.diag_nseg[0] = 1;
     a.split = split_k;
-    a.mode = EPI_BF16_POW2;
+    a.mode = epi;
     a.ea = ea;
     a.ew = ew;
+    a.bias = bias;
     a.C = C;
     a.ldc = ldc;
     return from_cuda(tc_gemm_launch(a, base + L.a, L.Kp, 1, wop, ldwop, 1, K, base + L.gemm, s));
+}
+
+detgemm_status detgemm_linear_w8a8(const void* X, int x_dtype, int64_t ldx, int mode, const int8_t* W, int64_t ldw,
+                                   const uint16_t* W16, int64_t ldw16, const int32_t* ew, uint16_t* C, int64_t ldc,
+                                   int32_t* ea_out, int M, int N, int K, int split_k, void* ws, size_t ws_bytes,
+                                   detgemm_stream_t stream) {
+    return linear_impl(X, x_dtype, ldx, mode, W, ldw, W16, ldw16, ew, nullptr, false, C, ldc, ea_out, M, N, K, split_k,
+                       ws, ws_bytes, stream);
+}
+
+detgemm_status detgemm_linear_w8a8_bias(const void* X, int x_dtype, int64_t ldx, int mode, const int8_t* W,
+                                        int64_t ldw, const uint16_t* W16, int64_t ldw16, const int32_t* ew,
+                                        const uint16_t* bias, uint16_t* C, int64_t ldc, int32_t* ea_out, int M, int N,
+                                        int K, int split_k, void* ws, size_t ws_bytes, detgemm_stream_t stream) {
+    return linear_impl(X, x_dtype, ldx, mode, W, ldw, W16, ldw16, ew, bias, true, C, ldc, ea_out, M, N, K, split_k, ws,
+                       ws_bytes, stream);
 }
 
 detgemm_status detgemm_quantize_pow2(const void* X, int x_dtype, int64_t ldx, int rows, int cols, int mode,

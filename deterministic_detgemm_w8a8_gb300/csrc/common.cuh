@@ -1,6 +1,7 @@
 // Shared device helpers of libdetgemm: status word, exact epilogues, bit utilities.
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -94,6 +95,112 @@ __device__ __forceinline__ uint16_t bf16_from_acc_pow2(int32_t acc, int32_t ea, 
     uint32_t bits = ((uint32_t)(eb - 1) << 7) + q;
     bits = bits >= 0x7F80u ? 0x7F80u : bits;
     return (uint16_t)(sign | bits);
+}
+
+// ------------------------------------------------------------------------------------
+// Epilogue E1 with a bias: rne_bf16(acc * 2^E + b), b a bfloat16 per output column,
+// rounded once. The pages define the epilogue as the one rounding of the exactly scaled
+// int32 accumulator ("Deterministic LLM Inference Across GPU Kernels ...", §II "Pipeline
+// and alibi"); the bias joins the exact value before that rounding, so the result is
+// still a function of the operands alone.
+//
+// Both terms are integers times powers of two: x = acc * 2^E and b = mb * 2^eb (mb < 2^8).
+// They are aligned on the smaller exponent in an int64 and the sum is rounded once. When
+// one term lies entirely below 2^-9 of the other's last unit, only its sign can matter (it
+// decides a tie or a value sitting on the bf16 grid, nothing else), so it is replaced by
+// one signed unit below that last unit, which keeps the int64 in range.
+// ------------------------------------------------------------------------------------
+// rne_bf16(S * 2^X) for an int64 S != 0 (|S| <= 2^63).
+static __device__ __noinline__ uint16_t bf16_from_i64_pow2(long long S, int X) {
+    const uint32_t sign = S < 0 ? 0x8000u : 0u;
+    const unsigned long long m = S < 0 ? 0ull - (unsigned long long)S : (unsigned long long)S;
+    const int p = 63 - __clzll(m);  // m in [2^p, 2^(p+1))
+    const int eb = p + X + 127;
+    int sh;
+    uint32_t base;
+    if (eb >= 1) {
+        sh = p - 7;
+        base = (uint32_t)(eb - 1) << 7;
+    } else {
+        sh = -(X + 133);
+        base = 0;
+    }
+    unsigned long long q;
+    if (sh <= 0) {
+        q = m << (-sh);  // at most 8 significant bits
+    } else if (sh > 63) {
+        q = 0;           // below half of the smallest subnormal (or exactly half: even)
+    } else {
+        q = m >> sh;
+        const unsigned long long rem = m - (q << sh);
+        const unsigned long long half = 1ull << (sh - 1);
+        if (rem > half || (rem == half && (q & 1ull))) q += 1;
+    }
+    unsigned long long bits = base + q;
+    if (bits >= 0x7F80ull) bits = 0x7F80ull;
+    return (uint16_t)(sign | (uint32_t)bits);
+}
+
+// General case: any accumulator, any exponents, any bias (a non-finite bias passes
+// through; an exact zero sum gives +0).
+static __device__ __noinline__ uint16_t bf16_from_acc_pow2_bias_general(int32_t acc, int32_t ea, int32_t ew,
+                                                                        uint16_t b) {
+    if ((b & 0x7FFFu) == 0) return bf16_from_acc_pow2(acc, ea, ew);  // x + (+-0) = x
+    if ((b & 0x7F80u) == 0x7F80u) return b;                           // +-inf, NaN
+    if (acc == 0) return b;                                           // b is on the grid
+    long long El = (long long)ea + (long long)ew;
+    const int E = (int)(El > 300 ? 300 : (El < -300 ? -300 : El));
+    const int field = (b >> 7) & 0xFF;
+    const int mbu = field == 0 ? (b & 0x7F) : ((b & 0x7F) | 0x80);
+    const int eb = field == 0 ? -133 : field - 134;
+    const long long mb = (b & 0x8000u) ? -(long long)mbu : (long long)mbu;
+    long long S;
+    int X;
+    if (E >= eb) {
+        if (E - eb > 31) {  // |b| < 2^(E - 23): a signed unit at 2^(E - 31)
+            S = ((long long)acc << 31) + (mb > 0 ? 1 : -1);
+            X = E - 31;
+        } else {
+            S = ((long long)acc << (E - eb)) + mb;
+            X = eb;
+        }
+    } else {
+        if (eb - E > 40) {  // |x| < 2^(eb - 9): a signed unit at 2^(eb - 40)
+            S = (mb << 40) + (acc > 0 ? 1 : -1);
+            X = eb - 40;
+        } else {
+            S = (mb << (eb - E)) + (long long)acc;
+            X = E;
+        }
+    }
+    if (S == 0) return 0;
+    return bf16_from_i64_pow2(S, X);
+}
+
+// Fast form for |acc| < 2^24, E = ea + ew in [-120, 80] (passed as the exact scales sa =
+// 2^ea, sw = 2^ew) and |b| < 2^64: x = acc * sa * sw is an exact fp32 number, the sum
+// x + b is split exactly into s + t (two-sum; no overflow in this range), the sum is
+// rounded to odd at 24 bits (s when t == 0; otherwise the fp32 number next to the sum
+// toward zero with its last bit set) and that is rounded to nearest-even at 8 bits. Rounding
+// to odd at 24 >= 8 + 2 bits and then to nearest at 8 bits equals one rounding to nearest,
+// so the result is that of the general form. Any other input takes the general form.
+__device__ __forceinline__ uint16_t bf16_from_acc_pow2_bias(int32_t acc, float sa, float sw, int32_t ea, int32_t ew,
+                                                            bool fast_exp, uint16_t b) {
+    const uint32_t ua = acc < 0 ? 0u - (uint32_t)acc : (uint32_t)acc;
+    if (!fast_exp || ua >= (1u << 24) || ((b >> 7) & 0xFFu) >= 191u)
+        return bf16_from_acc_pow2_bias_general(acc, ea, ew, b);
+    const float x = __fmul_rn(__fmul_rn(__int2float_rn(acc), sa), sw);
+    const float bv = __uint_as_float((uint32_t)b << 16);
+    const float s = __fadd_rn(x, bv);
+    const float bb = __fsub_rn(s, x);
+    const float t = __fadd_rn(__fsub_rn(x, __fsub_rn(s, bb)), __fsub_rn(bv, bb));
+    uint32_t sb = __float_as_uint(s);
+    if (t != 0.0f) {
+        if ((t < 0.0f) != (s < 0.0f)) sb -= 1;  // s was rounded away from zero: step back
+        sb |= 1u;
+    }
+    const __nv_bfloat16 h = __float2bfloat16_rn(__uint_as_float(sb));
+    return *reinterpret_cast<const uint16_t*>(&h);
 }
 
 // Exact power of two as a double for |k| <= 1022.

@@ -65,12 +65,15 @@ __device__ __forceinline__ void split_range(int F, int split, int z, int& f0, in
 __device__ __forceinline__ void store_pair(const IGemmArgs& p, int row, int col, int32_t v0, int32_t v1) {
     if (row >= p.M || col >= p.N) return;
     bool two = col + 1 < p.N;
-    if (p.mode == EPI_BF16_POW2) {
+    if (p.mode != EPI_STORE_I32) {
         int32_t ea = p.ea[row];
-        uint16_t h0 = bf16_from_acc_pow2(v0, ea, p.ew[col]);
+        const bool bias = p.mode == EPI_BF16_POW2_BIAS;
+        uint16_t h0 = bias ? bf16_from_acc_pow2_bias_general(v0, ea, p.ew[col], p.bias[col])
+                           : bf16_from_acc_pow2(v0, ea, p.ew[col]);
         uint16_t* C = reinterpret_cast<uint16_t*>(p.C) + (int64_t)row * p.ldc + col;
         if (two) {
-            uint16_t h1 = bf16_from_acc_pow2(v1, ea, p.ew[col + 1]);
+            uint16_t h1 = bias ? bf16_from_acc_pow2_bias_general(v1, ea, p.ew[col + 1], p.bias[col + 1])
+                               : bf16_from_acc_pow2(v1, ea, p.ew[col + 1]);
             *reinterpret_cast<uint32_t*>(C) = (uint32_t)h0 | ((uint32_t)h1 << 16);
         } else {
             C[0] = h0;
@@ -259,8 +262,8 @@ cudaError_t igemm_launch(const IGemmArgs& a_in, void* ws, cudaStream_t s) {
     if (a.M == 0 || a.N == 0) return cudaSuccess;
     if (use_skinny(a.M, a.K)) {
         if (a.nseg != 1) return cudaErrorInvalidValue;
-        return skinny_launch(a.seg[0].A, a.lda, a.seg[0].W, a.ldw, a.ea, a.ew, a.C, a.ldc, a.mode, a.M, a.N, a.K,
-                             a.split, ws, s);
+        return skinny_launch(a.seg[0].A, a.lda, a.seg[0].W, a.ldw, a.ea, a.ew, a.bias, a.C, a.ldc, a.mode, a.M, a.N,
+                             a.K, a.split, ws, s);
     }
     if (a.split > 1) {
         size_t accb = (((size_t)a.M * a.N * sizeof(int32_t)) + 255) & ~(size_t)255;

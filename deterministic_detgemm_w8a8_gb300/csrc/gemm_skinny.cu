@@ -71,9 +71,10 @@ struct SkArgs {
     int nblocks;        // 128-row blocks of W
     const int32_t* ea;
     const int32_t* ew;
+    const uint16_t* bias;  // [N] bf16 bits (EPI_BF16_POW2_BIAS)
     uint16_t* C;
     int64_t ldc;
-    int mode;           // EPI_BF16_POW2 or EPI_STORE_I32
+    int mode;           // EPI_BF16_POW2, EPI_BF16_POW2_BIAS or EPI_STORE_I32
     int32_t* ws_acc;    // [N x M] exact sums (token-contiguous: one warp atomic covers 8
                         // consecutive tokens of 4 columns)
 };
@@ -169,12 +170,15 @@ __device__ __forceinline__ void i8x16_to_f16x16(const uint4& v, uint32_t (&h)[8]
 __device__ __forceinline__ void store_pair(const SkArgs& p, int row, int col, int32_t v0, int32_t v1) {
     if (row >= p.M || col >= p.N) return;
     const bool two = col + 1 < p.N;
-    if (p.mode == EPI_BF16_POW2) {
+    if (p.mode != EPI_STORE_I32) {
         const int32_t ea = p.ea[row];
         uint16_t* C = p.C + (int64_t)row * p.ldc + col;
-        const uint16_t h0 = bf16_from_acc_pow2(v0, ea, p.ew[col]);
+        const bool bias = p.mode == EPI_BF16_POW2_BIAS;
+        const uint16_t h0 = bias ? bf16_from_acc_pow2_bias_general(v0, ea, p.ew[col], p.bias[col])
+                                 : bf16_from_acc_pow2(v0, ea, p.ew[col]);
         if (two) {
-            const uint16_t h1 = bf16_from_acc_pow2(v1, ea, p.ew[col + 1]);
+            const uint16_t h1 = bias ? bf16_from_acc_pow2_bias_general(v1, ea, p.ew[col + 1], p.bias[col + 1])
+                                     : bf16_from_acc_pow2(v1, ea, p.ew[col + 1]);
             *reinterpret_cast<uint32_t*>(C) = (uint32_t)h0 | ((uint32_t)h1 << 16);
         } else {
             C[0] = h0;
@@ -755,8 +759,8 @@ size_t skinny_workspace_bytes(int M, int N, int K, int split) {
 }
 
 cudaError_t skinny_launch(const int8_t* A, int64_t lda, const int8_t* W, int64_t ldw, const int32_t* ea,
-                          const int32_t* ew, void* C, int64_t ldc, int mode, int M, int N, int K, int split, void* ws,
-                          cudaStream_t s) {
+                          const int32_t* ew, const uint16_t* bias, void* C, int64_t ldc, int mode, int M, int N, int K,
+                          int split, void* ws, cudaStream_t s) {
     (void)split;  // the kernel divides K among the SMs itself; the bits never depend on it
     if (M == 0 || N == 0) return cudaSuccess;
     if (!decode_path(M, K)) return cudaErrorInvalidValue;
@@ -769,6 +773,7 @@ cudaError_t skinny_launch(const int8_t* A, int64_t lda, const int8_t* W, int64_t
         a.K = K;
         a.ea = ea;
         a.ew = ew;
+        a.bias = bias;
         a.C = reinterpret_cast<uint16_t*>(C);
         a.ldc = ldc;
         a.mode = mode;
@@ -792,6 +797,7 @@ cudaError_t skinny_launch(const int8_t* A, int64_t lda, const int8_t* W, int64_t
     a.nblocks = (N + SK_ROWS - 1) / SK_ROWS;
     a.ea = ea;
     a.ew = ew;
+    a.bias = bias;
     a.C = reinterpret_cast<uint16_t*>(C);
     a.ldc = ldc;
     a.mode = mode;

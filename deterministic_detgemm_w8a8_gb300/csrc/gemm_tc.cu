@@ -158,7 +158,7 @@ __device__ __forceinline__ void st_shared16(uint32_t addr, uint32_t a, uint32_t 
     asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
-template <int COLS>
+template <int COLS, bool kBias>
 __device__ __forceinline__ void finish_rows(const TcArgs& p, const CUtensorMap* tmC, uint8_t* slot, int d, int row0,
                                             int col0, const int32_t (&acc)[COLS], bool& pending) {
     constexpr int PER = COLS / 32;
@@ -166,13 +166,16 @@ __device__ __forceinline__ void finish_rows(const TcArgs& p, const CUtensorMap* 
     const int row = row0 + lane;
     const uint32_t sbase = smem_addr(slot) + (uint32_t)lane * 128u;
     const int sw = lane & 7;
-    if (p.mode == EPI_BF16_POW2) {
+    if (p.mode != EPI_STORE_I32) {
+        constexpr bool with_bias = kBias;
         int32_t ewv[PER];
+        uint32_t bv[PER];
         bool inrange = true;
 #pragma unroll
         for (int i = 0; i < PER; ++i) {
             const int c = col0 + PER * lane + i;
             ewv[i] = c < p.N ? __ldg(p.ew + c) : 0;
+            bv[i] = with_bias && c < p.N ? (uint32_t)__ldg(p.bias + c) : 0u;
             inrange &= ewv[i] >= -60 && ewv[i] <= 40;
         }
         const int32_t ea = row < p.M ? __ldg(p.ea + row) : 0;
@@ -189,7 +192,21 @@ __device__ __forceinline__ void finish_rows(const TcArgs& p, const CUtensorMap* 
             for (int jj = 0; jj < 8; ++jj) {
                 const int j = 64 * hh + 8 * jj;
                 uint32_t w[4];
-                if (fast) {
+                if constexpr (with_bias) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int c = j + 2 * i;
+                        const float s0 = __shfl_sync(0xffffffffu, swv[c % PER], c / PER);
+                        const float s1 = __shfl_sync(0xffffffffu, swv[(c + 1) % PER], (c + 1) / PER);
+                        const int32_t e0 = __shfl_sync(0xffffffffu, ewv[c % PER], c / PER);
+                        const int32_t e1 = __shfl_sync(0xffffffffu, ewv[(c + 1) % PER], (c + 1) / PER);
+                        const uint32_t b0 = __shfl_sync(0xffffffffu, bv[c % PER], c / PER);
+                        const uint32_t b1 = __shfl_sync(0xffffffffu, bv[(c + 1) % PER], (c + 1) / PER);
+                        w[i] = (uint32_t)bf16_from_acc_pow2_bias(acc[c], sa, s0, ea, e0, fast, (uint16_t)b0) |
+                               ((uint32_t)bf16_from_acc_pow2_bias(acc[c + 1], sa, s1, ea, e1, fast, (uint16_t)b1)
+                                << 16);
+                    }
+                } else if (fast) {
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         const int c = j + 2 * i;
@@ -292,8 +309,10 @@ static_assert(2 * 256 <= 512 && 2 * 192 <= 512, "two accumulator buffers in TMEM
 
 // kSplit: the instantiation for split > 1 (the split epilogue's registers stay out of the
 // other one); kGroups: several plane groups (the Ozaki diagonals), units assigned through
-// TcArgs::extra_of (one group: plain round-robin, with no table walk in the loops)
-template <int BNT, bool kSplit, bool kGroups>
+// TcArgs::extra_of (one group: plain round-robin, with no table walk in the loops); kBias:
+// the epilogue adds a bf16 bias per column before its rounding (EPI_BF16_POW2_BIAS; its
+// registers stay out of the other instantiations)
+template <int BNT, bool kSplit, bool kGroups, bool kBias>
 __global__ void __launch_bounds__(Geo<BNT>::THREADS, 1)
     tc2_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmS,
@@ -489,7 +508,7 @@ __global__ void __launch_bounds__(Geo<BNT>::THREADS, 1)
             const int row = un.tm * 256 + (int)rank * 128 + q * 32 + lane;
             const int col0 = un.tn * BN + h * COLS;
             if constexpr (!kSplit) {
-                finish_rows(p, &tmC, slot, un.d, row - lane, col0, acc, pending);
+                finish_rows<COLS, kBias>(p, &tmC, slot, un.d, row - lane, col0, acc, pending);
                 continue;
             }
             // a K part: add the exact partial into the tile's slot of the split workspace with
@@ -522,7 +541,7 @@ __global__ void __launch_bounds__(Geo<BNT>::THREADS, 1)
                 acc[4 * i + 2] = v.z;
                 acc[4 * i + 3] = v.w;
             }
-            finish_rows(p, &tmC, slot, un.d, row - lane, col0, acc, pending);
+            finish_rows<COLS, kBias>(p, &tmC, slot, un.d, row - lane, col0, acc, pending);
         }
         // the slot's last stores complete before the CTA's shared memory goes away
         if (pending && lane == 0) bulk_wait_all();
@@ -580,7 +599,7 @@ cudaError_t make_out_map(CUtensorMap* m, const TcArgs& a) {
     PFN_cuTensorMapEncodeTiled_v12000 enc;
     cudaError_t e = get_encode(&enc);
     if (e != cudaSuccess) return e;
-    const bool bf = a.mode == EPI_BF16_POW2;
+    const bool bf = a.mode != EPI_STORE_I32;
     const cuuint64_t es = bf ? 2 : 4;
     const int planes = bf ? 1 : a.ndiag;
     const cuuint64_t row_bytes = (cuuint64_t)a.ldc * es;
@@ -635,9 +654,9 @@ static cudaError_t make_ws_map(CUtensorMap* m, void* base, int cut) {
 namespace {
 int g_max_clusters[64][2];  // per device: 256-wide, 192-wide tiles
 
-template <int BNT, bool kSplit, bool kGroups>
+template <int BNT, bool kSplit, bool kGroups, bool kBias>
 cudaError_t opt_in() {
-    return cudaFuncSetAttribute(tc2_gemm_kernel<BNT, kSplit, kGroups>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    return cudaFuncSetAttribute(tc2_gemm_kernel<BNT, kSplit, kGroups, kBias>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 Geo<BNT>::SMEM_BYTES);
 }
 
@@ -655,7 +674,7 @@ int occupancy_clusters() {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, tc2_gemm_kernel<BNT, false, false>, &cfg) != cudaSuccess || n <= 0) n = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, tc2_gemm_kernel<BNT, false, false, false>, &cfg) != cudaSuccess || n <= 0) n = 1;
     return n;
 }
 
@@ -667,8 +686,9 @@ int max_pair_clusters(int bn) {
     if (dev < 0 || dev >= 64) return 1;
     std::lock_guard<std::mutex> lock(g_tc_mutex);
     if (g_max_clusters[dev][0] == 0) {
-        if (opt_in<256, false, false>() != cudaSuccess || opt_in<256, false, true>() != cudaSuccess ||
-            opt_in<256, true, true>() != cudaSuccess || opt_in<192, false, false>() != cudaSuccess)
+        if (opt_in<256, false, false, false>() != cudaSuccess || opt_in<256, false, true, false>() != cudaSuccess ||
+            opt_in<256, true, true, false>() != cudaSuccess || opt_in<192, false, false, false>() != cudaSuccess ||
+            opt_in<256, false, false, true>() != cudaSuccess || opt_in<256, true, true, true>() != cudaSuccess)
             return 0;
         g_max_clusters[dev][0] = occupancy_clusters<256>();
         g_max_clusters[dev][1] = occupancy_clusters<192>();
@@ -724,7 +744,7 @@ static void assign_leftovers(TcArgs& a, int C) {
     }
 }
 
-template <int BNT, bool kSplit, bool kGroups>
+template <int BNT, bool kSplit, bool kGroups, bool kBias>
 static cudaError_t launch_engine(const TcArgs& a, const CUtensorMap& tmA, const CUtensorMap& tmB,
                                  const CUtensorMap& tmC, const CUtensorMap& tmS, int clusters, cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};
@@ -741,7 +761,7 @@ static cudaError_t launch_engine(const TcArgs& a, const CUtensorMap& tmA, const 
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, tc2_gemm_kernel<BNT, kSplit, kGroups>, tmA, tmB, tmC, tmS, a);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, tc2_gemm_kernel<BNT, kSplit, kGroups, kBias>, tmA, tmB, tmC, tmS, a);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -751,7 +771,9 @@ cudaError_t tc_gemm_launch(const TcArgs& a0, const void* A16, int64_t lda, int a
     if (a0.M == 0 || a0.N == 0) return cudaSuccess;
     TcArgs a = a0;
     if (max_pair_clusters(256) <= 0) return cudaErrorInvalidConfiguration;
-    const int bn = choose_bn(a);
+    const bool bias = a.mode == EPI_BF16_POW2_BIAS;
+    if (bias && (a.ndiag != 1 || a.bias == nullptr)) return cudaErrorInvalidValue;
+    const int bn = bias ? 256 : choose_bn(a);
     set_tiles(a, kext, bn);
     CUtensorMap tmA, tmB, tmC;
     cudaError_t e = make_map(&tmA, A16, kext, lda, a.M, a_planes, 128);
@@ -777,10 +799,13 @@ cudaError_t tc_gemm_launch(const TcArgs& a0, const void* A16, int64_t lda, int a
     assign_leftovers(a, clusters);
     // split launches (and every multi-group launch) walk the assignment table; the one-group
     // unsplit ones keep a plain round-robin (the table walk's registers would spill there)
-    if (a.split > 1) return launch_engine<256, true, true>(a, tmA, tmB, tmC, tmS, clusters, s);
-    if (a.ndiag > 1) return launch_engine<256, false, true>(a, tmA, tmB, tmC, tmS, clusters, s);
-    if (bn == 192) return launch_engine<192, false, false>(a, tmA, tmB, tmC, tmS, clusters, s);
-    return launch_engine<256, false, false>(a, tmA, tmB, tmC, tmS, clusters, s);
+    // (the bias epilogue has 256-wide tiles only)
+    if (bias && a.split > 1) return launch_engine<256, true, true, true>(a, tmA, tmB, tmC, tmS, clusters, s);
+    if (bias) return launch_engine<256, false, false, true>(a, tmA, tmB, tmC, tmS, clusters, s);
+    if (a.split > 1) return launch_engine<256, true, true, false>(a, tmA, tmB, tmC, tmS, clusters, s);
+    if (a.ndiag > 1) return launch_engine<256, false, true, false>(a, tmA, tmB, tmC, tmS, clusters, s);
+    if (bn == 192) return launch_engine<192, false, false, false>(a, tmA, tmB, tmC, tmS, clusters, s);
+    return launch_engine<256, false, false, false>(a, tmA, tmB, tmC, tmS, clusters, s);
 }
 
 // Self-check of the bounded waits: one thread waits on an mbarrier that nothing ever

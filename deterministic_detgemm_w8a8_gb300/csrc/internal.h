@@ -13,7 +13,9 @@ struct Seg {
     const int8_t* W;
 };
 
-enum EpilogueMode : int { EPI_BF16_POW2 = 0, EPI_STORE_I32 = 1 };
+// EPI_BF16_POW2_BIAS: as EPI_BF16_POW2 with a bf16 bias per output column added to the
+// exactly scaled accumulator before the one rounding.
+enum EpilogueMode : int { EPI_BF16_POW2 = 0, EPI_STORE_I32 = 1, EPI_BF16_POW2_BIAS = 2 };
 
 constexpr int kMaxSeg = 9;  // an Ozaki diagonal holds at most nslices (<= 9) slice pairs
 
@@ -26,6 +28,7 @@ struct IGemmArgs {
     int mode;             // EpilogueMode
     const int32_t* ea;    // [M] (bf16 mode)
     const int32_t* ew;    // [N] (bf16 mode)
+    const uint16_t* bias; // [N] bf16 bits (bias mode)
     void* C;              // bf16 bits or int32
     int64_t ldc;
     int32_t* ws_acc;      // [M x N] int32, zero on entry (split > 1)
@@ -37,8 +40,8 @@ struct IGemmArgs {
 bool decode_path(int M, int K);
 size_t skinny_workspace_bytes(int M, int N, int K, int split);
 cudaError_t skinny_launch(const int8_t* A, int64_t lda, const int8_t* W, int64_t ldw, const int32_t* ea,
-                          const int32_t* ew, void* C, int64_t ldc, int mode, int M, int N, int K, int split, void* ws,
-                          cudaStream_t s);
+                          const int32_t* ew, const uint16_t* bias, void* C, int64_t ldc, int mode, int M, int N, int K,
+                          int split, void* ws, cudaStream_t s);
 cudaError_t skinny_take_status(uint32_t* bits);
 
 // Integer GEMM on the mma.sync int8 path (exact int32 accumulation); decode_path problems
@@ -101,6 +104,7 @@ struct TcArgs {
     int mode;                  // EpilogueMode
     const int32_t* ea;
     const int32_t* ew;
+    const uint16_t* bias;      // [N] bf16 bits (EPI_BF16_POW2_BIAS)
     void* C;                   // bf16 [M x ldc], or int32 planes [ndiag][c_plane]
     int64_t ldc;
     int64_t c_plane;           // elements between int32 output planes

@@ -110,6 +110,23 @@ DETGEMM_API detgemm_status detgemm_w8a8(const int8_t* A, int64_t lda, const int8
 DETGEMM_API size_t detgemm_w8a8_workspace_size(int M, int N, int K, int split_k);
 
 /*
+ * W8A8 linear layer with a bias, still rounded once [P4 §II "Pipeline and alibi": the
+ * epilogue is the single rounding of the exactly scaled int32 accumulator; the bias is
+ * added to that exact value before the rounding, not to the rounded output]:
+ *     C_ij = rne_bf16(acc_ij * 2^(ea_i + ew_j) + b_j)
+ * The sum is exact (both terms are dyadic), so the bits depend on the operands alone,
+ * as for detgemm_w8a8. An exact zero sum gives +0; b_j = +-0 gives detgemm_w8a8's bits; a
+ * non-finite b_j (+-inf, NaN) is returned unchanged in column j.
+ *   bias  bf16 bit patterns [N], device memory, 2-byte aligned, not NULL
+ * Everything else (operands, split_k, scratch: detgemm_w8a8_workspace_size, errors) as
+ * detgemm_w8a8; a NULL bias is INVALID_ARG, an odd address ALIGNMENT.
+ */
+DETGEMM_API detgemm_status detgemm_w8a8_bias(const int8_t* A, int64_t lda, const int8_t* W, int64_t ldw,
+                                             const int32_t* ea, const int32_t* ew, const uint16_t* bias,
+                                             uint16_t* C, int64_t ldc, int M, int N, int K, int split_k,
+                                             void* ws, size_t ws_bytes, detgemm_stream_t stream);
+
+/*
  * The exact integer accumulator alone [P4 §II: the int32 accumulator is the same for
  * every tiling, split of K and summation order]:  C_ij = sum_k A_ik * W_jk (int32).
  * Same operands, layout, split_k and errors as detgemm_w8a8; C is int32 [M x N].
@@ -165,6 +182,20 @@ DETGEMM_API detgemm_status detgemm_linear_w8a8(const void* X, int x_dtype, int64
                                                int split_k, void* ws, size_t ws_bytes, detgemm_stream_t stream);
 
 DETGEMM_API size_t detgemm_linear_w8a8_workspace_size(int M, int N, int K, int split_k, int have_w16);
+
+/*
+ * detgemm_linear_w8a8 with a bias per output column, added before the one rounding as in
+ * detgemm_w8a8_bias:  C_ij = rne_bf16((sum_k Q_ik W_jk) * 2^(ea_i + ew_j) + b_j).
+ *   bias  bf16 bit patterns [N], device memory, 2-byte aligned, not NULL
+ * Scratch: detgemm_linear_w8a8_workspace_size; other arguments and errors as
+ * detgemm_linear_w8a8.
+ */
+DETGEMM_API detgemm_status detgemm_linear_w8a8_bias(const void* X, int x_dtype, int64_t ldx, int mode,
+                                                    const int8_t* W, int64_t ldw, const uint16_t* W16,
+                                                    int64_t ldw16, const int32_t* ew, const uint16_t* bias,
+                                                    uint16_t* C, int64_t ldc, int32_t* ea_out, int M, int N,
+                                                    int K, int split_k, void* ws, size_t ws_bytes,
+                                                    detgemm_stream_t stream);
 
 /*
  * Ozaki slicing of an fp32 matrix [P3 §3 (a): each operand becomes 7-bit integer

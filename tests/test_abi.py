@@ -94,6 +94,36 @@ def test_w8a8_argument_validation(lib):
     assert _w8a8(lib, N=0) == dg.OK
 
 
+def test_bias_entry_points_validate(lib):
+    import torch
+    import deterministic_detgemm_w8a8_gb300 as dg
+    wb = lib.detgemm_w8a8_bias
+
+    def b(bias=P, M=64, split=1, ws=P, wsb=1 << 30, K=512):
+        # A, lda, W, ldw, ea, ew, bias, C, ldc, M, N, K, split, ws, ws_bytes
+        return wb(P, 512, P, 512, P, P, bias, P, 256, M, 256, K, split, ws, wsb, None)
+
+    assert b(bias=None) == dg.ERR_INVALID_ARG
+    assert b(bias=P1) == dg.ERR_ALIGNMENT
+    assert b(K=0) == dg.ERR_INVALID_ARG
+    assert b(K=1024) == dg.ERR_INVALID_ARG  # lda 512 < K
+    assert b(K=131072) == dg.ERR_PRECONDITION
+    assert b(split=2, ws=None, wsb=0) == dg.ERR_WORKSPACE
+    assert b(M=0, bias=None) == dg.OK  # empty: nothing read
+    lb = lib.detgemm_linear_w8a8_bias
+    # X, dtype, ldx, mode, W, ldw, W16, ldw16, ew, bias, C, ldc, ea_out, M, N, K, split, ws, ws_bytes
+    assert lb(P, 0, 64, 0, P, 64, None, 0, P, None, P, 64, None, 100, 64, 64, 1, P, 1 << 30, None) == \
+        dg.ERR_INVALID_ARG
+    assert lb(P, 0, 64, 0, P, 64, None, 0, P, P1, P, 64, None, 100, 64, 64, 1, P, 1 << 30, None) == \
+        dg.ERR_ALIGNMENT
+    assert lb(P, 2, 64, 0, P, 64, None, 0, P, P, P, 64, None, 4, 64, 64, 1, P, 1 << 30, None) == dg.ERR_INVALID_ARG
+    assert lb(P, 0, 64, 0, P, 64, None, 0, P, P, P, 64, None, 0, 64, 64, 1, None, 0, None) == dg.OK
+    if not torch.cuda.is_available():
+        assert b() == dg.ERR_UNSUPPORTED_DEVICE
+        assert lb(P, 0, 64, 0, P, 64, None, 0, P, P, P, 64, None, 100, 64, 64, 1, P, 1 << 30, None) == \
+            dg.ERR_UNSUPPORTED_DEVICE
+
+
 def test_w8a8_valid_call_stops_at_device_check_without_gpu(lib):
     import torch
     import deterministic_detgemm_w8a8_gb300 as dg
