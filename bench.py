@@ -11,7 +11,8 @@ decode-shaped GEMM (M=16, N=4096, K=65536, split-K 8/16/32) in GB/s against the 
 roofline, the Ozaki fp32 GEMM (4096^3) in effective fp32 TFLOP/s next to the library fp32
 GEMM, the fp64-target Ozaki GEMM (4096^3) next to the library fp64 GEMM, the fused linear layer
 on bf16 activations at the FFN gate/up size, the sweep linear (K=2048, N=6144) at
-M = 1, 7, 64, 257, 2048, and the tiny workload's latency.
+M = 1, 7, 64, 257, 2048, the biased epilogue (a bf16 bias per column added before the one
+rounding) beside the unbiased one on four of these shapes, and the tiny workload's latency.
 
 Timing: W warm-up steps, then K timed steps; L2 is flushed before every timed step,
 outside the timed events, by a 256 MiB write followed by a 256 MiB read of another buffer
@@ -47,7 +48,7 @@ OPS_STEP = 2.0 * M_FFN * (N1 * K1 + N2 * K2)
 # FFN GEMMs (profiles/tc2_gemm_kernel_ffn_gate_up.md, profiles/launches_ffn_tc2.md), keyed
 # by a digest of the engine source so that a changed kernel reports null, not stale counters
 PROFILED_TRAFFIC = {
-    "00eb2364097789cf": {"gate_up": 478853632 + 182162688, "down": 897511168 + 62855168},
+    "1213eebeb3d4d708": {"gate_up": 480365824 + 182138880, "down": 897600256 + 63176704},
 }
 
 
@@ -537,6 +538,24 @@ def extras(dg, torch, dev, pk, flush):
         sweep[str(m)] = {"us": round(ms * 1e3, 1), "TOPS": round(2.0 * m * 6144 * 2048 / (ms * 1e-3) / 1e12, 1),
                          "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1)}
     res["sweep_N6144_K2048"] = sweep
+    # the biased epilogue (a bf16 bias per column added before the one rounding) beside the
+    # unbiased one: the FFN gate/up GEMM, the sweep at M = 2048 and 64, the decode workload
+    rng_b = torch.Generator(device="cpu").manual_seed(7)
+    cases = [("ffn_gate_up", synthetic.ffn_gate_up(), 1), ("sweep_M2048", synthetic.sweep(2048), 1),
+             ("sweep_M64", synthetic.sweep(64), 1),
+             ("skinny_M16_K65536", synthetic.skinny(), 16)]
+    bias_res = {}
+    for name, ops_np, split in cases:
+        A, W, ea, ew = (tdev(np.ascontiguousarray(x)) for x in ops_np)
+        m, n = A.shape[0], W.shape[0]
+        C = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+        b = (torch.randn(n, generator=rng_b) * 2.0 ** -6).to(torch.bfloat16).to(dev)
+        wsb = torch.empty(max(dg.w8a8_workspace_size(m, n, A.shape[1], split), 1), dtype=torch.uint8, device=dev)
+        ms0 = _time(torch, lambda: dg.w8a8(A, W, ea, ew, split_k=split, out=C, ws=wsb), flush)
+        ms1 = _time(torch, lambda: dg.w8a8(A, W, ea, ew, split_k=split, out=C, ws=wsb, bias=b), flush)
+        bias_res[name] = {"unbiased_us": round(ms0 * 1e3, 1), "biased_us": round(ms1 * 1e3, 1)}
+        del A, W, ea, ew, C, wsb
+    res["bias_epilogue"] = bias_res
     # the tiny workload (64 x 256 x 512): launch-latency bound
     A, W, ea, ew = (tdev(x) for x in synthetic.tiny())
     C = torch.empty((64, 256), dtype=torch.bfloat16, device=dev)

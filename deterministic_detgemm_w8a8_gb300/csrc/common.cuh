@@ -177,30 +177,36 @@ static __device__ __noinline__ uint16_t bf16_from_acc_pow2_bias_general(int32_t 
     return bf16_from_i64_pow2(S, X);
 }
 
-// Fast form for |acc| < 2^24, E = ea + ew in [-120, 80] (passed as the exact scales sa =
-// 2^ea, sw = 2^ew) and |b| < 2^64: x = acc * sa * sw is an exact fp32 number, the sum
-// x + b is split exactly into s + t (two-sum; no overflow in this range), the sum is
-// rounded to odd at 24 bits (s when t == 0; otherwise the fp32 number next to the sum
-// toward zero with its last bit set) and that is rounded to nearest-even at 8 bits. Rounding
-// to odd at 24 >= 8 + 2 bits and then to nearest at 8 bits equals one rounding to nearest,
-// so the result is that of the general form. Any other input takes the general form.
-__device__ __forceinline__ uint16_t bf16_from_acc_pow2_bias(int32_t acc, float sa, float sw, int32_t ea, int32_t ew,
-                                                            bool fast_exp, uint16_t b) {
-    const uint32_t ua = acc < 0 ? 0u - (uint32_t)acc : (uint32_t)acc;
-    if (!fast_exp || ua >= (1u << 24) || ((b >> 7) & 0xFFu) >= 191u)
-        return bf16_from_acc_pow2_bias_general(acc, ea, ew, b);
-    const float x = __fmul_rn(__fmul_rn(__int2float_rn(acc), sa), sw);
-    const float bv = __uint_as_float((uint32_t)b << 16);
-    const float s = __fadd_rn(x, bv);
-    const float bb = __fsub_rn(s, x);
-    const float t = __fadd_rn(__fsub_rn(x, __fsub_rn(s, bb)), __fsub_rn(bv, bb));
-    uint32_t sb = __float_as_uint(s);
-    if (t != 0.0f) {
-        if ((t < 0.0f) != (s < 0.0f)) sb -= 1;  // s was rounded away from zero: step back
-        sb |= 1u;
-    }
-    const __nv_bfloat16 h = __float2bfloat16_rn(__uint_as_float(sb));
+// Fast form: sc = 2^(ea + ew) as an fp32 number with ea + ew in [-120, 80], |acc| < 2^24
+// and |b| < 2^64. Then x = acc * sc is an exact fp32 number and the sum x + b is rounded
+// both down and up: equal results mean the sum is exact (an exact zero comes out as +0 from
+// the upward rounding); otherwise the one toward zero with its last bit set is the sum
+// rounded to odd at 24 bits. Rounding to odd at 24 >= 8 + 2 bits and then to nearest-even at
+// 8 bits equals one rounding to nearest, so the result is that of the general form. (A sum
+// in the fp32 subnormal range is a multiple of 2^-133, hence exact.)
+__device__ __forceinline__ uint16_t bf16_from_scaled_bias_ro(int32_t acc, float sc, uint32_t b) {
+    const float x = __fmul_rn(__int2float_rn(acc), sc);
+    const float bv = __uint_as_float(b << 16);
+    const float lo = __fadd_rd(x, bv);
+    const float hi = __fadd_ru(x, bv);
+    const uint32_t r = lo == hi ? __float_as_uint(hi) : (__float_as_uint(lo >= 0.0f ? lo : hi) | 1u);
+    const __nv_bfloat16 h = __float2bfloat16_rn(__uint_as_float(r));
     return *reinterpret_cast<const uint16_t*>(&h);
+}
+
+// The fast form's scale for one output: 2^(ea + ew) when ea and ew lie in [-60, 40] and the
+// bias is below 2^64 in magnitude, else 0 (the general form).
+__device__ __forceinline__ float bias_fast_scale(int32_t ea, int32_t ew, uint32_t b) {
+    const bool ok = ea >= -60 && ea <= 40 && ew >= -60 && ew <= 40 && ((b >> 7) & 0xFFu) < 191u;
+    return ok ? __uint_as_float((uint32_t)(ea + ew + 127) << 23) : 0.0f;
+}
+
+// rne_bf16(acc * 2^(ea + ew) + b): the fast form where it applies, else the general one.
+__device__ __forceinline__ uint16_t bf16_from_acc_pow2_bias(int32_t acc, int32_t ea, int32_t ew, uint32_t b) {
+    const float sc = bias_fast_scale(ea, ew, b);
+    const uint32_t ua = acc < 0 ? 0u - (uint32_t)acc : (uint32_t)acc;
+    if (sc != 0.0f && ua < (1u << 24)) return bf16_from_scaled_bias_ro(acc, sc, b);
+    return bf16_from_acc_pow2_bias_general(acc, ea, ew, (uint16_t)b);
 }
 
 // Exact power of two as a double for |k| <= 1022.

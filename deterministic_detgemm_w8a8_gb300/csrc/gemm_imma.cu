@@ -68,11 +68,11 @@ __device__ __forceinline__ void store_pair(const IGemmArgs& p, int row, int col,
     if (p.mode != EPI_STORE_I32) {
         int32_t ea = p.ea[row];
         const bool bias = p.mode == EPI_BF16_POW2_BIAS;
-        uint16_t h0 = bias ? bf16_from_acc_pow2_bias_general(v0, ea, p.ew[col], p.bias[col])
+        uint16_t h0 = bias ? bf16_from_acc_pow2_bias(v0, ea, p.ew[col], p.bias[col])
                            : bf16_from_acc_pow2(v0, ea, p.ew[col]);
         uint16_t* C = reinterpret_cast<uint16_t*>(p.C) + (int64_t)row * p.ldc + col;
         if (two) {
-            uint16_t h1 = bias ? bf16_from_acc_pow2_bias_general(v1, ea, p.ew[col + 1], p.bias[col + 1])
+            uint16_t h1 = bias ? bf16_from_acc_pow2_bias(v1, ea, p.ew[col + 1], p.bias[col + 1])
                                : bf16_from_acc_pow2(v1, ea, p.ew[col + 1]);
             *reinterpret_cast<uint32_t*>(C) = (uint32_t)h0 | ((uint32_t)h1 << 16);
         } else {

@@ -167,7 +167,6 @@ __device__ __forceinline__ void finish_rows(const TcArgs& p, const CUtensorMap* 
     const uint32_t sbase = smem_addr(slot) + (uint32_t)lane * 128u;
     const int sw = lane & 7;
     if (p.mode != EPI_STORE_I32) {
-        constexpr bool with_bias = kBias;
         int32_t ewv[PER];
         uint32_t bv[PER];
         bool inrange = true;
@@ -175,7 +174,7 @@ __device__ __forceinline__ void finish_rows(const TcArgs& p, const CUtensorMap* 
         for (int i = 0; i < PER; ++i) {
             const int c = col0 + PER * lane + i;
             ewv[i] = c < p.N ? __ldg(p.ew + c) : 0;
-            bv[i] = with_bias && c < p.N ? (uint32_t)__ldg(p.bias + c) : 0u;
+            bv[i] = kBias && c < p.N ? (uint32_t)__ldg(p.bias + c) : 0u;
             inrange &= ewv[i] >= -60 && ewv[i] <= 40;
         }
         const int32_t ea = row < p.M ? __ldg(p.ea + row) : 0;
@@ -185,6 +184,16 @@ __device__ __forceinline__ void finish_rows(const TcArgs& p, const CUtensorMap* 
 #pragma unroll
         for (int i = 0; i < PER; ++i) swv[i] = exp2_f32(fast ? ewv[i] : 0);
         const float sa = exp2_f32(fast ? ea : 0);
+        float bsw[PER];
+        float sa_b = 0.0f;
+        if constexpr (kBias) {
+#pragma unroll
+            for (int i = 0; i < PER; ++i) {
+                const bool ok = ewv[i] >= -60 && ewv[i] <= 40 && ((bv[i] >> 7) & 0xFFu) < 191u;
+                bsw[i] = ok ? exp2_f32(ewv[i]) : 0.0f;
+            }
+            sa_b = ea >= -60 && ea <= 40 ? exp2_f32(ea) : 0.0f;
+        }
 #pragma unroll
         for (int hh = 0; hh < COLS / 64; ++hh) {
             slot_acquire(pending);
@@ -192,19 +201,34 @@ __device__ __forceinline__ void finish_rows(const TcArgs& p, const CUtensorMap* 
             for (int jj = 0; jj < 8; ++jj) {
                 const int j = 64 * hh + 8 * jj;
                 uint32_t w[4];
-                if constexpr (with_bias) {
+                if constexpr (kBias) {
+                    // the fast form where the scale allows it (bsw: the column's 2^ew, or 0
+                    // when its exponent or bias needs the general form; sa_b: the row's 2^ea,
+                    // or 0), else the general form (its column exponent read again; 0 past N)
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         const int c = j + 2 * i;
-                        const float s0 = __shfl_sync(0xffffffffu, swv[c % PER], c / PER);
-                        const float s1 = __shfl_sync(0xffffffffu, swv[(c + 1) % PER], (c + 1) / PER);
-                        const int32_t e0 = __shfl_sync(0xffffffffu, ewv[c % PER], c / PER);
-                        const int32_t e1 = __shfl_sync(0xffffffffu, ewv[(c + 1) % PER], (c + 1) / PER);
+                        const float s0 = __shfl_sync(0xffffffffu, bsw[c % PER], c / PER);
+                        const float s1 = __shfl_sync(0xffffffffu, bsw[(c + 1) % PER], (c + 1) / PER);
                         const uint32_t b0 = __shfl_sync(0xffffffffu, bv[c % PER], c / PER);
                         const uint32_t b1 = __shfl_sync(0xffffffffu, bv[(c + 1) % PER], (c + 1) / PER);
-                        w[i] = (uint32_t)bf16_from_acc_pow2_bias(acc[c], sa, s0, ea, e0, fast, (uint16_t)b0) |
-                               ((uint32_t)bf16_from_acc_pow2_bias(acc[c + 1], sa, s1, ea, e1, fast, (uint16_t)b1)
-                                << 16);
+                        const float sc0 = sa_b * s0, sc1 = sa_b * s1;
+                        const uint32_t u0 = acc[c] < 0 ? 0u - (uint32_t)acc[c] : (uint32_t)acc[c];
+                        const uint32_t u1 = acc[c + 1] < 0 ? 0u - (uint32_t)acc[c + 1] : (uint32_t)acc[c + 1];
+                        uint32_t h0, h1;
+                        if (sc0 != 0.0f && u0 < (1u << 24)) {
+                            h0 = bf16_from_scaled_bias_ro(acc[c], sc0, b0);
+                        } else {
+                            const int32_t e = col0 + c < p.N ? __ldg(p.ew + col0 + c) : 0;
+                            h0 = bf16_from_acc_pow2_bias_general(acc[c], ea, e, (uint16_t)b0);
+                        }
+                        if (sc1 != 0.0f && u1 < (1u << 24)) {
+                            h1 = bf16_from_scaled_bias_ro(acc[c + 1], sc1, b1);
+                        } else {
+                            const int32_t e = col0 + c + 1 < p.N ? __ldg(p.ew + col0 + c + 1) : 0;
+                            h1 = bf16_from_acc_pow2_bias_general(acc[c + 1], ea, e, (uint16_t)b1);
+                        }
+                        w[i] = h0 | (h1 << 16);
                     }
                 } else if (fast) {
 #pragma unroll
@@ -688,7 +712,8 @@ int max_pair_clusters(int bn) {
     if (g_max_clusters[dev][0] == 0) {
         if (opt_in<256, false, false, false>() != cudaSuccess || opt_in<256, false, true, false>() != cudaSuccess ||
             opt_in<256, true, true, false>() != cudaSuccess || opt_in<192, false, false, false>() != cudaSuccess ||
-            opt_in<256, false, false, true>() != cudaSuccess || opt_in<256, true, true, true>() != cudaSuccess)
+            opt_in<256, false, false, true>() != cudaSuccess || opt_in<256, true, true, true>() != cudaSuccess ||
+            opt_in<192, false, false, true>() != cudaSuccess)
             return 0;
         g_max_clusters[dev][0] = occupancy_clusters<256>();
         g_max_clusters[dev][1] = occupancy_clusters<192>();
@@ -773,7 +798,7 @@ cudaError_t tc_gemm_launch(const TcArgs& a0, const void* A16, int64_t lda, int a
     if (max_pair_clusters(256) <= 0) return cudaErrorInvalidConfiguration;
     const bool bias = a.mode == EPI_BF16_POW2_BIAS;
     if (bias && (a.ndiag != 1 || a.bias == nullptr)) return cudaErrorInvalidValue;
-    const int bn = bias ? 256 : choose_bn(a);
+    const int bn = bias && a.split > 1 ? 256 : choose_bn(a);
     set_tiles(a, kext, bn);
     CUtensorMap tmA, tmB, tmC;
     cudaError_t e = make_map(&tmA, A16, kext, lda, a.M, a_planes, 128);
@@ -799,8 +824,9 @@ cudaError_t tc_gemm_launch(const TcArgs& a0, const void* A16, int64_t lda, int a
     assign_leftovers(a, clusters);
     // split launches (and every multi-group launch) walk the assignment table; the one-group
     // unsplit ones keep a plain round-robin (the table walk's registers would spill there)
-    // (the bias epilogue has 256-wide tiles only)
+    // (split launches of the bias epilogue have 256-wide tiles)
     if (bias && a.split > 1) return launch_engine<256, true, true, true>(a, tmA, tmB, tmC, tmS, clusters, s);
+    if (bias && bn == 192) return launch_engine<192, false, false, true>(a, tmA, tmB, tmC, tmS, clusters, s);
     if (bias) return launch_engine<256, false, false, true>(a, tmA, tmB, tmC, tmS, clusters, s);
     if (a.split > 1) return launch_engine<256, true, true, false>(a, tmA, tmB, tmC, tmS, clusters, s);
     if (a.ndiag > 1) return launch_engine<256, false, true, false>(a, tmA, tmB, tmC, tmS, clusters, s);
