@@ -48,7 +48,7 @@ OPS_STEP = 2.0 * M_FFN * (N1 * K1 + N2 * K2)
 # FFN GEMMs (profiles/tc2_gemm_kernel_ffn_gate_up.md, profiles/launches_ffn_tc2.md), keyed
 # by a digest of the engine source so that a changed kernel reports null, not stale counters
 PROFILED_TRAFFIC = {
-    "1213eebeb3d4d708": {"gate_up": 480365824 + 182138880, "down": 897600256 + 63176704},
+    "e019bf955e54fe7d": {"gate_up": 479119872 + 182585600, "down": 897748480 + 62810112},
 }
 
 

@@ -312,14 +312,18 @@ __device__ __forceinline__ void reduce_rows(const CUtensorMap* tmS, uint8_t* slo
 //   tempty[b] in the even CTA: all 16 epilogue warps of the pair arrive on it
 // ------------------------------------------------------------------------------------
 // Tile geometry by tile width BN: 256 (eight epilogue warps of 32 rows x 128 columns) or
-// 192 (twelve of 32 x 64), chosen by choose_bn; B rows per CTA are BN / 2.
-template <int BNT>
+// 192 (twelve of 32 x 64), chosen by choose_bn; B rows per CTA are BN / 2. kNarrow: 256-wide
+// tiles with sixteen epilogue warps of 32 x 64 and five stages (the same shared memory, 96
+// registers a thread): a tile's finish runs on twice the warps, which pays where the finish
+// is exposed (short K, few rounds, the biased epilogue) and costs a few per cent of the main
+// loop elsewhere.
+template <int BNT, bool kNarrow = false>
 struct Geo {
     static constexpr int BN = BNT;
-    static constexpr int COLS = BNT == 256 ? 128 : 64;  // columns per epilogue warp
+    static constexpr int COLS = BNT == 256 && !kNarrow ? 128 : 64;  // columns per epilogue warp
     static constexpr int EPI_WARPS = 4 * BNT / COLS;
     static constexpr int THREADS = 64 + 32 * EPI_WARPS;
-    static constexpr int STAGES = 6;
+    static constexpr int STAGES = EPI_WARPS > 12 ? 5 : 6;
     static constexpr int A_BYTES = 128 * BK * 2;
     static constexpr int B_BYTES = (BNT / 2) * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
@@ -328,20 +332,24 @@ struct Geo {
     static constexpr int SMEM_BYTES =
         STAGES * STAGE_BYTES + EPI_WARPS * SLOT_BYTES + 1024 /*alignment slack*/ + 256 /*barriers*/;
 };
-static_assert(Geo<256>::SMEM_BYTES <= 227 * 1024 && Geo<192>::SMEM_BYTES <= 227 * 1024, "shared memory");
+static_assert(Geo<256>::SMEM_BYTES <= 227 * 1024 && Geo<192>::SMEM_BYTES <= 227 * 1024 &&
+                  Geo<256, true>::SMEM_BYTES <= 227 * 1024,
+              "shared memory");
+
 static_assert(2 * 256 <= 512 && 2 * 192 <= 512, "two accumulator buffers in TMEM");
 
 // kSplit: the instantiation for split > 1 (the split epilogue's registers stay out of the
 // other one); kGroups: several plane groups (the Ozaki diagonals), units assigned through
 // TcArgs::extra_of (one group: plain round-robin, with no table walk in the loops); kBias:
 // the epilogue adds a bf16 bias per column before its rounding (EPI_BF16_POW2_BIAS; its
-// registers stay out of the other instantiations)
-template <int BNT, bool kSplit, bool kGroups, bool kBias>
-__global__ void __launch_bounds__(Geo<BNT>::THREADS, 1)
+// registers stay out of the other instantiations); kNarrow: the 256-wide geometry with
+// sixteen epilogue warps
+template <int BNT, bool kSplit, bool kGroups, bool kBias, bool kNarrow>
+__global__ void __launch_bounds__(Geo<BNT, kNarrow>::THREADS, 1)
     tc2_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmS,
                     const __grid_constant__ TcArgs p) {
-    typedef Geo<BNT> G;
+    typedef Geo<BNT, kNarrow> G;
     constexpr int BN = G::BN, COLS = G::COLS, EPI_WARPS = G::EPI_WARPS, P_STAGES = G::STAGES;
     constexpr int P_A_BYTES = G::A_BYTES, P_STAGE_BYTES = G::STAGE_BYTES, P_SLOT_BYTES = G::SLOT_BYTES;
     constexpr uint32_t P_IDESC = G::IDESC;
@@ -678,10 +686,10 @@ static cudaError_t make_ws_map(CUtensorMap* m, void* base, int cut) {
 namespace {
 int g_max_clusters[64][2];  // per device: 256-wide, 192-wide tiles
 
-template <int BNT, bool kSplit, bool kGroups, bool kBias>
+template <int BNT, bool kSplit, bool kGroups, bool kBias, bool kNarrow>
 cudaError_t opt_in() {
-    return cudaFuncSetAttribute(tc2_gemm_kernel<BNT, kSplit, kGroups, kBias>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                Geo<BNT>::SMEM_BYTES);
+    return cudaFuncSetAttribute(tc2_gemm_kernel<BNT, kSplit, kGroups, kBias, kNarrow>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, Geo<BNT, kNarrow>::SMEM_BYTES);
 }
 
 template <int BNT>
@@ -698,7 +706,7 @@ int occupancy_clusters() {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, tc2_gemm_kernel<BNT, false, false, false>, &cfg) != cudaSuccess || n <= 0) n = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, tc2_gemm_kernel<BNT, false, false, false, false>, &cfg) != cudaSuccess || n <= 0) n = 1;
     return n;
 }
 
@@ -710,10 +718,14 @@ int max_pair_clusters(int bn) {
     if (dev < 0 || dev >= 64) return 1;
     std::lock_guard<std::mutex> lock(g_tc_mutex);
     if (g_max_clusters[dev][0] == 0) {
-        if (opt_in<256, false, false, false>() != cudaSuccess || opt_in<256, false, true, false>() != cudaSuccess ||
-            opt_in<256, true, true, false>() != cudaSuccess || opt_in<192, false, false, false>() != cudaSuccess ||
-            opt_in<256, false, false, true>() != cudaSuccess || opt_in<256, true, true, true>() != cudaSuccess ||
-            opt_in<192, false, false, true>() != cudaSuccess)
+        if (opt_in<256, false, false, false, false>() != cudaSuccess ||
+            opt_in<256, false, false, false, true>() != cudaSuccess ||
+            opt_in<256, false, true, false, false>() != cudaSuccess ||
+            opt_in<256, true, true, false, false>() != cudaSuccess ||
+            opt_in<192, false, false, false, false>() != cudaSuccess ||
+            opt_in<256, false, false, true, true>() != cudaSuccess ||
+            opt_in<256, true, true, true, false>() != cudaSuccess ||
+            opt_in<192, false, false, true, false>() != cudaSuccess)
             return 0;
         g_max_clusters[dev][0] = occupancy_clusters<256>();
         g_max_clusters[dev][1] = occupancy_clusters<192>();
@@ -769,7 +781,7 @@ static void assign_leftovers(TcArgs& a, int C) {
     }
 }
 
-template <int BNT, bool kSplit, bool kGroups, bool kBias>
+template <int BNT, bool kSplit, bool kGroups, bool kBias, bool kNarrow>
 static cudaError_t launch_engine(const TcArgs& a, const CUtensorMap& tmA, const CUtensorMap& tmB,
                                  const CUtensorMap& tmC, const CUtensorMap& tmS, int clusters, cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};
@@ -781,12 +793,12 @@ static cudaError_t launch_engine(const TcArgs& a, const CUtensorMap& tmA, const 
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see griddepcontrol.wait
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.gridDim = dim3(2 * clusters, 1, 1);
-    cfg.blockDim = dim3(Geo<BNT>::THREADS, 1, 1);
-    cfg.dynamicSmemBytes = Geo<BNT>::SMEM_BYTES;
+    cfg.blockDim = dim3(Geo<BNT, kNarrow>::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = Geo<BNT, kNarrow>::SMEM_BYTES;
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, tc2_gemm_kernel<BNT, kSplit, kGroups, kBias>, tmA, tmB, tmC, tmS, a);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, tc2_gemm_kernel<BNT, kSplit, kGroups, kBias, kNarrow>, tmA, tmB, tmC, tmS, a);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -824,14 +836,20 @@ cudaError_t tc_gemm_launch(const TcArgs& a0, const void* A16, int64_t lda, int a
     assign_leftovers(a, clusters);
     // split launches (and every multi-group launch) walk the assignment table; the one-group
     // unsplit ones keep a plain round-robin (the table walk's registers would spill there)
-    // (split launches of the bias epilogue have 256-wide tiles)
-    if (bias && a.split > 1) return launch_engine<256, true, true, true>(a, tmA, tmB, tmC, tmS, clusters, s);
-    if (bias && bn == 192) return launch_engine<192, false, false, true>(a, tmA, tmB, tmC, tmS, clusters, s);
-    if (bias) return launch_engine<256, false, false, true>(a, tmA, tmB, tmC, tmS, clusters, s);
-    if (a.split > 1) return launch_engine<256, true, true, false>(a, tmA, tmB, tmC, tmS, clusters, s);
-    if (a.ndiag > 1) return launch_engine<256, false, true, false>(a, tmA, tmB, tmC, tmS, clusters, s);
-    if (bn == 192) return launch_engine<192, false, false, false>(a, tmA, tmB, tmC, tmS, clusters, s);
-    return launch_engine<256, false, false, false>(a, tmA, tmB, tmC, tmS, clusters, s);
+    // Unsplit one-group launches of 256-wide tiles take the sixteen-warp geometry where a
+    // tile's finish is exposed: always for the biased epilogue; otherwise for K <= 1024 (one
+    // TMEM chunk per tile) or at most 12288 K-columns per CTA pair in all (rounds x K; measured
+    // from 2048 x 4096 x 1024: 38 -> 31 us to 8192 x 6144 x 2048: 158 -> 160 us).
+    const long long rounds = (total + clusters - 1) / clusters;
+    const bool narrow = kext <= 1024 || rounds * kext <= 12288;
+    if (bias && a.split > 1) return launch_engine<256, true, true, true, false>(a, tmA, tmB, tmC, tmS, clusters, s);
+    if (bias && bn == 192) return launch_engine<192, false, false, true, false>(a, tmA, tmB, tmC, tmS, clusters, s);
+    if (bias) return launch_engine<256, false, false, true, true>(a, tmA, tmB, tmC, tmS, clusters, s);
+    if (a.split > 1) return launch_engine<256, true, true, false, false>(a, tmA, tmB, tmC, tmS, clusters, s);
+    if (a.ndiag > 1) return launch_engine<256, false, true, false, false>(a, tmA, tmB, tmC, tmS, clusters, s);
+    if (bn == 192) return launch_engine<192, false, false, false, false>(a, tmA, tmB, tmC, tmS, clusters, s);
+    if (narrow) return launch_engine<256, false, false, false, true>(a, tmA, tmB, tmC, tmS, clusters, s);
+    return launch_engine<256, false, false, false, false>(a, tmA, tmB, tmC, tmS, clusters, s);
 }
 
 // Self-check of the bounded waits: one thread waits on an mbarrier that nothing ever
