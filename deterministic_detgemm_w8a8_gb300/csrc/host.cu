@@ -4,7 +4,8 @@
 //
 // The rows of A are cut into chunks; chunk c's rows are copied in on one stream while
 // chunk c - 1 is computed on the caller's stream and chunk c - 2's result is copied out on
-// a third stream. Every chunk runs the same exact W8A8 path as detgemm_w8a8 on its rows
+// a third stream. The first chunk is half the size of the others, so that the copy-out
+// stream starts sooner, and the last one takes what is left. Every chunk runs the same exact W8A8 path as detgemm_w8a8 on its rows
 // ("Deterministic LLM Inference Across GPU Kernels ...", §II: the int32 accumulator and
 // so the bf16 result of a row do not depend on which rows are computed with it), so the
 // result bits are those of detgemm_w8a8 on the whole matrix.
@@ -165,12 +166,14 @@ detgemm_status detgemm_w8a8_host(const int8_t* A, int64_t lda, const int8_t* W, 
     // tensor-core path: the weight is widened once, then the chunks are pipelined
     uint16_t* W16 = reinterpret_cast<uint16_t*>(b + L.w16);
     CHK(widen_i8_f16_launch(Wd, L.K16, N, K, W16, L.Kp, s));
-    const int nchunks = (M + L.R - 1) / L.R;
     const size_t wsb = detgemm_w8a8_f16ops_workspace_size(L.R, N, K, 1);
-    for (int c = 0; c < nchunks; ++c) {
+    const int first = L.R / 2 / 256 * 256 > 256 ? L.R / 2 / 256 * 256 : 256;
+    int nchunks = 0;
+    for (int c = 0, r0 = 0; r0 < M; ++c) {
+        const int want = c == 0 && L.R < M ? first : L.R;
+        const int rows = M - r0 < want ? M - r0 : want;
+        nchunks = c + 1;
         const int sl = c % kSlots;
-        const int r0 = c * L.R;
-        const int rows = M - r0 < L.R ? M - r0 : L.R;
         int8_t* Ad = reinterpret_cast<int8_t*>(b + L.a[sl]);
         int32_t* ead = reinterpret_cast<int32_t*>(b + L.ea[sl]);
         uint16_t* A16 = reinterpret_cast<uint16_t*>(b + L.a16[sl]);
@@ -193,6 +196,7 @@ detgemm_status detgemm_w8a8_host(const int8_t* A, int64_t lda, const int8_t* W, 
         CHK(cudaMemcpy2DAsync(C + (int64_t)r0 * ldc, (size_t)ldc * 2, Cd, (size_t)L.N8 * 2, (size_t)N * 2, rows,
                               cudaMemcpyDeviceToHost, p->out));
         CHK(cudaEventRecord(p->outd[sl], p->out));
+        r0 += rows;
     }
     // the caller's stream completes only when every result has reached host memory
     for (int sl = 0; sl < kSlots && sl < nchunks; ++sl) CHK(cudaStreamWaitEvent(s, p->outd[sl], 0));
