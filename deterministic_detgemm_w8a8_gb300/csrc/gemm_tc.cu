@@ -810,6 +810,15 @@ cudaError_t tc_gemm_launch(const TcArgs& a0, const void* A16, int64_t lda, int a
     if (max_pair_clusters(256) <= 0) return cudaErrorInvalidConfiguration;
     const bool bias = a.mode == EPI_BF16_POW2_BIAS;
     if (bias && (a.ndiag != 1 || a.bias == nullptr)) return cudaErrorInvalidValue;
+    // split_k is an upper bound (the bits do not depend on it): more parts than fill the CTA
+    // pairs once only add rounds of partial tiles, so it is lowered until every part of every
+    // tile runs in one round and each part keeps at least 256 K (measured: at 16 tiles and
+    // K = 16384, 125 -> 90 us at 4 parts; at 192 tiles and K = 2048, 58 -> 291 us at 8)
+    if (a.split > 1) {
+        const long long tiles = (long long)a.ndiag * ((a.M + 255) / 256) * ((a.N + 255) / 256);
+        const int c256 = max_pair_clusters(256);
+        while (a.split > 1 && (tiles * a.split > c256 || kext / a.split < 256)) --a.split;
+    }
     const int bn = bias && a.split > 1 ? 256 : choose_bn(a);
     set_tiles(a, kext, bn);
     CUtensorMap tmA, tmB, tmC;

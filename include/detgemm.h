@@ -95,6 +95,9 @@ DETGEMM_API int detgemm_version(void);
  *            choose their own cut: K <= 4096 gives each CTA whole rows of W over all of
  *            K, longer K is divided among all SMs so that every SM streams the same
  *            number of bytes; split_k is then accepted but does not change the cut.
+ *            Elsewhere split_k is an upper bound: the tensor-core engine lowers it until
+ *            every K part of every output tile runs in one round of its CTA pairs and each
+ *            part keeps at least 256 K (more parts would only add rounds).
  *   ws       scratch of ws_bytes >= detgemm_w8a8_workspace_size(M, N, K, split_k)
  *            (nonzero for decode-shaped problems at any split_k, and for split_k > 1).
  * Empty problems (M == 0 or N == 0) return DETGEMM_OK and launch nothing.
