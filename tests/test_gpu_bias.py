@@ -1,7 +1,7 @@
 """GPU parity of the biased W8A8 epilogue, C = rne_bf16(acc * 2^(ea + ew) + b_j) rounded
 once ("Deterministic LLM Inference Across GPU Kernels ...", §II "Pipeline and alibi": the
 epilogue is the one rounding of the exactly scaled accumulator; the bias joins the exact
-value first), against the oracle bit for bit: the tensor-core engine (its fp32 two-sum
+value first), against the oracle bit for bit: the tensor-core engine (its fp32 round-down/up
 form and its integer form), split-K, the decode-shaped kernels (whole-K and split chain),
 and the fused linear layer with a bias; special biases (+-0, +-inf, NaN, subnormal,
 huge, the negated output) in some columns."""
@@ -86,7 +86,7 @@ def test_bias_extreme_exponents_and_large_accumulators(lib, dev, oracle_mod, M, 
     ea = rng.integers(-150, 70, M).astype(np.int32)
     ew = rng.integers(-60, 60, N).astype(np.int32)
     # in-range exponents for two whole warps of rows and one 128-column group, so that the
-    # engine's two-sum form meets large accumulators and hands them to the integer form
+    # engine's fast form meets large accumulators and hands them to the integer form
     ea[: min(M, 64)] = rng.integers(-20, -5, min(M, 64))
     ew[: min(N, 128)] = rng.integers(-20, -5, min(N, 128))
     bias = _bf16(rng.standard_normal(N).astype(np.float32) * np.exp2(rng.integers(-120, 120, N)).astype(np.float32))
