@@ -79,7 +79,8 @@ HostLayout host_layout(int M, int N, int K) {
     L.K16 = ((int64_t)K + 15) / 16 * 16;
     L.Kp = tc_padded_k(K);
     L.N8 = ((int64_t)N + 7) / 8 * 8;
-    // about four chunks, each a multiple of the engine's 256-row tile
+    // chunks of about a quarter of M (the first one half that; see below), each a multiple
+    // of the engine's 256-row tile
     L.R = L.tc ? (int)((((int64_t)M + 3) / 4 + 255) / 256 * 256) : M;
     size_t off = 0;
     L.w = off; off += up256((size_t)N * L.K16);
