@@ -10,6 +10,7 @@ Functions mirror the C entry points:
 
 * :func:`w8a8`           C = rne_bf16((A W^T) * 2^(ea_i + ew_j))      (bf16 out)
 * :func:`w8a8_host`      the same on host (pinned) tensors, copies overlapped with compute
+* :func:`w8a8_split_exact`  w8a8 with exactly the K cut asked for (invariance checks)
 * :func:`gemm_s8_i32`    C = A W^T, exact int32
 * :func:`quantize_pow2`  per-row power-of-two scale and int8 values
 * :func:`linear_w8a8`    quantize_pow2 of bf16/fp32 activations + w8a8, fused
@@ -67,6 +68,10 @@ SIGNATURES = {
     "detgemm_w8a8_f16ops": ([_P, _I64, _P, _I64, _P, _P, _P, _I64, _I32, _I32, _I32, _I32, _P, _SZ, _P], _I32),
     "detgemm_w8a8_f16ops_workspace_size": ([_I32, _I32, _I32, _I32], _SZ),
     "detgemm_selftest_timeout": ([_I32, _P], _I32),
+    "detgemm_w8a8_split_exact": ([_P, _I64, _P, _I64, _P, _P, _P, _I64, _I32, _I32, _I32, _I32, _P, _SZ, _P, _P],
+                                 _I32),
+    "detgemm_ozaki_f32_split_exact": ([_P, _I64, _P, _I64, _P, _I64, _I32, _I32, _I32, _I32, _I32, _I32, _P, _SZ,
+                                       _P, _P], _I32),
 }
 
 _lock = threading.Lock()
@@ -197,6 +202,29 @@ def w8a8(A, W, ea, ew, split_k: int = 1, out=None, ws=None, stream=None, bias=No
                           wsb.data_ptr() if wsb is not None else None, wsn, _stream(stream))
     _check(st, "detgemm_w8a8")
     return out
+
+
+def w8a8_split_exact(A, W, ea, ew, split_k: int, out=None, ws=None, stream=None):
+    """w8a8 with the K cut made exactly as asked (detgemm_w8a8_split_exact): returns
+    (C, parts_run), parts_run being the number of contiguous K parts the call ran."""
+    lib = load()
+    _req(A, torch.int8, "A"); _req(W, torch.int8, "W")
+    _req(ea, torch.int32, "ea"); _req(ew, torch.int32, "ew")
+    M, K = A.shape
+    N = W.shape[0]
+    if W.shape[1] != K or ea.shape != (M,) or ew.shape != (N,):
+        raise ValueError("shape mismatch")
+    if out is None:
+        out = empty2d(M, N, torch.bfloat16, A.device)
+    _req(out, torch.bfloat16, "out")
+    wsb, wsn = _workspace(w8a8_workspace_size(M, N, K, split_k), A.device, ws)
+    parts = ctypes.c_int(0)
+    st = lib.detgemm_w8a8_split_exact(A.data_ptr(), _ld(A), W.data_ptr(), _ld(W), ea.data_ptr(), ew.data_ptr(),
+                                      out.data_ptr(), _ld(out), M, N, K, split_k,
+                                      wsb.data_ptr() if wsb is not None else None, wsn, ctypes.byref(parts),
+                                      _stream(stream))
+    _check(st, "detgemm_w8a8_split_exact")
+    return out, parts.value
 
 
 def _req_host(t: torch.Tensor, dtype, name):
@@ -365,6 +393,29 @@ def ozaki_f32(A, B, nslices: int = 7, max_diag: int = 8, split_k: int = 1, out=N
                                wsb.data_ptr() if wsb is not None else None, wsn, _stream(stream))
     _check(st, "detgemm_ozaki_f32")
     return out
+
+
+def ozaki_f32_split_exact(A, B, split_k: int, nslices: int = 7, max_diag: int = 8, out=None, ws=None,
+                          stream=None):
+    """ozaki_f32 with every diagonal's K range cut into exactly split_k parts
+    (detgemm_ozaki_f32_split_exact): returns (C, parts_run)."""
+    lib = load()
+    _req(A, torch.float32, "A"); _req(B, torch.float32, "B")
+    M, K = A.shape
+    K2, N = B.shape
+    if K2 != K:
+        raise ValueError("shape mismatch")
+    if out is None:
+        out = empty2d(M, N, torch.float32, A.device)
+    _req(out, torch.float32, "out")
+    wsb, wsn = _workspace(ozaki_workspace_size(M, N, K, nslices, max_diag, split_k), A.device, ws)
+    parts = ctypes.c_int(0)
+    st = lib.detgemm_ozaki_f32_split_exact(A.data_ptr(), _ld(A), B.data_ptr(), _ld(B), out.data_ptr(), _ld(out),
+                                           M, N, K, nslices, max_diag, split_k,
+                                           wsb.data_ptr() if wsb is not None else None, wsn, ctypes.byref(parts),
+                                           _stream(stream))
+    _check(st, "detgemm_ozaki_f32_split_exact")
+    return out, parts.value
 
 
 def ozaki_combine(T, e, f, out=None, dtype=torch.float32, stream=None) -> torch.Tensor:

@@ -144,7 +144,7 @@ size_t detgemm_w8a8_workspace_size(int M, int N, int K, int split_k) {
 
 static detgemm_status run_tc(const int8_t* A, int64_t lda, const int8_t* W, int64_t ldw, const int32_t* ea,
                              const int32_t* ew, const uint16_t* bias, void* C, int64_t ldc, int mode, int M, int N, int K, int split_k,
-                             void* ws, cudaStream_t stream) {
+                             void* ws, cudaStream_t stream, bool exact_split, int* parts_run) {
     const TcW8a8Layout L = tc_w8a8_layout(M, N, K, split_k);
     char* base = reinterpret_cast<char*>(ws);
     cudaError_t e = widen_pair_launch(A, lda, M, K, base + L.a16, L.Kp, W, ldw, N, K, base + L.w16, L.Kp, stream);
@@ -165,13 +165,23 @@ static detgemm_status run_tc(const int8_t* A, int64_t lda, const int8_t* W, int6
     a.C = C;
     a.ldc = ldc;
     a.c_plane = 0;
-    return from_cuda(tc_gemm_launch(a, base + L.a16, L.Kp, 1, base + L.w16, L.Kp, 1, L.Kp, base + L.split, stream));
+    return from_cuda(tc_gemm_launch(a, base + L.a16, L.Kp, 1, base + L.w16, L.Kp, 1, L.Kp, base + L.split, stream,
+                                    exact_split, parts_run));
 }
 
+// exact_split: run exactly the split_k contiguous K parts asked for (or, on the decode path,
+// skinny_exact_parts of them) instead of the launchers' own choice; parts_run (optional)
+// receives the number of parts run.
 static detgemm_status run_igemm(const int8_t* A, int64_t lda, const int8_t* W, int64_t ldw, const int32_t* ea,
                                 const int32_t* ew, const uint16_t* bias, void* C, int64_t ldc, int mode, int M, int N, int K, int split_k,
-                                void* ws, cudaStream_t stream) {
-    if (w8a8_uses_tc(M, K)) return run_tc(A, lda, W, ldw, ea, ew, bias, C, ldc, mode, M, N, K, split_k, ws, stream);
+                                void* ws, cudaStream_t stream, bool exact_split = false, int* parts_run = nullptr) {
+    if (w8a8_uses_tc(M, K))
+        return run_tc(A, lda, W, ldw, ea, ew, bias, C, ldc, mode, M, N, K, split_k, ws, stream, exact_split, parts_run);
+    if (exact_split) {
+        if (parts_run) *parts_run = skinny_exact_parts(K, split_k);
+        return from_cuda(skinny_launch(A, lda, W, ldw, ea, ew, bias, C, ldc, mode, M, N, K, split_k, ws, stream, true));
+    }
+    if (parts_run) *parts_run = 0;  // the decode kernels' own cut
     IGemmArgs a = {};
     a.seg[0] = Seg{A, W};
     a.nseg = 1;
@@ -193,7 +203,7 @@ static detgemm_status run_igemm(const int8_t* A, int64_t lda, const int8_t* W, i
 static detgemm_status w8a8_impl(const int8_t* A, int64_t lda, const int8_t* W, int64_t ldw, const int32_t* ea,
                                 const int32_t* ew, const uint16_t* bias, bool with_bias, uint16_t* C, int64_t ldc,
                                 int M, int N, int K, int split_k, void* ws, size_t ws_bytes,
-                                detgemm_stream_t stream) {
+                                detgemm_stream_t stream, bool exact_split = false, int* parts_run = nullptr) {
     detgemm_status st = validate_igemm(A, lda, W, ldw, C, ldc, 2, M, N, K, split_k, ws, ws_bytes);
     if (st != DETGEMM_OK) return st;
     if (M == 0 || N == 0) return DETGEMM_OK;
@@ -202,13 +212,22 @@ static detgemm_status w8a8_impl(const int8_t* A, int64_t lda, const int8_t* W, i
     if ((st = check_device()) != DETGEMM_OK) return st;
     return run_igemm(A, lda, W, ldw, ea, ew, with_bias ? bias : nullptr, C, ldc,
                      with_bias ? EPI_BF16_POW2_BIAS : EPI_BF16_POW2, M, N, K, split_k, ws,
-                     reinterpret_cast<cudaStream_t>(stream));
+                     reinterpret_cast<cudaStream_t>(stream), exact_split, parts_run);
 }
 
 detgemm_status detgemm_w8a8(const int8_t* A, int64_t lda, const int8_t* W, int64_t ldw, const int32_t* ea,
                             const int32_t* ew, uint16_t* C, int64_t ldc, int M, int N, int K, int split_k, void* ws,
                             size_t ws_bytes, detgemm_stream_t stream) {
     return w8a8_impl(A, lda, W, ldw, ea, ew, nullptr, false, C, ldc, M, N, K, split_k, ws, ws_bytes, stream);
+}
+
+detgemm_status detgemm_w8a8_split_exact(const int8_t* A, int64_t lda, const int8_t* W, int64_t ldw,
+                                        const int32_t* ea, const int32_t* ew, uint16_t* C, int64_t ldc, int M, int N,
+                                        int K, int split_k, void* ws, size_t ws_bytes, int* parts_run,
+                                        detgemm_stream_t stream) {
+    if (parts_run) *parts_run = 0;
+    return w8a8_impl(A, lda, W, ldw, ea, ew, nullptr, false, C, ldc, M, N, K, split_k, ws, ws_bytes, stream, true,
+                     parts_run);
 }
 
 detgemm_status detgemm_w8a8_bias(const int8_t* A, int64_t lda, const int8_t* W, int64_t ldw, const int32_t* ea,
@@ -405,7 +424,8 @@ size_t detgemm_ozaki_workspace_size(int M, int N, int K, int nslices, int max_di
 // diagonal g = max_diag - d and pairs A slice sA with B slice g - sA), then the combine.
 static detgemm_status ozaki_run(const void* A, int64_t lda, const void* B, int64_t ldb, void* C, int64_t ldc,
                                 bool f64, int M, int N, int K, int nslices, int max_diag, int split_k, void* ws,
-                                size_t ws_bytes, detgemm_stream_t stream) {
+                                size_t ws_bytes, detgemm_stream_t stream, bool exact_split = false,
+                                int* parts_run = nullptr) {
     if (M < 0 || N < 0 || K < 1) return DETGEMM_ERR_INVALID_ARG;
     const int max_slices = f64 ? 12 : 9;
     if (nslices < 1 || nslices > max_slices || max_diag < 2 || max_diag > 2 * nslices || max_diag > kTcMaxDiag)
@@ -468,7 +488,8 @@ static detgemm_status ozaki_run(const void* A, int64_t lda, const void* B, int64
     a.C = T;
     a.ldc = L.ldT;
     a.c_plane = (int64_t)M * L.ldT;
-    err = tc_gemm_launch(a, base + L.da, L.Kp, nslices, base + L.db, L.Kp, nslices, L.Kp, base + L.split, s);
+    err = tc_gemm_launch(a, base + L.da, L.Kp, nslices, base + L.db, L.Kp, nslices, L.Kp, base + L.split, s,
+                         exact_split, parts_run);
     if (err == cudaSuccess)
         err = f64 ? ozaki_combine_f64out_launch(T, L.ldT, max_diag, e, f, static_cast<double*>(C), ldc, M, N, s)
                   : ozaki_combine_launch(T, L.ldT, max_diag, e, f, static_cast<float*>(C), ldc, M, N, s);
@@ -479,6 +500,14 @@ detgemm_status detgemm_ozaki_f32(const float* A, int64_t lda, const float* B, in
                                  int M, int N, int K, int nslices, int max_diag, int split_k, void* ws,
                                  size_t ws_bytes, detgemm_stream_t stream) {
     return ozaki_run(A, lda, B, ldb, C, ldc, false, M, N, K, nslices, max_diag, split_k, ws, ws_bytes, stream);
+}
+
+detgemm_status detgemm_ozaki_f32_split_exact(const float* A, int64_t lda, const float* B, int64_t ldb, float* C,
+                                             int64_t ldc, int M, int N, int K, int nslices, int max_diag, int split_k,
+                                             void* ws, size_t ws_bytes, int* parts_run, detgemm_stream_t stream) {
+    if (parts_run) *parts_run = 0;
+    return ozaki_run(A, lda, B, ldb, C, ldc, false, M, N, K, nslices, max_diag, split_k, ws, ws_bytes, stream, true,
+                     parts_run);
 }
 
 detgemm_status detgemm_ozaki_f64(const double* A, int64_t lda, const double* B, int64_t ldb, double* C, int64_t ldc,

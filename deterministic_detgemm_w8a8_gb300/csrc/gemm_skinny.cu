@@ -77,6 +77,9 @@ struct SkArgs {
     int mode;           // EPI_BF16_POW2, EPI_BF16_POW2_BIAS or EPI_STORE_I32
     int32_t* ws_acc;    // [N x M] exact sums (token-contiguous: one warp atomic covers 8
                         // consecutive tokens of 4 columns)
+    int parts;          // 0: each CTA takes an equal share of the flattened (row block, K block)
+                        // space; > 0: exactly `parts` contiguous K parts per row block, CTA b
+                        // taking part b % parts of row block b / parts
 };
 
 // Workspace: [acc: N x M int32][A16: M x lda16 fp16], each part 256-byte aligned.
@@ -237,10 +240,17 @@ __global__ void __launch_bounds__(SK_THREADS, sk_ctas_per_sm(MT)) skinny_kernel(
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int kbr = (p.K + SK_BK - 1) / SK_BK;  // K blocks per row block
-    const long long F = (long long)p.nblocks * kbr;
-    const long long P = gridDim.x;
-    const int f0 = (int)(((long long)blockIdx.x * F) / P);
-    const int f1 = (int)(((long long)(blockIdx.x + 1) * F) / P);
+    int f0, f1;  // this CTA's range of the flattened (row block, K block) space
+    if (p.parts > 0) {
+        const int nb = (int)blockIdx.x / p.parts, z = (int)blockIdx.x - nb * p.parts;
+        f0 = nb * kbr + (int)(((long long)z * kbr) / p.parts);
+        f1 = nb * kbr + (int)(((long long)(z + 1) * kbr) / p.parts);
+    } else {
+        const long long F = (long long)p.nblocks * kbr;
+        const long long P = gridDim.x;
+        f0 = (int)(((long long)blockIdx.x * F) / P);
+        f1 = (int)(((long long)(blockIdx.x + 1) * F) / P);
+    }
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -718,6 +728,7 @@ cudaError_t sk_launch_mt(const CUtensorMap& tmW, const CUtensorMap& tmA, const S
     const long long blocks = (long long)a.nblocks * ((a.K + SK_BK - 1) / SK_BK);
     long long grid = (long long)per_sm * sk_num_sms();
     if (grid > blocks) grid = blocks;
+    if (a.parts > 0) grid = (long long)a.nblocks * a.parts;  // one CTA per (row block, K part)
     e = launch_pdl(skinny_kernel<MT>, dim3((unsigned)grid), dim3(SK_THREADS), (size_t)smem, s, tmW, tmA, a);
     if (e != cudaSuccess) return e;
     const unsigned fblocks = (unsigned)((a.N + SKF_COLS - 1) / SKF_COLS);
@@ -758,14 +769,21 @@ size_t skinny_workspace_bytes(int M, int N, int K, int split) {
     return sk_layout(M, N, K).total;
 }
 
+int skinny_exact_parts(int K, int split) {
+    const int kbr = (K + SK_BK - 1) / SK_BK;
+    return split < kbr ? split : kbr;
+}
+
 cudaError_t skinny_launch(const int8_t* A, int64_t lda, const int8_t* W, int64_t ldw, const int32_t* ea,
                           const int32_t* ew, const uint16_t* bias, void* C, int64_t ldc, int mode, int M, int N, int K,
-                          int split, void* ws, cudaStream_t s) {
-    (void)split;  // the kernel divides K among the SMs itself; the bits never depend on it
+                          int split, void* ws, cudaStream_t s, bool exact_split) {
+    // Without exact_split the kernels choose their own cut (the bits never depend on it);
+    // with it, every row block of W is cut into skinny_exact_parts(K, split) contiguous K
+    // parts on the split form below, whatever K is.
     if (M == 0 || N == 0) return cudaSuccess;
     if (!decode_path(M, K)) return cudaErrorInvalidValue;
     const int MT = (M + 15) / 16;
-    if (K <= WK_MAX_K) {
+    if (K <= WK_MAX_K && !exact_split) {
         // short K: one CTA per 32 W rows over the whole of K, int8 A read directly
         SkArgs a = {};
         a.M = M;
@@ -802,6 +820,7 @@ cudaError_t skinny_launch(const int8_t* A, int64_t lda, const int8_t* W, int64_t
     a.ldc = ldc;
     a.mode = mode;
     a.ws_acc = reinterpret_cast<int32_t*>(base + L.acc);
+    a.parts = exact_split ? skinny_exact_parts(K, split) : 0;
     __half* A16 = reinterpret_cast<__half*>(base + L.a16);
     CUtensorMap tmW, tmA;
     cudaError_t e = sk_map(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, W, K, ldw, N, SK_ROWS);

@@ -804,7 +804,8 @@ static cudaError_t launch_engine(const TcArgs& a, const CUtensorMap& tmA, const 
 }
 
 cudaError_t tc_gemm_launch(const TcArgs& a0, const void* A16, int64_t lda, int a_planes, const void* B16,
-                           int64_t ldb, int b_planes, int64_t kext, void* ws_split, cudaStream_t s) {
+                           int64_t ldb, int b_planes, int64_t kext, void* ws_split, cudaStream_t s, bool exact_split,
+                           int* split_run) {
     if (a0.M == 0 || a0.N == 0) return cudaSuccess;
     TcArgs a = a0;
     if (max_pair_clusters(256) <= 0) return cudaErrorInvalidConfiguration;
@@ -814,11 +815,12 @@ cudaError_t tc_gemm_launch(const TcArgs& a0, const void* A16, int64_t lda, int a
     // pairs once only add rounds of partial tiles, so it is lowered until every part of every
     // tile runs in one round and each part keeps at least 256 K (measured: at 16 tiles and
     // K = 16384, 125 -> 90 us at 4 parts; at 192 tiles and K = 2048, 58 -> 291 us at 8)
-    if (a.split > 1) {
+    if (a.split > 1 && !exact_split) {
         const long long tiles = (long long)a.ndiag * ((a.M + 255) / 256) * ((a.N + 255) / 256);
         const int c256 = max_pair_clusters(256);
         while (a.split > 1 && (tiles * a.split > c256 || kext / a.split < 256)) --a.split;
     }
+    if (split_run) *split_run = a.split;
     const int bn = bias && a.split > 1 ? 256 : choose_bn(a);
     set_tiles(a, kext, bn);
     CUtensorMap tmA, tmB, tmC;

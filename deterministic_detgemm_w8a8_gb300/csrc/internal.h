@@ -39,9 +39,12 @@ struct IGemmArgs {
 // problems decode_path accepts (M <= 64); everything else runs on the tensor-core engine.
 bool decode_path(int M, int K);
 size_t skinny_workspace_bytes(int M, int N, int K, int split);
+// exact_split: cut every 128-row block of W into exactly skinny_exact_parts(K, split)
+// contiguous K parts (128-wide K blocks) instead of the kernels' own cut.
 cudaError_t skinny_launch(const int8_t* A, int64_t lda, const int8_t* W, int64_t ldw, const int32_t* ea,
                           const int32_t* ew, const uint16_t* bias, void* C, int64_t ldc, int mode, int M, int N, int K,
-                          int split, void* ws, cudaStream_t s);
+                          int split, void* ws, cudaStream_t s, bool exact_split = false);
+int skinny_exact_parts(int K, int split);
 cudaError_t skinny_take_status(uint32_t* bits);
 
 // Integer GEMM on the mma.sync int8 path (exact int32 accumulation); decode_path problems
@@ -116,8 +119,11 @@ int64_t tc_padded_k(int K);
 size_t tc_split_bytes(int ndiag, int M, int N, int split);
 // A planes [a_planes][M][lda], B planes [b_planes][N][ldb] (fp16, 16-byte aligned rows);
 // the first kext columns of each row are the K extent (zeros are read beyond it)
+// exact_split: run a.split parts as given (otherwise it is lowered until every part of
+// every tile runs in one round of CTA pairs); split_run, if given, receives the parts run.
 cudaError_t tc_gemm_launch(const TcArgs& a, const void* A16, int64_t lda, int a_planes, const void* B16, int64_t ldb,
-                           int b_planes, int64_t kext, void* ws_split, cudaStream_t s);
+                           int b_planes, int64_t kext, void* ws_split, cudaStream_t s, bool exact_split = false,
+                           int* split_run = nullptr);
 // one-thread kernel whose bounded wait on a never-arriving mbarrier expires (DEV_TIMEOUT)
 cudaError_t selftest_wait_launch(uint64_t limit_ns, cudaStream_t s);
 // exact int8 -> fp16 copies of two matrices in one launch (row strides Kp0, Kp1 multiples

@@ -113,6 +113,29 @@ DETGEMM_API detgemm_status detgemm_w8a8(const int8_t* A, int64_t lda, const int8
 DETGEMM_API size_t detgemm_w8a8_workspace_size(int M, int N, int K, int split_k);
 
 /*
+ * detgemm_w8a8 with the K cut made exactly as asked, for verifying batch invariance
+ * [P4 §II "Pipeline and alibi": the int32 accumulator, hence every output bit, is the
+ * same for every tiling and split of K; P1 §3.2.2: split-K as contiguous parts of K whose
+ * partial sums are added afterwards]. detgemm_w8a8 treats split_k as a bound and may run
+ * fewer parts, or (decode-shaped problems) its own cut; this call runs the requested cut,
+ * whatever it costs, so that tests can compare results across cuts that really differ.
+ *  - M > 64 (tensor-core engine): every 256-row output tile's 64-wide K blocks are cut
+ *    into exactly split_k contiguous parts (part z: blocks [z*B/split_k, (z+1)*B/split_k)
+ *    of B), whose exact int32 partials are added in the split workspace.
+ *  - M <= 64 (decode kernels): every 128-row block of W has its 128-wide K blocks cut
+ *    into exactly min(split_k, ceil(K / 128)) contiguous parts, one CTA each, whose
+ *    partials meet through int32 atomics; this holds at split_k == 1 too (one CTA per row
+ *    block over all of K), where detgemm_w8a8 would use its whole-K kernel for K <= 4096.
+ *   parts_run  if not NULL, receives the number of K parts actually run (0 on error).
+ * Arguments, layout, result bits, workspace (detgemm_w8a8_workspace_size with the same
+ * split_k) and errors are those of detgemm_w8a8. Slower than detgemm_w8a8 at most cuts.
+ */
+DETGEMM_API detgemm_status detgemm_w8a8_split_exact(const int8_t* A, int64_t lda, const int8_t* W, int64_t ldw,
+                                                    const int32_t* ea, const int32_t* ew, uint16_t* C, int64_t ldc,
+                                                    int M, int N, int K, int split_k, void* ws, size_t ws_bytes,
+                                                    int* parts_run, detgemm_stream_t stream);
+
+/*
  * W8A8 linear layer with a bias, still rounded once [P4 §II "Pipeline and alibi": the
  * epilogue is the single rounding of the exactly scaled int32 accumulator; the bias is
  * added to that exact value before the rounding, not to the rounded output]:
@@ -234,6 +257,23 @@ DETGEMM_API detgemm_status detgemm_ozaki_f32(const float* A, int64_t lda, const 
 
 /* Bytes of scratch detgemm_ozaki_f32 needs for this problem. */
 DETGEMM_API size_t detgemm_ozaki_workspace_size(int M, int N, int K, int nslices, int max_diag, int split_k);
+
+/*
+ * detgemm_ozaki_f32 with every diagonal's slice-product sum cut into exactly split_k
+ * contiguous K parts, for verifying that the result does not depend on the cut [P3 §3 (a):
+ * each T_g is an exact integer; P1 §3.2.2: split-K as contiguous parts of K]. For each
+ * 256 x 256 output tile of diagonal g, the flattened range of its (g - 1 slice pairs) x
+ * (64-wide K blocks) is cut into split_k parts whose exact int32 partials are added in
+ * the split workspace. detgemm_ozaki_f32 may run fewer parts than split_k.
+ *   parts_run  if not NULL, receives the number of parts run (0 on error).
+ * Arguments, result bits, workspace (detgemm_ozaki_workspace_size with the same split_k)
+ * and errors are those of detgemm_ozaki_f32.
+ */
+DETGEMM_API detgemm_status detgemm_ozaki_f32_split_exact(const float* A, int64_t lda, const float* B,
+                                                         int64_t ldb, float* C, int64_t ldc, int M, int N, int K,
+                                                         int nslices, int max_diag, int split_k, void* ws,
+                                                         size_t ws_bytes, int* parts_run,
+                                                         detgemm_stream_t stream);
 
 /*
  * The recombination step of the Ozaki GEMMs alone [P3 §3 (a): the exact slice products

@@ -195,3 +195,32 @@ def test_binding_refuses_cpu_tensors(lib):
     A = torch.zeros((4, 16), dtype=torch.int8)
     with pytest.raises(ValueError):
         dg.w8a8(A, A, torch.zeros(4, dtype=torch.int32), torch.zeros(4, dtype=torch.int32))
+
+
+def test_split_exact_entry_points_validate(lib):
+    import torch
+    import deterministic_detgemm_w8a8_gb300 as dg
+    se = lib.detgemm_w8a8_split_exact
+    parts = ctypes.c_int(-7)
+
+    def w(M=300, K=512, split=2, ws=P, wsb=1 << 30, ea=P):
+        # A, lda, W, ldw, ea, ew, C, ldc, M, N, K, split, ws, ws_bytes, parts_run, stream
+        return se(P, 512, P, 512, ea, P, P, 256, M, 256, K, split, ws, wsb, ctypes.byref(parts), None)
+
+    # the same host-side checks as detgemm_w8a8, and parts_run reads 0 after an error
+    assert w(split=0) == dg.ERR_INVALID_ARG and parts.value == 0
+    parts.value = -7
+    assert w(split=9) == dg.ERR_INVALID_ARG and parts.value == 0
+    assert w(K=131072) == dg.ERR_PRECONDITION
+    assert w(ea=None) == dg.ERR_INVALID_ARG
+    assert w(split=2, ws=None, wsb=0) == dg.ERR_WORKSPACE
+    assert w(M=16, split=1, ws=None, wsb=0) == dg.ERR_WORKSPACE
+    assert w(M=0) == dg.OK
+    so = lib.detgemm_ozaki_f32_split_exact
+    parts.value = -7
+    assert so(P, 128, P, 64, P, 64, 64, 64, 128, 7, 8, 2, P, 16, ctypes.byref(parts), None) == dg.ERR_WORKSPACE
+    assert parts.value == 0
+    assert so(P, 64, P, 64, P, 64, 64, 64, 64, 7, 8, 0, P, 1 << 30, None, None) == dg.ERR_INVALID_ARG
+    if not torch.cuda.is_available():
+        assert w() == dg.ERR_UNSUPPORTED_DEVICE
+        assert so(P, 64, P, 64, P, 64, 64, 64, 64, 7, 8, 1, P, 1 << 30, None, None) == dg.ERR_UNSUPPORTED_DEVICE

@@ -56,7 +56,20 @@ def test_combine_order_case(lib, dev):
     assert got[0, 0] == 0
 
 
-def test_ozaki_workload_sampled_and_error_bound(lib, dev, oracle_mod):
+def _tile_columns(N, seed):
+    """One column at a random offset inside every 256-wide tile column, plus the edges."""
+    rng = np.random.default_rng(seed)
+    cols = {0, 1, 127, 128, 255, N - 256, N - 129, N - 1}
+    for t in range((N + 255) // 256):
+        cols.add(min(N - 1, 256 * t + int(rng.integers(0, 256))))
+    return sorted(cols)
+
+
+def test_ozaki_workload_bitexact_sampled_and_error_bound_everywhere(lib, dev, oracle_mod):
+    """4096^3: ten whole rows and every row of one column per 256-wide tile column
+    bit-exact against the oracle; the bound |C - AB| <= 4 * 2^-24 * (|A||B|)_ij on every
+    element (checked against an fp64 product, whose own error, at most K * 2^-53 * (|A||B|)_ij,
+    is taken off the allowance)."""
     A, B = synthetic.ozaki(4096)
     tA, tB = to_dev(A, dev), to_dev(B, dev)
     out = poison_like((4096, 4096), torch.float32, dev)
@@ -65,14 +78,48 @@ def test_ozaki_workload_sampled_and_error_bound(lib, dev, oracle_mod):
     rows = [0, 1, 127, 128, 2047, 4094, 4095] + np.random.default_rng(3).integers(0, 4096, 3).tolist()
     want = oracle_mod.ozaki_f32(A, B, rows=rows)
     assert (C[rows].view(np.uint32) == want.view(np.uint32)).all()
-    # error bound on the sampled rows, against an fp64 GEMM
-    ref = A[rows].astype(np.float64) @ B.astype(np.float64)
-    absab = np.abs(A[rows].astype(np.float64)) @ np.abs(B.astype(np.float64))
-    assert (np.abs(C[rows].astype(np.float64) - ref) <= 4 * 2.0 ** -24 * absab).all()
-    # split-K gives identical bits
-    out2 = poison_like((4096, 4096), torch.float32, dev)
-    lib.ozaki_f32(tA, tB, split_k=3, out=out2)
-    assert torch.equal(out.view(torch.int32), out2.view(torch.int32))
+    cols = _tile_columns(4096, 8)
+    want = oracle_mod.ozaki_f32(A, np.ascontiguousarray(B[:, cols]))
+    got = np.ascontiguousarray(C[:, cols])
+    assert (got.view(np.uint32) == want.view(np.uint32)).all(), int((got != want).sum())
+    A64, B64 = A.astype(np.float64), B.astype(np.float64)
+    ref = A64 @ B64
+    absab = np.abs(A64) @ np.abs(B64)
+    allowance = (4 * 2.0 ** -24 - 4096 * 2.0 ** -52) * absab
+    assert (np.abs(C.astype(np.float64) - ref) <= allowance).all()
+
+
+def test_ozaki_workload_identical_across_real_cuts(lib, dev, oracle_mod):
+    """4096^3 with every diagonal's K range cut into exactly 1 and 3 parts (reported by the
+    call): byte-identical to the plain call, and bit-exact against the oracle on sampled rows."""
+    A, B = synthetic.ozaki(4096)
+    tA, tB = to_dev(A, dev), to_dev(B, dev)
+    out = poison_like((4096, 4096), torch.float32, dev)
+    lib.ozaki_f32(tA, tB, out=out)
+    rows = [0, 255, 256, 3000, 4095]
+    want = oracle_mod.ozaki_f32(A, B, rows=rows).view(np.uint32)
+    for parts in (1, 3):
+        out2 = poison_like((4096, 4096), torch.float32, dev)
+        _, run = lib.ozaki_f32_split_exact(tA, tB, split_k=parts, out=out2)
+        assert run == parts
+        assert torch.equal(out.view(torch.int32), out2.view(torch.int32)), parts
+        assert (f32_bits(out2)[rows] == want).all(), parts
+
+
+def test_small_real_cuts(lib, dev, oracle_mod):
+    """Small Ozaki problems at cuts up to one 64-wide K block per part of the lightest
+    diagonal, bit-exact against the oracle."""
+    for M, N, K, split in [(130, 129, 513, 9), (257, 65, 1024, 16), (33, 17, 100, 2)]:
+        rng = np.random.default_rng(M + N + K)
+        A = (rng.standard_normal((M, K)) * np.exp2(rng.integers(-8, 9, size=(M, K)))).astype(np.float32)
+        B = (rng.standard_normal((K, N)) * np.exp2(rng.integers(-8, 9, size=(K, N)))).astype(np.float32)
+        tA = padded(A, dev, (K + 3) // 4 * 4)
+        tB = padded(B, dev, (N + 3) // 4 * 4)
+        out = poison_like((M, N), torch.float32, dev)
+        _, run = lib.ozaki_f32_split_exact(tA, tB, split_k=split, out=out)
+        assert run == split
+        want = oracle_mod.ozaki_f32(A, B).view(np.uint32)
+        assert (f32_bits(out) == want).all(), (M, N, K, split)
 
 
 def _diagonals(rng, nd, M, N):

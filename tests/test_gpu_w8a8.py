@@ -69,7 +69,15 @@ def test_ragged_shapes(lib, dev, oracle_mod, M, N, K, split, lda):
     assert (got == oracle_mod.gemm_s8_i32(A, W)).all()
 
 
-def test_sweep_workload_rows_identical_across_M_and_split(lib, dev, oracle_mod):
+def _bytes(out):
+    return bf16_bits(out).tobytes()
+
+
+def test_sweep_workload_rows_identical_across_M_and_real_cuts(lib, dev, oracle_mod):
+    """Each row's bits are the oracle's at every M, with split_k honoured exactly: the
+    split-exact entry runs 1, 2, 4 and 8 contiguous K parts (it reports how many), on the
+    engine for M = 257 and 2048 and on the decode kernels' split form for M <= 64; the
+    plain call (its own cut) is compared too."""
     A, W, ea, ew = synthetic.sweep(2048)
     want = oracle_mod.w8a8(A, W, ea, ew)
     tW = to_dev(W, dev)
@@ -77,33 +85,80 @@ def test_sweep_workload_rows_identical_across_M_and_split(lib, dev, oracle_mod):
     for M in (1, 7, 64, 257, 2048):
         tA = to_dev(A[:M], dev)
         tea = to_dev(ea[:M], dev)
-        for split in (1, 2, 4, 8):
+        out = poison_like((M, 6144), torch.bfloat16, dev)
+        lib.w8a8(tA, tW, tea, tew, split_k=1, out=out)
+        ref = _bytes(out)
+        assert (bf16_bits(out) == want[:M]).all(), M
+        for parts in (1, 2, 4, 8):
             out = poison_like((M, 6144), torch.bfloat16, dev)
-            lib.w8a8(tA, tW, tea, tew, split_k=split, out=out)
+            _, run = lib.w8a8_split_exact(tA, tW, tea, tew, split_k=parts, out=out)
+            assert run == parts, (M, parts, run)
             got = bf16_bits(out)
-            assert (got == want[:M]).all(), (M, split, int((got != want[:M]).sum()))
+            assert (got == want[:M]).all(), (M, parts, int((got != want[:M]).sum()))
+            assert _bytes(out) == ref, (M, parts)
 
 
-def test_skinny_workload_deep_split(lib, dev, oracle_mod):
+def test_skinny_workload_deep_split_real_cuts(lib, dev, oracle_mod):
+    """M = 16, K = 65536: 8, 16 and 32 contiguous K parts per 128-row block of W (reported
+    by the call), each bit-exact against the oracle and byte-identical to the others and to
+    the plain call's own cut."""
     A, W, ea, ew = synthetic.skinny()
     want = oracle_mod.w8a8(A, W, ea, ew)
     tA, tW, tea, tew = (to_dev(x, dev) for x in (A, W, ea, ew))
-    for split in (8, 16, 32):
+    out = poison_like((16, 4096), torch.bfloat16, dev)
+    lib.w8a8(tA, tW, tea, tew, split_k=8, out=out)
+    assert (bf16_bits(out) == want).all()
+    ref = _bytes(out)
+    for parts in (8, 16, 32):
         out = poison_like((16, 4096), torch.bfloat16, dev)
-        lib.w8a8(tA, tW, tea, tew, split_k=split, out=out)
-        assert (bf16_bits(out) == want).all(), split
+        _, run = lib.w8a8_split_exact(tA, tW, tea, tew, split_k=parts, out=out)
+        assert run == parts
+        assert (bf16_bits(out) == want).all(), parts
+        assert _bytes(out) == ref, parts
+
+
+def test_split_exact_reports_the_cut(lib, dev, oracle_mod):
+    """Ragged shapes through the split-exact entry: the parts run are split_k on the engine
+    and min(split_k, ceil(K / 128)) on the decode kernels, and the bits are the oracle's."""
+    for M, N, K, split, want_parts in [(65, 300, 1000, 15, 15), (300, 17, 130, 3, 3), (16, 200, 300, 5, 3),
+                                       (64, 129, 4100, 33, 33), (1, 1, 1, 1, 1), (3, 40, 4097, 2, 2)]:
+        rng = np.random.default_rng(M * 7 + N + K)
+        A = rng.integers(-128, 128, size=(M, K), dtype=np.int8)
+        W = rng.integers(-128, 128, size=(N, K), dtype=np.int8)
+        ea = rng.integers(-20, -2, size=M, dtype=np.int32)
+        ew = rng.integers(-20, -2, size=N, dtype=np.int32)
+        ld = (K + 15) // 16 * 16
+        out = poison_like((M, N), torch.bfloat16, dev)
+        _, run = lib.w8a8_split_exact(padded(A, dev, ld), padded(W, dev, ld), to_dev(ea, dev), to_dev(ew, dev),
+                                      split_k=split, out=out)
+        assert run == want_parts, (M, N, K, split, run)
+        assert (bf16_bits(out) == oracle_mod.w8a8(A, W, ea, ew)).all(), (M, N, K, split)
+
+
+def _tile_columns(N, seed):
+    """One column at a random offset inside every 256-wide tile column, plus the edges."""
+    rng = np.random.default_rng(seed)
+    cols = {0, 1, 127, 128, 255, N - 256, N - 129, N - 1}
+    for t in range((N + 255) // 256):
+        cols.add(min(N - 1, 256 * t + int(rng.integers(0, 256))))
+    return sorted(cols)
 
 
 @pytest.mark.parametrize("which", ["gate_up", "down"])
-def test_ffn_workload_sampled_rows(lib, dev, oracle_mod, which):
+def test_ffn_workload_sampled_rows_and_all_rows_of_sampled_columns(lib, dev, oracle_mod, which):
+    """8192-row FFN GEMMs: sixteen whole rows, and every row of one column per 256-wide tile
+    column (so every tile row, TMEM lane and epilogue warp of the persistent raster)."""
     A, W, ea, ew = synthetic.ffn_gate_up() if which == "gate_up" else synthetic.ffn_down()
     M = A.shape[0]
     out = poison_like((M, W.shape[0]), torch.bfloat16, dev)
     lib.w8a8(to_dev(A, dev), to_dev(W, dev), to_dev(ea, dev), to_dev(ew, dev), out=out)
     rows = sorted({0, 1, 127, 128, 129, 4095, 4096, M - 129, M - 128, M - 1} |
                   set(np.random.default_rng(5).integers(0, M, 6).tolist()))
-    got = bf16_bits(out)[rows]
-    assert (got == oracle_mod.w8a8(A, W, ea, ew, rows=rows)).all()
+    got = bf16_bits(out)
+    assert (got[rows] == oracle_mod.w8a8(A, W, ea, ew, rows=rows)).all()
+    cols = _tile_columns(W.shape[0], 6 if which == "gate_up" else 7)
+    want = oracle_mod.w8a8(A, np.ascontiguousarray(W[cols]), ea, np.ascontiguousarray(ew[cols]))
+    assert (got[:, cols] == want).all(), int((got[:, cols] != want).sum())
 
 
 def test_all_ones_probe(lib, dev):
