@@ -45,8 +45,8 @@ OPS_STEP = 2.0 * M_FFN * (N1 * K1 + N2 * K2)
 
 
 # dram bytes (read + write) per launch of tc2_gemm_kernel, from ncu captures of the two
-# FFN GEMMs (profiles/tc2_gemm_kernel_ffn_gate_up.md, profiles/launches_ffn_tc2.md), keyed
-# by a digest of the engine source so that a changed kernel reports null, not stale counters
+# FFN GEMMs, keyed by a digest of the engine source so that a changed kernel reports null,
+# not stale counters
 PROFILED_TRAFFIC = {
     "e019bf955e54fe7d": {"gate_up": 479119872 + 182585600, "down": 897748480 + 62810112},
 }
@@ -425,6 +425,47 @@ def _time(torch, fn, flush, reps=5, warm=2):
     return statistics.median(ts)
 
 
+def decode_amortised(dg, torch, dev, pk, ops_np, reps):
+    """Per-call GPU time of `reps` back-to-back calls, captured in one CUDA graph (so no host
+    overhead of the binding sits between them) on copies of W in turn: enough copies (more
+    than 300 MB in all) that every call reads its W from DRAM, not from L2 (126 MB). Bytes
+    per call are the algorithmic ones: A, W, the bf16 output and the exponents."""
+    A_np, W_np, ea_np, ew_np = ops_np
+    m, k = A_np.shape
+    n = W_np.shape[0]
+    tdev = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to(dev)
+    A, ea, ew = tdev(A_np), tdev(ea_np), tdev(ew_np)
+    W0 = tdev(W_np)
+    copies = max(1, -(-(300 << 20) // W0.numel()))
+    Ws = [W0] + [W0.clone() for _ in range(copies - 1)]
+    C = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(max(dg.w8a8_workspace_size(m, n, k, 1), 1), dtype=torch.uint8, device=dev)
+    for i in range(copies):
+        dg.w8a8(A, Ws[i % copies], ea, ew, out=C, ws=ws)
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            for i in range(reps):
+                dg.w8a8(A, Ws[i % copies], ea, ew, out=C, ws=ws)
+    torch.cuda.synchronize()
+    g.replay()
+    s = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(s)
+    g.replay()
+    e1.record(s)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / reps
+    nbytes = m * k + n * k + 2 * m * n + 4 * (m + n)
+    gbs = nbytes / (us * 1e-6) / 1e9
+    del g, Ws, W0
+    return {"us_per_call": round(us, 2), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / pk["hbm_gbs"], 4),
+            "calls": reps, "w_copies": copies, "timing": "one CUDA graph of back-to-back calls, CUDA events"}
+
+
 def extras(dg, torch, dev, pk, flush):
     import synthetic
     res = {}
@@ -442,8 +483,17 @@ def extras(dg, torch, dev, pk, flush):
         sk[str(split)] = {"us": round(ms * 1e3, 1), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / pk["hbm_gbs"], 4),
                           "TOPS": round(2.0 * 16 * 4096 * 65536 / (ms * 1e-3) / 1e12, 2)}
         outs.append(C.clone())
+    # the plain call chooses its own cut at every split_k; the invariance check runs the
+    # requested cuts exactly (8, 16, 32 contiguous K parts per row block of W, untimed)
+    cuts = {}
+    for split in (8, 16, 32):
+        Cx = torch.empty((16, 4096), dtype=torch.bfloat16, device=dev)
+        _, cuts[split] = dg.w8a8_split_exact(A, W, ea, ew, split_k=split, out=Cx)
+        outs.append(Cx)
+    sk["exact_cuts_parts_run"] = [cuts[s] for s in (8, 16, 32)]
     sk["identical_across_split"] = bool(all(torch.equal(outs[0].view(torch.int16), o.view(torch.int16))
                                             for o in outs))
+    sk["amortised"] = decode_amortised(dg, torch, dev, pk, synthetic.skinny(), reps=24)
     res["skinny_M16_N4096_K65536"] = sk
     del A, W
     # Ozaki fp32 GEMM 4096^3
@@ -538,6 +588,13 @@ def extras(dg, torch, dev, pk, flush):
         sweep[str(m)] = {"us": round(ms * 1e3, 1), "TOPS": round(2.0 * m * 6144 * 2048 / (ms * 1e-3) / 1e12, 1),
                          "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1)}
     res["sweep_N6144_K2048"] = sweep
+    del A, W, ea, ew
+    # the decode-shaped sweep calls back to back (per-call time visible, W read cold)
+    full = synthetic.sweep(2048)
+    res["sweep_N6144_K2048_amortised"] = {
+        str(m): decode_amortised(dg, torch, dev, pk, tuple(np.ascontiguousarray(x[:m]) if i in (0, 2) else x
+                                                          for i, x in enumerate(full)), reps=240)
+        for m in (1, 7, 16, 64)}
     # the biased epilogue (a bf16 bias per column added before the one rounding) beside the
     # unbiased one: the FFN gate/up GEMM, the sweep at M = 2048 and 64, the decode workload
     rng_b = torch.Generator(device="cpu").manual_seed(7)

@@ -64,6 +64,7 @@ SIGNATURES = {
                                   _I32, _P, _SZ, _P], _I32),
     "detgemm_get_device_status": ([_P], _I32),
     "detgemm_w8a8_noalloc": ([_P, _I64, _P, _I64, _P, _P, _P, _I64, _I32, _I32, _I32, _I32, _P], _I32),
+    "detgemm_w8a8_noalloc_scratch_size": ([_I32, _I32, _I32, _I32], _SZ),
     "detgemm_widen_i8_f16": ([_P, _I64, _I32, _I32, _P, _I64, _P], _I32),
     "detgemm_w8a8_f16ops": ([_P, _I64, _P, _I64, _P, _P, _P, _I64, _I32, _I32, _I32, _I32, _P, _SZ, _P], _I32),
     "detgemm_w8a8_f16ops_workspace_size": ([_I32, _I32, _I32, _I32], _SZ),

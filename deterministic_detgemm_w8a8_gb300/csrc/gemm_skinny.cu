@@ -79,7 +79,8 @@ struct SkArgs {
                         // consecutive tokens of 4 columns)
     int parts;          // 0: each CTA takes an equal share of the flattened (row block, K block)
                         // space; > 0: exactly `parts` contiguous K parts per row block, CTA b
-                        // taking part b % parts of row block b / parts
+                        // taking part b % parts of row block b / parts (the tensor-core decode
+                        // kernel: the cluster size)
 };
 
 // Workspace: [acc: N x M int32][A16: M x lda16 fp16], each part 256-byte aligned.
@@ -528,6 +529,9 @@ __global__ void __launch_bounds__(WK_THREADS, 2) skinny_wk_kernel(const __grid_c
         fence_mbar_init();
     }
     __syncthreads();
+    // launched as a programmatic dependent of the kernel before it: nothing below touches
+    // global memory before that kernel has completed
+    pdl_wait();
 
     if (warp == 0) {
         if (lane == 0) {
@@ -611,6 +615,7 @@ __global__ void __launch_bounds__(WK_THREADS, 2) skinny_wk_kernel(const __grid_c
         if (lane == 0) mbar_arrive(empty + st);
     }
 
+    if (cw == 0 && lane == 0) pdl_launch_dependents();  // the next call may start its set-up
     // The K groups' partials meet in the ring: every consumer is past its last stage, so
     // every load into it has landed (unless a wait gave up, which raised the abort flag and
     // the device status; then nothing is stored). Layout [warp][element][lane].
@@ -752,7 +757,432 @@ cudaError_t wk_launch_mt(const CUtensorMap& tmW, const CUtensorMap& tmA, const S
             g_wk_set[dev][MT] = 1;
         }
     }
-    skinny_wk_kernel<MT><<<(unsigned)((a.N + WK_ROWS - 1) / WK_ROWS), WK_THREADS, smem, s>>>(tmW, tmA, a);
+    cudaError_t le = launch_pdl(skinny_wk_kernel<MT>, dim3((unsigned)((a.N + WK_ROWS - 1) / WK_ROWS)), dim3(WK_THREADS),
+                                (size_t)smem, s, tmW, tmA, a);
+    if (le != cudaSuccess) return le;
+    return cudaGetLastError();
+}
+
+
+// ---------------------------------------------------------------------------- tensor-core decode
+// Decode-shaped problems with K <= DT_MAX_K on the fifth-generation tensor cores. The W rows
+// are the 128-row operand of tcgen05.mma (M = 128) and the tokens the narrow one (N = 16 MT),
+// so even one token wastes no multiply-add lanes on W: D[128 x 16 MT] += W[128 x 16] T[16 MT x 16]^T,
+// fp16 operands (exact for int8), fp32 accumulation in TMEM. Every partial sum of at most 1024
+// products of magnitude <= 2^14 is an integer below 2^24, so each 1024-K chunk accumulates
+// exactly in its own TMEM columns and the chunks are added as int32 at the end.
+// The widened W operand lives in tensor memory (the MMA reads A from TMEM): thread r of a
+// converter warp owns W row r, which is TMEM lane r, and stores its widened row there, so W
+// crosses shared memory once (its int8 TMA stage) instead of three times; shared memory
+// bandwidth, not HBM, bounded the form that staged fp16 W tiles in shared memory.
+// The K blocks (128 wide) of each 128-row block of W are cut into `parts` contiguous ranges,
+// one per CTA of a thread-block cluster of `parts` CTAs. Every CTA writes its int32 partial
+// sums into its shared memory; CTA z then reads, through distributed shared memory, the
+// partials of its slice of the 128 rows from every CTA of the cluster (16 bytes at a time),
+// adds them (integer addition: the order cannot change the sum) and rounds.
+// Roles (576 threads, one CTA per SM):
+//   warp 0     lane 0 streams, per K block, the int8 boxes W[128 x 128] (evict-first: W is
+//              read once) and T[16 MT x 128] (128-byte swizzle; zeros past N, M and K) into a
+//              ring of dt_s8(MT) stages;
+//   warp 1     allocates TMEM; lane 0 issues the MMAs (eight K = 16 steps per K block, A from
+//              TMEM, B from shared memory) and commits each stage back to the converters;
+//   warps 2-17 widen each stage exactly to fp16: warp w takes W rows 32 (w mod 4) .. +31 (its
+//              TMEM lanes) over K quarter (w - 2) / 4 into one of DT_SW TMEM stages, and one
+//              16-byte chunk of the token box per thread into a shared-memory tcgen05 operand
+//              tile (K-major, 128-byte swizzle: chunk c of row r at c ^ (r mod 8)). They stage
+//              the exponents of the outputs in shared memory while the stream runs; once the
+//              MMAs are done, warp w drains lanes 32 (w mod 4) .. +31 for token quarter (w - 2) / 4.
+constexpr int DT_CONV_WARPS = 16;
+constexpr int DT_THREADS = 64 + 32 * DT_CONV_WARPS;
+constexpr int DT_MAX_K = 4096;
+constexpr int DT_SW = 4;                // widened stages (W in TMEM, tokens in shared memory)
+constexpr uint32_t DT_TMEM_COLS = 512;  // W stages: columns [0, 64 DT_SW); accumulators above
+constexpr uint32_t DT_ACC_COL = 64 * DT_SW;
+constexpr int DT_W8 = 128 * 128;  // int8 W box bytes
+__host__ __device__ constexpr int dt_s8(int MT) { return MT <= 2 ? 7 : 6; }
+__host__ __device__ constexpr int dt_st8_bytes(int MT) { return DT_W8 + 16 * MT * 128; }
+__host__ __device__ constexpr int dt_stt_bytes(int MT) { return 2 * 16 * MT * 128; }  // fp16 token stage
+constexpr int DT_EPI_BYTES = 4 * (64 + 128 + 128);  // staged ea, ew and bias of one row block
+__host__ __device__ constexpr int dt_smem_bytes(int MT) {
+    return dt_s8(MT) * dt_st8_bytes(MT) + DT_SW * dt_stt_bytes(MT) + DT_EPI_BYTES + 1024 + 256;
+}
+// more than half of an SM's shared memory: one CTA per SM, so the whole TMEM is this CTA's
+static_assert(dt_smem_bytes(1) > 116 * 1024 && dt_smem_bytes(4) <= 227 * 1024, "shared memory");
+static_assert(DT_ACC_COL + 4 * 64 <= DT_TMEM_COLS, "TMEM: four 1024-K chunks of 64 tokens above the W stages");
+
+__device__ __forceinline__ void sts16(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+// integer addition into a shared-memory word of any CTA of the cluster
+__device__ __forceinline__ void red_dsmem_add(uint32_t cluster_addr, int32_t v) {
+    asm volatile("red.relaxed.cluster.shared::cluster.add.s32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ int4 ld_dsmem_v4(uint32_t cluster_addr) {
+    int4 v;
+    asm volatile("ld.shared::cluster.v4.s32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(cluster_addr)
+                 : "memory");
+    return v;
+}
+// 32 lanes x 16 consecutive 32-bit TMEM columns from 16 registers per thread
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+            taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+        "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+        : "memory");
+}
+// 32 lanes x 4 consecutive 32-bit TMEM columns
+__device__ __forceinline__ void tmem_ld4(uint32_t taddr, uint32_t (&r)[4]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+// D[tmem] (+)= A[tmem] * B[smem desc]^T, kind::f16: A is M x K with row m in TMEM lane m and
+// the K values in pairs per 32-bit column (k = 2c in the low half of column c)
+__device__ __forceinline__ void mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                               uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// rne_bf16(acc * 2^ea * 2^ew) for ea, ew in [-60, 40]: acc truncated to 24 significant bits
+// with the last kept bit set when anything was dropped (rounding to odd), scaled exactly by
+// the two powers of two, then rounded to nearest-even: odd rounding at 24 >= 8 + 2 bits
+// followed by one nearest rounding at 8 bits equals one nearest rounding, so the bits are
+// those of the integer construction bf16_from_acc_pow2.
+__device__ __forceinline__ uint16_t bf16_pow2_fast(int32_t acc, int32_t ea, int32_t ew) {
+    const float x = __int2float_rz(acc);
+    const uint32_t xb = __float_as_uint(x) | (uint32_t)(__float2int_rz(x) != acc);
+    const float y = __fmul_rn(__fmul_rn(__uint_as_float(xb), __uint_as_float((uint32_t)(ea + 127) << 23)),
+                              __uint_as_float((uint32_t)(ew + 127) << 23));
+    return __bfloat16_as_ushort(__float2bfloat16_rn(y));
+}
+
+// one output of the decode kernels: row m, column col, with its exponents (and bias) at hand
+__device__ __forceinline__ void store_one(const SkArgs& p, int m, int col, int32_t v, int32_t ea, int32_t ew,
+                                          uint32_t b) {
+    if (p.mode == EPI_STORE_I32) {
+        reinterpret_cast<int32_t*>(p.C)[(int64_t)m * p.ldc + col] = v;
+        return;
+    }
+    uint16_t h;
+    if (p.mode == EPI_BF16_POW2_BIAS) h = bf16_from_acc_pow2_bias(v, ea, ew, b);
+    else if (ea >= -60 && ea <= 40 && ew >= -60 && ew <= 40) h = bf16_pow2_fast(v, ea, ew);
+    else h = bf16_from_acc_pow2(v, ea, ew);
+    p.C[(int64_t)m * p.ldc + col] = h;
+}
+
+template <int MT>
+__global__ void __launch_bounds__(DT_THREADS, 1) decode_tc_kernel(const __grid_constant__ CUtensorMap tmW,
+                                                                  const __grid_constant__ CUtensorMap tmA,
+                                                                  const __grid_constant__ SkArgs p) {
+    constexpr int MP = 16 * MT, S8 = dt_s8(MT), ST8 = dt_st8_bytes(MT), STT = dt_stt_bytes(MT);
+    constexpr int MQ = MP / 4;  // tokens per epilogue warp
+    constexpr uint32_t IDESC = idesc_f16_f32(128, MP);
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* ringt = smem + S8 * ST8;  // fp16 token stages
+    int32_t* sea = reinterpret_cast<int32_t*>(ringt + DT_SW * STT);  // ea[0, 64), ew and bias of the rows
+    int32_t* sew = sea + 64;
+    uint32_t* sbias = reinterpret_cast<uint32_t*>(sew + 128);
+    uint64_t* full8 = reinterpret_cast<uint64_t*>(sbias + 128);
+    uint64_t* empty8 = full8 + S8;
+    uint64_t* fullw = empty8 + S8;
+    uint64_t* emptyw = fullw + DT_SW;
+    uint64_t* accf = emptyw + DT_SW;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accf + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int P = p.parts;
+    const int z = (int)cluster_ctarank();
+    const int n0 = (int)(blockIdx.x / P) * 128;
+    const int nkb = (p.K + 127) / 128;
+    const int f0 = (int)(((long long)z * nkb) / P);
+    const int nloc = (int)(((long long)(z + 1) * nkb) / P) - f0;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S8; ++s) {
+            mbar_init(full8 + s, 1);
+            mbar_init(empty8 + s, DT_CONV_WARPS);
+        }
+        for (int t = 0; t < DT_SW; ++t) {
+            mbar_init(fullw + t, DT_CONV_WARPS);
+            mbar_init(emptyw + t, 1);  // the MMA commit
+        }
+        mbar_init(accf, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, DT_TMEM_COLS);
+        tmem_relinquish();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&tmW);
+        prefetch_tmap(&tmA);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    // launched as a programmatic dependent of the kernel before it: the setup above overlaps
+    // that kernel's tail; nothing below touches global memory before it has completed
+    pdl_wait();
+
+    const bool epi = warp >= 2;
+    const int q4 = warp & 3;
+    const int row = 32 * q4 + lane;           // W row of this thread: its TMEM lane
+    const int qk = (warp - 2) >> 2;           // K quarter of the W stages / token quarter of the drain
+    const int mq0 = MQ * qk;                  // first token of this warp's quarter
+    const uint32_t lane_base = tmem_base + ((uint32_t)(32 * q4) << 16);
+    // the rounding's operands, staged now so that their latency hides behind the stream
+    if (epi) {
+        const int t = threadIdx.x - 64;
+        if (t < 64) sea[t] = t < p.M && p.mode != EPI_STORE_I32 ? __ldg(p.ea + t) : 0;
+        if (t < 128) {
+            const bool in = n0 + t < p.N && p.mode != EPI_STORE_I32;
+            sew[t] = in ? __ldg(p.ew + n0 + t) : 0;
+            sbias[t] = in && p.mode == EPI_BF16_POW2_BIAS ? (uint32_t)__ldg(p.bias + n0 + t) : 0u;
+        }
+    }
+
+    bool ok = true;
+    if (warp == 0) {
+        if (lane == 0) {
+            const uint64_t pol = l2_policy_evict_first();
+            int i = 0;
+            for (; i < nloc; ++i) {
+                const int s = i % S8;
+                if (i >= S8 && !mbar_wait(empty8 + s, (uint32_t)((i / S8) - 1) & 1u, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                uint8_t* d = smem + s * ST8;
+                mbar_arrive_expect_tx(full8 + s, ST8);
+                const int kx = (f0 + i) * 128;
+                tma_load_2d_hint(d, &tmW, full8 + s, kx, n0, pol);
+                tma_load_2d(d + DT_W8, &tmA, full8 + s, kx, 0);
+            }
+            if (!ok) {
+                // let the loads already issued land before the CTA's shared memory goes away
+                for (int j = i - 1; j >= 0 && j >= i - S8; --j)
+                    mbar_wait_drain(full8 + j % S8, (uint32_t)(j / S8) & 1u, kDrainLimitNs);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            for (int i = 0; i < nloc; ++i) {
+                const int t = i % DT_SW;
+                if (!mbar_wait(fullw + t, (uint32_t)(i / DT_SW) & 1u, abort_flag)) break;
+                tc_fence_after();
+                const uint32_t bt = smem_addr(ringt + t * STT);
+                const uint32_t d = tmem_base + DT_ACC_COL + (uint32_t)((i >> 3) * MP);  // 1024-K chunk i / 8
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const uint64_t bd = sdesc_sw128_kmajor(bt + (uint32_t)((k >> 2) * MP * 128)) + 2 * (k & 3);
+                    mma_f16_tmem_a(d, tmem_base + (uint32_t)(64 * t + 8 * k), bd, IDESC, ((i & 7) | k) != 0 ? 1u : 0u);
+                }
+                mma_commit(emptyw + t);
+            }
+            mma_commit(accf);  // every MMA issued above has completed when this arrives
+            mbar_wait_drain(accf, 0);  // ... and before TMEM is freed, even after an abort
+        }
+    } else {
+        // ------------------------------------------------------------ converters
+        const int t = threadIdx.x - 64;  // 0 .. 511
+        const int sw = row & 7;
+        for (int i = 0; i < nloc; ++i) {
+            const int s = i % S8, tw = i % DT_SW;
+            bool got = mbar_wait(full8 + s, (uint32_t)(i / S8) & 1u, abort_flag);
+            if (got && i >= DT_SW) got = mbar_wait(emptyw + tw, (uint32_t)((i / DT_SW) - 1) & 1u, abort_flag);
+            if (!__all_sync(0xffffffffu, got)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t s8 = smem_addr(smem + s * ST8);
+            // all of this thread's loads first (one latency), then the widening and the stores
+            uint4 wv[2];
+#pragma unroll
+            for (int c = 0; c < 2; ++c) wv[c] = lds16(s8 + (uint32_t)(row * 128 + (((2 * qk + c) ^ sw) << 4)));
+            // token chunk t (row t / 8, chunk t % 8) of the MP * 8 <= 512
+            constexpr int TQ = (MP * 8 + 511) / 512;
+            uint4 tv[TQ];
+#pragma unroll
+            for (int j = 0; j < TQ; ++j) {
+                const int q = t + 512 * j;
+                tv[j] = make_uint4(0, 0, 0, 0);
+                if (q < MP * 8) tv[j] = lds16(s8 + (uint32_t)(DT_W8 + (q >> 3) * 128 + (((q & 7) ^ ((q >> 3) & 7)) << 4)));
+            }
+            uint32_t h[16];
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                uint32_t hh[8];
+                i8x16_to_f16x16(wv[c], hh);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) h[8 * c + e] = hh[e];
+            }
+            tmem_st16(lane_base + (uint32_t)(64 * tw + 16 * qk), h);
+#pragma unroll
+            for (int j = 0; j < TQ; ++j) {
+                const int q = t + 512 * j;
+                const int m = q >> 3, c8 = q & 7, msw = m & 7;
+                if (q < MP * 8) {
+                    uint32_t hh[8];
+                    i8x16_to_f16x16(tv[j], hh);
+                    const uint32_t td = smem_addr(ringt + tw * STT) + (uint32_t)((c8 >> 2) * MP * 128 + m * 128);
+                    const int cc = 2 * (c8 & 3);
+                    sts16(td + (uint32_t)((cc ^ msw) << 4), hh[0], hh[1], hh[2], hh[3]);
+                    sts16(td + (uint32_t)(((cc + 1) ^ msw) << 4), hh[4], hh[5], hh[6], hh[7]);
+                }
+            }
+            tmem_wait_st();
+            // the TMEM stores, the generic-proxy reads of the int8 stage and writes of the token
+            // tile are ordered before the MMA and the TMA refill (async proxy)
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(empty8 + s);
+                mbar_arrive(fullw + tw);
+            }
+        }
+        // ------------------------------------------------------------ drain
+        const bool done = mbar_wait(accf, 0, abort_flag);
+        ok = __all_sync(0xffffffffu, ok && done) && *abort_flag == 0;
+    }
+    if (threadIdx.x == 0) pdl_launch_dependents();
+
+    int32_t acc[MQ];
+#pragma unroll
+    for (int j = 0; j < MQ; ++j) acc[j] = 0;
+    if (epi && ok) {
+        tc_fence_after();
+        const int nchunks = (nloc + 7) / 8;
+        for (int ch = 0; ch < nchunks; ++ch) {
+#pragma unroll
+            for (int j = 0; j < MQ / 4; ++j) {
+                uint32_t v[4];
+                tmem_ld4(lane_base + DT_ACC_COL + (uint32_t)(ch * MP + mq0 + 4 * j), v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[4 * j + e] += __float2int_rn(__uint_as_float(v[e]));
+            }
+        }
+    }
+    tc_fence_before();
+    // [token][W row] partial sums in the token ring: every MMA has completed (accf) and every
+    // conversion is done, so the ring is free
+    int32_t* red = reinterpret_cast<int32_t*>(ringt);
+    if (epi && ok) {
+#pragma unroll
+        for (int j = 0; j < MQ; ++j) red[(mq0 + j) * 128 + row] = acc[j];
+    }
+    if (P > 1) cluster_sync();  // every CTA's partials are in place (and every CTA has started)
+    else __syncthreads();
+    if (epi && ok) {
+        // this CTA's slice of the rows, in groups of four (one 16-byte load per CTA of the
+        // cluster): rows [4 g0, 4 g1)
+        const int g0 = (z * 32) / P, g1 = ((z + 1) * 32) / P, G = g1 - g0;
+        const uint32_t rbase = smem_addr(red);
+        for (int it = threadIdx.x - 64; it < p.M * G; it += 32 * DT_CONV_WARPS) {
+            const int m = it / G, r = 4 * (g0 + it - m * G);
+            const uint32_t a = rbase + (uint32_t)((m * 128 + r) * 4);
+            int4 v = make_int4(0, 0, 0, 0);
+            for (int zz = 0; zz < P; ++zz) {
+                const int4 u = P > 1 ? ld_dsmem_v4(mapa(a, (uint32_t)zz)) : *reinterpret_cast<const int4*>(red + m * 128 + r);
+                v.x += u.x;
+                v.y += u.y;
+                v.z += u.z;
+                v.w += u.w;
+            }
+            const int32_t vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if (n0 + r + e < p.N) store_one(p, m, n0 + r + e, vv[e], sea[m], sew[r + e], sbias[r + e]);
+        }
+    }
+    if (P > 1) cluster_sync();  // no CTA leaves while another may still read its partials
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem_base, DT_TMEM_COLS);
+}
+
+int g_dt_set[64][5];      // decode_tc_kernel<MT> opted into its shared memory, per device
+int g_dt_clusters[64][5][9];  // active clusters of `parts` CTAs at once, per device and MT (0: not known)
+
+template <int MT>
+int dt_active_clusters(int parts) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    std::lock_guard<std::mutex> lock(g_sk_mutex);
+    if (!g_dt_set[dev][MT]) {
+        if (cudaFuncSetAttribute(decode_tc_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 dt_smem_bytes(MT)) != cudaSuccess)
+            return 0;
+        g_dt_set[dev][MT] = 1;
+    }
+    if (g_dt_clusters[dev][MT][parts] == 0) {
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = parts;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3(parts * 64, 1, 1);
+        cfg.blockDim = dim3(DT_THREADS, 1, 1);
+        cfg.dynamicSmemBytes = dt_smem_bytes(MT);
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, decode_tc_kernel<MT>, &cfg) != cudaSuccess) n = 0;
+        g_dt_clusters[dev][MT][parts] = n > 0 ? n : -1;
+    }
+    return g_dt_clusters[dev][MT][parts];
+}
+
+// Cluster size: the largest number of K parts (<= 8, <= the K blocks) with which every row
+// block's cluster is resident at once; one part when even that does not fit.
+template <int MT>
+int dt_parts(int nrb, int nkb) {
+    for (int P = nkb < 8 ? nkb : 8; P > 1; --P) {
+        const int n = dt_active_clusters<MT>(P);
+        if (n > 0 && nrb <= n) return P;
+    }
+    return 1;
+}
+
+template <int MT>
+cudaError_t dt_launch_mt(const CUtensorMap& tmW, const CUtensorMap& tmA, SkArgs a, cudaStream_t s) {
+    const int nkb = (a.K + 127) / 128;
+    if (dt_active_clusters<MT>(1) == 0) return cudaErrorInvalidConfiguration;
+    a.parts = dt_parts<MT>(a.nblocks, nkb);
+    // every 1024-K chunk of a part has MP accumulator columns above the W stages
+    if (((nkb + a.parts - 1) / a.parts + 7) / 8 * 16 * MT > (int)(DT_TMEM_COLS - DT_ACC_COL)) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = a.parts;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3((unsigned)(a.nblocks * a.parts), 1, 1);
+    cfg.blockDim = dim3(DT_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = dt_smem_bytes(MT);
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, decode_tc_kernel<MT>, tmW, tmA, a);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
@@ -783,8 +1213,33 @@ cudaError_t skinny_launch(const int8_t* A, int64_t lda, const int8_t* W, int64_t
     if (M == 0 || N == 0) return cudaSuccess;
     if (!decode_path(M, K)) return cudaErrorInvalidValue;
     const int MT = (M + 15) / 16;
+    if (K <= DT_MAX_K && MT > 1 && !exact_split) {
+        // short K, 17 to 64 tokens: the tensor-core decode kernel (one launch, no workspace)
+        SkArgs a = {};
+        a.M = M;
+        a.N = N;
+        a.K = K;
+        a.nblocks = (N + 127) / 128;
+        a.ea = ea;
+        a.ew = ew;
+        a.bias = bias;
+        a.C = reinterpret_cast<uint16_t*>(C);
+        a.ldc = ldc;
+        a.mode = mode;
+        CUtensorMap tmW, tmA;
+        cudaError_t e = sk_map(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, W, K, ldw, N, 128);
+        if (e == cudaSuccess) e = sk_map(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A, K, lda, M, 16 * MT);
+        if (e != cudaSuccess) return e;
+        switch (MT) {
+            case 2: return dt_launch_mt<2>(tmW, tmA, a, s);
+            case 3: return dt_launch_mt<3>(tmW, tmA, a, s);
+            default: return dt_launch_mt<4>(tmW, tmA, a, s);
+        }
+    }
     if (K <= WK_MAX_K && !exact_split) {
-        // short K: one CTA per 32 W rows over the whole of K, int8 A read directly
+        // short K, at most 16 tokens: one CTA per 32 W rows over the whole of K, int8 A read
+        // directly (its one-launch set-up is cheaper than the tensor-core kernel's, which only
+        // pays once the warp MMA work grows with the tokens)
         SkArgs a = {};
         a.M = M;
         a.N = N;

@@ -398,11 +398,20 @@ DETGEMM_API detgemm_status detgemm_get_device_status(detgemm_stream_t stream);
  * handed only its input and output tensors, or a latency-critical serving loop that
  * bans cudaMalloc because an allocation can synchronize the device.
  *
- * Same operands, layout, result bits and errors as detgemm_w8a8. The split-K scratch
- * lives in a fixed device array of DETGEMM_NOALLOC_SCRATCH_BYTES inside the library,
- * which every GPU that loads the library keeps until the process exits. A problem
- * whose detgemm_w8a8_workspace_size(M, N, K, split_k) exceeds that size is refused
- * with DETGEMM_ERR_WORKSPACE before anything is launched.
+ * Same operands, layout and result bits as detgemm_w8a8. The split-K scratch lives in a
+ * fixed device array of DETGEMM_NOALLOC_SCRATCH_BYTES inside the library, which every GPU
+ * that loads the library keeps until the process exits. The call is refused with
+ * DETGEMM_ERR_WORKSPACE, before anything is launched, when the scratch it really uses,
+ * detgemm_w8a8_noalloc_scratch_size(M, N, K, split_k), exceeds that size:
+ *  - M <= 64: the decode kernels' accumulator and fp16 copy of A, M * N * 4 + M * K * 2
+ *    bytes (rounded up), at any split_k, as detgemm_w8a8 needs them;
+ *  - M > 64: M * N * 4 bytes plus a counter per tile when split_k > 1, else nothing.
+ * Problems of more than 64 rows run here on the int8 warp-MMA tile kernel (mma.sync
+ * m16n8k32, exact int32 accumulation, about 147 TOPS on GB300), not on the tcgen05 engine
+ * of detgemm_w8a8, whose fp16 operand copies would need tens of MB of scratch: the bits
+ * are the same, the throughput at large M is an order of magnitude lower.
+ * Errors are those of detgemm_w8a8, checked in the same order, except that the scratch
+ * size is checked last (after the device check) instead of detgemm_w8a8's workspace check.
  *  - The first call on each device looks up the array's device address (set-up done
  *    once per device, with that device current); make that first call before any
  *    stream capture begins.
@@ -412,6 +421,10 @@ DETGEMM_API detgemm_status detgemm_get_device_status(detgemm_stream_t stream);
  *  - The call allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
  */
 #define DETGEMM_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+/* Bytes of the fixed scratch array detgemm_w8a8_noalloc uses for this problem (0 for
+ * M > 64 at split_k == 1; 0 for empty or invalid sizes). */
+DETGEMM_API size_t detgemm_w8a8_noalloc_scratch_size(int M, int N, int K, int split_k);
 
 DETGEMM_API detgemm_status detgemm_w8a8_noalloc(const int8_t* A, int64_t lda, const int8_t* W, int64_t ldw,
                                                 const int32_t* ea, const int32_t* ew, uint16_t* C,

@@ -224,3 +224,29 @@ def test_split_exact_entry_points_validate(lib):
     if not torch.cuda.is_available():
         assert w() == dg.ERR_UNSUPPORTED_DEVICE
         assert so(P, 64, P, 64, P, 64, 64, 64, 64, 7, 8, 1, P, 1 << 30, None, None) == dg.ERR_UNSUPPORTED_DEVICE
+
+
+def test_noalloc_validates_in_w8a8_order(lib):
+    import torch
+    import deterministic_detgemm_w8a8_gb300 as dg
+    na = lib.detgemm_w8a8_noalloc
+
+    def n(A=P, ea=P, M=300, K=512, split=1):
+        # A, lda, W, ldw, ea, ew, C, ldc, M, N, K, split, stream
+        return na(A, 512, P, 512, ea, P, P, 256, M, 256, K, split, None)
+
+    # a misaligned A with a null ea reports ALIGNMENT, as detgemm_w8a8 does
+    assert n(A=P1, ea=None) == dg.ERR_ALIGNMENT
+    assert n(ea=None) == dg.ERR_INVALID_ARG
+    assert n(split=9) == dg.ERR_INVALID_ARG
+    assert n(M=0) == dg.OK
+    # the scratch-size rule: the decode kernels' scratch at M <= 64, the split accumulator above
+    ss = lib.detgemm_w8a8_noalloc_scratch_size
+    assert ss(300, 256, 512, 1) == 0
+    assert ss(300, 256, 512, 2) >= 300 * 256 * 4
+    assert ss(16, 256, 512, 1) >= 16 * 256 * 4 + 16 * 512 * 2
+    assert ss(0, 256, 512, 1) == 0
+    if not torch.cuda.is_available():
+        # the device check comes before the size check
+        assert na(P, 256, P, 256, P, P, P, 4096, 1024, 4096, 256, 2, None) == dg.ERR_UNSUPPORTED_DEVICE
+        assert n() == dg.ERR_UNSUPPORTED_DEVICE
