@@ -71,6 +71,7 @@ SIGNATURES = {
     "detgemm_selftest_timeout": ([_I32, _P], _I32),
     "detgemm_w8a8_split_exact": ([_P, _I64, _P, _I64, _P, _P, _P, _I64, _I32, _I32, _I32, _I32, _P, _SZ, _P, _P],
                                  _I32),
+    "detgemm_epilogue_inject": ([_P, _I64, _I32, _P, _P, _I32, _I32, ctypes.c_uint32, _P, _I64, _I32, _I32, _P], _I32),
     "detgemm_ozaki_f32_split_exact": ([_P, _I64, _P, _I64, _P, _I64, _I32, _I32, _I32, _I32, _I32, _I32, _P, _SZ,
                                        _P, _P], _I32),
 }
@@ -510,6 +511,37 @@ def w8a8_f16ops(A16, W16, ea, ew, split_k: int = 1, out=None, ws=None, stream=No
                                  out.data_ptr(), _ld(out), M, N, K, split_k,
                                  wsb.data_ptr() if wsb is not None else None, wsn, _stream(stream))
     _check(st, "detgemm_w8a8_f16ops")
+    return out
+
+
+FAULT_NONE, FAULT_F1_SCALE_PRECISION, FAULT_F2_DOUBLE_ROUNDING, FAULT_F3_ORDER, FAULT_F4_TRUNCATION = 0, 1, 2, 3, 4
+SEVERITY_ONE, SEVERITY_ONE_PERCENT, SEVERITY_ALL = 0, 1, 2
+SCALES_POW2, SCALES_F32 = 0, 1
+
+
+def epilogue_inject(acc, sa, sw, fault: int = FAULT_NONE, severity: int = SEVERITY_ALL, seed: int = 0, out=None,
+                    stream=None) -> torch.Tensor:
+    """The W8A8 epilogue, or one injected fault (see include/detgemm_conformance.h), on exact
+    int32 accumulators acc [M, N]; sa [M] / sw [N] are int32 exponents (power-of-two scales)
+    or float32 scales. Returns bf16 [M, N]."""
+    lib = load()
+    _req(acc, torch.int32, "acc")
+    M, N = acc.shape
+    if sa.dtype == torch.int32 and sw.dtype == torch.int32:
+        scales = SCALES_POW2
+    elif sa.dtype == torch.float32 and sw.dtype == torch.float32:
+        scales = SCALES_F32
+    else:
+        raise TypeError("sa and sw must both be int32 exponents or both float32 scales")
+    _req(sa, sa.dtype, "sa"); _req(sw, sw.dtype, "sw")
+    if sa.shape != (M,) or sw.shape != (N,):
+        raise ValueError("shape mismatch")
+    if out is None:
+        out = empty2d(M, N, torch.bfloat16, acc.device)
+    _req(out, torch.bfloat16, "out")
+    st = lib.detgemm_epilogue_inject(acc.data_ptr(), _ld(acc), scales, sa.data_ptr(), sw.data_ptr(), fault, severity,
+                                     seed & 0xFFFFFFFF, out.data_ptr(), _ld(out), M, N, _stream(stream))
+    _check(st, "detgemm_epilogue_inject")
     return out
 
 

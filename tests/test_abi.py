@@ -13,6 +13,7 @@ import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "detgemm.h")
+HEADERS = sorted(os.path.join(ROOT, "include", f) for f in os.listdir(os.path.join(ROOT, "include")) if f.endswith(".h"))
 
 
 @pytest.fixture(scope="module")
@@ -24,7 +25,7 @@ def lib():
 
 
 def _declared():
-    src = open(HEADER).read()
+    src = "".join(open(h).read() for h in HEADERS)
     return sorted(set(re.findall(r"DETGEMM_API\s+[\w\s\*]*?\b(detgemm_\w+)\s*\(", src)))
 
 
