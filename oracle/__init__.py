@@ -32,7 +32,7 @@ _lock = threading.Lock()
 _lib = None
 
 OK, ERR_PRECONDITION, ERR_NONFINITE = 0, 3, 8
-BF16, F32 = 0, 1
+BF16, F32, F16 = 0, 1, 3
 NEAREST, CEIL = 0, 1
 ROWS, COLS = 0, 1
 
@@ -73,10 +73,11 @@ def _load():
             lib.oracle_ozaki_combine_f64.argtypes = [p, i64, i32, p, p, p, i64, i32, i32]
             lib.oracle_slice_f64.argtypes = [p, i64, i32, i32, i32, i32, p, p]
             lib.oracle_ozaki_f64.argtypes = [p, i64, p, i64, p, i64, i32, i32, i32, i32, i32, p, i32]
+            lib.oracle_gemm_blockfma.argtypes = [p, i64, p, i64, i32, i32, i32, p, i64, i32, i32, i32]
             for f in (lib.oracle_w8a8, lib.oracle_w8a8_bias, lib.oracle_gemm_s8_i32, lib.oracle_quantize_pow2,
                       lib.oracle_slice_f32, lib.oracle_ozaki_f32, lib.oracle_ozaki_diagonals,
                       lib.oracle_ozaki_combine, lib.oracle_ozaki_combine_f64, lib.oracle_slice_f64,
-                      lib.oracle_ozaki_f64):
+                      lib.oracle_ozaki_f64, lib.oracle_gemm_blockfma):
                 f.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -260,4 +261,20 @@ def ozaki_combine_f64(T, e, f):
     assert e.shape == (M,) and f.shape == (N,) and 1 <= nd <= 17
     C = np.empty((M, N), dtype=np.float64)
     _load().oracle_ozaki_combine_f64(T.ctypes.data, N, nd + 1, e.ctypes.data, f.ctypes.data, C.ctypes.data, N, M, N)
+    return C
+
+
+def gemm_blockfma(A, W, dtype=BF16, nfma=16, neab=2):
+    """Fixed-order fp16/bf16 GEMM under the tensor-core block-FMA model: A [M, K] and W [N, K]
+    as uint16 bit patterns (dtype BF16 or F16); returns fp32 bit patterns [M, N] (uint32)."""
+    A = _c(A, np.uint16)
+    W = _c(W, np.uint16)
+    M, K = A.shape
+    N = W.shape[0]
+    assert W.shape[1] == K
+    C = np.zeros((M, N), np.uint32)
+    st = _load().oracle_gemm_blockfma(A.ctypes.data, K, W.ctypes.data, K, dtype, nfma, neab, C.ctypes.data, N,
+                                      M, N, K)
+    if st != OK:
+        raise OracleError(f"oracle_gemm_blockfma: status {st}")
     return C
