@@ -32,7 +32,7 @@ LIB_PATH = os.path.join(_HERE, "libdetgemm.so")
 
 OK, ERR_INVALID_ARG, ERR_ALIGNMENT, ERR_PRECONDITION, ERR_WORKSPACE = 0, 1, 2, 3, 4
 ERR_UNSUPPORTED_DEVICE, ERR_CUDA, ERR_TIMEOUT, ERR_NONFINITE = 5, 6, 7, 8
-DTYPE_BF16, DTYPE_F32, DTYPE_F64 = 0, 1, 2
+DTYPE_BF16, DTYPE_F32, DTYPE_F64, DTYPE_F16 = 0, 1, 2, 3
 POW2_NEAREST, POW2_CEIL = 0, 1
 AXIS_ROWS, AXIS_COLS = 0, 1
 MAX_K = 131071
@@ -71,6 +71,7 @@ SIGNATURES = {
     "detgemm_selftest_timeout": ([_I32, _P], _I32),
     "detgemm_w8a8_split_exact": ([_P, _I64, _P, _I64, _P, _P, _P, _I64, _I32, _I32, _I32, _I32, _P, _SZ, _P, _P],
                                  _I32),
+    "detgemm_gemm_fixed_f16": ([_P, _I64, _P, _I64, _P, _I64, _I32, _I32, _I32, _I32, _P], _I32),
     "detgemm_epilogue_inject": ([_P, _I64, _I32, _P, _P, _I32, _I32, ctypes.c_uint32, _P, _I64, _I32, _I32, _P], _I32),
     "detgemm_ozaki_f32_split_exact": ([_P, _I64, _P, _I64, _P, _I64, _I32, _I32, _I32, _I32, _I32, _I32, _P, _SZ,
                                        _P, _P], _I32),
@@ -479,6 +480,27 @@ def ozaki_f64(A, B, nslices: int = 8, max_diag: int = 9, split_k: int = 1, out=N
                                M, N, K, nslices, max_diag, split_k,
                                wsb.data_ptr() if wsb is not None else None, wsn, _stream(stream))
     _check(st, "detgemm_ozaki_f64")
+    return out
+
+
+def gemm_fixed_f16(A, W, out=None, stream=None) -> torch.Tensor:
+    """Fixed-order fp16/bf16 GEMM C = A W^T (A [M,K], W [N,K], both float16 or both bfloat16):
+    K walked in 16-wide tensor-core block FMAs from +0, never split; fp32 [M, N] out."""
+    lib = load()
+    if A.dtype not in (torch.float16, torch.bfloat16) or W.dtype != A.dtype:
+        raise TypeError("A and W must both be float16 or both bfloat16")
+    _req(A, A.dtype, "A"); _req(W, W.dtype, "W")
+    M, K = A.shape
+    N = W.shape[0]
+    if W.shape[1] != K:
+        raise ValueError("shape mismatch")
+    if out is None:
+        out = empty2d(M, N, torch.float32, A.device)
+    _req(out, torch.float32, "out")
+    dt = DTYPE_BF16 if A.dtype == torch.bfloat16 else DTYPE_F16
+    st = lib.detgemm_gemm_fixed_f16(A.data_ptr(), _ld(A), W.data_ptr(), _ld(W), out.data_ptr(), _ld(out), M, N, K, dt,
+                                    _stream(stream))
+    _check(st, "detgemm_gemm_fixed_f16")
     return out
 
 

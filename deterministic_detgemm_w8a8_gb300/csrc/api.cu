@@ -589,6 +589,30 @@ detgemm_status detgemm_w8a8_f16ops(const uint16_t* A16, int64_t lda, const uint1
     return from_cuda(tc_gemm_launch(a, A16, lda, 1, W16, ldw, 1, K, ws, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+detgemm_status detgemm_gemm_fixed_f16(const uint16_t* A, int64_t lda, const uint16_t* W, int64_t ldw, float* C,
+                                      int64_t ldc, int M, int N, int K, int dtype, detgemm_stream_t stream) {
+    if (M < 0 || N < 0 || K < 1) return DETGEMM_ERR_INVALID_ARG;
+    if (dtype != DETGEMM_DTYPE_F16 && dtype != DETGEMM_DTYPE_BF16) return DETGEMM_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return DETGEMM_OK;
+    if (!A || !W || !C || lda < K || ldw < K || ldc < N) return DETGEMM_ERR_INVALID_ARG;
+    if (!aligned16(A) || !aligned16(W) || !aligned16(C)) return DETGEMM_ERR_ALIGNMENT;
+    if (lda % 8 || ldw % 8 || ldc % 4) return DETGEMM_ERR_ALIGNMENT;
+    detgemm_status st = check_device();
+    if (st != DETGEMM_OK) return st;
+    TcArgs a = {};
+    a.M = M;
+    a.N = N;
+    a.ndiag = 1;
+    a.diag_first[0] = 0;
+    a.diag_nseg[0] = 1;
+    a.split = 1;
+    a.mode = EPI_STORE_I32;
+    a.C = C;
+    a.ldc = ldc;
+    a.fp_mode = dtype == DETGEMM_DTYPE_BF16 ? 2 : 1;
+    return from_cuda(tc_gemm_launch(a, A, lda, 1, W, ldw, 1, K, nullptr, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 detgemm_status detgemm_selftest_timeout(int limit_ms, detgemm_stream_t stream) {
     if (limit_ms < 1 || limit_ms > 2000) return DETGEMM_ERR_INVALID_ARG;
     detgemm_status st = check_device();

@@ -343,8 +343,10 @@ static_assert(2 * 256 <= 512 && 2 * 192 <= 512, "two accumulator buffers in TMEM
 // TcArgs::extra_of (one group: plain round-robin, with no table walk in the loops); kBias:
 // the epilogue adds a bf16 bias per column before its rounding (EPI_BF16_POW2_BIAS; its
 // registers stay out of the other instantiations); kNarrow: the 256-wide geometry with
-// sixteen epilogue warps
-template <int BNT, bool kSplit, bool kGroups, bool kBias, bool kNarrow>
+// sixteen epilogue warps; kFloat: the fixed-order floating-point GEMM -- fp16 or bf16
+// operands (TcArgs::idesc_fp), the whole K range of a tile accumulated in one TMEM buffer in
+// K order (no chunk drains), and the raw fp32 accumulator stored (EPI_STORE_I32 layout)
+template <int BNT, bool kSplit, bool kGroups, bool kBias, bool kNarrow, bool kFloat = false>
 __global__ void __launch_bounds__(Geo<BNT, kNarrow>::THREADS, 1)
     tc2_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmS,
@@ -457,8 +459,9 @@ __global__ void __launch_bounds__(Geo<BNT, kNarrow>::THREADS, 1)
                 const Unit un = unit_of(p, u);
                 int f0, f1;
                 kb_range(p, un, f0, f1);
-                for (int c0 = f0; c0 < f1 && ok; c0 += CHUNK_KB) {
-                    const int c1 = min(f1, c0 + CHUNK_KB);
+                const int chunk = kFloat ? f1 - f0 : CHUNK_KB;  // kFloat: one accumulation over all of K
+                for (int c0 = f0; c0 < f1 && ok; c0 += chunk) {
+                    const int c1 = min(f1, c0 + chunk);
                     if (!mbar_wait(tempty + buf, tphase ^ 1u, abort_flag)) {
                         ok = false;
                         break;
@@ -476,7 +479,8 @@ __global__ void __launch_bounds__(Geo<BNT, kNarrow>::THREADS, 1)
                         const uint64_t bd = sdesc_sw128_kmajor(sa + P_A_BYTES);
 #pragma unroll
                         for (int k = 0; k < BK / 16; ++k)
-                            mma_f16_pair(dt, ad + 2 * k, bd + 2 * k, P_IDESC, (f > c0 || k > 0) ? 1u : 0u);
+                            mma_f16_pair(dt, ad + 2 * k, bd + 2 * k, kFloat ? p.idesc_fp : P_IDESC,
+                                         (f > c0 || k > 0) ? 1u : 0u);
                         mma_commit_pair_mc(empty + stage, 0x3);
                         if (++stage == P_STAGES) {
                             stage = 0;
@@ -510,7 +514,8 @@ __global__ void __launch_bounds__(Geo<BNT, kNarrow>::THREADS, 1)
             int32_t acc[COLS];
 #pragma unroll
             for (int i = 0; i < COLS; ++i) acc[i] = 0;
-            for (int c0 = f0; c0 < f1; c0 += CHUNK_KB) {
+            const int chunk = kFloat ? f1 - f0 : CHUNK_KB;
+            for (int c0 = f0; c0 < f1; c0 += chunk) {
                 const bool got = mbar_wait(tfull + buf, tphase, abort_flag);
                 if (!__all_sync(0xffffffffu, got)) {
                     ok = false;
@@ -526,7 +531,10 @@ __global__ void __launch_bounds__(Geo<BNT, kNarrow>::THREADS, 1)
                     tmem_ld16(ta + 16 * j, r);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) acc[16 * j + i] += __float2int_rn(__uint_as_float(r[i]));
+                    for (int i = 0; i < 16; ++i) {
+                        if constexpr (kFloat) acc[16 * j + i] = (int32_t)r[i];  // the fp32 bits as they are
+                        else acc[16 * j + i] += __float2int_rn(__uint_as_float(r[i]));
+                    }
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -686,9 +694,9 @@ static cudaError_t make_ws_map(CUtensorMap* m, void* base, int cut) {
 namespace {
 int g_max_clusters[64][2];  // per device: 256-wide, 192-wide tiles
 
-template <int BNT, bool kSplit, bool kGroups, bool kBias, bool kNarrow>
+template <int BNT, bool kSplit, bool kGroups, bool kBias, bool kNarrow, bool kFloat = false>
 cudaError_t opt_in() {
-    return cudaFuncSetAttribute(tc2_gemm_kernel<BNT, kSplit, kGroups, kBias, kNarrow>,
+    return cudaFuncSetAttribute(tc2_gemm_kernel<BNT, kSplit, kGroups, kBias, kNarrow, kFloat>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, Geo<BNT, kNarrow>::SMEM_BYTES);
 }
 
@@ -725,7 +733,8 @@ int max_pair_clusters(int bn) {
             opt_in<192, false, false, false, false>() != cudaSuccess ||
             opt_in<256, false, false, true, true>() != cudaSuccess ||
             opt_in<256, true, true, true, false>() != cudaSuccess ||
-            opt_in<192, false, false, true, false>() != cudaSuccess)
+            opt_in<192, false, false, true, false>() != cudaSuccess ||
+            opt_in<256, false, false, false, false, true>() != cudaSuccess)
             return 0;
         g_max_clusters[dev][0] = occupancy_clusters<256>();
         g_max_clusters[dev][1] = occupancy_clusters<192>();
@@ -781,7 +790,7 @@ static void assign_leftovers(TcArgs& a, int C) {
     }
 }
 
-template <int BNT, bool kSplit, bool kGroups, bool kBias, bool kNarrow>
+template <int BNT, bool kSplit, bool kGroups, bool kBias, bool kNarrow, bool kFloat = false>
 static cudaError_t launch_engine(const TcArgs& a, const CUtensorMap& tmA, const CUtensorMap& tmB,
                                  const CUtensorMap& tmC, const CUtensorMap& tmS, int clusters, cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};
@@ -798,7 +807,8 @@ static cudaError_t launch_engine(const TcArgs& a, const CUtensorMap& tmA, const 
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, tc2_gemm_kernel<BNT, kSplit, kGroups, kBias, kNarrow>, tmA, tmB, tmC, tmS, a);
+    cudaError_t e =
+        cudaLaunchKernelEx(&cfg, tc2_gemm_kernel<BNT, kSplit, kGroups, kBias, kNarrow, kFloat>, tmA, tmB, tmC, tmS, a);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -821,7 +831,10 @@ cudaError_t tc_gemm_launch(const TcArgs& a0, const void* A16, int64_t lda, int a
         while (a.split > 1 && (tiles * a.split > c256 || kext / a.split < 256)) --a.split;
     }
     if (split_run) *split_run = a.split;
-    const int bn = bias && a.split > 1 ? 256 : choose_bn(a);
+    if (a.fp_mode && (a.split != 1 || a.ndiag != 1 || a.mode != EPI_STORE_I32)) return cudaErrorInvalidValue;
+    if (a.fp_mode)  // kind::f16 with fp16 (mode 1) or bf16 (mode 2) operands, fp32 accumulator
+        a.idesc_fp = Geo<256>::IDESC | (a.fp_mode == 2 ? (1u << 7) | (1u << 10) : 0u);
+    const int bn = a.fp_mode || (bias && a.split > 1) ? 256 : choose_bn(a);
     set_tiles(a, kext, bn);
     CUtensorMap tmA, tmB, tmC;
     cudaError_t e = make_map(&tmA, A16, kext, lda, a.M, a_planes, 128);
@@ -853,6 +866,7 @@ cudaError_t tc_gemm_launch(const TcArgs& a0, const void* A16, int64_t lda, int a
     // from 2048 x 4096 x 1024: 38 -> 31 us to 8192 x 6144 x 2048: 158 -> 160 us).
     const long long rounds = (total + clusters - 1) / clusters;
     const bool narrow = kext <= 1024 || rounds * kext <= 12288;
+    if (a.fp_mode) return launch_engine<256, false, false, false, false, true>(a, tmA, tmB, tmC, tmS, clusters, s);
     if (bias && a.split > 1) return launch_engine<256, true, true, true, false>(a, tmA, tmB, tmC, tmS, clusters, s);
     if (bias && bn == 192) return launch_engine<192, false, false, true, false>(a, tmA, tmB, tmC, tmS, clusters, s);
     if (bias) return launch_engine<256, false, false, true, true>(a, tmA, tmB, tmC, tmS, clusters, s);

@@ -113,6 +113,9 @@ struct TcArgs {
     int64_t c_plane;           // elements between int32 output planes
     int32_t* ws_acc;           // set by the launcher (split > 1): [tile units][256][256] sums
     uint32_t* ws_cnt;          // [tile units][2 CTAs][epilogue warps] arrival counters
+    int fp_mode;               // 1 / 2: the fixed-order floating-point GEMM on fp16 / bf16
+                               // operands (one group, split 1, EPI_STORE_I32 layout holding fp32 bits)
+    uint32_t idesc_fp;         // its MMA instruction descriptor (set by the launcher)
 };
 
 int64_t tc_padded_k(int K);
