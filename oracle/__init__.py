@@ -20,6 +20,7 @@ from __future__ import annotations
 
 import ctypes
 import os
+import platform
 import subprocess
 import threading
 
@@ -45,9 +46,11 @@ def build(force: bool = False) -> str:
     """Compile ``oracle.c`` into ``liboracle.so`` (gcc -O2, no FP contraction, OpenMP)."""
     if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
         tmp = _LIB + f".tmp{os.getpid()}"
+        # binary128 arithmetic: long double on AArch64, __float128 with libquadmath elsewhere
+        quad = [] if platform.machine() in ("aarch64", "arm64") else ["-lquadmath"]
         subprocess.check_call(
             ["gcc", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared",
-             "-fopenmp", _SRC, "-o", tmp, "-lm"])
+             "-fopenmp", _SRC, "-o", tmp, "-lm"] + quad)
         os.replace(tmp, _LIB)
     return _LIB
 
@@ -74,10 +77,13 @@ def _load():
             lib.oracle_slice_f64.argtypes = [p, i64, i32, i32, i32, i32, p, p]
             lib.oracle_ozaki_f64.argtypes = [p, i64, p, i64, p, i64, i32, i32, i32, i32, i32, p, i32]
             lib.oracle_gemm_blockfma.argtypes = [p, i64, p, i64, i32, i32, i32, p, i64, i32, i32, i32]
+            lib.oracle_silu_mul_bf16.argtypes = [i32, i32, i32, i32, p]
+            lib.oracle_w8a8_swiglu.argtypes = [p, i64, p, p, i64, p, p, p, p, i64, i32, i32, i32, p, i32]
             for f in (lib.oracle_w8a8, lib.oracle_w8a8_bias, lib.oracle_gemm_s8_i32, lib.oracle_quantize_pow2,
                       lib.oracle_slice_f32, lib.oracle_ozaki_f32, lib.oracle_ozaki_diagonals,
                       lib.oracle_ozaki_combine, lib.oracle_ozaki_combine_f64, lib.oracle_slice_f64,
-                      lib.oracle_ozaki_f64, lib.oracle_gemm_blockfma):
+                      lib.oracle_ozaki_f64, lib.oracle_gemm_blockfma, lib.oracle_silu_mul_bf16,
+                      lib.oracle_w8a8_swiglu):
                 f.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -277,4 +283,32 @@ def gemm_blockfma(A, W, dtype=BF16, nfma=16, neab=2):
                                       M, N, K)
     if st != OK:
         raise OracleError(f"oracle_gemm_blockfma: status {st}")
+    return C
+
+
+def silu_mul_bf16(gacc: int, uacc: int, Eg: int, Eu: int) -> int:
+    """bf16 bits of rne(SiLU(g) * u) for g = gacc * 2^Eg, u = uacc * 2^Eu (exact reals)."""
+    out = ctypes.c_uint16(0)
+    st = _load().oracle_silu_mul_bf16(int(gacc), int(uacc), int(Eg), int(Eu), ctypes.byref(out))
+    if st != OK:
+        raise OracleError(f"oracle_silu_mul_bf16: status {st}")
+    return int(out.value)
+
+
+def w8a8_swiglu(A, Wg, Wu, ea, ewg, ewu, rows=None):
+    """C = rne_bf16(SiLU(A Wg^T * 2^(ea+ewg)) * (A Wu^T * 2^(ea+ewu))), exact sums, one rounding."""
+    A = _c(A, np.int8)
+    Wg = _c(Wg, np.int8)
+    Wu = _c(Wu, np.int8)
+    ea, ewg, ewu = (_c(x, np.int32) for x in (ea, ewg, ewu))
+    M, K = A.shape
+    N = Wg.shape[0]
+    assert Wg.shape == Wu.shape == (N, K)
+    r, nr = _rows(rows)
+    C = np.zeros((nr if rows is not None else M, N), np.uint16)
+    st = _load().oracle_w8a8_swiglu(A.ctypes.data, K, Wg.ctypes.data, Wu.ctypes.data, K, ea.ctypes.data,
+                                    ewg.ctypes.data, ewu.ctypes.data, C.ctypes.data, N, M, N, K,
+                                    r.ctypes.data if r is not None else None, nr)
+    if st != OK:
+        raise OracleError(f"oracle_w8a8_swiglu: status {st}")
     return C

@@ -557,3 +557,133 @@ int oracle_gemm_blockfma(const uint16_t* A, int64_t lda, const uint16_t* W, int6
     }
     return 0;
 }
+
+/* ------------------------------------------------------------------------------------
+ * Gated linear unit epilogue (SiLU(gate) * up), rounded once to bf16. The gate and up GEMMs
+ * of a W8A8 FFN give exact int32 accumulators; with power-of-two scales the exact values are
+ * g = gacc * 2^Eg and u = uacc * 2^Eu ("Deterministic LLM Inference ...", §II "Pipeline and
+ * alibi": the epilogue rounds once). The output is the one round-to-nearest-even of the real
+ * number y = SiLU(g) * u = g * u / (1 + e^-g) to bf16 (subnormals kept, overflow to inf).
+ * y is evaluated in 113-bit floating point (IEEE binary128: __float128 with libquadmath on
+ * x86-64, long double on AArch64), whose relative error here is below 2^-100; a y within
+ * that bound of a rounding boundary is decided by the rule below or reported (status 9).
+ *  - gacc == 0 or uacc == 0: y = 0 exactly, result +0.
+ *  - y rounds to zero magnitude only when |y| < 2^-134: the sign is that of g * u.
+ *  - the only y the 113-bit value cannot place is P * sigma(g) for large g > 0 with the exact
+ *    dyadic P = g * u on a rounding boundary (a midpoint); then y is strictly smaller in
+ *    magnitude than P (0 < sigma(g) < 1), so it rounds toward zero from P.
+ * ------------------------------------------------------------------------------------ */
+#if defined(__aarch64__)
+typedef long double qreal;
+#define QEXP expl
+#define QLDEXP ldexpl
+#define QFREXP frexpl
+#define QFLOOR floorl
+#else
+#include <quadmath.h>
+typedef __float128 qreal;
+#define QEXP expq
+#define QLDEXP ldexpq
+#define QFREXP frexpq
+#define QFLOOR floorq
+#endif
+
+/* bf16 rounding of a positive quad y known to relative error releps: 0 ok, 1 undecidable
+ * (with *at_mid = 1 when the value sits within the bound of a midpoint) */
+static int bf16_round_quad(qreal y, qreal releps, uint16_t* mag, int* at_mid) {
+    *at_mid = 0;
+    int e;
+    QFREXP(y, &e); /* y = f * 2^e, f in [0.5, 1): leading bit 2^(e-1) */
+    int lead = e - 1;
+    qreal m;    /* y in units of the bf16 spacing at y */
+    int base;   /* bit pattern of the bf16 value m = 0 (units of the spacing) in this binade */
+    if (lead >= -126) {
+        if (lead > 127) {
+            *mag = 0x7F80;
+            return 0;
+        }
+        m = QLDEXP(y, 7 - lead); /* in [128, 256) */
+        base = ((lead + 127) << 7) - 128;
+    } else {
+        m = QLDEXP(y, 133); /* units of 2^-133, in [0, 128) */
+        base = 0;
+    }
+    qreal fl = QFLOOR(m);
+    qreal fr = m - fl;
+    qreal tol = releps * m;
+    qreal d = fr - (qreal)0.5;
+    if (d < 0) d = -d;
+    if (d <= tol) {
+        *at_mid = 1;
+        *mag = (uint16_t)(base + (int)fl); /* the value below the midpoint */
+        return 1;
+    }
+    int q = (int)fl + (fr > (qreal)0.5 ? 1 : 0);
+    int bits = base + q; /* a carry into the next binade or to inf works by itself */
+    if (bits > 0x7F80) bits = 0x7F80;
+    *mag = (uint16_t)bits;
+    return 0;
+}
+
+int oracle_silu_mul_bf16(int32_t gacc, int32_t uacc, int32_t Eg, int32_t Eu, uint16_t* out) {
+    if (gacc == 0 || uacc == 0) {
+        *out = 0x0000;
+        return 0;
+    }
+    if (Eg < -16000 || Eg > 16000 || Eu < -16000 || Eu > 16000) return 3;
+    const qreal g = QLDEXP((qreal)gacc, Eg);
+    const qreal u = QLDEXP((qreal)uacc, Eu);
+    const int neg = (gacc < 0) != (uacc < 0);
+    const qreal P = g * u; /* exact: two 31-bit significands */
+    const qreal y = P / (1 + QEXP(-g));
+    const qreal ay = y < 0 ? -y : y;
+    if (ay == 0 || ay < QLDEXP((qreal)1, -134)) {
+        *out = neg ? 0x8000 : 0x0000;
+        return 0;
+    }
+    uint16_t mag;
+    int at_mid;
+    if (bf16_round_quad(ay, QLDEXP((qreal)1, -100), &mag, &at_mid) == 0) {
+        *out = (uint16_t)(mag | (neg ? 0x8000 : 0));
+        return 0;
+    }
+    /* within 2^-100 of a midpoint: only P on a midpoint with e^-g below the precision (g > 0
+     * large) can land here; y is just below |P|, which rounds toward zero */
+    uint16_t pmag;
+    int pmid;
+    const qreal aP = P < 0 ? -P : P;
+    if (g > 0 && bf16_round_quad(aP, 0, &pmag, &pmid) == 1 && pmid && ay <= aP) {
+        *out = (uint16_t)(pmag | (neg ? 0x8000 : 0));
+        return 0;
+    }
+    return 9;
+}
+
+/* C = rne_bf16(SiLU(g) * u) for the gate GEMM A Wg^T and the up GEMM A Wu^T (int64 sums,
+ * exponents ea_i + ewg_j and ea_i + ewu_j); rows: optional subset of output rows */
+int oracle_w8a8_swiglu(const int8_t* A, int64_t lda, const int8_t* Wg, const int8_t* Wu, int64_t ldw,
+                       const int32_t* ea, const int32_t* ewg, const int32_t* ewu, uint16_t* C, int64_t ldc, int M,
+                       int N, int K, const int32_t* rows, int nrows) {
+    const int R = rows ? nrows : M;
+    int status = 0;
+#pragma omp parallel for schedule(dynamic)
+    for (int r = 0; r < R; ++r) {
+        const int i = rows ? rows[r] : r;
+        for (int j = 0; j < N; ++j) {
+            int64_t g = 0, u = 0;
+            for (int k = 0; k < K; ++k) {
+                g += (int64_t)A[(int64_t)i * lda + k] * Wg[(int64_t)j * ldw + k];
+                u += (int64_t)A[(int64_t)i * lda + k] * Wu[(int64_t)j * ldw + k];
+            }
+            int st = 3;
+            if (g > INT32_MIN && g <= INT32_MAX && u > INT32_MIN && u <= INT32_MAX)
+                st = oracle_silu_mul_bf16((int32_t)g, (int32_t)u, ea[i] + ewg[j], ea[i] + ewu[j],
+                                          &C[(int64_t)r * ldc + j]);
+            if (st) {
+#pragma omp atomic write
+                status = st;
+            }
+        }
+    }
+    return status;
+}
