@@ -31,7 +31,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libdetgemm.so")
 
 OK, ERR_INVALID_ARG, ERR_ALIGNMENT, ERR_PRECONDITION, ERR_WORKSPACE = 0, 1, 2, 3, 4
-ERR_UNSUPPORTED_DEVICE, ERR_CUDA, ERR_TIMEOUT, ERR_NONFINITE = 5, 6, 7, 8
+ERR_UNSUPPORTED_DEVICE, ERR_CUDA, ERR_TIMEOUT, ERR_NONFINITE, ERR_RANGE = 5, 6, 7, 8, 9
 DTYPE_BF16, DTYPE_F32, DTYPE_F64, DTYPE_F16 = 0, 1, 2, 3
 POW2_NEAREST, POW2_CEIL = 0, 1
 AXIS_ROWS, AXIS_COLS = 0, 1
@@ -71,6 +71,7 @@ SIGNATURES = {
     "detgemm_selftest_timeout": ([_I32, _P], _I32),
     "detgemm_w8a8_split_exact": ([_P, _I64, _P, _I64, _P, _P, _P, _I64, _I32, _I32, _I32, _I32, _P, _SZ, _P, _P],
                                  _I32),
+    "detgemm_swiglu_bf16": ([_P, _I64, _P, _I64, _P, _P, _P, _P, _I64, _I32, _I32, _P], _I32),
     "detgemm_gemm_fixed_f16": ([_P, _I64, _P, _I64, _P, _I64, _I32, _I32, _I32, _I32, _P], _I32),
     "detgemm_epilogue_inject": ([_P, _I64, _I32, _P, _P, _I32, _I32, ctypes.c_uint32, _P, _I64, _I32, _I32, _P], _I32),
     "detgemm_ozaki_f32_split_exact": ([_P, _I64, _P, _I64, _P, _I64, _I32, _I32, _I32, _I32, _I32, _I32, _P, _SZ,
@@ -480,6 +481,24 @@ def ozaki_f64(A, B, nslices: int = 8, max_diag: int = 9, split_k: int = 1, out=N
                                M, N, K, nslices, max_diag, split_k,
                                wsb.data_ptr() if wsb is not None else None, wsn, _stream(stream))
     _check(st, "detgemm_ozaki_f64")
+    return out
+
+
+def swiglu_bf16(G, U, ea, ewg, ewu, out=None, stream=None) -> torch.Tensor:
+    """C = rne_bf16(SiLU(G 2^(ea+ewg)) * U 2^(ea+ewu)) on exact int32 accumulators G, U [M, N]
+    (ea int32 [M], ewg / ewu int32 [N]); bf16 [M, N] out, rounded once."""
+    lib = load()
+    _req(G, torch.int32, "G"); _req(U, torch.int32, "U")
+    _req(ea, torch.int32, "ea"); _req(ewg, torch.int32, "ewg"); _req(ewu, torch.int32, "ewu")
+    M, N = G.shape
+    if U.shape != (M, N) or ea.shape != (M,) or ewg.shape != (N,) or ewu.shape != (N,):
+        raise ValueError("shape mismatch")
+    if out is None:
+        out = empty2d(M, N, torch.bfloat16, G.device)
+    _req(out, torch.bfloat16, "out")
+    st = lib.detgemm_swiglu_bf16(G.data_ptr(), _ld(G), U.data_ptr(), _ld(U), ea.data_ptr(), ewg.data_ptr(),
+                                 ewu.data_ptr(), out.data_ptr(), _ld(out), M, N, _stream(stream))
+    _check(st, "detgemm_swiglu_bf16")
     return out
 
 

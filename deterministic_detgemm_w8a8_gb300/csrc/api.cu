@@ -108,6 +108,7 @@ const char* detgemm_status_string(detgemm_status s) {
         case DETGEMM_ERR_CUDA: return "DETGEMM_ERR_CUDA";
         case DETGEMM_ERR_TIMEOUT: return "DETGEMM_ERR_TIMEOUT";
         case DETGEMM_ERR_NONFINITE: return "DETGEMM_ERR_NONFINITE";
+        case DETGEMM_ERR_RANGE: return "DETGEMM_ERR_RANGE";
     }
     return "DETGEMM_ERR_UNKNOWN";
 }
@@ -613,6 +614,20 @@ detgemm_status detgemm_gemm_fixed_f16(const uint16_t* A, int64_t lda, const uint
     return from_cuda(tc_gemm_launch(a, A, lda, 1, W, ldw, 1, K, nullptr, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+detgemm_status detgemm_swiglu_bf16(const int32_t* G, int64_t ldg, const int32_t* U, int64_t ldu, const int32_t* ea,
+                                   const int32_t* ewg, const int32_t* ewu, uint16_t* C, int64_t ldc, int M, int N,
+                                   detgemm_stream_t stream) {
+    if (M < 0 || N < 0) return DETGEMM_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return DETGEMM_OK;
+    if (!G || !U || !ea || !ewg || !ewu || !C || ldg < N || ldu < N || ldc < N) return DETGEMM_ERR_INVALID_ARG;
+    if (!aligned4(G) || !aligned4(U) || !aligned4(ea) || !aligned4(ewg) || !aligned4(ewu) || !aligned2(C))
+        return DETGEMM_ERR_ALIGNMENT;
+    detgemm_status st = check_device();
+    if (st != DETGEMM_OK) return st;
+    return from_cuda(swiglu_epilogue_launch(G, ldg, U, ldu, ea, ewg, ewu, C, ldc, M, N,
+                                            reinterpret_cast<cudaStream_t>(stream)));
+}
+
 detgemm_status detgemm_selftest_timeout(int limit_ms, detgemm_stream_t stream) {
     if (limit_ms < 1 || limit_ms > 2000) return DETGEMM_ERR_INVALID_ARG;
     detgemm_status st = check_device();
@@ -631,8 +646,11 @@ detgemm_status detgemm_get_device_status(detgemm_stream_t stream) {
     v |= bits;
     if (skinny_take_status(&bits) != cudaSuccess) return DETGEMM_ERR_CUDA;
     v |= bits;
+    if (swiglu_take_status(&bits) != cudaSuccess) return DETGEMM_ERR_CUDA;
+    v |= bits;
     if (v & DEV_TIMEOUT) return DETGEMM_ERR_TIMEOUT;
     if (v & DEV_NONFINITE) return DETGEMM_ERR_NONFINITE;
+    if (v & DEV_RANGE) return DETGEMM_ERR_RANGE;
     return DETGEMM_OK;
 }
 

@@ -11,7 +11,7 @@
 namespace detgemm {
 
 // Device status bits (first error wins in the host-visible translation).
-enum : uint32_t { DEV_NONFINITE = 1u, DEV_TIMEOUT = 2u };
+enum : uint32_t { DEV_NONFINITE = 1u, DEV_TIMEOUT = 2u, DEV_RANGE = 4u };
 
 // Device status word. Every translation unit that raises a device-side condition owns
 // one (internal linkage, so no relocatable device code is needed) and exports a host

@@ -138,6 +138,12 @@ cudaError_t widen_pair_launch(const int8_t* X0, int64_t ldx0, int rows0, int K0,
 cudaError_t widen_i8_f16_launch(const int8_t* X, int64_t ldx, int rows, int K, void* Y, int64_t Kp,
                                 cudaStream_t s);
 
+// rne_bf16(SiLU(G 2^(ea+ewg)) * U 2^(ea+ewu)) element by element (swiglu.cu)
+cudaError_t swiglu_epilogue_launch(const int32_t* G, int64_t ldg, const int32_t* U, int64_t ldu, const int32_t* ea,
+                                   const int32_t* ewg, const int32_t* ewu, uint16_t* C, int64_t ldc, int M, int N,
+                                   cudaStream_t s);
+cudaError_t swiglu_take_status(uint32_t* bits);
+
 // 1 when the current device is a compute-capability 10.3 GPU (checked once per device).
 int device_is_supported();
 

@@ -60,7 +60,8 @@ typedef enum detgemm_status {
     DETGEMM_ERR_UNSUPPORTED_DEVICE = 5, /* current device is not compute capability 10.3 */
     DETGEMM_ERR_CUDA = 6,               /* a CUDA runtime call or launch failed */
     DETGEMM_ERR_TIMEOUT = 7,            /* a bounded device-side wait expired */
-    DETGEMM_ERR_NONFINITE = 8           /* inf or NaN in a floating-point input */
+    DETGEMM_ERR_NONFINITE = 8,          /* inf or NaN in a floating-point input */
+    DETGEMM_ERR_RANGE = 9               /* a scale exponent outside an epilogue's range */
 } detgemm_status;
 
 enum { DETGEMM_DTYPE_BF16 = 0, DETGEMM_DTYPE_F32 = 1, DETGEMM_DTYPE_F64 = 2, DETGEMM_DTYPE_F16 = 3 };
@@ -338,6 +339,28 @@ DETGEMM_API detgemm_status detgemm_widen_i8_f16(const int8_t* X, int64_t ldx, in
                                                 int64_t ldy, detgemm_stream_t stream);
 
 /*
+ * Gated-linear-unit epilogue on exact accumulators [P4 §II "Pipeline and alibi": the epilogue
+ * is one rounding of the exactly scaled int32 accumulator; an FFN's gate SiLU(g) = g / (1 + e^-g)
+ * and the product with the up projection join before that rounding]:
+ *     g = G_ij 2^(ea_i + ewg_j),  u = U_ij 2^(ea_i + ewu_j)          (exact)
+ *     C_ij = rne_bf16(SiLU(g) * u)            (one rounding of the real value; +0 when g or u is 0)
+ * The value is transcendental; it is evaluated in fp32, fp64 and double-double arithmetic
+ * in turn, each with a proven error bound, until no bf16 rounding boundary lies within the
+ * bound (a gate g >= 64 is decided exactly from g * u), so the result is the correctly
+ * rounded one and depends on the operands alone.
+ *   G, U  int32 [M x N] (e.g. from detgemm_gemm_s8_i32 on the gate and up weights), row
+ *         strides ldg, ldu;   ea int32 [M], ewg, ewu int32 [N];   C bf16 bits [M x N] (ldc)
+ * The exponent sums ea_i + ewg_j and ea_i + ewu_j must lie in [-60, 40]; otherwise that
+ * output is a NaN and DETGEMM_ERR_RANGE is set in the device status word (also raised, at a
+ * rate far below one in 2^60 outputs, by a value within 2^-90 of a rounding boundary).
+ * All pointers device memory, 4-byte aligned (C 2-byte). Errors: INVALID_ARG, ALIGNMENT,
+ * UNSUPPORTED_DEVICE, CUDA.
+ */
+DETGEMM_API detgemm_status detgemm_swiglu_bf16(const int32_t* G, int64_t ldg, const int32_t* U, int64_t ldu,
+                                               const int32_t* ea, const int32_t* ewg, const int32_t* ewu,
+                                               uint16_t* C, int64_t ldc, int M, int N, detgemm_stream_t stream);
+
+/*
  * Fixed-order (batch-invariant) fp16 / bf16 GEMM. A floating-point GEMM's bits are fixed by
  * its reduction order, which can be written down as a descriptor [P1 §3.2.1-§3.2.2]; here the
  * order is the tensor core's own, one block FMA per 16 products ["GPU Arithmetic Emulator"
@@ -410,7 +433,7 @@ DETGEMM_API detgemm_status detgemm_selftest_timeout(int limit_ms, detgemm_stream
 
 /*
  * Synchronizes `stream`, then returns and clears the current device's status word:
- * DETGEMM_OK, DETGEMM_ERR_NONFINITE or DETGEMM_ERR_TIMEOUT (the first one raised
+ * DETGEMM_OK, DETGEMM_ERR_NONFINITE, DETGEMM_ERR_TIMEOUT or DETGEMM_ERR_RANGE (the first one raised
  * since the last read), or DETGEMM_ERR_CUDA if the synchronization itself failed.
  */
 DETGEMM_API detgemm_status detgemm_get_device_status(detgemm_stream_t stream);

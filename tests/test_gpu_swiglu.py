@@ -1,0 +1,121 @@
+"""GPU parity of the gated-linear-unit epilogue rne_bf16(SiLU(g) * u) with the oracle
+(binary128 evaluation, pinned to mpmath), bit for bit: random accumulators over the whole
+int32 range and exponent domain, inputs within 2^-20 and 2^-52 of a bf16 rounding boundary
+(the fp64 and double-double evaluations), large gates whose product sits on a midpoint, deep
+negative gates, subnormal and overflowing outputs, exponents outside the domain (NaN and
+DETGEMM_ERR_RANGE), and the composition with the library's exact int32 GEMM."""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from gpu_util import bf16_bits, cuda, dg, to_dev
+
+pytestmark = pytest.mark.gpu
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+@pytest.fixture(scope="module")
+def dev():
+    return cuda()
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return dg()
+
+
+def _run(lib, dev, G, U, ea, ewg, ewu):
+    return bf16_bits(lib.swiglu_bf16(to_dev(G, dev), to_dev(U, dev), to_dev(ea, dev), to_dev(ewg, dev),
+                                     to_dev(ewu, dev)))
+
+
+def _want(oracle_mod, G, U, ea, ewg, ewu):
+    M, N = G.shape
+    return np.array([[oracle_mod.silu_mul_bf16(int(G[i, j]), int(U[i, j]), int(ea[i] + ewg[j]), int(ea[i] + ewu[j]))
+                      for j in range(N)] for i in range(M)], np.uint16)
+
+
+@pytest.mark.parametrize("kind", ["ffn", "full", "large", "deep"])
+def test_random_accumulators(lib, dev, oracle_mod, kind):
+    rng = np.random.default_rng({"ffn": 1, "full": 2, "large": 3, "deep": 4}[kind])
+    M, N = 48, 160
+    if kind == "ffn":
+        G = rng.integers(-2 ** 22, 2 ** 22, (M, N)); U = rng.integers(-2 ** 22, 2 ** 22, (M, N))
+        ea = rng.integers(-12, -6, M); ewg = rng.integers(-12, -6, N); ewu = rng.integers(-12, -6, N)
+    elif kind == "full":
+        G = rng.integers(-2 ** 31 + 1, 2 ** 31, (M, N)); U = rng.integers(-2 ** 31 + 1, 2 ** 31, (M, N))
+        ea = rng.integers(-30, -10, M); ewg = rng.integers(-30, 5, N); ewu = rng.integers(-30, 50, N)
+    elif kind == "large":  # gates from ~30 to ~2^40
+        G = rng.integers(2 ** 10, 2 ** 31, (M, N)) * rng.choice([-1, 1], (M, N))
+        U = rng.integers(-2 ** 16, 2 ** 16, (M, N))
+        ea = rng.integers(-5, 0, M); ewg = rng.integers(-25, 10, N); ewu = rng.integers(-20, 0, N)
+    else:  # gates around -40 .. -2000: tiny, subnormal and zero outputs
+        G = -rng.integers(2 ** 20, 2 ** 30, (M, N)); U = rng.integers(1, 2 ** 31, (M, N))
+        ea = rng.integers(-20, -15, M); ewg = rng.integers(-8, 0, N); ewu = rng.integers(15, 55, N)
+    G, U = G.astype(np.int32), U.astype(np.int32)
+    ea, ewg, ewu = (x.astype(np.int32) for x in (ea, ewg, ewu))
+    got = _run(lib, dev, G, U, ea, ewg, ewu)
+    want = _want(oracle_mod, G, U, ea, ewg, ewu)
+    assert (got == want).all(), int((got != want).sum())
+    assert lib.device_status() == lib.OK
+
+
+def test_inputs_near_rounding_boundaries(lib, dev, oracle_mod):
+    rows = [line.split() for line in open(os.path.join(HERE, "golden", "swiglu_hard_inputs.txt"))
+            if not line.startswith("#")]
+    n = len(rows)
+    G = np.array([[int(r[0]) for r in rows]], np.int32)
+    U = np.array([[int(r[1]) for r in rows]], np.int32)
+    ea = np.zeros(1, np.int32)
+    ewg = np.array([int(r[2]) for r in rows], np.int32)
+    ewu = np.array([int(r[3]) for r in rows], np.int32)
+    got = _run(lib, dev, G, U, ea, ewg, ewu)
+    want = _want(oracle_mod, G, U, ea, ewg, ewu)
+    assert (got == want).all(), [rows[j] for j in np.nonzero(got[0] != want[0])[0]]
+    assert lib.device_status() == lib.OK
+    assert sum(r[4] == "fp64-ambiguous" for r in rows) >= 10 and n >= 50
+
+
+def test_special_values(lib, dev, oracle_mod):
+    # large gates with g * u on a midpoint; zero operands; deep negative gates; subnormal and
+    # overflowing outputs
+    cases = [(128, 259, 0, -7), (128, -259, 0, -7), (96, 1029, 0, -3), (2 ** 20, 513, -10, 0),
+             (0, 5, 0, 0), (7, 0, 0, 0), (-1400, 3, -1, 0), (-(2 ** 30), 2 ** 30, -20, 40),
+             (-90, 2 ** 30, 0, -40), (-88, 1, 0, 30), (2 ** 30, 2 ** 30, 40, 30), (-(2 ** 30), 2 ** 30, 40, 30),
+             (1, 1, 0, 0), (-3, 5, -2, -1), (80, 3, 0, 0), (-80, 3, 0, 0), (64, 129, 0, 0), (63, 129, 0, 0)]
+    G = np.array([[c[0] for c in cases]], np.int32)
+    U = np.array([[c[1] for c in cases]], np.int32)
+    ewg = np.array([c[2] for c in cases], np.int32)
+    ewu = np.array([c[3] for c in cases], np.int32)
+    ea = np.zeros(1, np.int32)
+    got = _run(lib, dev, G, U, ea, ewg, ewu)
+    want = _want(oracle_mod, G, U, ea, ewg, ewu)
+    assert (got == want).all(), [(cases[j], hex(got[0, j]), hex(want[0, j])) for j in np.nonzero(got[0] != want[0])[0]]
+    assert got[0, 0] == 0x4381 and got[0, 10] == 0x7F80
+
+
+def test_exponents_outside_the_domain(lib, dev):
+    G = np.array([[5, 5, 5]], np.int32)
+    U = np.array([[3, 3, 3]], np.int32)
+    got = _run(lib, dev, G, U, np.zeros(1, np.int32), np.array([41, 0, 0], np.int32), np.array([0, -61, 0], np.int32))
+    assert got[0, 0] == 0x7FC0 and got[0, 1] == 0x7FC0 and got[0, 2] != 0x7FC0
+    assert lib.device_status() == lib.ERR_RANGE
+    assert lib.device_status() == lib.OK  # read and cleared
+
+
+def test_composition_with_the_int32_gemm(lib, dev, oracle_mod):
+    rng = np.random.default_rng(6)
+    M, N, K = 96, 320, 1000
+    A = np.clip(np.rint(rng.standard_normal((M, K)) * 30), -127, 127).astype(np.int8)
+    Wg = np.clip(np.rint(rng.standard_normal((N, K)) * 30), -127, 127).astype(np.int8)
+    Wu = np.clip(np.rint(rng.standard_normal((N, K)) * 30), -127, 127).astype(np.int8)
+    ea = rng.integers(-14, -6, M).astype(np.int32)
+    ewg = rng.integers(-14, -6, N).astype(np.int32)
+    ewu = rng.integers(-14, -6, N).astype(np.int32)
+    pad = lambda x: torch.nn.functional.pad(torch.from_numpy(x), (0, 8)).to(dev)[:, :K]
+    G = lib.gemm_s8_i32(pad(A), pad(Wg))
+    U = lib.gemm_s8_i32(pad(A), pad(Wu))
+    got = bf16_bits(lib.swiglu_bf16(G, U, to_dev(ea, dev), to_dev(ewg, dev), to_dev(ewu, dev)))
+    assert (got == oracle_mod.w8a8_swiglu(A, Wg, Wu, ea, ewg, ewu)).all()

@@ -99,3 +99,15 @@ def test_gemm_composition(oracle_mod):
             assert C[i, j] == _mp_ref(g, u, int(ea[i] + ewg[j]), int(ea[i] + ewu[j]))
     rows = [4, 1]
     assert (oracle_mod.w8a8_swiglu(A, Wg, Wu, ea, ewg, ewu, rows=rows) == C[rows]).all()
+
+
+def test_hard_inputs_near_midpoints(oracle_mod):
+    # inputs within 2^-20 / 2^-52 of a rounding boundary (tests/golden/make_swiglu_hard_inputs.py)
+    n = 0
+    for line in open(os.path.join(HERE, "golden", "swiglu_hard_inputs.txt")):
+        if line.startswith("#"):
+            continue
+        g, u, eg, eu, _ = line.split()
+        assert oracle_mod.silu_mul_bf16(int(g), int(u), int(eg), int(eu)) == _mp_ref(int(g), int(u), int(eg), int(eu))
+        n += 1
+    assert n >= 50
