@@ -71,6 +71,8 @@ SIGNATURES = {
     "detgemm_selftest_timeout": ([_I32, _P], _I32),
     "detgemm_w8a8_split_exact": ([_P, _I64, _P, _I64, _P, _P, _P, _I64, _I32, _I32, _I32, _I32, _P, _SZ, _P, _P],
                                  _I32),
+    "detgemm_w8a8_swiglu": ([_P, _I64, _P, _P, _I64, _P, _P, _P, _P, _I64, _I32, _I32, _I32, _P, _SZ, _P], _I32),
+    "detgemm_w8a8_swiglu_workspace_size": ([_I32, _I32, _I32], _SZ),
     "detgemm_swiglu_bf16": ([_P, _I64, _P, _I64, _P, _P, _P, _P, _I64, _I32, _I32, _P], _I32),
     "detgemm_gemm_fixed_f16": ([_P, _I64, _P, _I64, _P, _I64, _I32, _I32, _I32, _I32, _P], _I32),
     "detgemm_epilogue_inject": ([_P, _I64, _I32, _P, _P, _I32, _I32, ctypes.c_uint32, _P, _I64, _I32, _I32, _P], _I32),
@@ -481,6 +483,29 @@ def ozaki_f64(A, B, nslices: int = 8, max_diag: int = 9, split_k: int = 1, out=N
                                M, N, K, nslices, max_diag, split_k,
                                wsb.data_ptr() if wsb is not None else None, wsn, _stream(stream))
     _check(st, "detgemm_ozaki_f64")
+    return out
+
+
+def w8a8_swiglu(A, Wg, Wu, ea, ewg, ewu, out=None, ws=None, stream=None) -> torch.Tensor:
+    """Fused gated-linear-unit W8A8: C = rne_bf16(SiLU(A Wg^T 2^(ea+ewg)) * A Wu^T 2^(ea+ewu));
+    A int8 [M,K], Wg / Wu int8 [N,K] (same row stride), exponents int32; bf16 [M, N] out."""
+    lib = load()
+    _req(A, torch.int8, "A"); _req(Wg, torch.int8, "Wg"); _req(Wu, torch.int8, "Wu")
+    _req(ea, torch.int32, "ea"); _req(ewg, torch.int32, "ewg"); _req(ewu, torch.int32, "ewu")
+    M, K = A.shape
+    N = Wg.shape[0]
+    if Wg.shape != (N, K) or Wu.shape != (N, K) or ea.shape != (M,) or ewg.shape != (N,) or ewu.shape != (N,):
+        raise ValueError("shape mismatch")
+    if _ld(Wg) != _ld(Wu):
+        raise ValueError("Wg and Wu must share a row stride")
+    if out is None:
+        out = empty2d(M, N, torch.bfloat16, A.device)
+    _req(out, torch.bfloat16, "out")
+    wsb, wsn = _workspace(int(lib.detgemm_w8a8_swiglu_workspace_size(M, N, K)), A.device, ws)
+    st = lib.detgemm_w8a8_swiglu(A.data_ptr(), _ld(A), Wg.data_ptr(), Wu.data_ptr(), _ld(Wg), ea.data_ptr(),
+                                 ewg.data_ptr(), ewu.data_ptr(), out.data_ptr(), _ld(out), M, N, K,
+                                 wsb.data_ptr() if wsb is not None else None, wsn, _stream(stream))
+    _check(st, "detgemm_w8a8_swiglu")
     return out
 
 

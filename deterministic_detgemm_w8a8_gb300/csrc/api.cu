@@ -614,6 +614,61 @@ detgemm_status detgemm_gemm_fixed_f16(const uint16_t* A, int64_t lda, const uint
     return from_cuda(tc_gemm_launch(a, A, lda, 1, W, ldw, 1, K, nullptr, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+// Gated W8A8 scratch: A16 [M][Kp] fp16 | W16 [2][N][Kp] fp16 (gate plane, up plane)
+static size_t swiglu_ws(int M, int N, int K, int64_t* Kp, size_t* w16_off) {
+    *Kp = tc_padded_k(K);
+    *w16_off = align256((size_t)M * *Kp * 2);
+    return *w16_off + align256((size_t)2 * N * *Kp * 2);
+}
+
+size_t detgemm_w8a8_swiglu_workspace_size(int M, int N, int K) {
+    if (M <= 0 || N <= 0 || K <= 0) return 0;
+    int64_t Kp;
+    size_t off;
+    return swiglu_ws(M, N, K, &Kp, &off);
+}
+
+detgemm_status detgemm_w8a8_swiglu(const int8_t* A, int64_t lda, const int8_t* Wg, const int8_t* Wu, int64_t ldw,
+                                   const int32_t* ea, const int32_t* ewg, const int32_t* ewu, uint16_t* C, int64_t ldc,
+                                   int M, int N, int K, void* ws, size_t ws_bytes, detgemm_stream_t stream) {
+    if (M < 0 || N < 0 || K < 1) return DETGEMM_ERR_INVALID_ARG;
+    if (K > DETGEMM_MAX_K) return DETGEMM_ERR_PRECONDITION;
+    if (M == 0 || N == 0) return DETGEMM_OK;
+    if (!A || !Wg || !Wu || !ea || !ewg || !ewu || !C || lda < K || ldw < K || ldc < N) return DETGEMM_ERR_INVALID_ARG;
+    if (!aligned16(A) || !aligned16(Wg) || !aligned16(Wu) || !aligned16(C) || !aligned4(ea) || !aligned4(ewg) ||
+        !aligned4(ewu))
+        return DETGEMM_ERR_ALIGNMENT;
+    if (lda % 16 || ldw % 16 || (ldc * 2) % 16) return DETGEMM_ERR_ALIGNMENT;
+    int64_t Kp;
+    size_t w16;
+    const size_t need = swiglu_ws(M, N, K, &Kp, &w16);
+    if (!ws || ws_bytes < need) return DETGEMM_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return DETGEMM_ERR_ALIGNMENT;
+    detgemm_status st = check_device();
+    if (st != DETGEMM_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    char* base = reinterpret_cast<char*>(ws);
+    char* Wp = base + w16;
+    cudaError_t e = widen_pair_launch(A, lda, M, K, base, Kp, Wg, ldw, N, K, Wp, Kp, s);
+    if (e == cudaSuccess) e = widen_i8_f16_launch(Wu, ldw, N, K, Wp + (size_t)N * Kp * 2, Kp, s);
+    if (e != cudaSuccess) return DETGEMM_ERR_CUDA;
+    TcArgs a = {};
+    a.M = M;
+    a.N = N;
+    a.ndiag = 1;
+    a.diag_first[0] = 0;
+    a.diag_nseg[0] = 1;
+    a.split = 1;
+    a.mode = EPI_BF16_POW2;
+    a.ea = ea;
+    a.ew = ewg;
+    a.ewu = ewu;
+    a.C = C;
+    a.ldc = ldc;
+    a.swiglu = 1;
+    return from_cuda(tc_gemm_launch(a, base, Kp, 1, Wp, Kp, 2, Kp, nullptr, s));
+}
+
 detgemm_status detgemm_swiglu_bf16(const int32_t* G, int64_t ldg, const int32_t* U, int64_t ldu, const int32_t* ea,
                                    const int32_t* ewg, const int32_t* ewu, uint16_t* C, int64_t ldc, int M, int N,
                                    detgemm_stream_t stream) {

@@ -44,6 +44,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "silu.cuh"
 #include "sm100.cuh"
 
 namespace detgemm {
@@ -269,6 +270,51 @@ __device__ __forceinline__ void finish_rows(const TcArgs& p, const CUtensorMap* 
     }
 }
 
+// Gated-linear-unit epilogue of a warp's 32 rows x COLS accumulator columns, which hold the
+// gate and up accumulators of COLS / 2 outputs in turn (column 2c: gate, 2c + 1: up, of output
+// column colo0 + c): each output is rne_bf16(SiLU(g) * u) (bf16_silu_mul), staged in the
+// warp's slot with the 128-byte swizzle and written by one TMA store of COLS / 2 columns.
+template <int COLS>
+__device__ __forceinline__ void finish_swiglu(const TcArgs& p, const CUtensorMap* tmC, uint8_t* slot, int row0,
+                                              int colo0, const int32_t (&acc)[COLS], bool& pending) {
+    constexpr int OUT = COLS / 2;
+    constexpr int PER = OUT / 32;  // outputs whose exponents one lane loads
+    const int lane = threadIdx.x & 31;
+    const int row = row0 + lane;
+    const uint32_t sbase = smem_addr(slot) + (uint32_t)lane * 128u;
+    const int sw = lane & 7;
+    int32_t egv[PER], euv[PER];
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+        const int c = colo0 + PER * lane + i;
+        egv[i] = c < p.N ? __ldg(p.ew + c) : 0;
+        euv[i] = c < p.N ? __ldg(p.ewu + c) : 0;
+    }
+    const long long ea = row < p.M ? __ldg(p.ea + row) : 0;
+    bool bad = false;
+    slot_acquire(pending);
+#pragma unroll
+    for (int jj = 0; jj < OUT / 8; ++jj) {
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            uint32_t h[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int c = 8 * jj + 2 * i + e;  // output index within the warp's OUT
+                const int32_t eg = __shfl_sync(0xffffffffu, egv[c % PER], c / PER);
+                const int32_t eu = __shfl_sync(0xffffffffu, euv[c % PER], c / PER);
+                const bool live = row < p.M && colo0 + c < p.N;
+                h[e] = live ? bf16_silu_mul(acc[2 * c], acc[2 * c + 1], ea + eg, ea + eu, bad) : 0u;
+            }
+            w[i] = h[0] | (h[1] << 16);
+        }
+        st_shared16(sbase + (uint32_t)((jj ^ sw) << 4), w[0], w[1], w[2], w[3]);
+    }
+    if (bad) raise_status(DEV_RANGE);
+    slot_release(tmC, slot, colo0, row0, 0, row0 < p.M && colo0 < p.N, pending);
+}
+
 // A warp's 32 x COLS int32 partial into the split workspace (int32 [tile units x 256][256],
 // row-major): 32 x 32 pieces staged in the warp's slot (128-byte swizzle) and added to
 // global memory by TMA reductions.
@@ -345,8 +391,10 @@ static_assert(2 * 256 <= 512 && 2 * 192 <= 512, "two accumulator buffers in TMEM
 // registers stay out of the other instantiations); kNarrow: the 256-wide geometry with
 // sixteen epilogue warps; kFloat: the fixed-order floating-point GEMM -- fp16 or bf16
 // operands (TcArgs::idesc_fp), the whole K range of a tile accumulated in one TMEM buffer in
-// K order (no chunk drains), and the raw fp32 accumulator stored (EPI_STORE_I32 layout)
-template <int BNT, bool kSplit, bool kGroups, bool kBias, bool kNarrow, bool kFloat = false>
+// K order (no chunk drains), and the raw fp32 accumulator stored (EPI_STORE_I32 layout);
+// kSwiglu: the gated-linear-unit W8A8 GEMM -- B planes 0 (gate) and 1 (up) loaded with their
+// rows interleaved, each output rounded once as rne_bf16(SiLU(g) * u) (finish_swiglu)
+template <int BNT, bool kSplit, bool kGroups, bool kBias, bool kNarrow, bool kFloat = false, bool kSwiglu = false>
 __global__ void __launch_bounds__(Geo<BNT, kNarrow>::THREADS, 1)
     tc2_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmS,
@@ -425,7 +473,10 @@ __global__ void __launch_bounds__(Geo<BNT, kNarrow>::THREADS, 1)
                     if (rank == 0) mbar_arrive_expect_tx(full + stage, 2 * P_STAGE_BYTES);
                     const uint32_t fb = full_lead + 8u * (uint32_t)stage;
                     tma_load_3d_pair(sa, &tmA, fb, kx, un.tm * 256 + (int)rank * 128, p.segA[seg]);
-                    tma_load_3d_pair(sa + P_A_BYTES, &tmB, fb, kx, un.tn * BN + (int)rank * (BN / 2), p.segB[seg]);
+                    if constexpr (kSwiglu)  // rows j of the gate and up planes, interleaved (map {K, plane, row})
+                        tma_load_3d_pair(sa + P_A_BYTES, &tmB, fb, kx, 0, (un.tn * BN + (int)rank * (BN / 2)) / 2);
+                    else
+                        tma_load_3d_pair(sa + P_A_BYTES, &tmB, fb, kx, un.tn * BN + (int)rank * (BN / 2), p.segB[seg]);
                     ++issued;
                     if (++stage == P_STAGES) {
                         stage = 0;
@@ -548,7 +599,8 @@ __global__ void __launch_bounds__(Geo<BNT, kNarrow>::THREADS, 1)
             const int row = un.tm * 256 + (int)rank * 128 + q * 32 + lane;
             const int col0 = un.tn * BN + h * COLS;
             if constexpr (!kSplit) {
-                finish_rows<COLS, kBias>(p, &tmC, slot, un.d, row - lane, col0, acc, pending);
+                if constexpr (kSwiglu) finish_swiglu<COLS>(p, &tmC, slot, row - lane, col0 / 2, acc, pending);
+                else finish_rows<COLS, kBias>(p, &tmC, slot, un.d, row - lane, col0, acc, pending);
                 continue;
             }
             // a K part: add the exact partial into the tile's slot of the split workspace with
@@ -633,6 +685,23 @@ cudaError_t make_map(CUtensorMap* m, const void* base, int64_t kext, int64_t ld,
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// 3-D map over two fp16 planes [2][rows][ld] read with their rows interleaved: dims {kext,
+// plane, row}, box {64, 2, 64}, so that a box holds rows j of plane 0, j of plane 1, j + 1 of
+// plane 0, ... (128-byte swizzle over the 128 interleaved rows)
+cudaError_t make_pair_map(CUtensorMap* m, const void* base, int64_t kext, int64_t ld, int rows) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc;
+    cudaError_t e = get_encode(&enc);
+    if (e != cudaSuccess) return e;
+    cuuint64_t dims[3] = {(cuuint64_t)kext, 2, (cuuint64_t)rows};
+    cuuint64_t strides[2] = {(cuuint64_t)ld * 2 * (cuuint64_t)rows, (cuuint64_t)ld * 2};
+    cuuint32_t box[3] = {(cuuint32_t)BK, 2, 64};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 // 3-D map over the output: bf16 [1][M][ldc] (box 64 x 32) or int32 planes [ndiag][M][ldc]
 // spaced c_plane elements apart (box 32 x 32); 128-byte swizzle, the epilogue's slot layout
 cudaError_t make_out_map(CUtensorMap* m, const TcArgs& a) {
@@ -694,9 +763,9 @@ static cudaError_t make_ws_map(CUtensorMap* m, void* base, int cut) {
 namespace {
 int g_max_clusters[64][2];  // per device: 256-wide, 192-wide tiles
 
-template <int BNT, bool kSplit, bool kGroups, bool kBias, bool kNarrow, bool kFloat = false>
+template <int BNT, bool kSplit, bool kGroups, bool kBias, bool kNarrow, bool kFloat = false, bool kSwiglu = false>
 cudaError_t opt_in() {
-    return cudaFuncSetAttribute(tc2_gemm_kernel<BNT, kSplit, kGroups, kBias, kNarrow, kFloat>,
+    return cudaFuncSetAttribute(tc2_gemm_kernel<BNT, kSplit, kGroups, kBias, kNarrow, kFloat, kSwiglu>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, Geo<BNT, kNarrow>::SMEM_BYTES);
 }
 
@@ -734,7 +803,8 @@ int max_pair_clusters(int bn) {
             opt_in<256, false, false, true, true>() != cudaSuccess ||
             opt_in<256, true, true, true, false>() != cudaSuccess ||
             opt_in<192, false, false, true, false>() != cudaSuccess ||
-            opt_in<256, false, false, false, false, true>() != cudaSuccess)
+            opt_in<256, false, false, false, false, true>() != cudaSuccess ||
+            opt_in<256, false, false, false, false, false, true>() != cudaSuccess)
             return 0;
         g_max_clusters[dev][0] = occupancy_clusters<256>();
         g_max_clusters[dev][1] = occupancy_clusters<192>();
@@ -790,7 +860,7 @@ static void assign_leftovers(TcArgs& a, int C) {
     }
 }
 
-template <int BNT, bool kSplit, bool kGroups, bool kBias, bool kNarrow, bool kFloat = false>
+template <int BNT, bool kSplit, bool kGroups, bool kBias, bool kNarrow, bool kFloat = false, bool kSwiglu = false>
 static cudaError_t launch_engine(const TcArgs& a, const CUtensorMap& tmA, const CUtensorMap& tmB,
                                  const CUtensorMap& tmC, const CUtensorMap& tmS, int clusters, cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};
@@ -808,7 +878,8 @@ static cudaError_t launch_engine(const TcArgs& a, const CUtensorMap& tmA, const 
     cfg.attrs = attr;
     cfg.numAttrs = 2;
     cudaError_t e =
-        cudaLaunchKernelEx(&cfg, tc2_gemm_kernel<BNT, kSplit, kGroups, kBias, kNarrow, kFloat>, tmA, tmB, tmC, tmS, a);
+        cudaLaunchKernelEx(&cfg, tc2_gemm_kernel<BNT, kSplit, kGroups, kBias, kNarrow, kFloat, kSwiglu>, tmA, tmB, tmC,
+                           tmS, a);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -834,11 +905,15 @@ cudaError_t tc_gemm_launch(const TcArgs& a0, const void* A16, int64_t lda, int a
     if (a.fp_mode && (a.split != 1 || a.ndiag != 1 || a.mode != EPI_STORE_I32)) return cudaErrorInvalidValue;
     if (a.fp_mode)  // kind::f16 with fp16 (mode 1) or bf16 (mode 2) operands, fp32 accumulator
         a.idesc_fp = Geo<256>::IDESC | (a.fp_mode == 2 ? (1u << 7) | (1u << 10) : 0u);
-    const int bn = a.fp_mode || (bias && a.split > 1) ? 256 : choose_bn(a);
+    if (a.swiglu && (a.split != 1 || a.ndiag != 1 || a.mode != EPI_BF16_POW2 || b_planes != 2))
+        return cudaErrorInvalidValue;
+    const int bn = a.fp_mode || a.swiglu || (bias && a.split > 1) ? 256 : choose_bn(a);
     set_tiles(a, kext, bn);
+    if (a.swiglu) a.tiles_n = (a.N + 127) / 128;  // 128 outputs (256 interleaved B rows) per tile
     CUtensorMap tmA, tmB, tmC;
     cudaError_t e = make_map(&tmA, A16, kext, lda, a.M, a_planes, 128);
-    if (e == cudaSuccess) e = make_map(&tmB, B16, kext, ldb, a.N, b_planes, bn / 2);
+    if (e == cudaSuccess)
+        e = a.swiglu ? make_pair_map(&tmB, B16, kext, ldb, a.N) : make_map(&tmB, B16, kext, ldb, a.N, b_planes, bn / 2);
     if (e == cudaSuccess) e = make_out_map(&tmC, a);
     if (e != cudaSuccess) return e;
     int clusters = max_pair_clusters(bn);
@@ -867,6 +942,8 @@ cudaError_t tc_gemm_launch(const TcArgs& a0, const void* A16, int64_t lda, int a
     const long long rounds = (total + clusters - 1) / clusters;
     const bool narrow = kext <= 1024 || rounds * kext <= 12288;
     if (a.fp_mode) return launch_engine<256, false, false, false, false, true>(a, tmA, tmB, tmC, tmS, clusters, s);
+    if (a.swiglu)
+        return launch_engine<256, false, false, false, false, false, true>(a, tmA, tmB, tmC, tmS, clusters, s);
     if (bias && a.split > 1) return launch_engine<256, true, true, true, false>(a, tmA, tmB, tmC, tmS, clusters, s);
     if (bias && bn == 192) return launch_engine<192, false, false, true, false>(a, tmA, tmB, tmC, tmS, clusters, s);
     if (bias) return launch_engine<256, false, false, true, true>(a, tmA, tmB, tmC, tmS, clusters, s);

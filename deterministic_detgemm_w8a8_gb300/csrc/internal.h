@@ -116,6 +116,10 @@ struct TcArgs {
     int fp_mode;               // 1 / 2: the fixed-order floating-point GEMM on fp16 / bf16
                                // operands (one group, split 1, EPI_STORE_I32 layout holding fp32 bits)
     uint32_t idesc_fp;         // its MMA instruction descriptor (set by the launcher)
+    int swiglu;                // 1: gated-linear-unit W8A8 -- B planes 0 (gate) and 1 (up), N
+                               // outputs, each rne_bf16(SiLU(g) * u) with exponents ea + ew
+                               // (gate) and ea + ewu (up)
+    const int32_t* ewu;        // [N] up-projection weight exponents (swiglu)
 };
 
 int64_t tc_padded_k(int K);

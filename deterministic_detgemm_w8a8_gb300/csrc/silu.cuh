@@ -162,7 +162,7 @@ __device__ __forceinline__ bool bf16_decide(double hi, double lo, double eps, ui
 
 // rne_bf16(SiLU(gacc 2^Eg) * uacc 2^Eu); `bad` is set on an exponent outside [-60, 40] or
 // an output no evaluation could decide
-__device__ __noinline__ uint16_t bf16_silu_mul(int32_t gacc, int32_t uacc, long long Eg, long long Eu, bool& bad) {
+static __device__ __noinline__ uint16_t bf16_silu_mul(int32_t gacc, int32_t uacc, long long Eg, long long Eu, bool& bad) {
     if (gacc == 0 || uacc == 0) return 0x0000;
     if (Eg < -60 || Eg > 40 || Eu < -60 || Eu > 40) {
         bad = true;

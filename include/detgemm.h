@@ -361,6 +361,27 @@ DETGEMM_API detgemm_status detgemm_swiglu_bf16(const int32_t* G, int64_t ldg, co
                                                uint16_t* C, int64_t ldc, int M, int N, detgemm_stream_t stream);
 
 /*
+ * Gated-linear-unit W8A8 layer, fused: the gate and up GEMMs on the same activations and the
+ * epilogue above, in one tensor-core pass [P4 §II "Pipeline and alibi"]:
+ *     C_ij = rne_bf16(SiLU(sum_k A_ik Wg_jk * 2^(ea_i + ewg_j)) * sum_k A_ik Wu_jk * 2^(ea_i + ewu_j))
+ * Exact int32 accumulation as in detgemm_w8a8, one rounding per output, bits identical to
+ * detgemm_gemm_s8_i32 on Wg and Wu followed by detgemm_swiglu_bf16. Every M runs on the
+ * tensor-core engine (rows of the gate and up weights interleaved in its B operand tile).
+ *   A  int8 [M x K] (lda);  Wg, Wu int8 [N x K] with the same row stride ldw;
+ *   ea int32 [M], ewg, ewu int32 [N];  C bf16 bits [M x N] (ldc)
+ *   ws scratch of ws_bytes >= detgemm_w8a8_swiglu_workspace_size(M, N, K), 256-byte aligned
+ * Exponent sums outside [-60, 40] give NaN and DETGEMM_ERR_RANGE on the device.
+ * Errors: INVALID_ARG, PRECONDITION (K > DETGEMM_MAX_K), ALIGNMENT, WORKSPACE,
+ * UNSUPPORTED_DEVICE, CUDA.
+ */
+DETGEMM_API detgemm_status detgemm_w8a8_swiglu(const int8_t* A, int64_t lda, const int8_t* Wg, const int8_t* Wu,
+                                               int64_t ldw, const int32_t* ea, const int32_t* ewg,
+                                               const int32_t* ewu, uint16_t* C, int64_t ldc, int M, int N, int K,
+                                               void* ws, size_t ws_bytes, detgemm_stream_t stream);
+
+DETGEMM_API size_t detgemm_w8a8_swiglu_workspace_size(int M, int N, int K);
+
+/*
  * Fixed-order (batch-invariant) fp16 / bf16 GEMM. A floating-point GEMM's bits are fixed by
  * its reduction order, which can be written down as a descriptor [P1 §3.2.1-§3.2.2]; here the
  * order is the tensor core's own, one block FMA per 16 products ["GPU Arithmetic Emulator"

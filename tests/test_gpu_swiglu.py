@@ -119,3 +119,40 @@ def test_composition_with_the_int32_gemm(lib, dev, oracle_mod):
     U = lib.gemm_s8_i32(pad(A), pad(Wu))
     got = bf16_bits(lib.swiglu_bf16(G, U, to_dev(ea, dev), to_dev(ewg, dev), to_dev(ewu, dev)))
     assert (got == oracle_mod.w8a8_swiglu(A, Wg, Wu, ea, ewg, ewu)).all()
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 64, 64), (64, 130, 1000), (300, 257, 520), (1024, 512, 4096)])
+def test_fused_w8a8_swiglu(lib, dev, oracle_mod, M, N, K):
+    rng = np.random.default_rng(M + N + K)
+    A = np.clip(np.rint(rng.standard_normal((M, K)) * 30), -127, 127).astype(np.int8)
+    Wg = np.clip(np.rint(rng.standard_normal((N, K)) * 30), -127, 127).astype(np.int8)
+    Wu = np.clip(np.rint(rng.standard_normal((N, K)) * 30), -127, 127).astype(np.int8)
+    ea = rng.integers(-14, -6, M).astype(np.int32)
+    ewg = rng.integers(-14, -6, N).astype(np.int32)
+    ewu = rng.integers(-14, -6, N).astype(np.int32)
+    ld = (K + 15) // 16 * 16
+    from gpu_util import padded
+    out = lib.w8a8_swiglu(padded(A, dev, ld), padded(Wg, dev, ld), padded(Wu, dev, ld), to_dev(ea, dev),
+                          to_dev(ewg, dev), to_dev(ewu, dev))
+    got = bf16_bits(out)
+    want = oracle_mod.w8a8_swiglu(A, Wg, Wu, ea, ewg, ewu)
+    assert (got == want).all(), int((got != want).sum())
+    assert lib.device_status() == lib.OK
+
+
+def test_fused_ffn_gate_up_sampled(lib, dev, oracle_mod):
+    # the 8B-class FFN's gate and up projections at 8192 tokens (K = 4096, N = 12288 each):
+    # every row of one column per 128-wide output tile column, and sixteen whole rows
+    import synthetic
+    A, Wg, ea, ewg = synthetic.ffn_gate_up()
+    Wu = synthetic.normal_i8(2, 9, Wg.shape, 30.0)
+    ewu = synthetic.uniform_i32(2, 10, (Wg.shape[0],), -14, -6)
+    got = bf16_bits(lib.w8a8_swiglu(to_dev(A, dev), to_dev(Wg, dev), to_dev(Wu, dev), to_dev(ea, dev),
+                                    to_dev(ewg, dev), to_dev(ewu, dev)))
+    rng = np.random.default_rng(12)
+    rows = sorted({0, 255, 256, 8191} | set(rng.integers(0, 8192, 12).tolist()))
+    assert (got[rows] == oracle_mod.w8a8_swiglu(A, Wg, Wu, ea, ewg, ewu, rows=rows)).all()
+    cols = sorted({0, 127, 128, 12287} | {128 * t + int(rng.integers(0, 128)) for t in range(0, 96, 3)})
+    want = oracle_mod.w8a8_swiglu(A, np.ascontiguousarray(Wg[cols]), np.ascontiguousarray(Wu[cols]), ea,
+                                  np.ascontiguousarray(ewg[cols]), np.ascontiguousarray(ewu[cols]))
+    assert (got[:, cols] == want).all()
