@@ -85,7 +85,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", default=None,
                     choices=["ffn_gate_up", "ffn_down", "skinny8", "skinny32", "ozaki", "ozaki_f64", "sweep",
-                             "sweep1", "sweep7", "sweep64", "sweep257", "tiny"],
+                             "sweep1", "sweep7", "sweep32", "sweep64", "sweep257", "tiny", "fixed_bf16", "swiglu"],
                     help="run one workload call twice (warm-up + one more) for an ncu capture, then exit")
     return ap.parse_args()
 
@@ -613,6 +613,43 @@ def extras(dg, torch, dev, pk, flush):
         bias_res[name] = {"unbiased_us": round(ms0 * 1e3, 1), "biased_us": round(ms1 * 1e3, 1)}
         del A, W, ea, ew, C, wsb
     res["bias_epilogue"] = bias_res
+    # the gated-linear-unit FFN layer at the 8B-class size: gate and up projections (K = 4096,
+    # N = 12288 each) on 8192 tokens, fused with the rne_bf16(SiLU(g) * u) epilogue, beside the
+    # two plain W8A8 GEMMs it replaces (whose outputs would still need a gating pass)
+    A, Wg, ea, ewg = (tdev(x) for x in synthetic.ffn_gate_up())
+    Wu = tdev(synthetic.normal_i8(2, 9, (12288, 4096), 30.0))
+    ewu = tdev(synthetic.uniform_i32(2, 10, (12288,), -14, -6))
+    C = torch.empty((8192, 12288), dtype=torch.bfloat16, device=dev)
+    wss = torch.empty(dg.load().detgemm_w8a8_swiglu_workspace_size(8192, 12288, 4096), dtype=torch.uint8, device=dev)
+    wsp = torch.empty(max(dg.w8a8_workspace_size(8192, 12288, 4096), 1), dtype=torch.uint8, device=dev)
+    ms_f = _time(torch, lambda: dg.w8a8_swiglu(A, Wg, Wu, ea, ewg, ewu, out=C, ws=wss), flush)
+    C2 = torch.empty((8192, 12288), dtype=torch.bfloat16, device=dev)
+
+    def two_gemms():
+        dg.w8a8(A, Wg, ea, ewg, out=C, ws=wsp)
+        dg.w8a8(A, Wu, ea, ewu, out=C2, ws=wsp)
+    ms_2 = _time(torch, two_gemms, flush)
+    ops = 2.0 * 2 * 8192 * 12288 * 4096
+    res["swiglu_ffn_M8192_N12288x2_K4096"] = {
+        "fused_us": round(ms_f * 1e3, 1), "fused_TOPS": round(ops / (ms_f * 1e-3) / 1e12, 1),
+        "two_w8a8_gemms_us": round(ms_2 * 1e3, 1), "two_w8a8_gemms_TOPS": round(ops / (ms_2 * 1e-3) / 1e12, 1)}
+    del A, Wg, Wu, ea, ewg, ewu, C, C2, wss, wsp
+    # the fixed-order bf16 GEMM (K walked in 16-wide tensor-core block FMAs, never split) beside
+    # the vendor library's bf16 GEMM on the same operands (its bits depend on its own order)
+    fx = {}
+    for name, (m, n, k) in (("8192^3", (8192, 8192, 8192)), ("ffn_gate_up", (8192, 12288, 4096))):
+        a16 = torch.randn((m, k), device=dev).to(torch.bfloat16)
+        b16 = torch.randn((n, k), device=dev).to(torch.bfloat16)
+        c32 = torch.empty((m, n), dtype=torch.float32, device=dev)
+        ms = _time(torch, lambda: dg.gemm_fixed_f16(a16, b16, out=c32), flush)
+        cb = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+        bt = b16.t()
+        ms_lib = _time(torch, lambda: torch.matmul(a16, bt, out=cb), flush)
+        tf = 2.0 * m * n * k / (ms * 1e-3) / 1e12
+        fx[name] = {"us": round(ms * 1e3, 1), "TFLOPs": round(tf, 1), "frac_bf16_peak": round(tf / pk["bf16_tflops"], 4),
+                    "library_bf16_gemm_us": round(ms_lib * 1e3, 1)}
+        del a16, b16, c32, cb, bt
+    res["fixed_order_bf16_gemm"] = fx
     # the tiny workload (64 x 256 x 512): launch-latency bound
     A, W, ea, ew = (tdev(x) for x in synthetic.tiny())
     C = torch.empty((64, 256), dtype=torch.bfloat16, device=dev)
@@ -636,12 +673,22 @@ def run_profile(name):
         elif name == "ffn_down":
             args = synthetic.ffn_down()
         elif name.startswith("sweep"):
-            args = synthetic.sweep({"sweep": 2048, "sweep1": 1, "sweep7": 7, "sweep64": 64, "sweep257": 257}[name])
+            args = synthetic.sweep({"sweep": 2048, "sweep1": 1, "sweep7": 7, "sweep32": 32, "sweep64": 64,
+                                    "sweep257": 257}[name])
         else:
             args = synthetic.skinny()
         split = {"skinny8": 8, "skinny32": 32}.get(name, 1)
         A, W, ea, ew = (tdev(x) for x in args)
         fn = lambda: dg.w8a8(A, W, ea, ew, split_k=split)
+    elif name == "fixed_bf16":
+        a16 = torch.randn((4096, 4096), device=dev).to(torch.bfloat16)
+        b16 = torch.randn((4096, 4096), device=dev).to(torch.bfloat16)
+        fn = lambda: dg.gemm_fixed_f16(a16, b16)
+    elif name == "swiglu":
+        A, Wg, ea, ewg = (tdev(x) for x in synthetic.ffn_gate_up(2048))
+        Wu = tdev(synthetic.normal_i8(2, 9, (12288, 4096), 30.0))
+        ewu = tdev(synthetic.uniform_i32(2, 10, (12288,), -14, -6))
+        fn = lambda: dg.w8a8_swiglu(A, Wg, Wu, ea, ewg, ewu)
     elif name == "ozaki_f64":
         Ad, Bd = (tdev(x) for x in synthetic.ozaki_f64(4096))
         fn = lambda: dg.ozaki_f64(Ad, Bd)

@@ -813,10 +813,6 @@ static_assert(DT_ACC_COL + 4 * 64 <= DT_TMEM_COLS, "TMEM: four 1024-K chunks of 
 __device__ __forceinline__ void sts16(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
-// integer addition into a shared-memory word of any CTA of the cluster
-__device__ __forceinline__ void red_dsmem_add(uint32_t cluster_addr, int32_t v) {
-    asm volatile("red.relaxed.cluster.shared::cluster.add.s32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
-}
 __device__ __forceinline__ int4 ld_dsmem_v4(uint32_t cluster_addr) {
     int4 v;
     asm volatile("ld.shared::cluster.v4.s32 {%0, %1, %2, %3}, [%4];"
@@ -825,22 +821,6 @@ __device__ __forceinline__ int4 ld_dsmem_v4(uint32_t cluster_addr) {
                  : "memory");
     return v;
 }
-// 32 lanes x 16 consecutive 32-bit TMEM columns from 16 registers per thread
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
-            taddr),
-        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
-        "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
-        : "memory");
-}
-// 32 lanes x 4 consecutive 32-bit TMEM columns
-__device__ __forceinline__ void tmem_ld4(uint32_t taddr, uint32_t (&r)[4]) {
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(taddr));
-}
-__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 // D[tmem] (+)= A[tmem] * B[smem desc]^T, kind::f16: A is M x K with row m in TMEM lane m and
 // the K values in pairs per 32-bit column (k = 2c in the low half of column c)
 __device__ __forceinline__ void mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,

@@ -158,6 +158,9 @@ __device__ __forceinline__ void slot_release(const CUtensorMap* tmC, uint8_t* sl
 __device__ __forceinline__ void st_shared16(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
+__device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
+    asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+}
 
 template <int COLS, bool kBias>
 __device__ __forceinline__ void finish_rows(const TcArgs& p, const CUtensorMap* tmC, uint8_t* slot, int d, int row0,
@@ -270,46 +273,70 @@ __device__ __forceinline__ void finish_rows(const TcArgs& p, const CUtensorMap* 
     }
 }
 
-// Gated-linear-unit epilogue of a warp's 32 rows x COLS accumulator columns, which hold the
-// gate and up accumulators of COLS / 2 outputs in turn (column 2c: gate, 2c + 1: up, of output
-// column colo0 + c): each output is rne_bf16(SiLU(g) * u) (bf16_silu_mul), staged in the
-// warp's slot with the 128-byte swizzle and written by one TMA store of COLS / 2 columns.
-template <int COLS>
+// Gated-linear-unit epilogue of a warp's 32 rows x 64 accumulator columns (the sixteen-warp
+// geometry), which hold the gate and up accumulators of 32 outputs in turn (column 2c: gate,
+// 2c + 1: up, of output column colo0 + c): each output is rne_bf16(SiLU(g) * u). A first pass
+// over the registers takes the call-free tiers (bf16_silu_mul_fast) and marks what they leave
+// undecided; the exact sums also sit in the warp's TMEM columns at ta (written there by the
+// caller, whose accumulator buffer stays held until this returns), from which a second pass,
+// once the registers are dead, reads the marked outputs' operands for bf16_silu_mul_careful.
+// The warp's 32 x 32 bf16 block is staged in its slot (64-byte rows, no swizzle) and written by
+// one TMA store.
 __device__ __forceinline__ void finish_swiglu(const TcArgs& p, const CUtensorMap* tmC, uint8_t* slot, int row0,
-                                              int colo0, const int32_t (&acc)[COLS], bool& pending) {
-    constexpr int OUT = COLS / 2;
-    constexpr int PER = OUT / 32;  // outputs whose exponents one lane loads
+                                              int colo0, const int32_t (&acc)[64], uint32_t ta, bool& pending) {
     const int lane = threadIdx.x & 31;
     const int row = row0 + lane;
-    const uint32_t sbase = smem_addr(slot) + (uint32_t)lane * 128u;
-    const int sw = lane & 7;
-    int32_t egv[PER], euv[PER];
-#pragma unroll
-    for (int i = 0; i < PER; ++i) {
-        const int c = colo0 + PER * lane + i;
-        egv[i] = c < p.N ? __ldg(p.ew + c) : 0;
-        euv[i] = c < p.N ? __ldg(p.ewu + c) : 0;
-    }
-    const long long ea = row < p.M ? __ldg(p.ea + row) : 0;
+    const uint32_t sbase = smem_addr(slot) + (uint32_t)lane * 64u;
+    const int c_own = colo0 + lane;  // lane l loads the exponents of output l
+    const int32_t eg_own = c_own < p.N ? __ldg(p.ew + c_own) : 0;
+    const int32_t eu_own = c_own < p.N ? __ldg(p.ewu + c_own) : 0;
+    const int32_t ea = row < p.M ? __ldg(p.ea + row) : 0;
+    // exponents within 2^20 in magnitude keep the first pass's int sums exact; a warp that
+    // holds a larger one leaves all its outputs to the second pass (warp-uniform)
+    const bool small = (uint32_t)(ea + (1 << 20)) <= (2u << 20) && (uint32_t)(eg_own + (1 << 20)) <= (2u << 20) &&
+                       (uint32_t)(eu_own + (1 << 20)) <= (2u << 20);
+    const bool general = !__all_sync(0xffffffffu, small);
     bool bad = false;
+    uint32_t undecided = 0;  // bit c: output c is left to the second pass
     slot_acquire(pending);
+    if (!general) {
 #pragma unroll
-    for (int jj = 0; jj < OUT / 8; ++jj) {
-        uint32_t w[4];
+        for (int jj = 0; jj < 4; ++jj) {
+            uint32_t w[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            uint32_t h[2];
+            for (int i = 0; i < 4; ++i) {
+                uint32_t h[2];
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int c = 8 * jj + 2 * i + e;  // output index within the warp's OUT
-                const int32_t eg = __shfl_sync(0xffffffffu, egv[c % PER], c / PER);
-                const int32_t eu = __shfl_sync(0xffffffffu, euv[c % PER], c / PER);
-                const bool live = row < p.M && colo0 + c < p.N;
-                h[e] = live ? bf16_silu_mul(acc[2 * c], acc[2 * c + 1], ea + eg, ea + eu, bad) : 0u;
+                for (int e = 0; e < 2; ++e) {
+                    const int c = 8 * jj + 2 * i + e;
+                    const int32_t eg = __shfl_sync(0xffffffffu, eg_own, c);
+                    const int32_t eu = __shfl_sync(0xffffffffu, eu_own, c);
+                    const bool live = row < p.M && colo0 + c < p.N;
+                    bool und = false;
+                    h[e] = live ? bf16_silu_mul_fast(acc[2 * c], acc[2 * c + 1], ea + eg, ea + eu, bad, und) : 0u;
+                    undecided |= und ? 1u << c : 0u;
+                }
+                w[i] = h[0] | (h[1] << 16);
             }
-            w[i] = h[0] | (h[1] << 16);
+            st_shared16(sbase + (uint32_t)(jj << 4), w[0], w[1], w[2], w[3]);
         }
-        st_shared16(sbase + (uint32_t)((jj ^ sw) << 4), w[0], w[1], w[2], w[3]);
+    } else {
+        const int live_cols = p.N - colo0;
+        undecided = row >= p.M || live_cols <= 0 ? 0u : live_cols >= 32 ? 0xFFFFFFFFu : (1u << live_cols) - 1u;
+    }
+    // second pass: one output column at a time (warp-uniform), its operands from TMEM
+    for (uint32_t cols = __reduce_or_sync(0xffffffffu, undecided); cols != 0; cols &= cols - 1) {
+        const int c = __ffs(cols) - 1;
+        uint32_t g, u;
+        tmem_ld2(ta + 2u * (uint32_t)c, g, u);
+        tmem_wait_ld();
+        const int32_t eg = __shfl_sync(0xffffffffu, eg_own, c);
+        const int32_t eu = __shfl_sync(0xffffffffu, eu_own, c);
+        if ((undecided >> c) & 1u) {
+            const uint32_t r = bf16_silu_mul_any((int32_t)g, (int32_t)u, (long long)ea + eg, (long long)ea + eu);
+            bad |= (r >> 16) != 0;
+            st_shared_u16(sbase + 2u * (uint32_t)c, (uint16_t)r);
+        }
     }
     if (bad) raise_status(DEV_RANGE);
     slot_release(tmC, slot, colo0, row0, 0, row0 < p.M && colo0 < p.N, pending);
@@ -393,7 +420,8 @@ static_assert(2 * 256 <= 512 && 2 * 192 <= 512, "two accumulator buffers in TMEM
 // operands (TcArgs::idesc_fp), the whole K range of a tile accumulated in one TMEM buffer in
 // K order (no chunk drains), and the raw fp32 accumulator stored (EPI_STORE_I32 layout);
 // kSwiglu: the gated-linear-unit W8A8 GEMM -- B planes 0 (gate) and 1 (up) loaded with their
-// rows interleaved, each output rounded once as rne_bf16(SiLU(g) * u) (finish_swiglu)
+// rows interleaved, each output rounded once as rne_bf16(SiLU(g) * u) (finish_swiglu; its
+// instantiation is the sixteen-warp geometry, whose finish runs on twice the warps)
 template <int BNT, bool kSplit, bool kGroups, bool kBias, bool kNarrow, bool kFloat = false, bool kSwiglu = false>
 __global__ void __launch_bounds__(Geo<BNT, kNarrow>::THREADS, 1)
     tc2_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -566,6 +594,8 @@ __global__ void __launch_bounds__(Geo<BNT, kNarrow>::THREADS, 1)
 #pragma unroll
             for (int i = 0; i < COLS; ++i) acc[i] = 0;
             const int chunk = kFloat ? f1 - f0 : CHUNK_KB;
+            uint32_t ta_fin = 0;  // kSwiglu: the last chunk's columns, held until the finish
+            int buf_fin = 0;
             for (int c0 = f0; c0 < f1; c0 += chunk) {
                 const bool got = mbar_wait(tfull + buf, tphase, abort_flag);
                 if (!__all_sync(0xffffffffu, got)) {
@@ -587,9 +617,27 @@ __global__ void __launch_bounds__(Geo<BNT, kNarrow>::THREADS, 1)
                         else acc[16 * j + i] += __float2int_rn(__uint_as_float(r[i]));
                     }
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive_cluster(tempty_lead + 8u * (uint32_t)buf);
+                if constexpr (kSwiglu) {
+                    if (c0 + chunk >= f1) {
+                        // the last chunk: the exact sums go back into the buffer's columns for the
+                        // finish's second pass, which releases the buffer
+                        ta_fin = ta;
+                        buf_fin = buf;
+#pragma unroll
+                        for (int j = 0; j < COLS / 16; ++j) {
+                            uint32_t v[16];
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) v[i] = (uint32_t)acc[16 * j + i];
+                            tmem_st16(ta + 16 * j, v);
+                        }
+                        tmem_wait_st();
+                    }
+                }
+                if (!kSwiglu || c0 + chunk < f1) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster(tempty_lead + 8u * (uint32_t)buf);
+                }
                 if (++buf == 2) {
                     buf = 0;
                     tphase ^= 1u;
@@ -599,8 +647,12 @@ __global__ void __launch_bounds__(Geo<BNT, kNarrow>::THREADS, 1)
             const int row = un.tm * 256 + (int)rank * 128 + q * 32 + lane;
             const int col0 = un.tn * BN + h * COLS;
             if constexpr (!kSplit) {
-                if constexpr (kSwiglu) finish_swiglu<COLS>(p, &tmC, slot, row - lane, col0 / 2, acc, pending);
-                else finish_rows<COLS, kBias>(p, &tmC, slot, un.d, row - lane, col0, acc, pending);
+                if constexpr (kSwiglu) {
+                    finish_swiglu(p, &tmC, slot, row - lane, col0 / 2, acc, ta_fin, pending);
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster(tempty_lead + 8u * (uint32_t)buf_fin);
+                } else finish_rows<COLS, kBias>(p, &tmC, slot, un.d, row - lane, col0, acc, pending);
                 continue;
             }
             // a K part: add the exact partial into the tile's slot of the split workspace with
@@ -715,10 +767,12 @@ cudaError_t make_out_map(CUtensorMap* m, const TcArgs& a) {
     const cuuint64_t plane_bytes = (planes > 1 ? (cuuint64_t)a.c_plane : (cuuint64_t)a.ldc * (cuuint64_t)a.M) * es;
     cuuint64_t dims[3] = {(cuuint64_t)a.N, (cuuint64_t)a.M, (cuuint64_t)planes};
     cuuint64_t strides[2] = {row_bytes, plane_bytes};
-    cuuint32_t box[3] = {(cuuint32_t)(128 / es), 32, 1};
+    // the gated-linear-unit epilogue stores 32 x 32 blocks from 64-byte slot rows
+    cuuint32_t box[3] = {(cuuint32_t)(a.swiglu ? 32 : 128 / es), 32, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = enc(m, bf ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_INT32, 3, a.C, dims, strides,
-                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     a.swiglu ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
@@ -804,7 +858,7 @@ int max_pair_clusters(int bn) {
             opt_in<256, true, true, true, false>() != cudaSuccess ||
             opt_in<192, false, false, true, false>() != cudaSuccess ||
             opt_in<256, false, false, false, false, true>() != cudaSuccess ||
-            opt_in<256, false, false, false, false, false, true>() != cudaSuccess)
+            opt_in<256, false, false, false, true, false, true>() != cudaSuccess)
             return 0;
         g_max_clusters[dev][0] = occupancy_clusters<256>();
         g_max_clusters[dev][1] = occupancy_clusters<192>();
@@ -943,7 +997,7 @@ cudaError_t tc_gemm_launch(const TcArgs& a0, const void* A16, int64_t lda, int a
     const bool narrow = kext <= 1024 || rounds * kext <= 12288;
     if (a.fp_mode) return launch_engine<256, false, false, false, false, true>(a, tmA, tmB, tmC, tmS, clusters, s);
     if (a.swiglu)
-        return launch_engine<256, false, false, false, false, false, true>(a, tmA, tmB, tmC, tmS, clusters, s);
+        return launch_engine<256, false, false, false, true, false, true>(a, tmA, tmB, tmC, tmS, clusters, s);
     if (bias && a.split > 1) return launch_engine<256, true, true, true, false>(a, tmA, tmB, tmC, tmS, clusters, s);
     if (bias && bn == 192) return launch_engine<192, false, false, true, false>(a, tmA, tmB, tmC, tmS, clusters, s);
     if (bias) return launch_engine<256, false, false, true, true>(a, tmA, tmB, tmC, tmS, clusters, s);
