@@ -275,15 +275,15 @@ __device__ __forceinline__ void finish_rows(const TcArgs& p, const CUtensorMap* 
 
 // Gated-linear-unit epilogue of a warp's 32 rows x 64 accumulator columns (the sixteen-warp
 // geometry), which hold the gate and up accumulators of 32 outputs in turn (column 2c: gate,
-// 2c + 1: up, of output column colo0 + c): each output is rne_bf16(SiLU(g) * u). A first pass
-// over the registers takes the call-free tiers (bf16_silu_mul_fast) and marks what they leave
-// undecided; the exact sums also sit in the warp's TMEM columns at ta (written there by the
-// caller, whose accumulator buffer stays held until this returns), from which a second pass,
-// once the registers are dead, reads the marked outputs' operands for bf16_silu_mul_careful.
-// The warp's 32 x 32 bf16 block is staged in its slot (64-byte rows, no swizzle) and written by
-// one TMA store.
+// 2c + 1: up, of output column colo0 + c): each output is rne_bf16(SiLU(g) * u). The exact
+// sums sit in the warp's TMEM columns at ta (written there by the caller, whose accumulator
+// buffer stays held until this returns), read 16 columns at a time, so that the registers
+// are free for the evaluations of eight outputs at once. A first pass takes the call-free
+// tiers (bf16_silu_mul_fast) and marks what they leave undecided; a second pass reads the
+// marked outputs' operands again for the out-of-line evaluations. The warp's 32 x 32 bf16
+// block is staged in its slot (64-byte rows, no swizzle) and written by one TMA store.
 __device__ __forceinline__ void finish_swiglu(const TcArgs& p, const CUtensorMap* tmC, uint8_t* slot, int row0,
-                                              int colo0, const int32_t (&acc)[64], uint32_t ta, bool& pending) {
+                                              int colo0, uint32_t ta, bool& pending) {
     const int lane = threadIdx.x & 31;
     const int row = row0 + lane;
     const uint32_t sbase = smem_addr(slot) + (uint32_t)lane * 64u;
@@ -291,17 +291,23 @@ __device__ __forceinline__ void finish_swiglu(const TcArgs& p, const CUtensorMap
     const int32_t eg_own = c_own < p.N ? __ldg(p.ew + c_own) : 0;
     const int32_t eu_own = c_own < p.N ? __ldg(p.ewu + c_own) : 0;
     const int32_t ea = row < p.M ? __ldg(p.ea + row) : 0;
-    // exponents within 2^20 in magnitude keep the first pass's int sums exact; a warp that
-    // holds a larger one leaves all its outputs to the second pass (warp-uniform)
-    const bool small = (uint32_t)(ea + (1 << 20)) <= (2u << 20) && (uint32_t)(eg_own + (1 << 20)) <= (2u << 20) &&
-                       (uint32_t)(eu_own + (1 << 20)) <= (2u << 20);
-    const bool general = !__all_sync(0xffffffffu, small);
+    // every live pair's exponents ea + ew, ea + ewu in [-60, 40] lets the first pass skip the
+    // per-output checks; a warp that holds any other leaves all its outputs to the second pass
+    const bool lr = row < p.M, lc = c_own < p.N;
+    const int ea_lo = __reduce_min_sync(0xffffffffu, lr ? ea : INT_MAX);
+    const int ea_hi = __reduce_max_sync(0xffffffffu, lr ? ea : INT_MIN);
+    const int eg_lo = __reduce_min_sync(0xffffffffu, lc ? min(eg_own, eu_own) : INT_MAX);
+    const int eg_hi = __reduce_max_sync(0xffffffffu, lc ? max(eg_own, eu_own) : INT_MIN);
+    const bool general = (long long)ea_lo + eg_lo < -60 || (long long)ea_hi + eg_hi > 40;
     bool bad = false;
     uint32_t undecided = 0;  // bit c: output c is left to the second pass
     slot_acquire(pending);
     if (!general) {
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
+            uint32_t acc[16];  // columns 16 jj ..: the gate and up sums of outputs 8 jj .. 8 jj + 7
+            tmem_ld16(ta + 16u * (uint32_t)jj, acc);
+            tmem_wait_ld();
             uint32_t w[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -313,7 +319,9 @@ __device__ __forceinline__ void finish_swiglu(const TcArgs& p, const CUtensorMap
                     const int32_t eu = __shfl_sync(0xffffffffu, eu_own, c);
                     const bool live = row < p.M && colo0 + c < p.N;
                     bool und = false;
-                    h[e] = live ? bf16_silu_mul_fast(acc[2 * c], acc[2 * c + 1], ea + eg, ea + eu, bad, und) : 0u;
+                    h[e] = live ? bf16_silu_mul_fast((int32_t)acc[4 * i + 2 * e], (int32_t)acc[4 * i + 2 * e + 1], ea + eg,
+                                                     ea + eu, und)
+                                : 0u;
                     undecided |= und ? 1u << c : 0u;
                 }
                 w[i] = h[0] | (h[1] << 16);
@@ -648,7 +656,7 @@ __global__ void __launch_bounds__(Geo<BNT, kNarrow>::THREADS, 1)
             const int col0 = un.tn * BN + h * COLS;
             if constexpr (!kSplit) {
                 if constexpr (kSwiglu) {
-                    finish_swiglu(p, &tmC, slot, row - lane, col0 / 2, acc, ta_fin, pending);
+                    finish_swiglu(p, &tmC, slot, row - lane, col0 / 2, ta_fin, pending);
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive_cluster(tempty_lead + 8u * (uint32_t)buf_fin);

@@ -8,19 +8,16 @@
 // evaluation decides when no bf16 rounding boundary (a midpoint between neighbours) lies
 // within its bound of the computed value:
 //   exact zero   gacc == 0 or uacc == 0: +0;
+//   fp32         -87 < g < 64 (by the fp32 value g32, within 2^-24 of g): one fp32
+//                evaluation with relative error below 13 * 2^-24, i.e. 13 units of the last
+//                place of the fp32 result (bf16_silu_mul_fast), which decides unless its low
+//                16 bits are within 16 of 0x8000 (the midpoint) -- about one output in two
+//                thousand, so that the slower evaluations below stay rare;
 //   g >= 64      e^-g < 2^-92 while the exact dyadic P = g * u (62 significant bits) is either
 //                on a midpoint or at least 2^-62 |P| from every one: y = P sigma(g) rounds as
 //                P does, except that a P on a midpoint rounds toward zero (|y| < |P|);
 //   g <= -700    |y| < 2^-800: a zero with the sign of g * u;
-//   fp32         g > -80: g = g32 + gl exactly (g32 = fp32(g), gl the exact remainder, |gl| <=
-//                2^-24 |g|), e^-g = expf(-g32) (at most 2 ulp) times (1 - gl) (a first-order
-//                factor off by gl^2 < 2^-35), g * u as an exact two-product of g32 u32 plus the
-//                cross terms, rounded once in effect, the quotient by __fdividef (at most 2 ulp for divisors in [2^-126, 2^126];
-//                here 1 + e^-g lies in [1, e^80]): relative error below 11 * 2^-24, i.e. 11
-//                units of the last place of the fp32 result, whatever g, which decides unless
-//                its low 16 bits are within 14 of 0x8000 (the midpoint) -- a few outputs in
-//                ten thousand, so that a warp rarely takes the slower evaluations below;
-//   float-float  g > -80, the fp32 result in range but too close: the same formula in fp32
+//   float-float  -80 < g < 64, |y| in [2^-100, 2^127): the same formula in fp32
 //                float-float arithmetic (error-free sums and products), e^-g by range
 //                reduction and a Taylor series: relative error below 2^-40;
 //   fp64         exp (at most 2 ulp) on the exact g and u: relative error below 2^-49;
@@ -292,11 +289,8 @@ __device__ __forceinline__ SiluParts silu_parts(int32_t gacc, int32_t uacc, int 
     return s;
 }
 
-// The fp32 evaluation of y for -80 < g32 < 64: e^-g = expf(-g32) (at most 2 ulp) times
-// (1 - gl) (first order, off by gl^2 < 2^-35); g u = ph + (pl + corr); the quotient by
-// __fdividef (at most 2 ulp for divisors in [2^-126, 2^126]; 1 + e^-g lies in [1, e^80]).
-// Error terms in units of 2^-24 relative: expf 4, the fma 1, 1 + t 1, the sum 1 (plus terms
-// below 2^-40), the quotient 4: 11.
+// An fp32 estimate of y for -80 < g32 < 64 (relative error below 11 * 2^-24: expf 4, the fma
+// 1, 1 + t 1, the sum 1, __fdividef 4), which places y for the float-float evaluation.
 __device__ __forceinline__ float silu_mul_f32(const SiluParts& s) {
     const float t0 = expf(-s.g32);
     const float t = __fmaf_rn(-s.gl, t0, t0);
@@ -304,29 +298,31 @@ __device__ __forceinline__ float silu_mul_f32(const SiluParts& s) {
     return __fdividef(q, __fadd_rn(1.0f, t));
 }
 
-// rne_bf16(SiLU(gacc 2^Eg) * uacc 2^Eu) by the tiers that need no call: the exact zero, the
-// range check, g <= -700 and the fp32 evaluation (|Eg|, |Eu| below 2^30, so that int
-// arithmetic on them is exact). Sets `undecided` (and returns 0) for the rest, which
-// bf16_silu_mul_careful decides. The evaluation is routed by the fp32 gate value g32 (within
-// 2^-24 of g): every evaluation stays valid across that margin of its range. No function call
-// is reachable from here, so a caller holding many live registers (the GEMM epilogue's
-// accumulators) keeps them in registers.
-__device__ __forceinline__ uint16_t bf16_silu_mul_fast(int32_t gacc, int32_t uacc, int Eg, int Eu, bool& bad,
-                                                       bool& undecided) {
-    if (gacc == 0 || uacc == 0) return 0x0000;
-    if ((uint32_t)(Eg + 60) > 100u || (uint32_t)(Eu + 60) > 100u) {
-        bad = true;
-        return 0x7FC0;
-    }
-    const SiluParts s = silu_parts(gacc, uacc, Eg, Eu);
-    if (s.g32 <= -700.0f) return ((gacc ^ uacc) < 0) ? 0x8000 : 0x0000;
-    if (s.g32 > -80.0f && s.g32 < 64.0f) {
-        const uint32_t b = __float_as_uint(silu_mul_f32(s));
-        const uint32_t mag = b & 0x7FFFFFFFu;
-        // decided unless the low 16 bits are within 11 (+3 spare) of 0x8000, the midpoint;
-        // then the nearest-even rounding of a finite fp32 value to its top 16 bits
-        if (mag - 0x0D800000u < 0x7F000000u - 0x0D800000u && (b & 0xFFFFu) - (0x8000u - 14u) > 28u)
-            return (uint16_t)((b + 0x7FFFu + ((b >> 16) & 1u)) >> 16);
+// rne_bf16(SiLU(gacc 2^Eg) * uacc 2^Eu) by one fp32 evaluation, for exponents already known
+// to lie in [-60, 40]: the zero (g u = 0 exactly when an accumulator is 0: otherwise |g u| >=
+// 2^-120), and -87 < g32 < 64, where
+//   g32 = fp32(g) and gl = g - g32 exactly (split_i32 and the exact power-of-two scaling),
+//   e^-g = expf(-g32) (at most 2 ulp) times (1 - gl), to first order (gl^2 < 2^-34),
+//   g u as fp32(g32 u32) with u32 = fp32(u),
+//   y = __fdividef(g u, 1 + e^-g) (at most 2 ulp; 1 + e^-g lies in [1, e^87] within 2^126);
+// in units of 2^-24 relative: g u 3, e^-g 5 (expf 4, the fma 1), 1 + e^-g 6, the quotient 4:
+// 13, so that the fp32 result decides unless its low 16 bits lie within 13 (+3 spare) of
+// 0x8000, the midpoint, or |y| < 2^-100 (|y| < 2^77 here). Sets `undecided` (and returns 0)
+// otherwise, for bf16_silu_mul_careful. No function call is reachable from here, so a caller
+// holding many live registers keeps them in registers.
+__device__ __forceinline__ uint16_t bf16_silu_mul_fast(int32_t gacc, int32_t uacc, int Eg, int Eu, bool& undecided) {
+    const float sg = __int_as_float((Eg + 127) << 23), su = __int_as_float((Eu + 127) << 23);
+    float gh, glo;
+    split_i32(gacc, gh, glo);
+    const float g32 = __fmul_rn(gh, sg);
+    const float q = __fmul_rn(g32, __fmul_rn(__int2float_rn(uacc), su));
+    if (q == 0.0f) return 0x0000;
+    if (g32 > -87.0f && g32 < 64.0f) {
+        const float t0 = expf(-g32);
+        const float t = __fmaf_rn(-__fmul_rn(glo, sg), t0, t0);
+        const uint32_t b = __float_as_uint(__fdividef(q, __fadd_rn(1.0f, t)));
+        if ((b & 0x7FFFFFFFu) >= 0x0D800000u && (b & 0xFFFFu) - (0x8000u - 16u) > 32u)
+            return (uint16_t)((b + 0x7FFFu + ((b >> 16) & 1u)) >> 16);  // nearest-even to the top 16 bits
     }
     undecided = true;
     return 0x0000;
@@ -334,14 +330,15 @@ __device__ __forceinline__ uint16_t bf16_silu_mul_fast(int32_t gacc, int32_t uac
 
 // The evaluations for what bf16_silu_mul_fast leaves undecided (about one output in two
 // thousand; GB300 runs fp64 arithmetic at a small fraction of its fp32 rate, so the common
-// path stays free of it): g >= 64 by the exact product, float-float (|y| in [2^-100, 2^127)
-// and -80 < g32 < 64), fp64, then double-double. Exponents in [-60, 40], gacc and uacc
+// path stays free of it): g >= 64 by the exact product, g <= -700 as a signed zero, then
+// float-float (|y| in [2^-100, 2^127) and -80 < g32 < 64), fp64 and double-double. Exponents in [-60, 40], gacc and uacc
 // nonzero. Returns the bits, with bit 16 set when even the last evaluation could not decide
 // (DEV_RANGE).
 static __device__ __noinline__ uint32_t bf16_silu_mul_careful(int32_t gacc, int32_t uacc, int Eg, int Eu) {
     uint16_t out;
     const SiluParts s = silu_parts(gacc, uacc, Eg, Eu);
     if (s.g32 >= 64.0f) return bf16_round_i64((long long)gacc * (long long)uacc, Eg + Eu, true);
+    if (s.g32 <= -700.0f) return ((gacc ^ uacc) < 0) ? 0x8000 : 0x0000;
     if (s.g32 > -80.0f) {
         const float ay = fabsf(silu_mul_f32(s));
         if (ay >= 0x1p-100f && ay < 0x1p127f) {
@@ -372,7 +369,7 @@ __device__ __forceinline__ uint16_t bf16_silu_mul(int32_t gacc, int32_t uacc, lo
         return 0x7FC0;
     }
     bool undecided = false;
-    const uint16_t v = bf16_silu_mul_fast(gacc, uacc, (int)Eg, (int)Eu, bad, undecided);
+    const uint16_t v = bf16_silu_mul_fast(gacc, uacc, (int)Eg, (int)Eu, undecided);
     if (!undecided) return v;
     const uint32_t r = bf16_silu_mul_careful(gacc, uacc, (int)Eg, (int)Eu);
     bad |= (r >> 16) != 0;
