@@ -280,10 +280,12 @@ __device__ __forceinline__ void finish_rows(const TcArgs& p, const CUtensorMap* 
 // buffer stays held until this returns), read 16 columns at a time, so that the registers
 // are free for the evaluations of eight outputs at once. A first pass takes the call-free
 // tiers (bf16_silu_mul_fast) and marks what they leave undecided; a second pass reads the
-// marked outputs' operands again for the out-of-line evaluations. The warp's 32 x 32 bf16
-// block is staged in its slot (64-byte rows, no swizzle) and written by one TMA store.
+// marked outputs' operands again for the out-of-line evaluations; release_buffer() hands the
+// accumulator buffer back to the MMA once the operands are no longer needed. The warp's 32 x
+// 32 bf16 block is staged in its slot (64-byte rows, no swizzle) and written by one TMA store.
+template <typename Release>
 __device__ __forceinline__ void finish_swiglu(const TcArgs& p, const CUtensorMap* tmC, uint8_t* slot, int row0,
-                                              int colo0, uint32_t ta, bool& pending) {
+                                              int colo0, uint32_t ta, Release release_buffer, bool& pending) {
     const int lane = threadIdx.x & 31;
     const int row = row0 + lane;
     const uint32_t sbase = smem_addr(slot) + (uint32_t)lane * 64u;
@@ -318,11 +320,11 @@ __device__ __forceinline__ void finish_swiglu(const TcArgs& p, const CUtensorMap
                     const int32_t eg = __shfl_sync(0xffffffffu, eg_own, c);
                     const int32_t eu = __shfl_sync(0xffffffffu, eu_own, c);
                     const bool live = row < p.M && colo0 + c < p.N;
-                    bool und = false;
-                    h[e] = live ? bf16_silu_mul_fast((int32_t)acc[4 * i + 2 * e], (int32_t)acc[4 * i + 2 * e + 1], ea + eg,
-                                                     ea + eu, und)
-                                : 0u;
-                    undecided |= und ? 1u << c : 0u;
+                    bool und;  // evaluated for every pair (straight-line code), kept for live ones
+                    const uint16_t v = bf16_silu_mul_fast((int32_t)acc[4 * i + 2 * e], (int32_t)acc[4 * i + 2 * e + 1],
+                                                          ea + eg, ea + eu, und);
+                    h[e] = live ? v : 0u;
+                    undecided |= live && und ? 1u << c : 0u;
                 }
                 w[i] = h[0] | (h[1] << 16);
             }
@@ -332,19 +334,50 @@ __device__ __forceinline__ void finish_swiglu(const TcArgs& p, const CUtensorMap
         const int live_cols = p.N - colo0;
         undecided = row >= p.M || live_cols <= 0 ? 0u : live_cols >= 32 ? 0xFFFFFFFFu : (1u << live_cols) - 1u;
     }
-    // second pass: one output column at a time (warp-uniform), its operands from TMEM
-    for (uint32_t cols = __reduce_or_sync(0xffffffffu, undecided); cols != 0; cols &= cols - 1) {
-        const int c = __ffs(cols) - 1;
-        uint32_t g, u;
-        tmem_ld2(ta + 2u * (uint32_t)c, g, u);
-        tmem_wait_ld();
-        const int32_t eg = __shfl_sync(0xffffffffu, eg_own, c);
-        const int32_t eu = __shfl_sync(0xffffffffu, eu_own, c);
-        if ((undecided >> c) & 1u) {
-            const uint32_t r = bf16_silu_mul_any((int32_t)g, (int32_t)u, (long long)ea + eg, (long long)ea + eu);
-            bad |= (r >> 16) != 0;
-            st_shared_u16(sbase + 2u * (uint32_t)c, (uint16_t)r);
+    // second pass, one output column at a time (warp-uniform). Up to four columns (nearly
+    // always the case) have their operands copied into registers first, so that the buffer is
+    // released before the slower evaluations; more are read from TMEM one at a time, and the
+    // buffer is released after them.
+    uint32_t cols = __reduce_or_sync(0xffffffffu, undecided);
+    if (__popc(cols) <= 4) {
+        uint32_t gv[4], uv[4];
+        int cv[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            cv[k] = cols != 0 ? __ffs(cols) - 1 : -1;
+            gv[k] = uv[k] = 0;
+            if (cols != 0) tmem_ld2(ta + 2u * (uint32_t)cv[k], gv[k], uv[k]);
+            cols &= cols - 1;
         }
+        tmem_wait_ld();
+        release_buffer();
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            if (cv[k] < 0) break;
+            const int c = cv[k];
+            const int32_t eg = __shfl_sync(0xffffffffu, eg_own, c);
+            const int32_t eu = __shfl_sync(0xffffffffu, eu_own, c);
+            if ((undecided >> c) & 1u) {
+                const uint32_t r = bf16_silu_mul_any((int32_t)gv[k], (int32_t)uv[k], (long long)ea + eg, (long long)ea + eu);
+                bad |= (r >> 16) != 0;
+                st_shared_u16(sbase + 2u * (uint32_t)c, (uint16_t)r);
+            }
+        }
+    } else {
+        for (; cols != 0; cols &= cols - 1) {
+            const int c = __ffs(cols) - 1;
+            uint32_t g, u;
+            tmem_ld2(ta + 2u * (uint32_t)c, g, u);
+            tmem_wait_ld();
+            const int32_t eg = __shfl_sync(0xffffffffu, eg_own, c);
+            const int32_t eu = __shfl_sync(0xffffffffu, eu_own, c);
+            if ((undecided >> c) & 1u) {
+                const uint32_t r = bf16_silu_mul_any((int32_t)g, (int32_t)u, (long long)ea + eg, (long long)ea + eu);
+                bad |= (r >> 16) != 0;
+                st_shared_u16(sbase + 2u * (uint32_t)c, (uint16_t)r);
+            }
+        }
+        release_buffer();
     }
     if (bad) raise_status(DEV_RANGE);
     slot_release(tmC, slot, colo0, row0, 0, row0 < p.M && colo0 < p.N, pending);
@@ -656,10 +689,12 @@ __global__ void __launch_bounds__(Geo<BNT, kNarrow>::THREADS, 1)
             const int col0 = un.tn * BN + h * COLS;
             if constexpr (!kSplit) {
                 if constexpr (kSwiglu) {
-                    finish_swiglu(p, &tmC, slot, row - lane, col0 / 2, ta_fin, pending);
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive_cluster(tempty_lead + 8u * (uint32_t)buf_fin);
+                    const auto release = [&]() {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive_cluster(tempty_lead + 8u * (uint32_t)buf_fin);
+                    };
+                    finish_swiglu(p, &tmC, slot, row - lane, col0 / 2, ta_fin, release, pending);
                 } else finish_rows<COLS, kBias>(p, &tmC, slot, un.d, row - lane, col0, acc, pending);
                 continue;
             }

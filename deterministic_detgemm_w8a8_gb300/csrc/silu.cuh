@@ -311,21 +311,21 @@ __device__ __forceinline__ float silu_mul_f32(const SiluParts& s) {
 // otherwise, for bf16_silu_mul_careful. No function call is reachable from here, so a caller
 // holding many live registers keeps them in registers.
 __device__ __forceinline__ uint16_t bf16_silu_mul_fast(int32_t gacc, int32_t uacc, int Eg, int Eu, bool& undecided) {
-    const float sg = __int_as_float((Eg + 127) << 23), su = __int_as_float((Eu + 127) << 23);
+    // straight-line code (the decision is a predicate, not a branch), so that the evaluations
+    // of neighbouring outputs interleave
+    const float sg = __uint_as_float((uint32_t)(Eg + 127) << 23), su = __uint_as_float((uint32_t)(Eu + 127) << 23);
     float gh, glo;
     split_i32(gacc, gh, glo);
     const float g32 = __fmul_rn(gh, sg);
     const float q = __fmul_rn(g32, __fmul_rn(__int2float_rn(uacc), su));
-    if (q == 0.0f) return 0x0000;
-    if (g32 > -87.0f && g32 < 64.0f) {
-        const float t0 = expf(-g32);
-        const float t = __fmaf_rn(-__fmul_rn(glo, sg), t0, t0);
-        const uint32_t b = __float_as_uint(__fdividef(q, __fadd_rn(1.0f, t)));
-        if ((b & 0x7FFFFFFFu) >= 0x0D800000u && (b & 0xFFFFu) - (0x8000u - 16u) > 32u)
-            return (uint16_t)((b + 0x7FFFu + ((b >> 16) & 1u)) >> 16);  // nearest-even to the top 16 bits
-    }
-    undecided = true;
-    return 0x0000;
+    const float t0 = expf(-g32);
+    const float t = __fmaf_rn(-__fmul_rn(glo, sg), t0, t0);
+    const uint32_t b = __float_as_uint(__fdividef(q, __fadd_rn(1.0f, t)));
+    const bool zero = q == 0.0f;
+    const bool ok = (g32 > -87.0f) & (g32 < 64.0f) & ((b & 0x7FFFFFFFu) >= 0x0D800000u) &
+                    ((b & 0xFFFFu) - (0x8000u - 16u) > 32u);
+    undecided = !(zero | ok);
+    return zero ? (uint16_t)0 : (uint16_t)((b + 0x7FFFu + ((b >> 16) & 1u)) >> 16);  // nearest-even, top 16 bits
 }
 
 // The evaluations for what bf16_silu_mul_fast leaves undecided (about one output in two
