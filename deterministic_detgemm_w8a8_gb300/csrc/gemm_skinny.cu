@@ -139,6 +139,15 @@ __device__ __forceinline__ void tma_load_2d_hint(void* dst, const CUtensorMap* m
         : "memory");
 }
 
+// L2 prefetch of the box at (x, y): a hint that moves no data into shared memory, so it may be
+// issued before the wait on the prerequisite grid (any write that grid makes to the same lines
+// lands in L2 before the real loads after the wait read them)
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* m, int x, int y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(m)),
+                 "r"(x), "r"(y)
+                 : "memory");
+}
+
 // programmatic dependent launch: let the dependent grid start / wait for the prerequisite
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
@@ -528,14 +537,21 @@ __global__ void __launch_bounds__(WK_THREADS, 2) skinny_wk_kernel(const __grid_c
         *abort_flag = 0;
         fence_mbar_init();
     }
+    // The CTA's W rows go to L2 at once (DRAM latency paid once, not per ring refill), and the
+    // next call may be scheduled now: it runs this same prologue while this grid works, so
+    // that back-to-back calls keep HBM busy across the launch boundary.
+    if (threadIdx.x == 0) {
+        prefetch_tmap(&tmW);
+        for (int kb = 0; kb < nkb; ++kb) tma_prefetch_2d(&tmW, kb * 128, row0);
+        pdl_launch_dependents();
+    }
     __syncthreads();
-    // launched as a programmatic dependent of the kernel before it: nothing below touches
-    // global memory before that kernel has completed
+    // launched as a programmatic dependent of the kernel before it: apart from the L2 hints
+    // above, nothing below touches global memory before that kernel has completed
     pdl_wait();
 
     if (warp == 0) {
         if (lane == 0) {
-            prefetch_tmap(&tmW);
             prefetch_tmap(&tmA);
             const uint64_t stream_policy = l2_policy_evict_first();
             bool ok = true;
@@ -615,7 +631,6 @@ __global__ void __launch_bounds__(WK_THREADS, 2) skinny_wk_kernel(const __grid_c
         if (lane == 0) mbar_arrive(empty + st);
     }
 
-    if (cw == 0 && lane == 0) pdl_launch_dependents();  // the next call may start its set-up
     // The K groups' partials meet in the ring: every consumer is past its last stage, so
     // every load into it has landed (unless a wait gave up, which raised the abort flag and
     // the device status; then nothing is stored). Layout [warp][element][lane].
@@ -908,13 +923,17 @@ __global__ void __launch_bounds__(DT_THREADS, 1) decode_tc_kernel(const __grid_c
     if (warp == 0 && lane == 0) {
         prefetch_tmap(&tmW);
         prefetch_tmap(&tmA);
+        // the CTA's W boxes go to L2 at once (DRAM latency paid once, not per ring refill)
+        for (int i = 0; i < nloc; ++i) tma_prefetch_2d(&tmW, (f0 + i) * 128, n0);
+        pdl_launch_dependents();  // the next call may be scheduled (it waits for this grid)
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     // launched as a programmatic dependent of the kernel before it: the setup above overlaps
-    // that kernel's tail; nothing below touches global memory before it has completed
+    // that kernel's tail; apart from the L2 hints, nothing below touches global memory before
+    // it has completed
     pdl_wait();
 
     const bool epi = warp >= 2;
@@ -1039,8 +1058,6 @@ __global__ void __launch_bounds__(DT_THREADS, 1) decode_tc_kernel(const __grid_c
         const bool done = mbar_wait(accf, 0, abort_flag);
         ok = __all_sync(0xffffffffu, ok && done) && *abort_flag == 0;
     }
-    if (threadIdx.x == 0) pdl_launch_dependents();
-
     int32_t acc[MQ];
 #pragma unroll
     for (int j = 0; j < MQ; ++j) acc[j] = 0;
