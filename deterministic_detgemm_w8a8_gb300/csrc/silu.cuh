@@ -331,9 +331,9 @@ __device__ __forceinline__ uint16_t bf16_silu_mul_fast(int32_t gacc, int32_t uac
 // The evaluations for what bf16_silu_mul_fast leaves undecided (about one output in two
 // thousand; GB300 runs fp64 arithmetic at a small fraction of its fp32 rate, so the common
 // path stays free of it): g >= 64 by the exact product, g <= -700 as a signed zero, then
-// float-float (|y| in [2^-100, 2^127) and -80 < g32 < 64), fp64 and double-double. Exponents in [-60, 40], gacc and uacc
-// nonzero. Returns the bits, with bit 16 set when even the last evaluation could not decide
-// (DEV_RANGE).
+// float-float (|y| in [2^-100, 2^127) and -80 < g32 < 64), fp64 and double-double.
+// Exponents in [-60, 40], gacc and uacc nonzero. Returns the bits, with bit 16 set when even
+// the last evaluation could not decide (DEV_RANGE).
 static __device__ __noinline__ uint32_t bf16_silu_mul_careful(int32_t gacc, int32_t uacc, int Eg, int Eu) {
     uint16_t out;
     const SiluParts s = silu_parts(gacc, uacc, Eg, Eu);

@@ -344,10 +344,10 @@ DETGEMM_API detgemm_status detgemm_widen_i8_f16(const int8_t* X, int64_t ldx, in
  * and the product with the up projection join before that rounding]:
  *     g = G_ij 2^(ea_i + ewg_j),  u = U_ij 2^(ea_i + ewu_j)          (exact)
  *     C_ij = rne_bf16(SiLU(g) * u)            (one rounding of the real value; +0 when g or u is 0)
- * The value is transcendental; it is evaluated in fp32, fp64 and double-double arithmetic
- * in turn, each with a proven error bound, until no bf16 rounding boundary lies within the
- * bound (a gate g >= 64 is decided exactly from g * u), so the result is the correctly
- * rounded one and depends on the operands alone.
+ * The value is transcendental; it is evaluated in fp32, float-float, fp64 and double-double
+ * arithmetic in turn, each with a proven error bound, until no bf16 rounding boundary lies
+ * within the bound (a gate g >= 64 is decided exactly from g * u), so the result is the
+ * correctly rounded one and depends on the operands alone.
  *   G, U  int32 [M x N] (e.g. from detgemm_gemm_s8_i32 on the gate and up weights), row
  *         strides ldg, ldu;   ea int32 [M], ewg, ewu int32 [N];   C bf16 bits [M x N] (ldc)
  * The exponent sums ea_i + ewg_j and ea_i + ewu_j must lie in [-60, 40]; otherwise that

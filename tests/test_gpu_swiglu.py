@@ -1,7 +1,7 @@
 """GPU parity of the gated-linear-unit epilogue rne_bf16(SiLU(g) * u) with the oracle
 (binary128 evaluation, pinned to mpmath), bit for bit: random accumulators over the whole
 int32 range and exponent domain, inputs within 2^-20 and 2^-52 of a bf16 rounding boundary
-(the fp64 and double-double evaluations), large gates whose product sits on a midpoint, deep
+(the float-float, fp64 and double-double evaluations), large gates whose product sits on a midpoint, deep
 negative gates, subnormal and overflowing outputs, exponents outside the domain (NaN and
 DETGEMM_ERR_RANGE), and the composition with the library's exact int32 GEMM."""
 import os
