@@ -11,8 +11,11 @@ decode-shaped GEMM (M=16, N=4096, K=65536, split-K 8/16/32) in GB/s against the 
 roofline, the Ozaki fp32 GEMM (4096^3) in effective fp32 TFLOP/s next to the library fp32
 GEMM, the fp64-target Ozaki GEMM (4096^3) next to the library fp64 GEMM, the fused linear layer
 on bf16 activations at the FFN gate/up size, the sweep linear (K=2048, N=6144) at
-M = 1, 7, 64, 257, 2048, the biased epilogue (a bf16 bias per column added before the one
-rounding) beside the unbiased one on four of these shapes, and the tiny workload's latency.
+M = 1, 7, 64, 257, 2048 (single calls and back-to-back calls in a CUDA graph), the biased
+epilogue (a bf16 bias per column added before the one rounding) beside the unbiased one on four
+of these shapes, the fused gated-linear-unit FFN layer (rne_bf16(SiLU(g) * u), one rounding)
+beside the two plain W8A8 GEMMs it replaces, the fixed-order bf16 GEMM beside the library bf16
+GEMM, and the tiny workload's latency.
 
 Timing: W warm-up steps, then K timed steps; L2 is flushed before every timed step,
 outside the timed events, by a 256 MiB write followed by a 256 MiB read of another buffer
@@ -71,8 +74,12 @@ def _traffic():
     if t is None:
         return None
     return {"bytes_per_launch": (t["gate_up"] + t["down"]) // 2, "gate_up": t["gate_up"], "down": t["down"],
-            "algorithmic_bytes": {"gate_up": 2 * (M_FFN * K1 + N1 * K1 + M_FFN * N1),
-                                  "down": 2 * (M_FFN * K2 + N2 * K2 + M_FFN * N2)}}
+            # the step's algorithmic bytes: int8 A and W read once, bf16 C written once
+            "algorithmic_bytes": {"gate_up": M_FFN * K1 + N1 * K1 + 2 * M_FFN * N1,
+                                  "down": M_FFN * K2 + N2 * K2 + 2 * M_FFN * N2},
+            # what this kernel launch reads and writes at least: its fp16 operand copies and C
+            "kernel_operand_bytes": {"gate_up": 2 * (M_FFN * K1 + N1 * K1 + M_FFN * N1),
+                                     "down": 2 * (M_FFN * K2 + N2 * K2 + M_FFN * N2)}}
 
 
 def parse():
