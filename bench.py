@@ -537,8 +537,8 @@ def extras(dg, torch, dev, pk, flush):
     # on the FFN shapes, operands resident, L2 flushed
     lib_ffn = {}
     for name, (m, n, k) in (("gate_up", (M_FFN, N1, K1)), ("down", (M_FFN, N2, K2))):
-        a16 = torch.randn((m, k), device=dev).to(torch.float16)
-        b16 = torch.randn((k, n), device=dev).to(torch.float16)
+        a16 = tdev(synthetic.normal_f32(31, 0, (m, k))).to(torch.float16)
+        b16 = tdev(synthetic.normal_f32(31, 1, (k, n))).to(torch.float16)
         c16 = torch.empty((m, n), dtype=torch.float16, device=dev)
         ms = _time(torch, lambda: torch.matmul(a16, b16, out=c16), flush)
         lib_ffn[name] = {"us": round(ms * 1e3, 1), "TFLOPs": round(2.0 * m * n * k / (ms * 1e-3) / 1e12, 1)}
@@ -645,8 +645,8 @@ def extras(dg, torch, dev, pk, flush):
     # the vendor library's bf16 GEMM on the same operands (its bits depend on its own order)
     fx = {}
     for name, (m, n, k) in (("8192^3", (8192, 8192, 8192)), ("ffn_gate_up", (8192, 12288, 4096))):
-        a16 = torch.randn((m, k), device=dev).to(torch.bfloat16)
-        b16 = torch.randn((n, k), device=dev).to(torch.bfloat16)
+        a16 = tdev(synthetic.normal_f32(30, 0, (m, k))).to(torch.bfloat16)
+        b16 = tdev(synthetic.normal_f32(30, 1, (n, k))).to(torch.bfloat16)
         c32 = torch.empty((m, n), dtype=torch.float32, device=dev)
         ms = _time(torch, lambda: dg.gemm_fixed_f16(a16, b16, out=c32), flush)
         cb = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
@@ -688,8 +688,8 @@ def run_profile(name):
         A, W, ea, ew = (tdev(x) for x in args)
         fn = lambda: dg.w8a8(A, W, ea, ew, split_k=split)
     elif name == "fixed_bf16":
-        a16 = torch.randn((4096, 4096), device=dev).to(torch.bfloat16)
-        b16 = torch.randn((4096, 4096), device=dev).to(torch.bfloat16)
+        a16 = tdev(synthetic.normal_f32(30, 0, (4096, 4096))).to(torch.bfloat16)
+        b16 = tdev(synthetic.normal_f32(30, 1, (4096, 4096))).to(torch.bfloat16)
         fn = lambda: dg.gemm_fixed_f16(a16, b16)
     elif name == "swiglu":
         A, Wg, ea, ewg = (tdev(x) for x in synthetic.ffn_gate_up(2048))
