@@ -180,6 +180,50 @@ __device__ __forceinline__ void i8x16_to_f16x16(const uint4& v, uint32_t (&h)[8]
     i8x4_to_f16x4(v.w, h[6], h[7]);
 }
 
+// rne_bf16(acc * 2^ea * 2^ew) for ea, ew in [-60, 40]: acc truncated to 24 significant bits
+// with the last kept bit set when anything was dropped (rounding to odd), scaled exactly by
+// the two powers of two, then rounded to nearest-even: odd rounding at 24 >= 8 + 2 bits
+// followed by one nearest rounding at 8 bits equals one nearest rounding, so the bits are
+// those of the integer construction bf16_from_acc_pow2.
+__device__ __forceinline__ uint16_t bf16_pow2_fast(int32_t acc, int32_t ea, int32_t ew) {
+    const float x = __int2float_rz(acc);
+    const uint32_t xb = __float_as_uint(x) | (uint32_t)(__float2int_rz(x) != acc);
+    const float y = __fmul_rn(__fmul_rn(__uint_as_float(xb), __uint_as_float((uint32_t)(ea + 127) << 23)),
+                              __uint_as_float((uint32_t)(ew + 127) << 23));
+    return __bfloat16_as_ushort(__float2bfloat16_rn(y));
+}
+
+__device__ __forceinline__ void sts16(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+// store_pair with the exponents (and bias bits) already at hand, for rows < p.M, cols < p.N
+__device__ __forceinline__ void store_pair_pre(const SkArgs& p, int row, int col, int32_t v0, int32_t v1, int32_t ea,
+                                               int32_t ew0, int32_t ew1, uint32_t b0, uint32_t b1) {
+    if (row >= p.M || col >= p.N) return;
+    const bool two = col + 1 < p.N;
+    if (p.mode == EPI_STORE_I32) {
+        int32_t* C = reinterpret_cast<int32_t*>(p.C) + (int64_t)row * p.ldc + col;
+        if (two) *reinterpret_cast<int2*>(C) = make_int2(v0, v1);
+        else C[0] = v0;
+        return;
+    }
+    uint16_t h0, h1;
+    if (p.mode == EPI_BF16_POW2_BIAS) {
+        h0 = bf16_from_acc_pow2_bias(v0, ea, ew0, b0);
+        h1 = bf16_from_acc_pow2_bias(v1, ea, ew1, b1);
+    } else if (ea >= -60 && ea <= 40 && ew0 >= -60 && ew0 <= 40 && ew1 >= -60 && ew1 <= 40) {
+        h0 = bf16_pow2_fast(v0, ea, ew0);
+        h1 = bf16_pow2_fast(v1, ea, ew1);
+    } else {
+        h0 = bf16_from_acc_pow2(v0, ea, ew0);
+        h1 = bf16_from_acc_pow2(v1, ea, ew1);
+    }
+    uint16_t* C = p.C + (int64_t)row * p.ldc + col;
+    if (two) *reinterpret_cast<uint32_t*>(C) = (uint32_t)h0 | ((uint32_t)h1 << 16);
+    else C[0] = h0;
+}
+
 __device__ __forceinline__ void store_pair(const SkArgs& p, int row, int col, int32_t v0, int32_t v1) {
     if (row >= p.M || col >= p.N) return;
     const bool two = col + 1 < p.N;
@@ -481,11 +525,14 @@ __global__ void __launch_bounds__(256) skinny_finish_kernel(const __grid_constan
 }
 
 // ---------------------------------------------------------------------------- whole K
-// Decode-shaped problems with a short K (one launch, no workspace): CTA b owns W rows
-// [32 b, 32 b + 32) over the whole of K, so its sums are complete inside the CTA. Warp 0,
-// lane 0, streams per 128-wide K block one int8 box W[32 x 128] (evict-first) and one int8
-// box A[16 MT x 128] (128-byte swizzle, zero fill past M, N and K) into a ring of
-// wk_stages(MT) stages (16 for up to 16 tokens: the whole of a K = 2048 problem in flight). The eight consumer warps are two row groups (16 W rows each) times four K groups:
+// Decode-shaped problems with a short K and at most 16 tokens (one launch, no workspace):
+// CTA b owns W rows [32 b, 32 b + 32) over the whole of K, so its sums are complete inside
+// the CTA. Warp 0, lane 0, streams per 128-wide K block one int8 box W[32 x 128]
+// (evict-first) and one int8 box A[M x 128] of the real token rows (128-byte swizzle, zero
+// fill past N and K; the tile's rows M .. 15 are zeroed in shared memory once) into a ring
+// of 16 stages (the whole of a K = 2048 problem in flight). The exponents the rounding needs
+// are loaded into registers while W streams. The eight consumer warps are two row groups
+// (16 W rows each) times four K groups:
 // K group kg takes the K blocks kb = kg mod 4 (their stages, kb mod WK_STAGES, are released
 // by its two warps). Both operands are widened to fp16 in registers and multiplied with the
 // fp16 warp MMA into fp32 accumulators. With K <= WK_MAX_K = 4096 a warp's K blocks hold at
@@ -545,6 +592,16 @@ __global__ void __launch_bounds__(WK_THREADS, 2) skinny_wk_kernel(const __grid_c
         for (int kb = 0; kb < nkb; ++kb) tma_prefetch_2d(&tmW, kb * 128, row0);
         pdl_launch_dependents();
     }
+    // one token tile: the A box holds the M real token rows only, so the tile's rows M .. 15
+    // of every stage are zeroed once here and never written by the TMA
+    const int a_rows = MT == 1 ? p.M : 16 * MT;  // (launched with one token tile only)
+    if (MT == 1 && a_rows < 16) {
+        const int words = (16 - a_rows) * 8;  // 16-byte words of one stage's unused rows
+        for (int i = threadIdx.x; i < WK_STAGES * words; i += WK_THREADS) {
+            const int st = i / words, w = i - st * words;
+            sts16(smem_addr(smem + st * STAGE + wk_w_bytes() + a_rows * 128) + 16u * (uint32_t)w, 0u, 0u, 0u, 0u);
+        }
+    }
     __syncthreads();
     // launched as a programmatic dependent of the kernel before it: apart from the L2 hints
     // above, nothing below touches global memory before that kernel has completed
@@ -563,7 +620,7 @@ __global__ void __launch_bounds__(WK_THREADS, 2) skinny_wk_kernel(const __grid_c
                     break;
                 }
                 uint8_t* d = smem + st * STAGE;
-                mbar_arrive_expect_tx(full + st, STAGE);
+                mbar_arrive_expect_tx(full + st, wk_w_bytes() + a_rows * 128);
                 tma_load_2d_hint(d, &tmW, full + st, kb * 128, row0, stream_policy);
                 tma_load_2d(d + wk_w_bytes(), &tmA, full + st, kb * 128, 0);
             }
@@ -580,11 +637,28 @@ __global__ void __launch_bounds__(WK_THREADS, 2) skinny_wk_kernel(const __grid_c
     const int cw = warp - 1;
     const int rg = cw & 1, kg = cw >> 1;
     const int g = lane >> 2, t = lane & 3;
-    // the epilogue's exponents: fetched into L1 now, read after the main loop
-    if (cw == 0 && lane < 3) {
-        const void* a = lane == 0 ? (const void*)(p.ew + min(row0, p.N - 1))
-                                  : (const void*)(p.ea + min(32 * (lane - 1), p.M - 1));
-        asm volatile("prefetch.global.L1 [%0];" ::"l"(a));
+    // the epilogue's operands, loaded now by the warps that store (K group 0) so that their
+    // latency hides behind the main loop: the exponents of this lane's token rows and W columns
+    // (and the bias bits)
+    int32_t pre_ea[MT][2], pre_ew[2][2];
+    uint32_t pre_b[2][2];
+    if (kg == 0) {
+        const bool bf = p.mode != EPI_STORE_I32, bi = p.mode == EPI_BF16_POW2_BIAS;
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int r = 16 * mt + g + 8 * h;
+                pre_ea[mt][h] = bf && r < p.M ? __ldg(p.ea + r) : 0;
+            }
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int c = row0 + 16 * rg + 8 * j + 2 * t + e;
+                pre_ew[j][e] = bf && c < p.N ? __ldg(p.ew + c) : 0;
+                pre_b[j][e] = bi && c < p.N ? (uint32_t)__ldg(p.bias + c) : 0u;
+            }
     }
     const uint32_t sbase = smem_addr(smem);
     float accf[MT][2][4];
@@ -658,8 +732,10 @@ __global__ void __launch_bounds__(WK_THREADS, 2) skinny_wk_kernel(const __grid_c
                        red[((rg + 4) * (MT * 8) + e) * 32 + lane] + red[((rg + 6) * (MT * 8) + e) * 32 + lane];
             }
             const int col = row0 + 16 * rg + 8 * j + 2 * t;
-            store_pair(p, 16 * mt + g, col, v[0], v[1]);
-            store_pair(p, 16 * mt + g + 8, col, v[2], v[3]);
+            store_pair_pre(p, 16 * mt + g, col, v[0], v[1], pre_ea[mt][0], pre_ew[j][0], pre_ew[j][1], pre_b[j][0],
+                           pre_b[j][1]);
+            store_pair_pre(p, 16 * mt + g + 8, col, v[2], v[3], pre_ea[mt][1], pre_ew[j][0], pre_ew[j][1], pre_b[j][0],
+                           pre_b[j][1]);
         }
 }
 // launch with the programmatic-stream-serialization attribute (may overlap the kernel before)
@@ -825,9 +901,6 @@ __host__ __device__ constexpr int dt_smem_bytes(int MT) {
 static_assert(dt_smem_bytes(1) > 116 * 1024 && dt_smem_bytes(4) <= 227 * 1024, "shared memory");
 static_assert(DT_ACC_COL + 4 * 64 <= DT_TMEM_COLS, "TMEM: four 1024-K chunks of 64 tokens above the W stages");
 
-__device__ __forceinline__ void sts16(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
-}
 __device__ __forceinline__ int4 ld_dsmem_v4(uint32_t cluster_addr) {
     int4 v;
     asm volatile("ld.shared::cluster.v4.s32 {%0, %1, %2, %3}, [%4];"
@@ -847,18 +920,6 @@ __device__ __forceinline__ void mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem,
         : "memory");
 }
 
-// rne_bf16(acc * 2^ea * 2^ew) for ea, ew in [-60, 40]: acc truncated to 24 significant bits
-// with the last kept bit set when anything was dropped (rounding to odd), scaled exactly by
-// the two powers of two, then rounded to nearest-even: odd rounding at 24 >= 8 + 2 bits
-// followed by one nearest rounding at 8 bits equals one nearest rounding, so the bits are
-// those of the integer construction bf16_from_acc_pow2.
-__device__ __forceinline__ uint16_t bf16_pow2_fast(int32_t acc, int32_t ea, int32_t ew) {
-    const float x = __int2float_rz(acc);
-    const uint32_t xb = __float_as_uint(x) | (uint32_t)(__float2int_rz(x) != acc);
-    const float y = __fmul_rn(__fmul_rn(__uint_as_float(xb), __uint_as_float((uint32_t)(ea + 127) << 23)),
-                              __uint_as_float((uint32_t)(ew + 127) << 23));
-    return __bfloat16_as_ushort(__float2bfloat16_rn(y));
-}
 
 // one output of the decode kernels: row m, column col, with its exponents (and bias) at hand
 __device__ __forceinline__ void store_one(const SkArgs& p, int m, int col, int32_t v, int32_t ea, int32_t ew,
@@ -1233,7 +1294,7 @@ cudaError_t skinny_launch(const int8_t* A, int64_t lda, const int8_t* W, int64_t
             default: return dt_launch_mt<4>(tmW, tmA, a, s);
         }
     }
-    if (K <= WK_MAX_K && !exact_split) {
+    if (K <= WK_MAX_K && MT == 1 && !exact_split) {
         // short K, at most 16 tokens: one CTA per 32 W rows over the whole of K, int8 A read
         // directly (its one-launch set-up is cheaper than the tensor-core kernel's, which only
         // pays once the warp MMA work grows with the tokens)
@@ -1249,14 +1310,10 @@ cudaError_t skinny_launch(const int8_t* A, int64_t lda, const int8_t* W, int64_t
         a.mode = mode;
         CUtensorMap tmW, tmA;
         cudaError_t e = sk_map(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, W, K, ldw, N, WK_ROWS);
-        if (e == cudaSuccess) e = sk_map(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A, K, lda, M, 16 * MT);
+        // the token box holds the M real rows (the tile's other rows stay zero in shared memory)
+        if (e == cudaSuccess) e = sk_map(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A, K, lda, M, M);
         if (e != cudaSuccess) return e;
-        switch (MT) {
-            case 1: return wk_launch_mt<1>(tmW, tmA, a, s);
-            case 2: return wk_launch_mt<2>(tmW, tmA, a, s);
-            case 3: return wk_launch_mt<3>(tmW, tmA, a, s);
-            default: return wk_launch_mt<4>(tmW, tmA, a, s);
-        }
+        return wk_launch_mt<1>(tmW, tmA, a, s);
     }
     const SkLayout L = sk_layout(M, N, K);
     char* base = reinterpret_cast<char*>(ws);

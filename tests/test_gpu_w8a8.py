@@ -357,7 +357,8 @@ def test_skinny_many_ctas_repeated(lib, dev, oracle_mod):
 
 
 @pytest.mark.parametrize("M,N,K", [(64, 40, 4096), (17, 100, 4096), (1, 33, 4097), (48, 70, 3969), (64, 96, 5000),
-                                   (65, 100, 2048), (128, 64, 4096), (100, 33, 1000), (128, 70, 4097)])
+                                   (65, 100, 2048), (128, 64, 4096), (100, 33, 1000), (128, 70, 4097),
+                                   (16, 100, 4096), (1, 40, 4096), (5, 77, 384), (16, 130, 640), (9, 65, 128)])
 def test_decode_short_and_long_k(lib, dev, oracle_mod, M, N, K):
     # up to K = 4096 the decode path (M <= 64) keeps whole rows of W per CTA (each warp's fp32
     # partials hold at most 1024 products); longer K splits K over the SMs; M > 64 runs on
