@@ -526,60 +526,59 @@ __global__ void __launch_bounds__(256) skinny_finish_kernel(const __grid_constan
 
 // ---------------------------------------------------------------------------- whole K
 // Decode-shaped problems with a short K and at most 16 tokens (one launch, no workspace):
-// CTA b owns W rows [32 b, 32 b + 32) over the whole of K, so its sums are complete inside
-// the CTA. Warp 0, lane 0, streams per 128-wide K block one int8 box W[32 x 128]
+// CTA b owns W rows [R b, R b + R) over the whole of K (R = 16 as launched), so its sums are
+// complete inside the CTA. Warp 0, lane 0, streams per 128-wide K block one int8 box W[R x 128]
 // (evict-first) and one int8 box A[M x 128] of the real token rows (128-byte swizzle, zero
 // fill past N and K; the tile's rows M .. 15 are zeroed in shared memory once) into a ring
 // of 16 stages (the whole of a K = 2048 problem in flight). The exponents the rounding needs
-// are loaded into registers while W streams. The eight consumer warps are two row groups
-// (16 W rows each) times four K groups:
-// K group kg takes the K blocks kb = kg mod 4 (their stages, kb mod WK_STAGES, are released
-// by its two warps). Both operands are widened to fp16 in registers and multiplied with the
-// fp16 warp MMA into fp32 accumulators. With K <= WK_MAX_K = 4096 a warp's K blocks hold at
-// most 1024 k values, so every partial sum is an integer of magnitude <= 2^24, exact in fp32,
-// and no int32 drain is needed on the way. At the end the four K groups' partials, converted
-// to int32, meet in shared memory (integer sums, exact) and each row group's first warp
-// rounds and stores them.
-constexpr int WK_ROWS = 32;
+// are loaded into registers while W streams. The consumer warps are R / 16 row groups (16 W
+// rows each; one group of 8 rows for R = 8) times four K groups: K group kg takes the K blocks
+// kb = kg mod 4 (their stages, kb mod WK_STAGES, are released by its row-group warps). Both
+// operands are widened to fp16 in registers and multiplied with the fp16 warp MMA into fp32
+// accumulators. With K <= WK_MAX_K = 4096 a warp's K blocks hold at most 1024 k values, so
+// every partial sum is an integer of magnitude <= 2^24, exact in fp32, and no int32 drain is
+// needed on the way. At the end the four K groups' partials, converted to int32, meet in
+// shared memory (integer sums, exact) and each row group's first warp rounds and stores them.
 constexpr int WK_KG = 4;
-constexpr int WK_CONSUMERS = 2 * WK_KG;
-constexpr int WK_THREADS = 32 * (1 + WK_CONSUMERS);
 constexpr int WK_MAX_K = WK_KG * 1024;  // longer K goes to the split kernel (all SMs share K)
+constexpr int WK_STAGES = 16;           // the whole of a K = 2048 problem in flight
 
-__host__ __device__ constexpr int wk_w_bytes() { return WK_ROWS * 128; }
-__host__ __device__ constexpr int wk_a_bytes(int MT) { return 16 * MT * 128; }
-__host__ __device__ constexpr int wk_stage_bytes(int MT) { return wk_w_bytes() + wk_a_bytes(MT); }
-// a multiple of WK_KG, so that stage s is always released by K group s mod WK_KG
-// (at most 96 KB of ring: two CTAs per SM)
-__host__ __device__ constexpr int wk_stages(int MT) { return MT == 1 ? 16 : (MT == 2 ? 12 : 8); }
-// the ring, reused for the partial sums at the end: WK_CONSUMERS x 32 lanes x 8 MT words
-__host__ __device__ constexpr int wk_smem_bytes(int MT) {
-    return (wk_stages(MT) * wk_stage_bytes(MT) > WK_CONSUMERS * 32 * 8 * MT * 4 ? wk_stages(MT) * wk_stage_bytes(MT)
-                                                                                  : WK_CONSUMERS * 32 * 8 * MT * 4) +
-           1024 + 512;
-}
+// Geometry by the number of W rows per CTA (32, 16 or 8): RG row groups of consumer warps,
+// each over NJ 8-row MMA tiles, times WK_KG K groups.
+template <int ROWS>
+struct WkGeo {
+    static_assert(ROWS == 32 || ROWS == 16 || ROWS == 8, "rows per CTA");
+    static constexpr int RG = ROWS >= 16 ? ROWS / 16 : 1;
+    static constexpr int NJ = ROWS >= 16 ? 2 : 1;
+    static constexpr int CONSUMERS = RG * WK_KG;
+    static constexpr int THREADS = 32 * (1 + CONSUMERS);
+    static constexpr int W_BYTES = ROWS * 128;
+    static constexpr int A_BYTES = 16 * 128;  // one 16-token tile
+    static constexpr int STAGE = W_BYTES + A_BYTES;
+    static constexpr int RED_BYTES = CONSUMERS * 32 * NJ * 4 * 4;
+    static constexpr int SMEM = (WK_STAGES * STAGE > RED_BYTES ? WK_STAGES * STAGE : RED_BYTES) + 1024 + 512;
+    static constexpr int PER_SM = 227 * 1024 / SMEM < 8 ? 227 * 1024 / SMEM : 8;
+};
 
-__device__ __forceinline__ void consumer_bar() { asm volatile("bar.sync 1, %0;" ::"n"(WK_CONSUMERS * 32) : "memory"); }
-
-template <int MT>
-__global__ void __launch_bounds__(WK_THREADS, 2) skinny_wk_kernel(const __grid_constant__ CUtensorMap tmW,
-                                                                  const __grid_constant__ CUtensorMap tmA,
-                                                                  const __grid_constant__ SkArgs p) {
-    constexpr int STAGE = wk_stage_bytes(MT);
-    constexpr int WK_STAGES = wk_stages(MT);
+template <int ROWS>
+__global__ void __launch_bounds__(WkGeo<ROWS>::THREADS, WkGeo<ROWS>::PER_SM)
+    skinny_wk_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA,
+                     const __grid_constant__ SkArgs p) {
+    using G = WkGeo<ROWS>;
+    constexpr int STAGE = G::STAGE;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + (wk_smem_bytes(MT) - 1024 - 512));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + (G::SMEM - 1024 - 512));
     uint64_t* empty = full + WK_STAGES;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + WK_STAGES);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nkb = (p.K + 127) / 128;
-    const int row0 = blockIdx.x * WK_ROWS;
+    const int row0 = blockIdx.x * ROWS;
     if (threadIdx.x == 0) {
         for (int s = 0; s < WK_STAGES; ++s) {
             mbar_init(full + s, 1);
-            mbar_init(empty + s, 2);  // the two row-group warps of the stage's K group
+            mbar_init(empty + s, G::RG);  // the row-group warps of the stage's K group
         }
         *abort_flag = 0;
         fence_mbar_init();
@@ -592,14 +591,14 @@ __global__ void __launch_bounds__(WK_THREADS, 2) skinny_wk_kernel(const __grid_c
         for (int kb = 0; kb < nkb; ++kb) tma_prefetch_2d(&tmW, kb * 128, row0);
         pdl_launch_dependents();
     }
-    // one token tile: the A box holds the M real token rows only, so the tile's rows M .. 15
-    // of every stage are zeroed once here and never written by the TMA
-    const int a_rows = MT == 1 ? p.M : 16 * MT;  // (launched with one token tile only)
-    if (MT == 1 && a_rows < 16) {
+    // the A box holds the M real token rows only, so the tile's rows M .. 15 of every stage
+    // are zeroed once here and never written by the TMA
+    const int a_rows = p.M;
+    if (a_rows < 16) {
         const int words = (16 - a_rows) * 8;  // 16-byte words of one stage's unused rows
-        for (int i = threadIdx.x; i < WK_STAGES * words; i += WK_THREADS) {
+        for (int i = threadIdx.x; i < WK_STAGES * words; i += G::THREADS) {
             const int st = i / words, w = i - st * words;
-            sts16(smem_addr(smem + st * STAGE + wk_w_bytes() + a_rows * 128) + 16u * (uint32_t)w, 0u, 0u, 0u, 0u);
+            sts16(smem_addr(smem + st * STAGE + G::W_BYTES + a_rows * 128) + 16u * (uint32_t)w, 0u, 0u, 0u, 0u);
         }
     }
     __syncthreads();
@@ -620,9 +619,9 @@ __global__ void __launch_bounds__(WK_THREADS, 2) skinny_wk_kernel(const __grid_c
                     break;
                 }
                 uint8_t* d = smem + st * STAGE;
-                mbar_arrive_expect_tx(full + st, wk_w_bytes() + a_rows * 128);
+                mbar_arrive_expect_tx(full + st, G::W_BYTES + a_rows * 128);
                 tma_load_2d_hint(d, &tmW, full + st, kb * 128, row0, stream_policy);
-                tma_load_2d(d + wk_w_bytes(), &tmA, full + st, kb * 128, 0);
+                tma_load_2d(d + G::W_BYTES, &tmA, full + st, kb * 128, 0);
             }
             if (!ok) {
                 // let the loads already issued land before the CTA's shared memory goes away
@@ -635,39 +634,33 @@ __global__ void __launch_bounds__(WK_THREADS, 2) skinny_wk_kernel(const __grid_c
 
     // ---------------------------------------------------------------- consumers
     const int cw = warp - 1;
-    const int rg = cw & 1, kg = cw >> 1;
+    const int rg = cw % G::RG, kg = cw / G::RG;
     const int g = lane >> 2, t = lane & 3;
+    const int wr0 = 8 * G::NJ * rg;  // this row group's first W row in the CTA
     // the epilogue's operands, loaded now by the warps that store (K group 0) so that their
     // latency hides behind the main loop: the exponents of this lane's token rows and W columns
     // (and the bias bits)
-    int32_t pre_ea[MT][2], pre_ew[2][2];
-    uint32_t pre_b[2][2];
+    int32_t pre_ea[2], pre_ew[G::NJ][2];
+    uint32_t pre_b[G::NJ][2];
     if (kg == 0) {
         const bool bf = p.mode != EPI_STORE_I32, bi = p.mode == EPI_BF16_POW2_BIAS;
 #pragma unroll
-        for (int mt = 0; mt < MT; ++mt)
+        for (int h = 0; h < 2; ++h) pre_ea[h] = bf && g + 8 * h < p.M ? __ldg(p.ea + g + 8 * h) : 0;
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int r = 16 * mt + g + 8 * h;
-                pre_ea[mt][h] = bf && r < p.M ? __ldg(p.ea + r) : 0;
-            }
-#pragma unroll
-        for (int j = 0; j < 2; ++j)
+        for (int j = 0; j < G::NJ; ++j)
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
-                const int c = row0 + 16 * rg + 8 * j + 2 * t + e;
+                const int c = row0 + wr0 + 8 * j + 2 * t + e;
                 pre_ew[j][e] = bf && c < p.N ? __ldg(p.ew + c) : 0;
                 pre_b[j][e] = bi && c < p.N ? (uint32_t)__ldg(p.bias + c) : 0u;
             }
     }
     const uint32_t sbase = smem_addr(smem);
-    float accf[MT][2][4];
+    float accf[G::NJ][4];
 #pragma unroll
-    for (int a = 0; a < MT; ++a)
+    for (int b = 0; b < G::NJ; ++b)
 #pragma unroll
-        for (int b = 0; b < 2; ++b)
-#pragma unroll
-            for (int c = 0; c < 4; ++c) accf[a][b][c] = 0.f;
+        for (int c = 0; c < 4; ++c) accf[b][c] = 0.f;
     bool ok = true;
     for (int kb = kg; kb < nkb; kb += WK_KG) {
         const int st = kb % WK_STAGES;
@@ -677,26 +670,23 @@ __global__ void __launch_bounds__(WK_THREADS, 2) skinny_wk_kernel(const __grid_c
             break;
         }
         const uint32_t wb = sbase + st * STAGE;
-        const uint32_t ab = wb + wk_w_bytes();
+        const uint32_t ab = wb + G::W_BYTES;
         // lane (g, t) takes the 16-byte chunks t and t + 4 of each 128-byte row (16 k values
         // each) of W and of A alike, so both operands see the same k order
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
             const int c = t + 4 * half;
-            uint32_t hw[2][8];
+            uint32_t hw[G::NJ][8];
 #pragma unroll
-            for (int j = 0; j < 2; ++j) i8x16_to_f16x16(lds16(wb + sw128(16 * rg + 8 * j + g, c)), hw[j]);
+            for (int j = 0; j < G::NJ; ++j) i8x16_to_f16x16(lds16(wb + sw128(wr0 + 8 * j + g, c)), hw[j]);
+            uint32_t h0[8], h1[8];
+            i8x16_to_f16x16(lds16(ab + sw128(g, c)), h0);
+            i8x16_to_f16x16(lds16(ab + sw128(g + 8, c)), h1);
 #pragma unroll
-            for (int mt = 0; mt < MT; ++mt) {
-                uint32_t h0[8], h1[8];
-                i8x16_to_f16x16(lds16(ab + sw128(16 * mt + g, c)), h0);
-                i8x16_to_f16x16(lds16(ab + sw128(16 * mt + g + 8, c)), h1);
+            for (int q = 0; q < 4; ++q) {
+                const uint32_t a[4] = {h0[2 * q], h1[2 * q], h0[2 * q + 1], h1[2 * q + 1]};
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const uint32_t a[4] = {h0[2 * q], h1[2 * q], h0[2 * q + 1], h1[2 * q + 1]};
-#pragma unroll
-                    for (int j = 0; j < 2; ++j) mma_f16(accf[mt][j], a, hw[j][2 * q], hw[j][2 * q + 1]);
-                }
+                for (int j = 0; j < G::NJ; ++j) mma_f16(accf[j], a, hw[j][2 * q], hw[j][2 * q + 1]);
             }
         }
         // generic-proxy reads of the stage ordered before its release to the TMA refill
@@ -708,35 +698,30 @@ __global__ void __launch_bounds__(WK_THREADS, 2) skinny_wk_kernel(const __grid_c
     // The K groups' partials meet in the ring: every consumer is past its last stage, so
     // every load into it has landed (unless a wait gave up, which raised the abort flag and
     // the device status; then nothing is stored). Layout [warp][element][lane].
-    consumer_bar();
+    asm volatile("bar.sync 1, %0;" ::"r"(G::CONSUMERS * 32) : "memory");
     int32_t* red = reinterpret_cast<int32_t*>(smem);
 #pragma unroll
-    for (int mt = 0; mt < MT; ++mt)
+    for (int j = 0; j < G::NJ; ++j)
 #pragma unroll
-        for (int j = 0; j < 2; ++j)
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-                red[(cw * (MT * 8) + (mt * 2 + j) * 4 + c) * 32 + lane] = __float2int_rn(accf[mt][j][c]);
-    consumer_bar();
+        for (int c = 0; c < 4; ++c) red[(cw * (G::NJ * 4) + j * 4 + c) * 32 + lane] = __float2int_rn(accf[j][c]);
+    asm volatile("bar.sync 1, %0;" ::"r"(G::CONSUMERS * 32) : "memory");
     if (kg != 0 || !ok || *abort_flag) return;
-    // accumulator (mt, j, c): token 16 mt + g (+8 for c >= 2), W row 16 rg + 8 j + 2 t (+1 odd c)
+    // accumulator (j, c): token g (+8 for c >= 2), W row wr0 + 8 j + 2 t (+1 for odd c)
 #pragma unroll
-    for (int mt = 0; mt < MT; ++mt)
+    for (int j = 0; j < G::NJ; ++j) {
+        int32_t v[4];
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            int32_t v[4];
+        for (int c = 0; c < 4; ++c) {
+            const int e = j * 4 + c;
+            int32_t sum = 0;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const int e = (mt * 2 + j) * 4 + c;
-                v[c] = red[((rg + 0) * (MT * 8) + e) * 32 + lane] + red[((rg + 2) * (MT * 8) + e) * 32 + lane] +
-                       red[((rg + 4) * (MT * 8) + e) * 32 + lane] + red[((rg + 6) * (MT * 8) + e) * 32 + lane];
-            }
-            const int col = row0 + 16 * rg + 8 * j + 2 * t;
-            store_pair_pre(p, 16 * mt + g, col, v[0], v[1], pre_ea[mt][0], pre_ew[j][0], pre_ew[j][1], pre_b[j][0],
-                           pre_b[j][1]);
-            store_pair_pre(p, 16 * mt + g + 8, col, v[2], v[3], pre_ea[mt][1], pre_ew[j][0], pre_ew[j][1], pre_b[j][0],
-                           pre_b[j][1]);
+            for (int k = 0; k < WK_KG; ++k) sum += red[((rg + G::RG * k) * (G::NJ * 4) + e) * 32 + lane];
+            v[c] = sum;
         }
+        const int col = row0 + wr0 + 8 * j + 2 * t;
+        store_pair_pre(p, g, col, v[0], v[1], pre_ea[0], pre_ew[j][0], pre_ew[j][1], pre_b[j][0], pre_b[j][1]);
+        store_pair_pre(p, g + 8, col, v[2], v[3], pre_ea[1], pre_ew[j][0], pre_ew[j][1], pre_b[j][0], pre_b[j][1]);
+    }
 }
 // launch with the programmatic-stream-serialization attribute (may overlap the kernel before)
 template <typename... KArgs, typename... Args>
@@ -831,25 +816,26 @@ cudaError_t sk_launch_mt(const CUtensorMap& tmW, const CUtensorMap& tmA, const S
     return launch_pdl(skinny_finish_kernel, dim3(fblocks), dim3(256), 0, s, a);
 }
 
-int g_wk_set[64][5];  // skinny_wk_kernel<MT> opted into its shared memory, per device
+int g_wk_set[64][3];  // skinny_wk_kernel<ROWS> opted into its shared memory, per device
 
-template <int MT>
-cudaError_t wk_launch_mt(const CUtensorMap& tmW, const CUtensorMap& tmA, const SkArgs& a, cudaStream_t s) {
-    const int smem = wk_smem_bytes(MT);
+template <int ROWS>
+cudaError_t wk_launch_rows(const CUtensorMap& tmW, const CUtensorMap& tmA, const SkArgs& a, cudaStream_t s) {
+    using G = WkGeo<ROWS>;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    const int gi = ROWS == 32 ? 0 : (ROWS == 16 ? 1 : 2);
     {
         std::lock_guard<std::mutex> lock(g_sk_mutex);
-        if (!g_wk_set[dev][MT]) {
-            e = cudaFuncSetAttribute(skinny_wk_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (!g_wk_set[dev][gi]) {
+            e = cudaFuncSetAttribute(skinny_wk_kernel<ROWS>, cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM);
             if (e != cudaSuccess) return e;
-            g_wk_set[dev][MT] = 1;
+            g_wk_set[dev][gi] = 1;
         }
     }
-    cudaError_t le = launch_pdl(skinny_wk_kernel<MT>, dim3((unsigned)((a.N + WK_ROWS - 1) / WK_ROWS)), dim3(WK_THREADS),
-                                (size_t)smem, s, tmW, tmA, a);
+    cudaError_t le = launch_pdl(skinny_wk_kernel<ROWS>, dim3((unsigned)((a.N + ROWS - 1) / ROWS)), dim3(G::THREADS),
+                                (size_t)G::SMEM, s, tmW, tmA, a);
     if (le != cudaSuccess) return le;
     return cudaGetLastError();
 }
@@ -1309,11 +1295,15 @@ cudaError_t skinny_launch(const int8_t* A, int64_t lda, const int8_t* W, int64_t
         a.ldc = ldc;
         a.mode = mode;
         CUtensorMap tmW, tmA;
-        cudaError_t e = sk_map(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, W, K, ldw, N, WK_ROWS);
+        // 16 W rows per CTA (up to three CTAs per SM): measured against 32 rows (two per SM) and
+        // 8 rows (four per SM) on back-to-back calls at N = 6144, K = 2048: 5.16 against 5.62
+        // and 8.91 us at M = 1, 5.30 against 5.82 and 8.48 us at M = 16
+        constexpr int ROWS = 16;
+        cudaError_t e = sk_map(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, W, K, ldw, N, ROWS);
         // the token box holds the M real rows (the tile's other rows stay zero in shared memory)
         if (e == cudaSuccess) e = sk_map(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A, K, lda, M, M);
         if (e != cudaSuccess) return e;
-        return wk_launch_mt<1>(tmW, tmA, a, s);
+        return wk_launch_rows<ROWS>(tmW, tmA, a, s);
     }
     const SkLayout L = sk_layout(M, N, K);
     char* base = reinterpret_cast<char*>(ws);
