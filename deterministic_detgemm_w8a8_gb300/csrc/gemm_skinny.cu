@@ -1149,9 +1149,28 @@ __global__ void __launch_bounds__(DT_THREADS, 1) decode_tc_kernel(const __grid_c
                 v.w += u.w;
             }
             const int32_t vv[4] = {v.x, v.y, v.z, v.w};
+            const int col = n0 + r;
+            if (col + 3 < p.N && p.mode != EPI_BF16_POW2_BIAS) {
+                // four whole outputs in one store (rows of C are 16-byte aligned, col a multiple of 4)
+                if (p.mode == EPI_STORE_I32) {
+                    *reinterpret_cast<int4*>(reinterpret_cast<int32_t*>(p.C) + (int64_t)m * p.ldc + col) = v;
+                } else {
+                    const int32_t ea = sea[m];
+                    uint16_t h[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-                if (n0 + r + e < p.N) store_one(p, m, n0 + r + e, vv[e], sea[m], sew[r + e], sbias[r + e]);
+                    for (int e = 0; e < 4; ++e) {
+                        const int32_t ew = sew[r + e];
+                        h[e] = ea >= -60 && ea <= 40 && ew >= -60 && ew <= 40 ? bf16_pow2_fast(vv[e], ea, ew)
+                                                                               : bf16_from_acc_pow2(vv[e], ea, ew);
+                    }
+                    *reinterpret_cast<uint2*>(p.C + (int64_t)m * p.ldc + col) =
+                        make_uint2((uint32_t)h[0] | ((uint32_t)h[1] << 16), (uint32_t)h[2] | ((uint32_t)h[3] << 16));
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (col + e < p.N) store_one(p, m, col + e, vv[e], sea[m], sew[r + e], sbias[r + e]);
+            }
         }
     }
     if (P > 1) cluster_sync();  // no CTA leaves while another may still read its partials
