@@ -622,7 +622,9 @@ def extras(dg, torch, dev, pk, flush):
     res["bias_epilogue"] = bias_res
     # the gated-linear-unit FFN layer at the 8B-class size: gate and up projections (K = 4096,
     # N = 12288 each) on 8192 tokens, fused with the rne_bf16(SiLU(g) * u) epilogue, beside the
-    # two plain W8A8 GEMMs it replaces (whose outputs would still need a gating pass)
+    # two plain W8A8 GEMMs it replaces (whose outputs would still need a gating pass) and beside
+    # the same result computed unfused (the two exact int32 accumulators, then the element-wise
+    # epilogue)
     A, Wg, ea, ewg = (tdev(x) for x in synthetic.ffn_gate_up())
     Wu = tdev(synthetic.normal_i8(2, 9, (12288, 4096), 30.0))
     ewu = tdev(synthetic.uniform_i32(2, 10, (12288,), -14, -6))
@@ -636,10 +638,20 @@ def extras(dg, torch, dev, pk, flush):
         dg.w8a8(A, Wg, ea, ewg, out=C, ws=wsp)
         dg.w8a8(A, Wu, ea, ewu, out=C2, ws=wsp)
     ms_2 = _time(torch, two_gemms, flush)
+    G = torch.empty((8192, 12288), dtype=torch.int32, device=dev)
+    U = torch.empty((8192, 12288), dtype=torch.int32, device=dev)
+
+    def unfused():
+        dg.gemm_s8_i32(A, Wg, out=G, ws=wsp)
+        dg.gemm_s8_i32(A, Wu, out=U, ws=wsp)
+        dg.swiglu_bf16(G, U, ea, ewg, ewu, out=C2)
+    ms_u = _time(torch, unfused, flush)
+    del G, U
     ops = 2.0 * 2 * 8192 * 12288 * 4096
     res["swiglu_ffn_M8192_N12288x2_K4096"] = {
         "fused_us": round(ms_f * 1e3, 1), "fused_TOPS": round(ops / (ms_f * 1e-3) / 1e12, 1),
-        "two_w8a8_gemms_us": round(ms_2 * 1e3, 1), "two_w8a8_gemms_TOPS": round(ops / (ms_2 * 1e-3) / 1e12, 1)}
+        "two_w8a8_gemms_us": round(ms_2 * 1e3, 1), "two_w8a8_gemms_TOPS": round(ops / (ms_2 * 1e-3) / 1e12, 1),
+        "unfused_exact_us": round(ms_u * 1e3, 1)}
     del A, Wg, Wu, ea, ewg, ewu, C, C2, wss, wsp
     # the fixed-order bf16 GEMM (K walked in 16-wide tensor-core block FMAs, never split) beside
     # the vendor library's bf16 GEMM on the same operands (its bits depend on its own order)

@@ -263,7 +263,6 @@ __global__ void __launch_bounds__(256) slice_cols_kernel(const X* __restrict__ X
     int ecol[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) ecol[q] = cq + q < cols ? keys[cq + q] : KEY_ZERO;
-#pragma unroll
     // rows 4 ty .. 4 ty + 3 of columns cq .. cq + 3: all four rows are loaded first, then each
     // (plane, column) gets its four row digits in one 32-bit shared-memory store
     B v[4][4];
