@@ -156,3 +156,60 @@ def test_fused_ffn_gate_up_sampled(lib, dev, oracle_mod):
     want = oracle_mod.w8a8_swiglu(A, np.ascontiguousarray(Wg[cols]), np.ascontiguousarray(Wu[cols]), ea,
                                   np.ascontiguousarray(ewg[cols]), np.ascontiguousarray(ewu[cols]))
     assert (got[:, cols] == want).all()
+
+
+def test_fused_second_pass_paths(lib, dev, oracle_mod):
+    """The fused epilogue's out-of-line evaluations, which random FFN-like inputs rarely reach:
+    (1) exponents of magnitude above 2^20 whose sums stay in the domain (the whole warp's
+    outputs go to the second pass); (2) gates of magnitude >= 64 on nearly every output (more
+    than four output columns of a warp left to the second pass, so the accumulator buffer is
+    held through it); (3) zero activation rows (+0 whatever the exponents); (4) exponent sums
+    outside the domain on two columns (NaN there, DETGEMM_ERR_RANGE, every other output exact)."""
+    from gpu_util import padded
+    rng = np.random.default_rng(41)
+    M, N, K = 300, 260, 64
+    mk = lambda *s: np.clip(np.rint(rng.standard_normal(s) * 30), -127, 127).astype(np.int8)
+    A, Wg, Wu = mk(M, K), mk(N, K), mk(N, K)
+    A[7] = 0
+    A[200] = 0
+    dA, dWg, dWu = padded(A, dev, K), padded(Wg, dev, K), padded(Wu, dev, K)
+
+    def run(ea, ewg, ewu):
+        return bf16_bits(lib.w8a8_swiglu(dA, dWg, dWu, to_dev(ea, dev), to_dev(ewg, dev), to_dev(ewu, dev)))
+
+    # (1) and (3): large exponents, in-range sums
+    ea = (2 ** 21 + rng.integers(-14, -6, M)).astype(np.int32)
+    ewg = (-(2 ** 21) + rng.integers(-4, 4, N)).astype(np.int32)
+    ewu = (-(2 ** 21) + rng.integers(-4, 4, N)).astype(np.int32)
+    got = run(ea, ewg, ewu)
+    assert (got == oracle_mod.w8a8_swiglu(A, Wg, Wu, ea, ewg, ewu)).all()
+    assert (got[7] == 0).all() and (got[200] == 0).all()
+    assert lib.device_status() == lib.OK
+    # (2): g = the accumulator itself, |g| in the thousands
+    ea = np.zeros(M, np.int32)
+    ewg = np.zeros(N, np.int32)
+    ewu = rng.integers(-12, -4, N).astype(np.int32)
+    G = A.astype(np.int64) @ Wg.astype(np.int64).T
+    assert (np.abs(G) >= 64).mean() > 0.9
+    got = run(ea, ewg, ewu)
+    assert (got == oracle_mod.w8a8_swiglu(A, Wg, Wu, ea, ewg, ewu)).all()
+    assert lib.device_status() == lib.OK
+    # (4): columns 5 and 131 with a gate exponent sum of 100
+    ea = rng.integers(-14, -6, M).astype(np.int32)
+    ewg = rng.integers(-14, -6, N).astype(np.int32)
+    ewu = rng.integers(-14, -6, N).astype(np.int32)
+    bad = [5, 131]
+    ewg_bad = ewg.copy()
+    ewg_bad[bad] = 100 - ea.max()
+    got = run(ea, ewg_bad, ewu)
+    assert lib.device_status() == lib.ERR_RANGE
+    good = [j for j in range(N) if j not in bad]
+    want = oracle_mod.w8a8_swiglu(A, np.ascontiguousarray(Wg[good]), np.ascontiguousarray(Wu[good]), ea,
+                                  np.ascontiguousarray(ewg[good]), np.ascontiguousarray(ewu[good]))
+    assert (got[:, good] == want).all()
+    U = A.astype(np.int64) @ Wu.astype(np.int64).T
+    for j in bad:
+        # exponent sums 100 - max(ea) + ea_i lie outside [-60, 40] for every row: NaN where both
+        # accumulators are nonzero, +0 where one is zero
+        nz = (G[:, j] != 0) & (U[:, j] != 0)
+        assert (got[nz, j] == 0x7FC0).all() and (got[~nz, j] == 0).all()
