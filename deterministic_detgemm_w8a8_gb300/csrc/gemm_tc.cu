@@ -162,6 +162,7 @@ __device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
     asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
 }
 
+
 template <int COLS, bool kBias>
 __device__ __forceinline__ void finish_rows(const TcArgs& p, const CUtensorMap* tmC, uint8_t* slot, int d, int row0,
                                             int col0, const int32_t (&acc)[COLS], bool& pending) {
@@ -293,18 +294,29 @@ __device__ __forceinline__ void finish_swiglu(const TcArgs& p, const CUtensorMap
     const int32_t eg_own = c_own < p.N ? __ldg(p.ew + c_own) : 0;
     const int32_t eu_own = c_own < p.N ? __ldg(p.ewu + c_own) : 0;
     const int32_t ea = row < p.M ? __ldg(p.ea + row) : 0;
-    // every live pair's exponents ea + ew, ea + ewu in [-60, 40] lets the first pass skip the
-    // per-output checks; a warp that holds any other leaves all its outputs to the second pass
+    // every live pair's exponents ea + ew, ea + ewu in [-60, 40], and each exponent within
+    // [-120, 120] (so that 2^ea, 2^ew, 2^ewu and their products are exact fp32 numbers), lets
+    // the first pass skip the per-output checks; a warp that holds any other leaves all its
+    // outputs to the second pass
     const bool lr = row < p.M, lc = c_own < p.N;
     const int ea_lo = __reduce_min_sync(0xffffffffu, lr ? ea : INT_MAX);
     const int ea_hi = __reduce_max_sync(0xffffffffu, lr ? ea : INT_MIN);
     const int eg_lo = __reduce_min_sync(0xffffffffu, lc ? min(eg_own, eu_own) : INT_MAX);
     const int eg_hi = __reduce_max_sync(0xffffffffu, lc ? max(eg_own, eu_own) : INT_MIN);
-    const bool general = (long long)ea_lo + eg_lo < -60 || (long long)ea_hi + eg_hi > 40;
+    const bool general = (long long)ea_lo + eg_lo < -60 || (long long)ea_hi + eg_hi > 40 || ea_lo < -120 ||
+                         ea_hi > 120 || eg_lo < -120 || eg_hi > 120;
     bool bad = false;
     uint32_t undecided = 0;  // bit c: output c is left to the second pass
     slot_acquire(pending);
     if (!general) {
+        // the scales 2^ewg and 2^ewu of the warp's 32 output columns, in the slot's upper half
+        // (the staged outputs take its first 2 KB), read back as broadcasts
+        float* sc = reinterpret_cast<float*>(slot + 2048);
+        const bool in = lc && eg_own >= -120 && eg_own <= 120 && eu_own >= -120 && eu_own <= 120;
+        sc[lane] = in ? __uint_as_float((uint32_t)(eg_own + 127) << 23) : 1.0f;
+        sc[32 + lane] = in ? __uint_as_float((uint32_t)(eu_own + 127) << 23) : 1.0f;
+        __syncwarp();
+        const float sa = lr ? __uint_as_float((uint32_t)(ea + 127) << 23) : 1.0f;
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
             uint32_t acc[16];  // columns 16 jj ..: the gate and up sums of outputs 8 jj .. 8 jj + 7
@@ -313,20 +325,23 @@ __device__ __forceinline__ void finish_swiglu(const TcArgs& p, const CUtensorMap
             uint32_t w[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                uint32_t h[2];
+                float y[2];
+                uint32_t keep = 0xFFFFFFFFu;  // halves of the packed pair that hold a result
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     const int c = 8 * jj + 2 * i + e;
-                    const int32_t eg = __shfl_sync(0xffffffffu, eg_own, c);
-                    const int32_t eu = __shfl_sync(0xffffffffu, eu_own, c);
-                    const bool live = row < p.M && colo0 + c < p.N;
-                    bool und;  // evaluated for every pair (straight-line code), kept for live ones
-                    const uint16_t v = bf16_silu_mul_fast((int32_t)acc[4 * i + 2 * e], (int32_t)acc[4 * i + 2 * e + 1],
-                                                          ea + eg, ea + eu, und);
-                    h[e] = live ? v : 0u;
-                    undecided |= live && und ? 1u << c : 0u;
+                    const float sg = __fmul_rn(sa, sc[c]);
+                    const float su = __fmul_rn(sa, sc[32 + c]);
+                    const bool live = lr && colo0 + c < p.N;
+                    bool zero, ok;  // evaluated for every pair (straight-line code), kept for live ones
+                    y[e] = silu_mul_f32_scaled((int32_t)acc[4 * i + 2 * e], (int32_t)acc[4 * i + 2 * e + 1], sg, su,
+                                               zero, ok);
+                    keep &= zero || !live ? (e == 0 ? 0xFFFF0000u : 0x0000FFFFu) : 0xFFFFFFFFu;
+                    undecided |= live && !(zero || ok) ? 1u << c : 0u;
                 }
-                w[i] = h[0] | (h[1] << 16);
+                // both nearest-even roundings in one conversion; exact zeros and dead outputs +0
+                const __nv_bfloat162 pr = __floats2bfloat162_rn(y[0], y[1]);
+                w[i] = *reinterpret_cast<const uint32_t*>(&pr) & keep;
             }
             st_shared16(sbase + (uint32_t)(jj << 4), w[0], w[1], w[2], w[3]);
         }

@@ -298,34 +298,43 @@ __device__ __forceinline__ float silu_mul_f32(const SiluParts& s) {
     return __fdividef(q, __fadd_rn(1.0f, t));
 }
 
-// rne_bf16(SiLU(gacc 2^Eg) * uacc 2^Eu) by one fp32 evaluation, for exponents already known
-// to lie in [-60, 40]: the zero (g u = 0 exactly when an accumulator is 0: otherwise |g u| >=
-// 2^-120), and -87 < g32 < 64, where
+// SiLU(gacc 2^Eg) * uacc 2^Eu by one fp32 evaluation, for exponents already known to lie in
+// [-60, 40], given as the fp32 powers of two sg = 2^Eg and su = 2^Eu (exact): returns y with
+// `zero` (g u = 0 exactly when an accumulator is 0: otherwise |g u| >= 2^-120) and `ok` (y is
+// decided: its nearest-even bf16 rounding is the correct one), for -87 < g32 < 64, where
 //   g32 = fp32(g) and gl = g - g32 exactly (split_i32 and the exact power-of-two scaling),
 //   e^-g = expf(-g32) (at most 2 ulp) times (1 - gl), to first order (gl^2 < 2^-34),
 //   g u as fp32(g32 u32) with u32 = fp32(u),
 //   y = __fdividef(g u, 1 + e^-g) (at most 2 ulp; 1 + e^-g lies in [1, e^87] within 2^126);
 // in units of 2^-24 relative: g u 3, e^-g 5 (expf 4, the fma 1), 1 + e^-g 6, the quotient 4:
 // 13, so that the fp32 result decides unless its low 16 bits lie within 13 (+3 spare) of
-// 0x8000, the midpoint, or |y| < 2^-100 (|y| < 2^77 here). Sets `undecided` (and returns 0)
-// otherwise, for bf16_silu_mul_careful. No function call is reachable from here, so a caller
-// holding many live registers keeps them in registers.
-__device__ __forceinline__ uint16_t bf16_silu_mul_fast(int32_t gacc, int32_t uacc, int Eg, int Eu, bool& undecided) {
+// 0x8000, the midpoint, or |y| < 2^-100 (|y| < 2^77 here); what is neither zero nor decided
+// goes to bf16_silu_mul_careful. No function call is reachable from here, so a caller holding
+// many live registers keeps them in registers.
+__device__ __forceinline__ float silu_mul_f32_scaled(int32_t gacc, int32_t uacc, float sg, float su, bool& zero,
+                                                     bool& ok) {
     // straight-line code (the decision is a predicate, not a branch), so that the evaluations
     // of neighbouring outputs interleave
-    const float sg = __uint_as_float((uint32_t)(Eg + 127) << 23), su = __uint_as_float((uint32_t)(Eu + 127) << 23);
     float gh, glo;
     split_i32(gacc, gh, glo);
     const float g32 = __fmul_rn(gh, sg);
     const float q = __fmul_rn(g32, __fmul_rn(__int2float_rn(uacc), su));
     const float t0 = expf(-g32);
     const float t = __fmaf_rn(-__fmul_rn(glo, sg), t0, t0);
-    const uint32_t b = __float_as_uint(__fdividef(q, __fadd_rn(1.0f, t)));
-    const bool zero = q == 0.0f;
-    const bool ok = (g32 > -87.0f) & (g32 < 64.0f) & ((b & 0x7FFFFFFFu) >= 0x0D800000u) &
-                    ((b & 0xFFFFu) - (0x8000u - 16u) > 32u);
+    const float y = __fdividef(q, __fadd_rn(1.0f, t));
+    const uint32_t b = __float_as_uint(y);
+    zero = q == 0.0f;
+    ok = (g32 > -87.0f) & (g32 < 64.0f) & ((b & 0x7FFFFFFFu) >= 0x0D800000u) & ((b & 0xFFFFu) - (0x8000u - 16u) > 32u);
+    return y;
+}
+
+// the same with int exponents: the rounded bits, or `undecided` (and 0)
+__device__ __forceinline__ uint16_t bf16_silu_mul_fast(int32_t gacc, int32_t uacc, int Eg, int Eu, bool& undecided) {
+    bool zero, ok;
+    const float y = silu_mul_f32_scaled(gacc, uacc, __uint_as_float((uint32_t)(Eg + 127) << 23),
+                                        __uint_as_float((uint32_t)(Eu + 127) << 23), zero, ok);
     undecided = !(zero | ok);
-    return zero ? (uint16_t)0 : (uint16_t)((b + 0x7FFFu + ((b >> 16) & 1u)) >> 16);  // nearest-even, top 16 bits
+    return zero ? (uint16_t)0 : __bfloat16_as_ushort(__float2bfloat16_rn(y));
 }
 
 // The evaluations for what bf16_silu_mul_fast leaves undecided (about one output in two
