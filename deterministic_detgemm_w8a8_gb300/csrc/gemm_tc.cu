@@ -326,25 +326,29 @@ __device__ __forceinline__ void finish_swiglu(const TcArgs& p, const CUtensorMap
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 float y[2];
-                uint32_t keep = 0xFFFFFFFFu;  // halves of the packed pair that hold a result
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     const int c = 8 * jj + 2 * i + e;
                     const float sg = __fmul_rn(sa, sc[c]);
                     const float su = __fmul_rn(sa, sc[32 + c]);
-                    const bool live = lr && colo0 + c < p.N;
-                    bool zero, ok;  // evaluated for every pair (straight-line code), kept for live ones
+                    bool zero, ok;  // evaluated for every pair (straight-line code)
                     y[e] = silu_mul_f32_scaled((int32_t)acc[4 * i + 2 * e], (int32_t)acc[4 * i + 2 * e + 1], sg, su,
                                                zero, ok);
-                    keep &= zero || !live ? (e == 0 ? 0xFFFF0000u : 0x0000FFFFu) : 0xFFFFFFFFu;
-                    undecided |= live && !(zero || ok) ? 1u << c : 0u;
+                    // an exact zero (g u = 0) is +0, whatever the evaluation gave (-0, or a NaN
+                    // from 0 / (1 + e^-g) when e^-g overflows)
+                    y[e] = zero ? 0.0f : y[e];
+                    undecided |= zero || ok ? 0u : 1u << c;
                 }
-                // both nearest-even roundings in one conversion; exact zeros and dead outputs +0
+                // both nearest-even roundings in one conversion (outputs past M or N are computed
+                // and staged too; the TMA store writes none of them)
                 const __nv_bfloat162 pr = __floats2bfloat162_rn(y[0], y[1]);
-                w[i] = *reinterpret_cast<const uint32_t*>(&pr) & keep;
+                w[i] = *reinterpret_cast<const uint32_t*>(&pr);
             }
             st_shared16(sbase + (uint32_t)(jj << 4), w[0], w[1], w[2], w[3]);
         }
+        // only live outputs go to the second pass
+        const int live_cols = p.N - colo0;
+        undecided &= !lr || live_cols <= 0 ? 0u : live_cols >= 32 ? 0xFFFFFFFFu : (1u << live_cols) - 1u;
     } else {
         const int live_cols = p.N - colo0;
         undecided = row >= p.M || live_cols <= 0 ? 0u : live_cols >= 32 ? 0xFFFFFFFFu : (1u << live_cols) - 1u;
