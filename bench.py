@@ -51,7 +51,7 @@ OPS_STEP = 2.0 * M_FFN * (N1 * K1 + N2 * K2)
 # FFN GEMMs, keyed by a digest of the engine source so that a changed kernel reports null,
 # not stale counters
 PROFILED_TRAFFIC = {
-    "ce5bf83ee96d6606": {"gate_up": 487437568 + 182206976, "down": 897488384 + 62470144},
+    "994b9e423ada20d9": {"gate_up": 486764288 + 182261760, "down": 897466880 + 63083520},
 }
 
 
