@@ -212,7 +212,8 @@ __device__ __forceinline__ void store_pair_pre(const SkArgs& p, int row, int col
     if (p.mode == EPI_BF16_POW2_BIAS) {
         h0 = bf16_from_acc_pow2_bias(v0, ea, ew0, b0);
         h1 = bf16_from_acc_pow2_bias(v1, ea, ew1, b1);
-    } else if (ea >= -60 && ea <= 40 && ew0 >= -60 && ew0 <= 40 && ew1 >= -60 && ew1 <= 40) {
+    } else if (__all_sync(__activemask(), ea >= -60 && ea <= 40 && ew0 >= -60 && ew0 <= 40 && ew1 >= -60 && ew1 <= 40)) {
+        // a warp-uniform branch, not a select: the integer form is evaluated only where needed
         h0 = bf16_pow2_fast(v0, ea, ew0);
         h1 = bf16_pow2_fast(v1, ea, ew1);
     } else {
@@ -1156,12 +1157,21 @@ __global__ void __launch_bounds__(DT_THREADS, 1) decode_tc_kernel(const __grid_c
                     *reinterpret_cast<int4*>(reinterpret_cast<int32_t*>(p.C) + (int64_t)m * p.ldc + col) = v;
                 } else {
                     const int32_t ea = sea[m];
-                    uint16_t h[4];
+                    int32_t ew[4];
+                    bool inr = ea >= -60 && ea <= 40;
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const int32_t ew = sew[r + e];
-                        h[e] = ea >= -60 && ea <= 40 && ew >= -60 && ew <= 40 ? bf16_pow2_fast(vv[e], ea, ew)
-                                                                               : bf16_from_acc_pow2(vv[e], ea, ew);
+                        ew[e] = sew[r + e];
+                        inr = inr && ew[e] >= -60 && ew[e] <= 40;
+                    }
+                    uint16_t h[4];
+                    // a branch, not a select: the integer form is evaluated only where needed
+                    if (__all_sync(__activemask(), inr)) {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) h[e] = bf16_pow2_fast(vv[e], ea, ew[e]);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) h[e] = bf16_from_acc_pow2(vv[e], ea, ew[e]);
                     }
                     *reinterpret_cast<uint2*>(p.C + (int64_t)m * p.ldc + col) =
                         make_uint2((uint32_t)h[0] | ((uint32_t)h[1] << 16), (uint32_t)h[2] | ((uint32_t)h[3] << 16));
