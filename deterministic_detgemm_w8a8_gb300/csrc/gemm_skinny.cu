@@ -1113,14 +1113,15 @@ __global__ void __launch_bounds__(DT_THREADS, 1) decode_tc_kernel(const __grid_c
         tc_fence_after();
         const int nchunks = (nloc + 7) / 8;
         for (int ch = 0; ch < nchunks; ++ch) {
+            // all of the chunk's loads in flight, then one wait
+            uint32_t v[MQ / 4][4];
 #pragma unroll
-            for (int j = 0; j < MQ / 4; ++j) {
-                uint32_t v[4];
-                tmem_ld4(lane_base + DT_ACC_COL + (uint32_t)(ch * MP + mq0 + 4 * j), v);
-                tmem_wait_ld();
+            for (int j = 0; j < MQ / 4; ++j) tmem_ld4(lane_base + DT_ACC_COL + (uint32_t)(ch * MP + mq0 + 4 * j), v[j]);
+            tmem_wait_ld();
 #pragma unroll
-                for (int e = 0; e < 4; ++e) acc[4 * j + e] += __float2int_rn(__uint_as_float(v[e]));
-            }
+            for (int j = 0; j < MQ / 4; ++j)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[4 * j + e] += __float2int_rn(__uint_as_float(v[j][e]));
         }
     }
     tc_fence_before();
