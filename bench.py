@@ -534,15 +534,27 @@ def extras(dg, torch, dev, pk, flush):
     del ws4, Ad, Bd
     del Af, Bf, Cf, ws
     # context for the tensor-core roofline: the vendor library's fp16 GEMM (fp32 accumulate)
-    # on the FFN shapes, operands resident, L2 flushed
+    # on the FFN shapes, operands resident, L2 flushed; on random normal operands, and on the
+    # step's own operands (int8 values in fp16, both K-major, as the engine multiplies them),
+    # beside the engine on those same widened operands
     lib_ffn = {}
-    for name, (m, n, k) in (("gate_up", (M_FFN, N1, K1)), ("down", (M_FFN, N2, K2))):
+    for name, (m, n, k), ops_np in (("gate_up", (M_FFN, N1, K1), synthetic.ffn_gate_up(M_FFN)),
+                                    ("down", (M_FFN, N2, K2), synthetic.ffn_down(M_FFN))):
         a16 = tdev(synthetic.normal_f32(31, 0, (m, k))).to(torch.float16)
         b16 = tdev(synthetic.normal_f32(31, 1, (k, n))).to(torch.float16)
         c16 = torch.empty((m, n), dtype=torch.float16, device=dev)
         ms = _time(torch, lambda: torch.matmul(a16, b16, out=c16), flush)
-        lib_ffn[name] = {"us": round(ms * 1e3, 1), "TFLOPs": round(2.0 * m * n * k / (ms * 1e-3) / 1e12, 1)}
-        del a16, b16, c16
+        del a16, b16
+        A16, W16 = (tdev(x).to(torch.float16) for x in ops_np[:2])
+        ea, ew = (tdev(x) for x in ops_np[2:])
+        ms_same = _time(torch, lambda: torch.matmul(A16, W16.t(), out=c16), flush)
+        cb = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+        ms_eng = _time(torch, lambda: dg.w8a8_f16ops(A16, W16, ea, ew, out=cb), flush)
+        tf = lambda t: round(2.0 * m * n * k / (t * 1e-3) / 1e12, 1)
+        lib_ffn[name] = {"us": round(ms * 1e3, 1), "TFLOPs": tf(ms), "operands": "random normal, [K,N] B",
+                         "same_operands_us": round(ms_same * 1e3, 1), "same_operands_TFLOPs": tf(ms_same),
+                         "engine_same_operands_us": round(ms_eng * 1e3, 1)}
+        del A16, W16, ea, ew, c16, cb
     res["library_fp16_gemm_ffn_shapes"] = lib_ffn
     # fp64-target Ozaki GEMM 4096^3 (8 slices, 36 slice pairs), next to the fp64 GEMM of the
     # vendor library on the same operands (context: GB300's fp64 rate)
